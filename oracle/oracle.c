@@ -1,0 +1,386 @@
+/*
+ * oracle.c -- float64 CPU reference for the row-wise normalization layers
+ * (DyT, LayerNorm, Llama-style RMSNorm), forward and backward, including
+ * the per-feature parameter-gradient column sums.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file; it exists so that tests, the smoke check and the CPU
+ * baseline timing can compare the CUDA kernels against an independent,
+ * plainly written definition.  It shares no code, header or constant with
+ * the CUDA library.
+ *
+ * Every computation is the textbook definition written out in float64,
+ * row by row, with serial sums in index order and no blocking or
+ * reordering.  Inputs arrive as raw float32, bfloat16 (raw 16-bit
+ * patterns) or float64 arrays and are widened exactly to float64.
+ *
+ * Two modes:
+ *   ORC_MATH   -- pure float64, no intermediate rounding (closed-form,
+ *                 finite-difference and invariant checks);
+ *   ORC_PARITY -- float64 plus round-to-nearest-even to the activation
+ *                 dtype at the intermediate rounding points that the
+ *                 fused-RMSNorm page (DeepSpeed PR 8645, quoted in PR
+ *                 8664, section "Semantics") fixes: the normalized value,
+ *                 grad_out * weight, and grad_out * normalized when the
+ *                 weight has the activation dtype.  DyT and LayerNorm have
+ *                 no intermediate rounding point; their only rounding is
+ *                 the final store, which the caller applies.
+ *
+ * Outputs are float64 values BEFORE the final rounding to the output
+ * dtype, plus a "scale" companion (the sum of the magnitudes of the
+ * addends, or the square root of the sum of squared terms for column sums)
+ * that the tests use to judge cancellation.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
+enum { ORC_MATH = 0, ORC_PARITY = 1 };
+
+/* Largest finite bfloat16: significand 0xFF (8 bits) times 2^(127-7). */
+#define BF16_MAX_FINITE (255.0 * 1329227995784915872903807060280344576.0 /* 2^120 */)
+
+/* Relative distance to a bfloat16 rounding midpoint below which a value
+ * computed in float32 elsewhere may legitimately round the other way. */
+#define NEAR_TIE_REL (1.0 / 131072.0) /* 2^-17 */
+
+/* ---------------------------------------------------------------- inputs */
+
+static double widen(const void* p, int dt, int64_t i)
+{
+    if (dt == ORC_F64) return ((const double*)p)[i];
+    if (dt == ORC_F32) return (double)((const float*)p)[i];
+    /* bfloat16 is the upper half of a float32 bit pattern. */
+    uint32_t u = (uint32_t)((const uint16_t*)p)[i] << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------- rounding */
+
+/*
+ * Round a float64 to the nearest bfloat16, ties to even, directly (never
+ * through float32).  bfloat16 keeps 8 significant bits and float32's
+ * exponent range, so a normal value a in [2^(k-1), 2^k) is a multiple of
+ * 2^(k-8); below the normal range (2^-126) the spacing stays 2^-133.
+ * nearbyint() rounds half to even in the default rounding mode.
+ * *near_tie is set when the value lies within NEAR_TIE_REL (relative) of a
+ * rounding midpoint.
+ */
+static double round_bf16(double v, int* near_tie)
+{
+    if (near_tie) *near_tie = 0;
+    if (isnan(v) || isinf(v) || v == 0.0) return v;
+    double a = fabs(v);
+    int k;
+    (void)frexp(a, &k); /* a = f * 2^k, f in [0.5, 1) */
+    int qe = k - 8;
+    if (qe < -133) qe = -133;
+    double m = ldexp(a, -qe); /* exact: scaling by a power of two */
+    double mr = nearbyint(m);
+    if (near_tie) {
+        double frac = m - floor(m);
+        if (fabs(frac - 0.5) < NEAR_TIE_REL * m) *near_tie = 1;
+    }
+    double r = ldexp(mr, qe);
+    if (r > BF16_MAX_FINITE) r = INFINITY;
+    return copysign(r, v);
+}
+
+/* Round to the activation dtype: bfloat16 as above, float32 by the C
+ * conversion (round to nearest even), float64 unchanged. */
+static double round_to(double v, int dt, int* near_tie)
+{
+    if (dt == ORC_BF16) return round_bf16(v, near_tie);
+    if (near_tie) *near_tie = 0;
+    if (dt == ORC_F32) return (double)(float)v;
+    return v;
+}
+
+double orc_round_bf16(double v) { return round_bf16(v, NULL); }
+void orc_round_bf16_array(const double* in, double* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = round_bf16(in[i], NULL);
+}
+
+int orc_bf16_near_tie(double v)
+{
+    int t;
+    (void)round_bf16(v, &t);
+    return t;
+}
+
+static int64_t row_of(const int64_t* rows, int64_t r) { return rows ? rows[r] : r; }
+
+/* ================================================================== DyT
+ * Dynamic Tanh: y = gamma_j * tanh(alpha * x_ij) + beta_j with a scalar
+ * alpha and per-channel gamma, beta (the fused DyT kernels of Liger-Kernel
+ * PR 1617, "fix(dyt): use a 1D grid and tile small-width rows").
+ * The backward uses the exact derivatives with sech^2 = 1 / cosh^2:
+ *   dx_ij   = dy_ij * gamma_j * alpha * sech^2(alpha x_ij)
+ *   dgamma_j = sum_i dy_ij * tanh(alpha x_ij)
+ *   dbeta_j  = sum_i dy_ij
+ *   dalpha   = sum_ij dy_ij * gamma_j * x_ij * sech^2(alpha x_ij)
+ * IEEE evaluation throughout: with alpha = +inf every real element gives
+ * tanh = +-1 and sech^2 = 0, so dx = (inf * 0) = NaN while the parameter
+ * gradients stay finite, as that page's Summary requires of real rows.
+ */
+
+static double sech2(double z)
+{
+    double c = cosh(z);
+    return 1.0 / (c * c);
+}
+
+int orc_dyt_fwd_rows(const void* x, int xt, int64_t M, int64_t N, double alpha,
+                     const double* gamma, const double* beta, const int64_t* rows,
+                     int64_t nrows, double* y, double* y_scale)
+{
+    (void)M;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = row_of(rows, r);
+        for (int64_t j = 0; j < N; ++j) {
+            double t = tanh(alpha * widen(x, xt, i * N + j));
+            double gt = gamma[j] * t;
+            y[r * N + j] = gt + beta[j];
+            if (y_scale) y_scale[r * N + j] = fabs(gt) + fabs(beta[j]);
+        }
+    }
+    return 0;
+}
+
+int orc_dyt_bwd_rows(const void* x, const void* dy, int xt, int64_t M, int64_t N,
+                     double alpha, const double* gamma, const int64_t* rows,
+                     int64_t nrows, double* dx)
+{
+    (void)M;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = row_of(rows, r);
+        for (int64_t j = 0; j < N; ++j) {
+            double xv = widen(x, xt, i * N + j);
+            double g = widen(dy, xt, i * N + j);
+            dx[r * N + j] = g * gamma[j] * alpha * sech2(alpha * xv);
+        }
+    }
+    return 0;
+}
+
+/* Column sums over all M rows, serial in row order.  *_ss receive the sum
+ * of the squared terms (the natural magnitude of a sum of random terms). */
+int orc_dyt_bwd_cols(const void* x, const void* dy, int xt, int64_t M, int64_t N,
+                     double alpha, const double* gamma, double* dgamma, double* dgamma_ss,
+                     double* dbeta, double* dbeta_ss, double* dalpha, double* dalpha_ss)
+{
+    double da = 0.0, da_ss = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        dgamma[j] = dgamma_ss[j] = dbeta[j] = dbeta_ss[j] = 0.0;
+    }
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double xv = widen(x, xt, i * N + j);
+            double g = widen(dy, xt, i * N + j);
+            double z = alpha * xv;
+            double tg = g * tanh(z);
+            double ta = g * gamma[j] * xv * sech2(z);
+            dgamma[j] += tg;
+            dgamma_ss[j] += tg * tg;
+            dbeta[j] += g;
+            dbeta_ss[j] += g * g;
+            da += ta;
+            da_ss += ta * ta;
+        }
+    }
+    *dalpha = da;
+    *dalpha_ss = da_ss;
+    return 0;
+}
+
+/* ============================================================ LayerNorm
+ * Standard LayerNorm over the last dimension with the biased variance and
+ * eps inside the square root:
+ *   mu_i = (1/N) sum_j x_ij,  var_i = (1/N) sum_j (x_ij - mu_i)^2,
+ *   r_i = 1 / sqrt(var_i + eps),  xhat = (x - mu) r,
+ *   y = xhat * gamma_j + beta_j  (gamma absent = 1, beta absent = 0).
+ * The backward takes the saved per-row mean and rstd as inputs (the
+ * torch-xpu-ops page "Layernorm bwd OPT #1880" describes a backward fed
+ * with the forward's statistics):
+ *   g = dy * gamma,  dx = r (g - mean_j g - xhat mean_j(g xhat)),
+ *   dgamma_j = sum_i dy xhat,  dbeta_j = sum_i dy.
+ */
+
+int orc_ln_fwd_rows(const void* x, int xt, int64_t M, int64_t N, double eps,
+                    const double* gamma, const double* beta, const int64_t* rows,
+                    int64_t nrows, double* y, double* y_scale, double* mean, double* rstd)
+{
+    (void)M;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = row_of(rows, r);
+        double s = 0.0;
+        for (int64_t j = 0; j < N; ++j) s += widen(x, xt, i * N + j);
+        double mu = s / (double)N;
+        double ss = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double d = widen(x, xt, i * N + j) - mu;
+            ss += d * d;
+        }
+        double var = ss / (double)N;
+        double rs = 1.0 / sqrt(var + eps);
+        if (mean) mean[r] = mu;
+        if (rstd) rstd[r] = rs;
+        for (int64_t j = 0; j < N; ++j) {
+            double xh = (widen(x, xt, i * N + j) - mu) * rs;
+            double g = gamma ? gamma[j] : 1.0;
+            double b = beta ? beta[j] : 0.0;
+            y[r * N + j] = xh * g + b;
+            if (y_scale) y_scale[r * N + j] = fabs(xh * g) + fabs(b);
+        }
+    }
+    return 0;
+}
+
+int orc_ln_bwd_rows(const void* x, const void* dy, int xt, int64_t M, int64_t N,
+                    const double* mean, const double* rstd, const double* gamma,
+                    const int64_t* rows, int64_t nrows, double* dx, double* dx_scale)
+{
+    (void)M;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = row_of(rows, r);
+        double mu = mean[i], rs = rstd[i];
+        double sg = 0.0, sgx = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double xh = (widen(x, xt, i * N + j) - mu) * rs;
+            double g = widen(dy, xt, i * N + j) * (gamma ? gamma[j] : 1.0);
+            sg += g;
+            sgx += g * xh;
+        }
+        double a = sg / (double)N;
+        double b = sgx / (double)N;
+        for (int64_t j = 0; j < N; ++j) {
+            double xh = (widen(x, xt, i * N + j) - mu) * rs;
+            double g = widen(dy, xt, i * N + j) * (gamma ? gamma[j] : 1.0);
+            dx[r * N + j] = rs * (g - a - xh * b);
+            if (dx_scale) dx_scale[r * N + j] = fabs(rs) * (fabs(g) + fabs(a) + fabs(xh * b));
+        }
+    }
+    return 0;
+}
+
+int orc_ln_bwd_cols(const void* x, const void* dy, int xt, int64_t M, int64_t N,
+                    const double* mean, const double* rstd, double* dgamma,
+                    double* dgamma_ss, double* dbeta, double* dbeta_ss)
+{
+    for (int64_t j = 0; j < N; ++j) dgamma[j] = dgamma_ss[j] = dbeta[j] = dbeta_ss[j] = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double xh = (widen(x, xt, i * N + j) - mean[i]) * rstd[i];
+            double g = widen(dy, xt, i * N + j);
+            dgamma[j] += g * xh;
+            dgamma_ss[j] += (g * xh) * (g * xh);
+            dbeta[j] += g;
+            dbeta_ss[j] += g * g;
+        }
+    }
+    return 0;
+}
+
+/* ============================================================== RMSNorm
+ * Llama-style RMSNorm, weight * (x.float() * rsqrt(mean(x.float()^2) + eps))
+ * .to(x.dtype), with the rounding points of the fused-RMSNorm page
+ * (DeepSpeed PR 8645 quoted in PR 8664, section "Semantics"):
+ *   r = 1 / sqrt(mean_j x^2 + eps)           (float64 here)
+ *   n = round_x(x r)                          (one rounding of the normalized value)
+ *   y = w * n                                 (final rounding by the caller)
+ * Backward, rounding where eager autograd rounds:
+ *   xhat = x r (unrounded),  dn = round_x(dy w),
+ *   dx   = r (dn - xhat mean_j(dn xhat))      (final rounding by the caller)
+ *   dw_j = sum_i term,  term = round_x(dy n) when the weight has the
+ *          activation dtype, and dy n unrounded when the weight is float32.
+ * r is always recomputed from x: the saved rstd is an optional cache of the
+ * GPU path, not part of the definition.  At width one the input derivative
+ * is dn eps / (x^2 + eps)^(3/2) (the PR 8664 page, "Numerics").
+ * amb[] flags elements whose value passed through a bfloat16 rounding
+ * point within NEAR_TIE_REL of a midpoint (parity mode only).
+ */
+
+static double rms_r(const void* x, int xt, int64_t i, int64_t N, double eps)
+{
+    double s = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        double v = widen(x, xt, i * N + j);
+        s += v * v;
+    }
+    return 1.0 / sqrt(s / (double)N + eps);
+}
+
+int orc_rms_fwd_rows(const void* x, int xt, int64_t M, int64_t N, double eps,
+                     const double* w, int mode, const int64_t* rows, int64_t nrows,
+                     double* y, double* y_scale, double* rstd, unsigned char* amb)
+{
+    (void)M;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = row_of(rows, r);
+        double rs = rms_r(x, xt, i, N, eps);
+        if (rstd) rstd[r] = rs;
+        for (int64_t j = 0; j < N; ++j) {
+            double v = widen(x, xt, i * N + j) * rs;
+            int tie = 0;
+            if (mode == ORC_PARITY) v = round_to(v, xt, &tie);
+            y[r * N + j] = w[j] * v;
+            if (y_scale) y_scale[r * N + j] = fabs(w[j] * v);
+            if (amb) amb[r * N + j] = (unsigned char)tie;
+        }
+    }
+    return 0;
+}
+
+int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int64_t M, int64_t N,
+                     double eps, const double* w, int mode, const int64_t* rows,
+                     int64_t nrows, double* dx, double* dx_scale, unsigned char* amb)
+{
+    (void)M;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = row_of(rows, r);
+        double rs = rms_r(x, xt, i, N, eps);
+        double s = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double xh = widen(x, xt, i * N + j) * rs;
+            double dn = widen(dy, xt, i * N + j) * w[j];
+            if (mode == ORC_PARITY) dn = round_to(dn, xt, NULL);
+            s += dn * xh;
+        }
+        double b = s / (double)N;
+        for (int64_t j = 0; j < N; ++j) {
+            double xh = widen(x, xt, i * N + j) * rs;
+            double dn = widen(dy, xt, i * N + j) * w[j];
+            int tie = 0;
+            if (mode == ORC_PARITY) dn = round_to(dn, xt, &tie);
+            dx[r * N + j] = rs * (dn - xh * b);
+            if (dx_scale) dx_scale[r * N + j] = fabs(rs) * (fabs(dn) + fabs(xh * b));
+            if (amb) amb[r * N + j] = (unsigned char)tie;
+        }
+    }
+    return 0;
+}
+
+/* wt: dtype of the weight (ORC_F32 or ORC_BF16); it selects whether each
+ * dw term is rounded to the activation dtype before the sum. */
+int orc_rms_bwd_cols(const void* x, const void* dy, int xt, int wt, int64_t M, int64_t N,
+                     double eps, int mode, double* dw, double* dw_ss)
+{
+    for (int64_t j = 0; j < N; ++j) dw[j] = dw_ss[j] = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        double rs = rms_r(x, xt, i, N, eps);
+        for (int64_t j = 0; j < N; ++j) {
+            double n = widen(x, xt, i * N + j) * rs;
+            if (mode == ORC_PARITY) n = round_to(n, xt, NULL);
+            double term = widen(dy, xt, i * N + j) * n;
+            if (mode == ORC_PARITY && wt != ORC_F32) term = round_to(term, xt, NULL);
+            dw[j] += term;
+            dw_ss[j] += term * term;
+        }
+    }
+    return 0;
+}

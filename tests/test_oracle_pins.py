@@ -1,0 +1,421 @@
+"""Pins of the float64 oracle to facts outside itself.
+
+Each check ties an oracle function to a closed form, an invariant, a
+brute-force enumeration or a central finite difference, chosen so that a
+plausible slip (a dropped term, a wrong sign, a wrong index, a transposed
+operand) fails at least one of them.  No GPU is involved.
+"""
+import math
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from _golden import kv
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+@pytest.fixture(scope="module")
+def O(oracle_lib):
+    return oracle_lib
+
+
+# ------------------------------------------------------------ bf16 rounding
+
+def _bf16_table():
+    """All finite non-negative bfloat16 values, ascending, by enumeration."""
+    vals = []
+    for bits in range(0, 0x7F80):  # 0x7F80 is +inf
+        vals.append((struct.unpack(">f", struct.pack(">I", bits << 16))[0], bits))
+    return vals
+
+
+def _brute_round(v, table):
+    """Nearest bfloat16 to v by exact comparison; ties go to the even pattern."""
+    if v == 0.0:
+        return v
+    a = abs(v)
+    fa = Fraction(a)
+    maxv, maxbits = table[-1]
+    # Overflow: beyond max + half spacing (the tie goes to the even pattern,
+    # i.e. to 2^128, which is infinity).
+    half_gap = (Fraction(2) ** 128 - Fraction(maxv)) / 2
+    if fa >= Fraction(maxv) + half_gap:
+        return math.copysign(math.inf, v)
+    lo, hi = 0, len(table) - 1
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if Fraction(table[mid][0]) <= fa:
+            lo = mid
+        else:
+            hi = mid
+    cands = [table[lo]] if lo == hi else [table[lo], table[hi]]
+    best = min(cands, key=lambda c: (abs(Fraction(c[0]) - fa), c[1] & 1))
+    return math.copysign(best[0], v)
+
+
+def test_bf16_rounding_matches_brute_force(O):
+    table = _bf16_table()
+    rng = np.random.default_rng(7)
+    vals = []
+    # random magnitudes across the whole bfloat16 range, incl. subnormals
+    for e in range(-140, 129, 3):
+        vals += list(rng.uniform(0.5, 1.0, 4) * 2.0 ** e)
+    # exact midpoints and their neighbours, in several binades
+    for bits in list(range(0x3F80, 0x3F90)) + [0x0001, 0x0002, 0x0080, 0x7F7E, 0x7F7F, 0x0C35]:
+        lo = struct.unpack(">f", struct.pack(">I", bits << 16))[0]
+        hi = struct.unpack(">f", struct.pack(">I", (bits + 1) << 16))[0]
+        if math.isinf(hi):
+            hi = 2.0 ** 128  # the spacing continues past the largest finite value
+        midv = (lo + hi) / 2  # exact in float64
+        vals += [midv, math.nextafter(midv, 0), math.nextafter(midv, math.inf)]
+        # a value that float32 would round onto the midpoint first (double rounding)
+        vals.append(midv + (hi - lo) * 2.0 ** -20)
+    vals += [2.0 ** -134, 2.0 ** -135, 3 * 2.0 ** -135, 1e-300, 3.5e38, 3.4e38, 1e39]
+    vals += [-v for v in vals[::5]]
+    for v in vals:
+        want = _brute_round(v, table)
+        got = O.round_bf16(v)
+        assert got == want or (math.isinf(want) and math.isinf(got) and (got > 0) == (want > 0)), \
+            (v, got, want)
+    assert math.isnan(O.round_bf16(math.nan))
+
+
+def test_bf16_array_matches_scalar(O):
+    v = np.random.default_rng(3).standard_normal(1000) * 10
+    a = O.round_bf16_array(v)
+    assert all(a[i] == O.round_bf16(v[i]) for i in range(v.size))
+
+
+def test_near_tie_flag(O):
+    mid = 1.0 + 2.0 ** -8  # midpoint between 1 and 1 + 2^-7
+    assert O.bf16_near_tie(mid)
+    assert O.bf16_near_tie(mid * (1 + 2.0 ** -20))
+    assert not O.bf16_near_tie(1.0)
+    assert not O.bf16_near_tie(1.0 + 2.0 ** -9)
+
+
+# ------------------------------------------------------------------- DyT
+
+def _L_dyt(O, x, dy, alpha, g, b):
+    y, _ = O.dyt_fwd(x, alpha, g, b)
+    return float(np.sum(dy * y))
+
+
+def test_dyt_fwd_closed_form_tanh_of_log(O):
+    # tanh(ln a) = (a^2 - 1) / (a^2 + 1)
+    a = np.array([1.5, 2.0, 3.0, 7.0, 1.0 / 3.0])
+    x = np.log(a)[None, :]
+    y, _ = O.dyt_fwd(x, 1.0, np.ones(5), np.zeros(5))
+    np.testing.assert_allclose(y[0], (a * a - 1) / (a * a + 1), rtol=4e-16, atol=0)
+    # alpha and x enter only through their product; gamma scales, beta shifts
+    y2, _ = O.dyt_fwd(x / 4.0, 4.0, 3.0 * np.ones(5), 0.5 * np.ones(5))
+    np.testing.assert_allclose(y2[0], 3.0 * (a * a - 1) / (a * a + 1) + 0.5, rtol=4e-16)
+
+
+def test_dyt_fwd_limits(O):
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((3, 6))
+    g = rng.standard_normal(6); b = rng.standard_normal(6)
+    # alpha -> +inf: gamma * sign(x) + beta
+    y, _ = O.dyt_fwd(x, math.inf, g, b)
+    np.testing.assert_array_equal(y, g * np.sign(x) + b)
+    # alpha -> 0: beta + gamma alpha x to first order
+    al = 1e-7
+    y, _ = O.dyt_fwd(x, al, g, b)
+    np.testing.assert_allclose(y, b + g * al * x, rtol=0, atol=1e-19 + 1e-15 * np.abs(b).max())
+    # tanh is odd
+    y1, _ = O.dyt_fwd(x, 0.7, np.ones(6), np.zeros(6))
+    y2, _ = O.dyt_fwd(-x, 0.7, np.ones(6), np.zeros(6))
+    np.testing.assert_array_equal(y1, -y2)
+
+
+def test_dyt_bwd_finite_differences(O):
+    rng = np.random.default_rng(1)
+    M, N = 4, 7
+    x = rng.standard_normal((M, N)); dy = rng.standard_normal((M, N))
+    g = 1 + 0.3 * rng.standard_normal(N); b = rng.standard_normal(N)
+    al = 0.8
+    dx = O.dyt_bwd_rows(x, dy, al, g)
+    c = O.dyt_bwd_cols(x, dy, al, g)
+
+    def fd(f, v):
+        h = 1e-6 * max(1.0, abs(v))
+        return (f(v + h) - f(v - h)) / (2 * h)
+
+    for i in range(M):
+        for j in range(N):
+            def f(v, i=i, j=j):
+                xx = x.copy(); xx[i, j] = v
+                return _L_dyt(O, xx, dy, al, g, b)
+            assert abs(fd(f, x[i, j]) - dx[i, j]) <= 1e-7 * max(1, abs(dx[i, j]))
+    for j in range(N):
+        def fg(v, j=j):
+            gg = g.copy(); gg[j] = v
+            return _L_dyt(O, x, dy, al, gg, b)
+
+        def fb(v, j=j):
+            bb = b.copy(); bb[j] = v
+            return _L_dyt(O, x, dy, al, g, bb)
+        assert abs(fd(fg, g[j]) - c["dgamma"][j]) <= 1e-7 * max(1, abs(c["dgamma"][j]))
+        assert abs(fd(fb, b[j]) - c["dbeta"][j]) <= 1e-7 * max(1, abs(c["dbeta"][j]))
+    fa = fd(lambda v: _L_dyt(O, x, dy, v, g, b), al)
+    assert abs(fa - c["dalpha"]) <= 1e-7 * max(1, abs(c["dalpha"]))
+
+
+def test_dyt_dbeta_is_column_sum_and_sumsq(O):
+    rng = np.random.default_rng(2)
+    # values on a 1/8 grid: every float64 sum is exact in any order
+    dy = rng.integers(-64, 64, (50, 9)) / 8.0
+    x = rng.standard_normal((50, 9))
+    c = O.dyt_bwd_cols(x, dy, 0.5, np.ones(9))
+    np.testing.assert_array_equal(c["dbeta"], dy.sum(axis=0))
+    np.testing.assert_array_equal(c["dbeta_ss"], (dy * dy).sum(axis=0))
+
+
+def test_dyt_sech2_identity(O):
+    rng = np.random.default_rng(4)
+    x = rng.uniform(-2, 2, (3, 5)); dy = np.ones((3, 5))
+    dx = O.dyt_bwd_rows(x, dy, 1.3, np.ones(5))
+    t = np.tanh(1.3 * x)
+    np.testing.assert_allclose(dx, 1.3 * (1 - t * t), rtol=1e-13)
+
+
+def test_dyt_alpha_inf_and_padding_rows(O):
+    rng = np.random.default_rng(5)
+    M, N = 6, 8
+    x = rng.standard_normal((M, N)); dy = rng.standard_normal((M, N))
+    g = 1 + 0.1 * rng.standard_normal(N)
+    c = O.dyt_bwd_cols(x, dy, math.inf, g)
+    assert np.all(np.isfinite(c["dgamma"])) and np.all(np.isfinite(c["dbeta"]))
+    assert c["dalpha"] == 0.0
+    np.testing.assert_allclose(c["dgamma"], (dy * np.sign(x)).sum(axis=0), rtol=1e-15)
+    dx = O.dyt_bwd_rows(x, dy, math.inf, g)
+    assert np.all(np.isnan(dx))  # dy * gamma * inf * 0 under IEEE rules
+    # rows with dy = 0 appended: no parameter gradient changes
+    xp = np.vstack([x, rng.standard_normal((3, N))]); dyp = np.vstack([dy, np.zeros((3, N))])
+    for al in (0.6, math.inf):
+        c0 = O.dyt_bwd_cols(x, dy, al, g)
+        c1 = O.dyt_bwd_cols(xp, dyp, al, g)
+        for k in ("dgamma", "dbeta"):
+            np.testing.assert_array_equal(c0[k], c1[k])
+        assert c0["dalpha"] == c1["dalpha"]
+
+
+def test_dyt_rows_subset_and_dtypes(O):
+    rng = np.random.default_rng(6)
+    x32 = rng.standard_normal((5, 4)).astype(np.float32)
+    g = rng.standard_normal(4); b = rng.standard_normal(4)
+    full, _ = O.dyt_fwd(x32, 0.9, g, b)
+    sub, _ = O.dyt_fwd(x32, 0.9, g, b, rows=[3, 1])
+    np.testing.assert_array_equal(sub, full[[3, 1]])
+    # bf16 bit patterns widen exactly: compare against the float32 path
+    bf = (x32.view(np.uint32) >> 16).astype(np.uint16)
+    as32 = (bf.astype(np.uint32) << 16).view(np.float32)
+    np.testing.assert_array_equal(O.dyt_fwd(bf, 0.9, g, b)[0], O.dyt_fwd(as32, 0.9, g, b)[0])
+
+
+# -------------------------------------------------------------- LayerNorm
+
+def test_ln_fwd_invariants(O):
+    rng = np.random.default_rng(10)
+    M, N = 5, 33
+    x = 3 + 2 * rng.standard_normal((M, N))
+    eps = 1e-3
+    y, _, mu, rs = O.ln_fwd(x, eps)
+    np.testing.assert_allclose(y.mean(axis=1), 0, atol=1e-14)
+    var = ((x - x.mean(axis=1, keepdims=True)) ** 2).mean(axis=1)
+    np.testing.assert_allclose((y * y).mean(axis=1), var / (var + eps), rtol=1e-13)
+    # shift invariance, and scale invariance at eps = 0
+    y2, *_ = O.ln_fwd(x + 17.0, eps)
+    np.testing.assert_allclose(y2, y, atol=1e-12)
+    ya, *_ = O.ln_fwd(x, 0.0)
+    yb, *_ = O.ln_fwd(2.5 * x, 0.0)
+    np.testing.assert_allclose(ya, yb, atol=1e-13)
+    # affine applied per column
+    g = rng.standard_normal(N); b = rng.standard_normal(N)
+    y3, *_ = O.ln_fwd(x, eps, g, b)
+    np.testing.assert_allclose(y3, y * g + b, atol=1e-13)
+
+
+def test_ln_fwd_degenerate(O):
+    b = np.array([0.25])
+    y, _, mu, rs = O.ln_fwd(np.array([[3.0], [-2.0]]), 1e-5, np.array([2.0]), b)
+    np.testing.assert_array_equal(y, [[0.25], [0.25]])  # width one: y = beta
+    y, *_ = O.ln_fwd(np.full((1, 6), 4.0), 1e-5, np.ones(6), np.arange(6.0))
+    np.testing.assert_array_equal(y[0], np.arange(6.0))  # constant row: y = beta
+
+
+def _L_ln(O, x, dy, eps, g, b):
+    y, *_ = O.ln_fwd(x, eps, g, b)
+    return float(np.sum(dy * y))
+
+
+def test_ln_bwd_invariants_and_closed_form(O):
+    rng = np.random.default_rng(11)
+    M, N = 4, 19
+    x = rng.standard_normal((M, N)); dy = rng.standard_normal((M, N))
+    g = 1 + 0.2 * rng.standard_normal(N); eps = 0.05
+    _, _, mu, rs = O.ln_fwd(x, eps, g)
+    dx, _ = O.ln_bwd_rows(x, dy, mu, rs, g)
+    np.testing.assert_allclose(dx.sum(axis=1), 0, atol=1e-13)
+    xh = (x - mu[:, None]) * rs[:, None]
+    gg = dy * g
+    m = (gg * xh).mean(axis=1)
+    var = ((x - mu[:, None]) ** 2).mean(axis=1)
+    want = rs * N * m * eps / (var + eps)
+    np.testing.assert_allclose((dx * xh).sum(axis=1), want, rtol=1e-11, atol=1e-13)
+    # width one: dx = 0
+    x1 = rng.standard_normal((3, 1)); _, _, m1, r1 = O.ln_fwd(x1, eps)
+    d1, _ = O.ln_bwd_rows(x1, rng.standard_normal((3, 1)), m1, r1)
+    np.testing.assert_array_equal(d1, 0.0)
+
+
+def test_ln_bwd_finite_differences(O):
+    rng = np.random.default_rng(12)
+    M, N = 3, 6
+    x = rng.standard_normal((M, N)); dy = rng.standard_normal((M, N))
+    g = 1 + 0.3 * rng.standard_normal(N); b = rng.standard_normal(N); eps = 0.1
+    _, _, mu, rs = O.ln_fwd(x, eps, g, b)
+    dx, _ = O.ln_bwd_rows(x, dy, mu, rs, g)
+    c = O.ln_bwd_cols(x, dy, mu, rs)
+
+    def fd(f, v):
+        h = 1e-6 * max(1.0, abs(v))
+        return (f(v + h) - f(v - h)) / (2 * h)
+
+    for i in range(M):
+        for j in range(N):
+            def f(v, i=i, j=j):
+                xx = x.copy(); xx[i, j] = v
+                return _L_ln(O, xx, dy, eps, g, b)
+            assert abs(fd(f, x[i, j]) - dx[i, j]) <= 1e-7 * max(1, abs(dx[i, j]))
+    for j in range(N):
+        def fg(v, j=j):
+            gg = g.copy(); gg[j] = v
+            return _L_ln(O, x, dy, eps, gg, b)
+
+        def fb(v, j=j):
+            bb = b.copy(); bb[j] = v
+            return _L_ln(O, x, dy, eps, g, bb)
+        assert abs(fd(fg, g[j]) - c["dgamma"][j]) <= 1e-7 * max(1, abs(c["dgamma"][j]))
+        assert abs(fd(fb, b[j]) - c["dbeta"][j]) <= 1e-7 * max(1, abs(c["dbeta"][j]))
+
+
+def test_ln_dbeta_and_padding(O):
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((20, 5)); dy = rng.integers(-40, 40, (20, 5)) / 4.0
+    _, _, mu, rs = O.ln_fwd(x, 1e-5)
+    c = O.ln_bwd_cols(x, dy, mu, rs)
+    np.testing.assert_array_equal(c["dbeta"], dy.sum(axis=0))
+    xp = np.vstack([x, rng.standard_normal((2, 5))]); dyp = np.vstack([dy, np.zeros((2, 5))])
+    _, _, mup, rsp = O.ln_fwd(xp, 1e-5)
+    cp = O.ln_bwd_cols(xp, dyp, mup, rsp)
+    np.testing.assert_array_equal(c["dgamma"], cp["dgamma"])
+    np.testing.assert_array_equal(c["dbeta"], cp["dbeta"])
+
+
+# ---------------------------------------------------------------- RMSNorm
+
+def test_rms_fwd_invariants(O):
+    rng = np.random.default_rng(20)
+    x = rng.standard_normal((4, 23)); w = 1 + 0.1 * rng.standard_normal(23)
+    ya, *_ = O.rms_fwd(x, 0.0, w, O.MATH)
+    yb, *_ = O.rms_fwd(3.7 * x, 0.0, w, O.MATH)
+    np.testing.assert_allclose(ya, yb, rtol=1e-14)
+    eps = 0.3
+    y, _, rs, _ = O.rms_fwd(x, eps, np.ones(23), O.MATH)
+    ms = (x * x).mean(axis=1)
+    np.testing.assert_allclose((y * y).mean(axis=1), ms / (ms + eps), rtol=1e-13)
+    np.testing.assert_allclose(rs, 1 / np.sqrt(ms + eps), rtol=1e-15)
+    yw, *_ = O.rms_fwd(x, eps, w, O.MATH)
+    np.testing.assert_allclose(yw, y * w, rtol=1e-15)
+
+
+def test_rms_width_one(O):
+    eps = kv("rmsnorm_width_one.txt")["eps"]
+    x = np.array([[-2.0], [-0.3], [0.1], [0.5], [1.7]])
+    w = np.array([1.25])
+    y, *_ = O.rms_fwd(x, eps, w, O.MATH)
+    np.testing.assert_allclose(y[:, 0], w[0] * x[:, 0] / np.sqrt(x[:, 0] ** 2 + eps), rtol=1e-15)
+    dy = np.array([[0.7], [-1.1], [2.0], [1.0], [-0.4]])
+    dx, *_ = O.rms_bwd_rows(x, dy, eps, w, O.MATH)
+    dn = dy[:, 0] * w[0]
+    want = dn * eps / (x[:, 0] ** 2 + eps) ** 1.5  # the page's closed form
+    np.testing.assert_allclose(dx[:, 0], want, rtol=1e-14)
+
+
+def test_rms_bwd_closed_form_and_fd(O):
+    rng = np.random.default_rng(21)
+    M, N = 3, 7
+    x = rng.standard_normal((M, N)); dy = rng.standard_normal((M, N))
+    w = 1 + 0.2 * rng.standard_normal(N); eps = 0.2
+    dx, *_ = O.rms_bwd_rows(x, dy, eps, w, O.MATH)
+    ms = (x * x).mean(axis=1); r = 1 / np.sqrt(ms + eps)
+    dn = dy * w
+    lhs = (dx * x).sum(axis=1)
+    rhs = eps * r * r * (dn * x * r[:, None]).sum(axis=1)
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-12, atol=1e-14)
+    dw, _ = O.rms_bwd_cols(x, dy, eps, O.F32, O.MATH)
+
+    def L(xx, ww):
+        y, *_ = O.rms_fwd(xx, eps, ww, O.MATH)
+        return float(np.sum(dy * y))
+
+    def fd(f, v):
+        h = 1e-6 * max(1.0, abs(v))
+        return (f(v + h) - f(v - h)) / (2 * h)
+
+    for i in range(M):
+        for j in range(N):
+            def f(v, i=i, j=j):
+                xx = x.copy(); xx[i, j] = v
+                return L(xx, w)
+            assert abs(fd(f, x[i, j]) - dx[i, j]) <= 1e-7 * max(1, abs(dx[i, j]))
+    for j in range(N):
+        def fw(v, j=j):
+            ww = w.copy(); ww[j] = v
+            return L(x, ww)
+        assert abs(fd(fw, w[j]) - dw[j]) <= 1e-7 * max(1, abs(dw[j]))
+
+
+def test_rms_parity_rounding_points(O):
+    rng = np.random.default_rng(22)
+    x32 = rng.standard_normal((6, 16)).astype(np.float32)
+    bf = (x32.view(np.uint32) >> 16).astype(np.uint16)
+    xw = (bf.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    eps = 1e-6
+    # parity mode with unit weight: y is the normalized value rounded to bf16
+    y, _, rs, amb = O.rms_fwd(bf, eps, np.ones(16), O.PARITY)
+    ym, *_ = O.rms_fwd(bf, eps, np.ones(16), O.MATH)
+    np.testing.assert_array_equal(y, O.round_bf16_array(ym))
+    assert not np.array_equal(y, ym)
+    # float64 activations: parity mode has no rounding points
+    y64, *_ = O.rms_fwd(xw, eps, np.ones(16), O.PARITY)
+    np.testing.assert_array_equal(y64, ym)
+    # dw: with a bf16 weight each term dy*n is rounded; with unit dy the term
+    # is n itself, already a bf16 value, so both weight dtypes agree
+    ones = np.full_like(bf, 0x3F80)  # bf16 1.0
+    d_b, _ = O.rms_bwd_cols(bf, ones, eps, O.BF16, O.PARITY)
+    d_f, _ = O.rms_bwd_cols(bf, ones, eps, O.F32, O.PARITY)
+    np.testing.assert_array_equal(d_b, d_f)
+    np.testing.assert_allclose(d_b, y.sum(axis=0), rtol=1e-15)
+    # a dy with a 3-bit significand times n (8 bits) needs 11 bits: the bf16
+    # weight path rounds each term, the float32 weight path does not
+    three = np.full_like(bf, 0x3FE0)  # bf16 1.75
+    t_b, _ = O.rms_bwd_cols(bf, three, eps, O.BF16, O.PARITY)
+    t_f, _ = O.rms_bwd_cols(bf, three, eps, O.F32, O.PARITY)
+    np.testing.assert_allclose(t_f, 1.75 * y.sum(axis=0), rtol=1e-15)
+    np.testing.assert_allclose(t_b, O.round_bf16_array(1.75 * y).sum(axis=0), rtol=1e-15)
+    assert not np.array_equal(t_b, t_f)
+
+
+def test_rms_padding_rows(O):
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((9, 6)); dy = rng.standard_normal((9, 6))
+    xp = np.vstack([x, rng.standard_normal((4, 6))]); dyp = np.vstack([dy, np.zeros((4, 6))])
+    a, _ = O.rms_bwd_cols(x, dy, 1e-6, O.F32, O.MATH)
+    b, _ = O.rms_bwd_cols(xp, dyp, 1e-6, O.F32, O.MATH)
+    np.testing.assert_array_equal(a, b)

@@ -1,0 +1,558 @@
+"""Benchmark of the row-normalization hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload sweep|dyt_f32_4096x64|layernorm_bwd_401408x24|
+                                dyt_bf16_1048576x128|rmsnorm_bf16_16384x2048]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+for the default "sweep" workload, DyT, LayerNorm and RMSNorm forward +
+backward (each backward including its parameter-gradient column reduction)
+at N in {16, 24, 64, 128, 256, 512, 1024, 2048, 4096, 8192} with
+M = 2^28 // N rows, bf16 activations and fp32 parameters.  Every tensor is
+larger than L2, and every (layer, width) point has its own inputs.
+
+The metric is achieved HBM bandwidth: algorithmic bytes (what the layer
+must read and write) divided by device time.  One JSON line is printed by
+rank 0.  Under torchrun (N > 1) every rank runs an independent replica on
+its own GPU (no data-path collective); `value` sums all ranks' bytes over
+the slowest rank's time.
+
+`--impl reference` times the float64 CPU oracle (the correctness
+reference) on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "fwd+bwd achieved HBM GB/s and % of GB300 8 TB/s roofline, per op and [M,N]"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash():
+    """Hash of the kernel sources (ncu counters are valid only for this hash)."""
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "normalization_layers_fwd_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_hash") != source_hash():
+        return None
+    return rec.get("launches", {}).get(kernel_key)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gbn_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}", "--format=csv,noheader",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def mhz(s):
+            try:
+                return float(s.split()[0])
+            except (ValueError, IndexError):
+                return None
+        sm = [mhz(r[1]) for r in rows if mhz(r[1])]
+        mx = max((mhz(r[2]) or 0) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ workloads
+
+def alg_bytes(op, direction, M, N, sx, sp):
+    """Bytes the layer must move (activations, parameters, saved statistics)."""
+    E = M * N
+    if op == "dyt":
+        return 2 * E * sx + (2 * N + 1) * sp if direction == "fwd" else \
+            3 * E * sx + (N + 1) * sp + (2 * N + 1) * sp
+    if op == "layernorm":
+        return 2 * E * sx + 8 * M + 2 * N * sp if direction == "fwd" else \
+            3 * E * sx + 8 * M + N * sp + 2 * N * sp
+    return 2 * E * sx + 4 * M + N * sp if direction == "fwd" else \
+        3 * E * sx + 4 * M + N * sp + N * sp
+
+
+class Point:
+    """One (layer, shape) of a workload with its device buffers and the C-ABI
+    argument tuples of its forward and backward calls."""
+
+    def __init__(self, lib, wl, dev, shared, fwd=True):
+        from normalization_layers_fwd_gb300 import _lib
+        self.wl, self.lib, self.fwd_enabled = wl, lib, fwd and not wl.bwd_only
+        M, N = wl.M, wl.N
+        inp = wl.inputs(device=dev)
+        self.inp = inp
+        self.x, self.dy = inp["x"], inp["dy"]
+        E = M * N
+        self.y = shared["y"][:E].view(M, N)
+        self.dx = shared["dx"][:E].view(M, N)
+        self.mean = shared["mean"][:M]
+        self.rstd = shared["rstd"][:M]
+        xt = _lib._code(self.x)
+        p = inp.get("gamma", inp.get("weight"))
+        pt = _lib._code(p)
+        self.sx, self.sp = self.x.element_size(), p.element_size()
+        self.g1 = torch.empty(N, dtype=p.dtype, device=dev)
+        self.g2 = torch.empty(N, dtype=p.dtype, device=dev)
+        self.g3 = torch.empty(1, dtype=p.dtype, device=dev)
+        opcode = {"dyt": 0, "layernorm": 1, "rmsnorm": 2}[wl.op]
+        nws = lib.gbn_bwd_workspace_bytes(opcode, M, N, xt, pt, dev.index)
+        self.ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+        s = torch.cuda.current_stream(dev).cuda_stream
+        P = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        X, DY, Y, DX = P(self.x), P(self.dy), P(self.y), P(self.dx)
+        if wl.op == "dyt":
+            A, G, B = P(inp["alpha"]), P(inp["gamma"]), P(inp["beta"])
+            self.fwd_call = (lib.dyt_fwd, (X, A, G, B, Y, M, N, xt, pt, s))
+            self.bwd_call = (lib.dyt_bwd, (X, DY, A, G, DX, P(self.g3), P(self.g1), P(self.g2), M,
+                                           N, xt, pt, P(self.ws), nws, s))
+        elif wl.op == "layernorm":
+            G, B = P(inp["gamma"]), P(inp["beta"])
+            self.fwd_call = (lib.layernorm_fwd, (X, G, B, Y, P(self.mean), P(self.rstd), M, N,
+                                                 wl.eps, xt, pt, s))
+            self.bwd_call = (lib.layernorm_bwd, (X, DY, P(self.mean), P(self.rstd), G, DX,
+                                                 P(self.g1), P(self.g2), M, N, xt, pt, P(self.ws),
+                                                 nws, s))
+        else:
+            W = P(inp["weight"])
+            self.fwd_call = (lib.rmsnorm_fwd, (X, W, Y, P(self.rstd), M, N, wl.eps, xt, pt, s))
+            self.bwd_call = (lib.rmsnorm_bwd, (X, DY, W, P(self.rstd), DX, P(self.g1), M, N,
+                                               wl.eps, xt, pt, P(self.ws), nws, s))
+        if wl.bwd_only:
+            # saved statistics for the backward-only workload come from one
+            # forward, outside the timed region
+            rc = lib.layernorm_fwd(X, P(inp["gamma"]), P(inp["beta"]), Y, P(self.mean),
+                                   P(self.rstd), M, N, wl.eps, xt, pt, s)
+            assert rc == 0
+        self.bytes = {d: alg_bytes(wl.op, d, M, N, self.sx, self.sp) for d in ("fwd", "bwd")}
+
+    def launches(self):
+        return (2 if self.fwd_enabled else 1) + 1  # fwd, bwd, column-sum stage
+
+    def run(self, which=("fwd", "bwd")):
+        if "fwd" in which and self.fwd_enabled:
+            fn, args = self.fwd_call
+            rc = fn(*args)
+            if rc:
+                raise RuntimeError(f"{self.wl.name} fwd: status {rc}")
+        if "bwd" in which:
+            fn, args = self.bwd_call
+            rc = fn(*args)
+            if rc:
+                raise RuntimeError(f"{self.wl.name} bwd: status {rc}")
+
+    def step_bytes(self):
+        return (self.bytes["fwd"] if self.fwd_enabled else 0) + self.bytes["bwd"]
+
+    def key(self, d):
+        return f"{self.wl.op}_{d}[{self.wl.M}x{self.wl.N}]"
+
+
+def workloads(name):
+    from normalization_layers_fwd_gb300 import synth
+    if name == "sweep":
+        return synth.sweep_all(), ("sweep: DyT, LayerNorm, RMSNorm fwd+bwd, bf16 x, fp32 params, "
+                                   "N in {16..8192}, M = 2^28 // N")
+    table = {w.name: w for w in (synth.DYT_F32_SMALL, synth.LN_BWD_TALL, synth.DYT_BF16_TALL,
+                                 synth.RMS_BF16)}
+    if name not in table:
+        raise SystemExit(f"unknown workload {name}")
+    w = table[name]
+    return [w], w.name
+
+
+# ------------------------------------------------------------------ timing
+
+def time_launches(points, dev, reps=3):
+    """Mean device time of every launch, with CUDA events on the launch stream."""
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for _ in range(reps):
+        evs = []
+        for p in points:
+            for d in ("fwd", "bwd"):
+                if d == "fwd" and not p.fwd_enabled:
+                    continue
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                p.run((d,))
+                b.record(stream)
+                evs.append((p, d, a, b))
+        torch.cuda.synchronize(dev)
+        for p, d, a, b in evs:
+            out.setdefault((p, d), []).append(a.elapsed_time(b))
+    return {k: sum(v) / len(v) for k, v in out.items()}
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def run_ours(args, rank, world, dev):
+    from normalization_layers_fwd_gb300 import _lib, build
+    build.build()
+    lib = _lib.load()
+    wls, wdesc = workloads(args.workload)
+    maxE = max(w.M * w.N for w in wls)
+    maxM = max(w.M for w in wls)
+    dtype = wls[0].xdtype
+    shared = {"y": torch.empty(maxE, dtype=dtype, device=dev),
+              "dx": torch.empty(maxE, dtype=dtype, device=dev),
+              "mean": torch.empty(maxM, dtype=torch.float32, device=dev),
+              "rstd": torch.empty(maxM, dtype=torch.float32, device=dev)}
+    points = [Point(lib, w, dev, shared) for w in wls]
+    torch.cuda.synchronize(dev)
+    per_tensor = min(w.M * w.N * w.xdtype.itemsize for w in wls)
+    big = per_tensor > 2 * L2_BYTES
+    flush = None if big else torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for p in points:
+            p.run()
+
+    for _ in range(max(args.warmup, 3)):
+        if flush is not None:
+            flush_l2(flush)
+        step()
+    torch.cuda.synchronize(dev)
+
+    # dominant launch: the largest mean device time (live events, warm state)
+    lt = time_launches(points, dev)
+    dom_key = max(lt, key=lt.get)
+    dom_point, dom_dir = dom_key
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first readings
+    torch.cuda.synchronize(dev)
+    if big:
+        # inputs larger than L2: K back-to-back steps, one event pair; the
+        # dominant launch is bracketed by its own events inside the region
+        dom_evs = []
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            for p in points:
+                if p is dom_point:
+                    for d in ("fwd", "bwd"):
+                        if d == "fwd" and not p.fwd_enabled:
+                            continue
+                        if d == dom_dir:
+                            a = torch.cuda.Event(enable_timing=True)
+                            b = torch.cuda.Event(enable_timing=True)
+                            a.record(stream)
+                            p.run((d,))
+                            b.record(stream)
+                            dom_evs.append((a, b))
+                        else:
+                            p.run((d,))
+                else:
+                    p.run()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = t0.elapsed_time(t1)
+        dom_ms = sum(a.elapsed_time(b) for a, b in dom_evs) / len(dom_evs)
+    else:
+        # small working set: flush L2 before every step, time each step alone
+        times, dom_t = [], []
+        for _ in range(args.steps):
+            flush_l2(flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b))
+            flush_l2(flush)
+            c, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c.record(stream)
+            dom_point.run((dom_dir,))
+            e.record(stream)
+            torch.cuda.synchronize(dev)
+            dom_t.append(c.elapsed_time(e))
+        total_ms = sum(times)
+        dom_ms = statistics.median(dom_t)
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_step = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    step_bytes = sum(p.step_bytes() for p in points)
+    rows = sum(p.wl.M for p in points)
+    gbs = step_bytes * world / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    dom_bytes = dom_point.bytes[dom_dir]
+    dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
+    dom_name = dom_point.key(dom_dir)
+
+    breakdown = []
+    for (p, d), ms in sorted(lt.items(), key=lambda kv: (kv[0][0].wl.op, kv[0][0].wl.N, kv[0][1])):
+        b = p.bytes[d]
+        breakdown.append({"kernel": p.key(d), "ms": round(ms, 4),
+                          "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                          "frac_measured": round(b / (ms * 1e-3) / 1e9 / peak, 3)})
+
+    e2e = run_e2e(lib, points, dev, shared, min(args.steps, 3), world)
+    line = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if dtype == torch.bfloat16 else "f32", "data": "synthetic (seeded, generated on the GPU)",
+        "config": {"workload": wdesc, "points": len(points), "rows_per_step": rows,
+                   "x_dtype": str(dtype)[6:], "param_dtype": str(wls[0].pdtype)[6:],
+                   "l2": "inputs larger than L2" if big else "L2 flushed (512 MiB write) before every step",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_8tbs": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_copy": round(100 * gbs / world / peak, 2),
+        "rows_per_s": round(rows * world / (ms_step * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(dom_gbs, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(dom_gbs / peak, 4), "alg_bytes": dom_bytes,
+                     "traffic": recorded_traffic(dom_name)},
+        "gpu_launches": sum(p.launches() for p in points) * args.steps,
+        "e2e": e2e,
+        "clocks": clocks,
+        "breakdown": breakdown,
+    }
+    return line
+
+
+def run_e2e(lib, points, dev, shared, steps, world):
+    """The same metric through the C ABI with HOST buffers: every step copies
+    each point's inputs from pinned host memory, runs forward + backward, and
+    reads the outputs and parameter gradients back."""
+    maxE = max(p.wl.M * p.wl.N for p in points)
+    dtype = points[0].x.dtype
+    hx = torch.empty(maxE, dtype=dtype, pin_memory=True)
+    hdy = torch.empty(maxE, dtype=dtype, pin_memory=True)
+    hy = torch.empty(maxE, dtype=dtype, pin_memory=True)
+    hdx = torch.empty(maxE, dtype=dtype, pin_memory=True)
+    # the host inputs are one point's inputs (values do not affect timing)
+    p0 = max(points, key=lambda p: p.wl.M * p.wl.N)
+    hx[: p0.x.numel()].copy_(p0.x.view(-1))
+    hdy[: p0.dy.numel()].copy_(p0.dy.view(-1))
+    stream = torch.cuda.current_stream(dev)
+    h2d = d2h = 0
+    for p in points:
+        E = p.wl.M * p.wl.N
+        h2d += 2 * E * p.sx
+        d2h += (2 if p.fwd_enabled else 1) * E * p.sx + p.g1.numel() * p.sp * 2 + p.sp
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        for p in points:
+            E = p.wl.M * p.wl.N
+            p.x.view(-1).copy_(hx[:E], non_blocking=True)
+            p.dy.view(-1).copy_(hdy[:E], non_blocking=True)
+            p.run()
+            if p.fwd_enabled:
+                hy[:E].copy_(p.y.reshape(-1), non_blocking=True)
+            hdx[:E].copy_(p.dx.reshape(-1), non_blocking=True)
+            p.g1.cpu(), p.g2.cpu(), p.g3.cpu()  # parameter gradients (synchronizing reads)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / steps
+    step_bytes = sum(p.step_bytes() for p in points)
+    return {"value": round(step_bytes * world / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps}
+
+
+# --------------------------------------------------------- CPU (oracle) arm
+
+def oracle_sample(wls, target_elems):
+    """Time the float64 oracle (as it stands, one thread) on the first rows of
+    every point of the workload; returns (bytes, seconds, sample text)."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    per = max(1, target_elems // len(wls))
+    tot_bytes, tot_s, n_elems = 0, 0.0, 0
+    for w in wls:
+        from normalization_layers_fwd_gb300 import synth
+        rows = max(1, min(w.M, per // w.N))
+        sw = synth.scaled(w, rows)
+        inp = sw.inputs(device="cpu")
+
+        def arr(t):
+            if t.dtype == torch.bfloat16:
+                return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+            return t.contiguous().numpy()
+        x, dy = arr(inp["x"]), arr(inp["dy"])
+        t0 = time.perf_counter()
+        if w.op == "dyt":
+            a = float(inp["alpha"].double()[0])
+            g, b = inp["gamma"].double().numpy(), inp["beta"].double().numpy()
+            oracle.dyt_fwd(x, a, g, b)
+            oracle.dyt_bwd_rows(x, dy, a, g)
+            oracle.dyt_bwd_cols(x, dy, a, g)
+        elif w.op == "layernorm":
+            g, b = inp["gamma"].double().numpy(), inp["beta"].double().numpy()
+            _, _, mu, rs = oracle.ln_fwd(x, w.eps, g, b)
+            oracle.ln_bwd_rows(x, dy, mu, rs, g)
+            oracle.ln_bwd_cols(x, dy, mu, rs)
+        else:
+            wt = inp["weight"].double().numpy()
+            code = oracle.BF16 if inp["weight"].dtype == torch.bfloat16 else oracle.F32
+            oracle.rms_fwd(x, w.eps, wt)
+            oracle.rms_bwd_rows(x, dy, w.eps, wt, code)
+            oracle.rms_bwd_cols(x, dy, w.eps, code)
+        tot_s += time.perf_counter() - t0
+        sx, sp = inp["x"].element_size(), 4
+        tot_bytes += (0 if w.bwd_only else alg_bytes(w.op, "fwd", rows, w.N, sx, sp)) + \
+            alg_bytes(w.op, "bwd", rows, w.N, sx, sp)
+        n_elems += rows * w.N
+    desc = f"first rows of each of the {len(wls)} points, {n_elems} elements in total, fwd+bwd"
+    return tot_bytes, tot_s, desc
+
+
+def run_reference(args, rank, world):
+    wls, wdesc = workloads(args.workload)
+    target = args.ref_elems
+    vals = []
+    for i in range(args.warmup + args.steps):
+        b, s, desc = oracle_sample(wls, target)
+        if i >= args.warmup:
+            vals.append((b, s))
+    bytes_ = sum(v[0] for v in vals)
+    secs = sum(v[1] for v in vals)
+    gbs = bytes_ / secs / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, CPU)",
+        "config": {"workload": wdesc, "note": "float64 CPU oracle on a bounded sample per step"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="sweep")
+    ap.add_argument("--ref-elems", type=int, default=1 << 22,
+                    help="elements per step of the CPU oracle sample")
+    ap.add_argument("--cpu-baseline-elems", type=int, default=1 << 25,
+                    help="elements of the CPU oracle sample reported as cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    line = run_ours(args, rank, world, dev)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        b, s, desc = oracle_sample(workloads(args.workload)[0], args.cpu_baseline_elems)
+        line["cpu_baseline"] = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": desc,
+                                "seconds": round(s, 2)}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

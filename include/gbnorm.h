@@ -1,0 +1,138 @@
+/*
+ * gbnorm.h -- C ABI of the GB300 row-normalization library (libgbnorm.so).
+ *
+ * Forward and backward of three row-wise normalization layers over a
+ * row-major activation x of shape [M, N] (M rows, normalized over N):
+ *
+ *   DyT        y = gamma_j * tanh(alpha * x_ij) + beta_j, scalar alpha
+ *              (the fused DyT kernels of Liger-Kernel PR 1617, "fix(dyt):
+ *              use a 1D grid and tile small-width rows", Summary)
+ *   LayerNorm  y = (x - mean) * rstd * gamma_j + beta_j, biased variance,
+ *              rstd = 1/sqrt(var + eps) (the backward's saved-statistics
+ *              interface follows torch-xpu-ops "Layernorm bwd OPT #1880")
+ *   RMSNorm    y = weight * (x.float() * rsqrt(mean(x.float()^2) + eps))
+ *              .to(x.dtype), with the rounding points of DeepSpeed PR 8645
+ *              (quoted in PR 8664), section "Semantics"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Pointers.  Every tensor argument is a DEVICE pointer on the current CUDA
+ *   device (cudaGetDevice()).  Activations (x, dy, y, dx) are contiguous
+ *   row-major [M, N] in the activation dtype `xt`; parameters (alpha [1],
+ *   gamma/beta/weight [N]) and parameter gradients are in the parameter
+ *   dtype `pt`/`wt`; saved statistics (mean, rstd) are float32 [M].
+ *   Every pointer must be aligned to its element size (else GBN_EINVAL).
+ *   Beyond that any alignment is accepted: 16-byte aligned activations with
+ *   N*sizeof a multiple of 16 take the vector path, the rest the general path.
+ * Ownership.  The caller owns all memory.  The library never allocates,
+ *   never frees, never synchronizes and launches only on `stream` (which may
+ *   be 0, the legacy default stream).  Calls are asynchronous: a GBN_OK
+ *   return means the work was enqueued.
+ * Outputs.  y and dx take x's dtype; parameter gradients take the
+ *   parameters' dtype (Liger-Kernel PR 1617, Summary).  Parameter-gradient
+ *   outputs are nullable: a null pointer skips that output.
+ * Workspace.  A backward call needs `gbn_bwd_workspace_bytes(...)` bytes of
+ *   4-byte aligned device scratch for its per-CTA partial column sums.  It
+ *   needs no initialization: every launch writes every partial row it later
+ *   reads.  One workspace must not serve two calls that may overlap on the
+ *   GPU.  With every parameter-gradient output null, ws may be null.
+ * Determinism.  The launch layout is a fixed function of (M, N, dtypes,
+ *   alignment, SM count) and no float atomics are used: identical inputs
+ *   give bit-identical outputs on the same device.
+ * Empty input.  M == 0 is a successful call that writes zero parameter
+ *   gradients (it still needs `stream` to be valid).
+ * Errors.  Invalid arguments return an error status BEFORE anything is
+ *   launched; a failed launch returns GBN_ELAUNCH.  No error is fatal and
+ *   no kernel traps.
+ */
+#ifndef GBNORM_H
+#define GBNORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+typedef enum { GBN_F32 = 0, GBN_BF16 = 1 } gbn_dtype;
+
+/* Return codes. */
+typedef enum {
+    GBN_OK = 0,
+    GBN_EINVAL = 1,     /* null required pointer, M < 0, N < 1, N > INT32_MAX, bad eps, a pointer
+                           not aligned to its element size, misaligned ws */
+    GBN_EDTYPE = 2,     /* dtype code not in gbn_dtype */
+    GBN_EWORKSPACE = 3, /* ws_bytes smaller than the call needs */
+    GBN_ELAUNCH = 4,    /* a kernel launch failed (cudaGetLastError after the launch) */
+    GBN_EDEVICE = 5     /* the current device could not be queried */
+} gbn_status;
+
+/* Layer selector of gbn_bwd_workspace_bytes. */
+typedef enum { GBN_OP_DYT = 0, GBN_OP_LAYERNORM = 1, GBN_OP_RMSNORM = 2 } gbn_op;
+
+/* Human-readable name of a gbn_status value (static storage). */
+const char* gbn_status_string(int status);
+
+/* Workspace bytes a backward call of layer `op` on [M, N] activations of
+ * dtype xt with parameters of dtype pt needs on `device` (an upper bound
+ * over both pointer-alignment paths).  Returns 0 for M == 0 and (size_t)-1
+ * on invalid arguments or when the device cannot be queried. */
+size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int device);
+
+/* ---------------------------------------------------------------- DyT
+ * dyt_fwd: y[i,j] = gamma[j] * tanh(alpha[0] * x[i,j]) + beta[j].
+ *   x, y [M,N] xt; alpha [1], gamma [N], beta [N] pt (all required).
+ * dyt_bwd: dx = dy * gamma * alpha * sech^2(alpha x);
+ *   dgamma[j] = sum_i dy tanh(alpha x), dbeta[j] = sum_i dy,
+ *   dalpha[0] = sum_ij dy gamma_j x sech^2(alpha x).
+ *   Padded rows of a tile are masked after the arithmetic, so alpha = +inf
+ *   gives finite dgamma, dbeta, dalpha (Liger-Kernel PR 1617, Summary);
+ *   dx itself is NaN there (dy * gamma * inf * 0 under IEEE rules).
+ *   x, dy, dx [M,N] xt (required); dalpha [1], dgamma/dbeta [N] pt (nullable). */
+int dyt_fwd(const void* x, const void* alpha, const void* gamma, const void* beta, void* y,
+            int64_t M, int64_t N, int xt, int pt, cudaStream_t stream);
+int dyt_bwd(const void* x, const void* dy, const void* alpha, const void* gamma, void* dx,
+            void* dalpha, void* dgamma, void* dbeta, int64_t M, int64_t N, int xt, int pt,
+            void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ----------------------------------------------------------- LayerNorm
+ * layernorm_fwd: mean_i, rstd_i = 1/sqrt(var_i + eps) (biased variance);
+ *   y = (x - mean) * rstd * gamma + beta.  gamma, beta nullable (1 and 0);
+ *   mean, rstd [M] f32 nullable (written when given).  eps >= 0, finite.
+ * layernorm_bwd: with xhat = (x - mean) rstd and g = dy * gamma,
+ *   dx = rstd * (g - mean_j g - xhat * mean_j(g xhat)),
+ *   dgamma[j] = sum_i dy xhat, dbeta[j] = sum_i dy.
+ *   mean, rstd (required) are the forward's saved statistics; gamma
+ *   nullable (1); dgamma, dbeta nullable.  The column sums run as per-CTA
+ *   partials plus a second pass (torch-xpu-ops "Layernorm bwd OPT #1880"). */
+int layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean,
+                  float* rstd, int64_t M, int64_t N, float eps, int xt, int pt,
+                  cudaStream_t stream);
+int layernorm_bwd(const void* x, const void* dy, const float* mean, const float* rstd,
+                  const void* gamma, void* dx, void* dgamma, void* dbeta, int64_t M, int64_t N,
+                  int xt, int pt, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------- RMSNorm
+ * rmsnorm_fwd: r_i = rsqrt(mean_j x^2 + eps) in f32, n = round_x(x r),
+ *   y = round_x(w * n).  w [N] wt (required); rstd [M] f32 nullable.
+ * rmsnorm_bwd: xhat = x r, dn = round_x(dy w),
+ *   dx = round_x(r (dn - xhat mean_j(dn xhat))),
+ *   dw[j] = sum_i round_x(dy n) when wt == xt, sum_i dy n when wt is f32
+ *   (DeepSpeed PR 8645 quoted in PR 8664, "Semantics").  rstd nullable:
+ *   when null r is recomputed with the forward's exact arithmetic, so the
+ *   result is bit-identical either way.  dw nullable.  eps >= 0, finite. */
+int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
+                float eps, int xt, int wt, cudaStream_t stream);
+int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd, void* dx,
+                void* dw, int64_t M, int64_t N, float eps, int xt, int wt, void* ws,
+                size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBNORM_H */

@@ -1,0 +1,241 @@
+"""ctypes binding of libgbnorm.so: the C ABI of include/gbnorm.h, one Python
+function per entry point, under the same names.
+
+Argument marshalling only: tensors become device pointers, shapes become
+(M, N) with every leading dimension folded into M, dtypes become the
+library's codes, and the current torch stream is passed as the CUDA stream.
+Every step of the computation runs in the CUDA kernels; there is no
+fallback, and a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+GBN_F32, GBN_BF16 = 0, 1
+GBN_OP_DYT, GBN_OP_LAYERNORM, GBN_OP_RMSNORM = 0, 1, 2
+GBN_OK = 0
+SIZE_MAX = ctypes.c_size_t(-1).value
+
+_DTYPES = {torch.float32: GBN_F32, torch.bfloat16: GBN_BF16}
+
+# The entry points the header declares, with their ctypes signatures.
+_P, _I64, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "gbn_status_string": ([_I], ctypes.c_char_p),
+    "gbn_bwd_workspace_bytes": ([_I, _I64, _I64, _I, _I, _I], _SZ),
+    "dyt_fwd": ([_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _P], _I),
+    "dyt_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _I, _P, _SZ, _P], _I),
+    "layernorm_fwd": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P], _I),
+    "layernorm_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _I, _P, _SZ, _P], _I),
+    "rmsnorm_fwd": ([_P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P], _I),
+    "rmsnorm_bwd": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P, _SZ, _P], _I),
+}
+
+_lock = threading.Lock()
+_handle = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libgbnorm.so (built in-tree by normalization_layers_fwd_gb300.build)."""
+    global _handle
+    with _lock:
+        if _handle is not None and path is None:
+            return _handle
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is missing: build it with `python -m normalization_layers_fwd_gb300.build`"
+                " (nvcc, sm_103a); there is no fallback implementation")
+        lib = ctypes.CDLL(p)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        if path is None:
+            _handle = lib
+        return lib
+
+
+class GbnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = load().gbn_status_string(status).decode()
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+def _check(status: int, where: str):
+    if status != GBN_OK:
+        raise GbnError(status, where)
+
+
+# -------------------------------------------------------------- marshalling
+
+def _code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}: float32 or bfloat16") from None
+
+
+def _rows(x: torch.Tensor):
+    """(contiguous x, M, N): leading dimensions fold into rows."""
+    if not x.is_cuda:
+        raise ValueError("activations must be CUDA tensors")
+    if x.dim() < 1:
+        raise ValueError("activations need at least one dimension")
+    x = x.contiguous()
+    N = x.shape[-1]
+    M = x.numel() // N if N else 0
+    return x, M, N
+
+
+def _param(p, like: torch.Tensor, n: int, name: str, required: bool = True):
+    if p is None:
+        if required:
+            raise ValueError(f"{name} is required")
+        return None
+    if not p.is_cuda or p.device != like.device:
+        raise ValueError(f"{name} must be on {like.device}")
+    if p.numel() != n:
+        raise ValueError(f"{name} has {p.numel()} elements, expected {n}")
+    return p.contiguous()
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+_ws_cache: dict = {}
+
+
+def workspace(op: int, M: int, N: int, xt: int, pt: int, device: torch.device):
+    """A cached device scratch buffer large enough for one backward call."""
+    n = load().gbn_bwd_workspace_bytes(op, M, N, xt, pt, device.index)
+    if n == SIZE_MAX:
+        raise GbnError(1, "gbn_bwd_workspace_bytes")
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < n:
+        buf = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf, n
+
+
+# ---------------------------------------------------------------------- DyT
+
+def dyt_fwd(x, alpha, gamma, beta, y=None):
+    """y = gamma * tanh(alpha * x) + beta (alpha: 1 element)."""
+    x, M, N = _rows(x)
+    alpha = _param(alpha, x, 1, "alpha")
+    gamma = _param(gamma, x, N, "gamma")
+    beta = _param(beta, x, N, "beta")
+    if beta.dtype != gamma.dtype or alpha.dtype != gamma.dtype:
+        raise TypeError("alpha, gamma and beta must share one dtype")
+    y = torch.empty_like(x) if y is None else y
+    _check(load().dyt_fwd(_ptr(x), _ptr(alpha), _ptr(gamma), _ptr(beta), _ptr(y), M, N, _code(x),
+                          _code(gamma), _stream(x.device)), "dyt_fwd")
+    return y
+
+
+def dyt_bwd(x, dy, alpha, gamma, need_dalpha=True, need_dgamma=True, need_dbeta=True):
+    """(dx, dalpha, dgamma, dbeta); parameter gradients in gamma's dtype."""
+    x, M, N = _rows(x)
+    dy = dy.contiguous()
+    if dy.shape != x.shape or dy.dtype != x.dtype:
+        raise ValueError("dy must match x in shape and dtype")
+    alpha = _param(alpha, x, 1, "alpha")
+    gamma = _param(gamma, x, N, "gamma")
+    dx = torch.empty_like(x)
+    da = torch.empty(1, dtype=gamma.dtype, device=x.device) if need_dalpha else None
+    dg = torch.empty(N, dtype=gamma.dtype, device=x.device) if need_dgamma else None
+    db = torch.empty(N, dtype=gamma.dtype, device=x.device) if need_dbeta else None
+    ws, nbytes = workspace(GBN_OP_DYT, M, N, _code(x), _code(gamma), x.device)
+    _check(load().dyt_bwd(_ptr(x), _ptr(dy), _ptr(alpha), _ptr(gamma), _ptr(dx), _ptr(da),
+                          _ptr(dg), _ptr(db), M, N, _code(x), _code(gamma), _ptr(ws), nbytes,
+                          _stream(x.device)), "dyt_bwd")
+    return dx, da, dg, db
+
+
+# ---------------------------------------------------------------- LayerNorm
+
+def layernorm_fwd(x, gamma=None, beta=None, eps=1e-5, save_stats=True):
+    """(y, mean, rstd); mean/rstd are float32 [M] (None when not saved)."""
+    x, M, N = _rows(x)
+    gamma = _param(gamma, x, N, "gamma", required=False)
+    beta = _param(beta, x, N, "beta", required=False)
+    if gamma is not None and beta is not None and gamma.dtype != beta.dtype:
+        raise TypeError("gamma and beta must share one dtype")
+    p = gamma if gamma is not None else beta
+    pt = _code(p) if p is not None else GBN_F32
+    y = torch.empty_like(x)
+    mean = torch.empty(M, dtype=torch.float32, device=x.device) if save_stats else None
+    rstd = torch.empty(M, dtype=torch.float32, device=x.device) if save_stats else None
+    _check(load().layernorm_fwd(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), _ptr(mean), _ptr(rstd),
+                                M, N, float(eps), _code(x), pt, _stream(x.device)), "layernorm_fwd")
+    return y, mean, rstd
+
+
+def layernorm_bwd(x, dy, mean, rstd, gamma=None, need_dgamma=True, need_dbeta=True,
+                  param_dtype=None):
+    """(dx, dgamma, dbeta) from the forward's saved mean and rstd."""
+    x, M, N = _rows(x)
+    dy = dy.contiguous()
+    if dy.shape != x.shape or dy.dtype != x.dtype:
+        raise ValueError("dy must match x in shape and dtype")
+    gamma = _param(gamma, x, N, "gamma", required=False)
+    mean = _param(mean, x, M, "mean").float()
+    rstd = _param(rstd, x, M, "rstd").float()
+    pdt = gamma.dtype if gamma is not None else (param_dtype or torch.float32)
+    dx = torch.empty_like(x)
+    dg = torch.empty(N, dtype=pdt, device=x.device) if need_dgamma else None
+    db = torch.empty(N, dtype=pdt, device=x.device) if need_dbeta else None
+    pt = _DTYPES[pdt]
+    ws, nbytes = workspace(GBN_OP_LAYERNORM, M, N, _code(x), pt, x.device)
+    _check(load().layernorm_bwd(_ptr(x), _ptr(dy), _ptr(mean), _ptr(rstd), _ptr(gamma), _ptr(dx),
+                                _ptr(dg), _ptr(db), M, N, _code(x), pt, _ptr(ws), nbytes,
+                                _stream(x.device)), "layernorm_bwd")
+    return dx, dg, db
+
+
+# ------------------------------------------------------------------ RMSNorm
+
+def rmsnorm_fwd(x, w, eps=1e-6, save_rstd=True):
+    """(y, rstd): weight * (x.float() * rsqrt(mean(x^2) + eps)).to(x.dtype)."""
+    x, M, N = _rows(x)
+    w = _param(w, x, N, "w")
+    y = torch.empty_like(x)
+    rstd = torch.empty(M, dtype=torch.float32, device=x.device) if save_rstd else None
+    _check(load().rmsnorm_fwd(_ptr(x), _ptr(w), _ptr(y), _ptr(rstd), M, N, float(eps), _code(x),
+                              _code(w), _stream(x.device)), "rmsnorm_fwd")
+    return y, rstd
+
+
+def rmsnorm_bwd(x, dy, w, rstd=None, eps=1e-6, need_dw=True):
+    """(dx, dw); rstd None recomputes it exactly as the forward does."""
+    x, M, N = _rows(x)
+    dy = dy.contiguous()
+    if dy.shape != x.shape or dy.dtype != x.dtype:
+        raise ValueError("dy must match x in shape and dtype")
+    w = _param(w, x, N, "w")
+    rstd = _param(rstd, x, M, "rstd", required=False)
+    dx = torch.empty_like(x)
+    dw = torch.empty(N, dtype=w.dtype, device=x.device) if need_dw else None
+    ws, nbytes = workspace(GBN_OP_RMSNORM, M, N, _code(x), _code(w), x.device)
+    _check(load().rmsnorm_bwd(_ptr(x), _ptr(dy), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw), M, N,
+                              float(eps), _code(x), _code(w), _ptr(ws), nbytes, _stream(x.device)),
+           "rmsnorm_bwd")
+    return dx, dw

@@ -1,0 +1,296 @@
+// api.cu -- the extern "C" entry points of libgbnorm.so: argument checks,
+// the fixed launch-layout table, and the launches (kernel files hold the
+// kernels).  Nothing here allocates memory or synchronizes.
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <initializer_list>
+
+#include "common.cuh"
+#include "gbnorm.h"
+#include "internal.h"
+
+using gbn::Launch;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];  // 0 = not yet queried
+
+int sm_count(int device)
+{
+    if (device < 0 || device >= kMaxDevices) return -1;
+    int v = g_sms[device].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0) {
+        cudaGetLastError();  // do not leave a sticky error for the caller
+        return -1;
+    }
+    g_sms[device].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+int current_sms()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return sm_count(dev);
+}
+
+bool dtype_ok(int t) { return t == gbn::kF32 || t == gbn::kBF16; }
+int elem_bytes(int t) { return t == gbn::kF32 ? 4 : 2; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Every pointer must at least be aligned to its element size (null passes):
+// even the general path's scalar loads need that.
+bool elem_aligned(const void* p, int t)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (uintptr_t)(elem_bytes(t) - 1)) == 0;
+}
+bool all_aligned(int t, std::initializer_list<const void*> ps)
+{
+    for (const void* p : ps)
+        if (!elem_aligned(p, t)) return false;
+    return true;
+}
+
+// Cap on the general path's warps: each warp owns one workspace row.
+int64_t general_warps(int64_t M, int sms) { return M < 4LL * sms ? M : 4LL * sms; }
+
+// Whether [M, N] of dtype xt can take the 16-byte vector path (alignment
+// aside), and its schedule index.
+int fast_sid(int64_t N, int xt)
+{
+    const int vec = 16 / elem_bytes(xt);
+    if (N % vec != 0) return -1;
+    const int64_t nvec = N / vec;
+    for (int s = 0; s < gbn::kNumSched; ++s)
+        if (nvec <= gbn::kSched[s].max_nvec) return s;
+    return -1;
+}
+
+// The launch layout of one row-wise kernel.  two_streams: the kernel uses the
+// schedule's UB rows per group (backward kernels, LayerNorm forward).
+Launch plan(int64_t M, int64_t N, int xt, bool aligned, int sms, cudaStream_t stream,
+            bool two_streams)
+{
+    Launch L{};
+    L.stream = stream;
+    const int sid = aligned ? fast_sid(N, xt) : -1;
+    if (sid >= 0) {
+        const gbn::SchedEntry& e = gbn::kSched[sid];
+        const int64_t rows_per_block = (int64_t)(e.T / e.W) * (two_streams ? e.UB : e.UF);
+        L.fast = 1;
+        L.sid = sid;
+        L.nblocks = (M + rows_per_block - 1) / rows_per_block;
+        const int64_t cap = (int64_t)sms * e.MINB;
+        L.grid = (int)(L.nblocks < cap ? L.nblocks : cap);
+        L.P = L.grid;
+    } else {
+        const int64_t warps = general_warps(M, sms);
+        L.fast = 0;
+        L.grid = (int)((warps + gbn::kGenWarps - 1) / gbn::kGenWarps);
+        L.P = (int64_t)L.grid * gbn::kGenWarps;
+    }
+    return L;
+}
+
+bool shape_ok(int64_t M, int64_t N)
+{
+    if (M < 0 || N < 1 || N > INT_MAX) return false;
+    // keep M*N*8 (the widest byte offset computed anywhere) inside int64
+    return M <= (INT64_MAX / 8) / N;
+}
+
+bool eps_ok(float eps) { return std::isfinite(eps) && eps >= 0.f; }
+
+int launch_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return GBN_OK;
+    return GBN_ELAUNCH;
+}
+
+size_t ws_needed(int op, const Launch& L, int64_t N)
+{
+    return (size_t)L.P * (size_t)gbn::ws_row_floats(op, N) * sizeof(float);
+}
+
+// Common tail of every backward: the second reduction stage (also for M ==
+// 0, where it writes zeros).
+int finish_bwd(cudaStream_t s, const float* ws, int64_t P, int op, int64_t N, int pt, void* o0,
+               void* o1, void* o2)
+{
+    if (!o0 && !o1 && !o2) return GBN_OK;
+    const int64_t rowlen = gbn::ws_row_floats(op, N);
+    return launch_status(gbn::launch_colsum(s, ws, P, rowlen, N, pt, o0, o1, o2));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gbn_status_string(int status)
+{
+    switch (status) {
+        case GBN_OK: return "GBN_OK";
+        case GBN_EINVAL: return "GBN_EINVAL: invalid argument";
+        case GBN_EDTYPE: return "GBN_EDTYPE: unsupported dtype";
+        case GBN_EWORKSPACE: return "GBN_EWORKSPACE: workspace too small";
+        case GBN_ELAUNCH: return "GBN_ELAUNCH: kernel launch failed";
+        case GBN_EDEVICE: return "GBN_EDEVICE: cannot query the CUDA device";
+        default: return "GBN_UNKNOWN";
+    }
+}
+
+size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int device)
+{
+    if (op < GBN_OP_DYT || op > GBN_OP_RMSNORM || !shape_ok(M, N) || !dtype_ok(xt) ||
+        !dtype_ok(pt))
+        return (size_t)-1;
+    if (M == 0) return 0;
+    const int sms = sm_count(device);
+    if (sms <= 0) return (size_t)-1;
+    const Launch a = plan(M, N, xt, true, sms, nullptr, true);
+    const Launch b = plan(M, N, xt, false, sms, nullptr, true);
+    const size_t need = ws_needed(op, a.P > b.P ? a : b, N);
+    return (need + 255) & ~(size_t)255;
+}
+
+// ---------------------------------------------------------------------- DyT
+int dyt_fwd(const void* x, const void* alpha, const void* gamma, const void* beta, void* y,
+            int64_t M, int64_t N, int xt, int pt, cudaStream_t stream)
+{
+    if (!dtype_ok(xt) || !dtype_ok(pt)) return GBN_EDTYPE;
+    if (!shape_ok(M, N) || !alpha || !gamma || !beta) return GBN_EINVAL;
+    if (M > 0 && (!x || !y)) return GBN_EINVAL;
+    if (!all_aligned(xt, {x, y}) || !all_aligned(pt, {alpha, gamma, beta})) return GBN_EINVAL;
+    if (M == 0) return GBN_OK;
+    const int sms = current_sms();
+    if (sms <= 0) return GBN_EDEVICE;
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, false);
+    if (!L.fast) {  // elementwise general path: one thread per element, grid-stride
+        const int64_t E = M * N;
+        const int64_t blocks = (E + gbn::kGenThreads - 1) / gbn::kGenThreads;
+        const int64_t cap = 8LL * sms;
+        L.grid = (int)(blocks < cap ? blocks : cap);
+    }
+    return launch_status(gbn::launch_dyt_fwd(L, xt, pt, x, alpha, gamma, beta, y, M, (int)N));
+}
+
+int dyt_bwd(const void* x, const void* dy, const void* alpha, const void* gamma, void* dx,
+            void* dalpha, void* dgamma, void* dbeta, int64_t M, int64_t N, int xt, int pt,
+            void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!dtype_ok(xt) || !dtype_ok(pt)) return GBN_EDTYPE;
+    if (!shape_ok(M, N) || !alpha || !gamma) return GBN_EINVAL;
+    if (M > 0 && (!x || !dy || !dx)) return GBN_EINVAL;
+    if (!all_aligned(xt, {x, dy, dx}) || !all_aligned(pt, {alpha, gamma, dalpha, dgamma, dbeta}))
+        return GBN_EINVAL;
+    const bool grads = dalpha || dgamma || dbeta;
+    if (grads && ws && !aligned4(ws)) return GBN_EINVAL;
+    const int sms = current_sms();
+    if (sms <= 0) return GBN_EDEVICE;
+    const Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
+                          true);
+    if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_DYT, L, N))) return GBN_EWORKSPACE;
+    float* wsf = grads ? static_cast<float*>(ws) : nullptr;
+    if (M > 0) {
+        const int rc = launch_status(
+            gbn::launch_dyt_bwd(L, xt, pt, x, dy, alpha, gamma, dx, wsf, M, (int)N));
+        if (rc != GBN_OK) return rc;
+    }
+    return finish_bwd(stream, wsf, M > 0 ? L.P : 0, GBN_OP_DYT, N, pt, dgamma, dbeta, dalpha);
+}
+
+// ---------------------------------------------------------------- LayerNorm
+int layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean,
+                  float* rstd, int64_t M, int64_t N, float eps, int xt, int pt,
+                  cudaStream_t stream)
+{
+    if (!dtype_ok(xt) || !dtype_ok(pt)) return GBN_EDTYPE;
+    if (!shape_ok(M, N) || !eps_ok(eps)) return GBN_EINVAL;
+    if (M > 0 && (!x || !y)) return GBN_EINVAL;
+    if (!all_aligned(xt, {x, y}) || !all_aligned(pt, {gamma, beta}) ||
+        !all_aligned(GBN_F32, {mean, rstd}))
+        return GBN_EINVAL;
+    if (M == 0) return GBN_OK;
+    const int sms = current_sms();
+    if (sms <= 0) return GBN_EDEVICE;
+    const Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, true);
+    return launch_status(
+        gbn::launch_ln_fwd(L, xt, pt, x, gamma, beta, y, mean, rstd, M, (int)N, eps));
+}
+
+int layernorm_bwd(const void* x, const void* dy, const float* mean, const float* rstd,
+                  const void* gamma, void* dx, void* dgamma, void* dbeta, int64_t M, int64_t N,
+                  int xt, int pt, void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!dtype_ok(xt) || !dtype_ok(pt)) return GBN_EDTYPE;
+    if (!shape_ok(M, N)) return GBN_EINVAL;
+    if (M > 0 && (!x || !dy || !dx || !mean || !rstd)) return GBN_EINVAL;
+    if (!all_aligned(xt, {x, dy, dx}) || !all_aligned(pt, {gamma, dgamma, dbeta}) ||
+        !all_aligned(GBN_F32, {mean, rstd}))
+        return GBN_EINVAL;
+    const bool grads = dgamma || dbeta;
+    if (grads && ws && !aligned4(ws)) return GBN_EINVAL;
+    const int sms = current_sms();
+    if (sms <= 0) return GBN_EDEVICE;
+    const Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
+                          true);
+    if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_LAYERNORM, L, N)))
+        return GBN_EWORKSPACE;
+    float* wsf = grads ? static_cast<float*>(ws) : nullptr;
+    if (M > 0) {
+        const int rc = launch_status(
+            gbn::launch_ln_bwd(L, xt, pt, x, dy, mean, rstd, gamma, dx, wsf, M, (int)N));
+        if (rc != GBN_OK) return rc;
+    }
+    return finish_bwd(stream, wsf, M > 0 ? L.P : 0, GBN_OP_LAYERNORM, N, pt, dgamma, dbeta,
+                      nullptr);
+}
+
+// ------------------------------------------------------------------ RMSNorm
+int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
+                float eps, int xt, int wt, cudaStream_t stream)
+{
+    if (!dtype_ok(xt) || !dtype_ok(wt)) return GBN_EDTYPE;
+    if (!shape_ok(M, N) || !eps_ok(eps) || !w) return GBN_EINVAL;
+    if (M > 0 && (!x || !y)) return GBN_EINVAL;
+    if (!all_aligned(xt, {x, y}) || !all_aligned(wt, {w}) || !all_aligned(GBN_F32, {rstd}))
+        return GBN_EINVAL;
+    if (M == 0) return GBN_OK;
+    const int sms = current_sms();
+    if (sms <= 0) return GBN_EDEVICE;
+    const Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, false);
+    return launch_status(gbn::launch_rms_fwd(L, xt, wt, x, w, y, rstd, M, (int)N, eps));
+}
+
+int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd, void* dx,
+                void* dw, int64_t M, int64_t N, float eps, int xt, int wt, void* ws,
+                size_t ws_bytes, cudaStream_t stream)
+{
+    if (!dtype_ok(xt) || !dtype_ok(wt)) return GBN_EDTYPE;
+    if (!shape_ok(M, N) || !eps_ok(eps) || !w) return GBN_EINVAL;
+    if (M > 0 && (!x || !dy || !dx)) return GBN_EINVAL;
+    if (!all_aligned(xt, {x, dy, dx}) || !all_aligned(wt, {w, dw}) || !all_aligned(GBN_F32, {rstd}))
+        return GBN_EINVAL;
+    if (dw && ws && !aligned4(ws)) return GBN_EINVAL;
+    const int sms = current_sms();
+    if (sms <= 0) return GBN_EDEVICE;
+    const Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
+                          true);
+    if (dw && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_RMSNORM, L, N))) return GBN_EWORKSPACE;
+    float* wsf = dw ? static_cast<float*>(ws) : nullptr;
+    if (M > 0) {
+        const int rc = launch_status(
+            gbn::launch_rms_bwd(L, xt, wt, x, dy, w, rstd, dx, wsf, M, (int)N, eps));
+        if (rc != GBN_OK) return rc;
+    }
+    return finish_bwd(stream, wsf, M > 0 ? L.P : 0, GBN_OP_RMSNORM, N, wt, dw, nullptr, nullptr);
+}
+
+}  // extern "C"

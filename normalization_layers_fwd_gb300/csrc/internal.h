@@ -1,0 +1,55 @@
+// internal.h -- launch descriptors shared by the host dispatch (api.cu) and
+// the per-layer kernel files.  Not part of the public C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbn {
+
+// How one call is laid out on the GPU.  Decided on the host from (M, N,
+// dtypes, pointer alignment, SM count) by a fixed table, never by runtime
+// tuning, so the same inputs always give the same summation order.
+struct Launch {
+    int fast;           // 1: 16-byte vector path (schedule `sid`); 0: general path
+    int sid;            // index into kSched (fast path only)
+    int grid;           // CTAs launched (persistent: each loops over row blocks)
+    int64_t nblocks;    // row blocks of the fast path
+    int64_t P;          // partial rows the backward writes into the workspace
+    cudaStream_t stream;
+};
+
+// Workspace row length (floats) per layer: the per-column partial sums of
+// every parameter gradient, plus one scalar for DyT's alpha.
+inline int64_t ws_row_floats(int op, int64_t N)
+{
+    return op == 0 ? 2 * N + 1 : (op == 1 ? 2 * N : N);
+}
+
+cudaError_t launch_dyt_fwd(const Launch& L, int xt, int pt, const void* x, const void* alpha,
+                           const void* gamma, const void* beta, void* y, int64_t M, int N);
+cudaError_t launch_dyt_bwd(const Launch& L, int xt, int pt, const void* x, const void* dy,
+                           const void* alpha, const void* gamma, void* dx, float* ws,
+                           int64_t M, int N);
+
+cudaError_t launch_ln_fwd(const Launch& L, int xt, int pt, const void* x, const void* gamma,
+                          const void* beta, void* y, float* mean, float* rstd, int64_t M, int N,
+                          float eps);
+cudaError_t launch_ln_bwd(const Launch& L, int xt, int pt, const void* x, const void* dy,
+                          const float* mean, const float* rstd, const void* gamma, void* dx,
+                          float* ws, int64_t M, int N);
+
+cudaError_t launch_rms_fwd(const Launch& L, int xt, int pt, const void* x, const void* w,
+                           void* y, float* rstd, int64_t M, int N, float eps);
+cudaError_t launch_rms_bwd(const Launch& L, int xt, int pt, const void* x, const void* dy,
+                           const void* w, const float* rstd, void* dx, float* ws, int64_t M,
+                           int N, float eps);
+
+// Second stage of the parameter-gradient reduction: out[c] = sum over the P
+// workspace rows of column c, in a fixed order, written in the parameter
+// dtype.  Columns [0,N) go to out0, [N,2N) to out1, [2N] to out2 (each
+// nullable: skipped).
+cudaError_t launch_colsum(cudaStream_t s, const float* ws, int64_t P, int64_t rowlen, int64_t N,
+                          int pt, void* out0, void* out1, void* out2);
+
+}  // namespace gbn

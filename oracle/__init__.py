@@ -70,8 +70,8 @@ def _lib():
             "orc_ln_bwd_rows": ([P, P, I, I64, I64, P, P, P, P, I64, P, P], I),
             "orc_ln_bwd_cols": ([P, P, I, I64, I64, P, P, P, P, P, P], I),
             "orc_rms_fwd_rows": ([P, I, I64, I64, D, P, I, P, I64, P, P, P, P], I),
-            "orc_rms_bwd_rows": ([P, P, I, I64, I64, D, P, I, P, I64, P, P, P], I),
-            "orc_rms_bwd_cols": ([P, P, I, I, I64, I64, D, I, P, P], I),
+            "orc_rms_bwd_rows": ([P, P, I, I, I64, I64, D, P, I, P, I64, P, P, P], I),
+            "orc_rms_bwd_cols": ([P, P, I, I, I64, I64, D, I, P, P, P], I),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -220,37 +220,38 @@ def ln_bwd_cols(x, dy, mean, rstd):
 # --------------------------------------------------------------- RMSNorm
 
 def rms_fwd(x, eps, w, mode=PARITY, rows=None):
-    """(y, y_scale, rstd, amb): amb flags near-tie intermediate roundings."""
+    """(y, y_scale, rstd, y_allow).  y_allow: largest change of y that a
+    float32 implementation may legitimately show where the rounding of the
+    normalized value is near a bfloat16 tie (zero elsewhere)."""
     x, xt, M, N = _act(x)
     wv = _f64(w)
     r, nr = _rows(rows, M)
-    y = np.empty((nr, N)); ys = np.empty((nr, N)); rs = np.empty(nr)
-    amb = np.zeros((nr, N), dtype=np.uint8)
+    y = np.empty((nr, N)); ys = np.empty((nr, N)); rs = np.empty(nr); al = np.empty((nr, N))
     _check(_lib().orc_rms_fwd_rows(_ptr(x), xt, M, N, float(eps), _ptr(wv), int(mode), _ptr(r),
-                                   nr, _ptr(y), _ptr(ys), _ptr(rs), _ptr(amb)), "rms_fwd")
-    return y, ys, rs, amb
+                                   nr, _ptr(y), _ptr(ys), _ptr(rs), _ptr(al)), "rms_fwd")
+    return y, ys, rs, al
 
 
-def rms_bwd_rows(x, dy, eps, w, mode=PARITY, rows=None):
-    """(dx, dx_scale, amb)."""
+def rms_bwd_rows(x, dy, eps, w, w_dtype_code=F32, mode=PARITY, rows=None):
+    """(dx, dx_scale, dx_allow); w_dtype_code is F32 or BF16."""
     x, xt, M, N = _act(x)
     dy, dt, _, _ = _act(dy)
     assert dt == xt and dy.shape == x.shape
     wv = _f64(w)
     r, nr = _rows(rows, M)
-    dx = np.empty((nr, N)); dxs = np.empty((nr, N))
-    amb = np.zeros((nr, N), dtype=np.uint8)
-    _check(_lib().orc_rms_bwd_rows(_ptr(x), _ptr(dy), xt, M, N, float(eps), _ptr(wv), int(mode),
-                                   _ptr(r), nr, _ptr(dx), _ptr(dxs), _ptr(amb)), "rms_bwd_rows")
-    return dx, dxs, amb
+    dx = np.empty((nr, N)); dxs = np.empty((nr, N)); al = np.empty((nr, N))
+    _check(_lib().orc_rms_bwd_rows(_ptr(x), _ptr(dy), xt, int(w_dtype_code), M, N, float(eps),
+                                   _ptr(wv), int(mode), _ptr(r), nr, _ptr(dx), _ptr(dxs), _ptr(al)),
+           "rms_bwd_rows")
+    return dx, dxs, al
 
 
 def rms_bwd_cols(x, dy, eps, w_dtype_code, mode=PARITY):
-    """(dw, dw_ss); w_dtype_code is F32 or BF16 (selects the term rounding)."""
+    """(dw, dw_ss, dw_allow); w_dtype_code is F32 or BF16 (selects the term rounding)."""
     x, xt, M, N = _act(x)
     dy, dt, _, _ = _act(dy)
     assert dt == xt and dy.shape == x.shape
-    dw = np.empty(N); ss = np.empty(N)
+    dw = np.empty(N); ss = np.empty(N); al = np.empty(N)
     _check(_lib().orc_rms_bwd_cols(_ptr(x), _ptr(dy), xt, int(w_dtype_code), M, N, float(eps),
-                                   int(mode), _ptr(dw), _ptr(ss)), "rms_bwd_cols")
-    return dw, ss
+                                   int(mode), _ptr(dw), _ptr(ss), _ptr(al)), "rms_bwd_cols")
+    return dw, ss, al

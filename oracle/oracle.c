@@ -100,6 +100,19 @@ static double round_to(double v, int dt, int* near_tie)
     return v;
 }
 
+/* Spacing of bfloat16 at |v|: the gap between the two neighbours that a
+ * near-tie rounding of v chooses between. */
+static double bf16_spacing(double v)
+{
+    double a = fabs(v);
+    if (a == 0.0 || isnan(a) || isinf(a)) return ldexp(1.0, -133);
+    int k;
+    (void)frexp(a, &k);
+    int qe = k - 8;
+    if (qe < -133) qe = -133;
+    return ldexp(1.0, qe);
+}
+
 double orc_round_bf16(double v) { return round_bf16(v, NULL); }
 void orc_round_bf16_array(const double* in, double* out, int64_t n)
 {
@@ -301,8 +314,14 @@ int orc_ln_bwd_cols(const void* x, const void* dy, int xt, int64_t M, int64_t N,
  * r is always recomputed from x: the saved rstd is an optional cache of the
  * GPU path, not part of the definition.  At width one the input derivative
  * is dn eps / (x^2 + eps)^(3/2) (the PR 8664 page, "Numerics").
- * amb[] flags elements whose value passed through a bfloat16 rounding
- * point within NEAR_TIE_REL of a midpoint (parity mode only).
+ *
+ * Near-tie allowances (parity mode, bfloat16 activations): where a value
+ * reaches a bfloat16 rounding point within NEAR_TIE_REL of a midpoint, an
+ * implementation that computes it in float32 may round it to the other
+ * neighbour.  The *_allow outputs give, per output, the largest change such
+ * a flip can cause (zero where no rounding is near a tie).  dy*w is exact
+ * in float32 when both are bfloat16, so it is only flagged for a float32
+ * weight.
  */
 
 static double rms_r(const void* x, int xt, int64_t i, int64_t N, double eps)
@@ -317,7 +336,7 @@ static double rms_r(const void* x, int xt, int64_t i, int64_t N, double eps)
 
 int orc_rms_fwd_rows(const void* x, int xt, int64_t M, int64_t N, double eps,
                      const double* w, int mode, const int64_t* rows, int64_t nrows,
-                     double* y, double* y_scale, double* rstd, unsigned char* amb)
+                     double* y, double* y_scale, double* rstd, double* y_allow)
 {
     (void)M;
     for (int64_t r = 0; r < nrows; ++r) {
@@ -330,28 +349,31 @@ int orc_rms_fwd_rows(const void* x, int xt, int64_t M, int64_t N, double eps,
             if (mode == ORC_PARITY) v = round_to(v, xt, &tie);
             y[r * N + j] = w[j] * v;
             if (y_scale) y_scale[r * N + j] = fabs(w[j] * v);
-            if (amb) amb[r * N + j] = (unsigned char)tie;
+            if (y_allow) y_allow[r * N + j] = tie ? fabs(w[j]) * bf16_spacing(v) : 0.0;
         }
     }
     return 0;
 }
 
-int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int64_t M, int64_t N,
+int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int wt, int64_t M, int64_t N,
                      double eps, const double* w, int mode, const int64_t* rows,
-                     int64_t nrows, double* dx, double* dx_scale, unsigned char* amb)
+                     int64_t nrows, double* dx, double* dx_scale, double* dx_allow)
 {
     (void)M;
     for (int64_t r = 0; r < nrows; ++r) {
         int64_t i = row_of(rows, r);
         double rs = rms_r(x, xt, i, N, eps);
-        double s = 0.0;
+        double s = 0.0, flip = 0.0;
         for (int64_t j = 0; j < N; ++j) {
             double xh = widen(x, xt, i * N + j) * rs;
             double dn = widen(dy, xt, i * N + j) * w[j];
-            if (mode == ORC_PARITY) dn = round_to(dn, xt, NULL);
+            int tie = 0;
+            if (mode == ORC_PARITY) dn = round_to(dn, xt, &tie);
+            if (tie && wt == ORC_F32) flip += bf16_spacing(dn) * fabs(xh);
             s += dn * xh;
         }
         double b = s / (double)N;
+        flip /= (double)N; /* largest change of b from flipped dn roundings */
         for (int64_t j = 0; j < N; ++j) {
             double xh = widen(x, xt, i * N + j) * rs;
             double dn = widen(dy, xt, i * N + j) * w[j];
@@ -359,7 +381,10 @@ int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int64_t M, int64_t N
             if (mode == ORC_PARITY) dn = round_to(dn, xt, &tie);
             dx[r * N + j] = rs * (dn - xh * b);
             if (dx_scale) dx_scale[r * N + j] = fabs(rs) * (fabs(dn) + fabs(xh * b));
-            if (amb) amb[r * N + j] = (unsigned char)tie;
+            if (dx_allow) {
+                double own = (tie && wt == ORC_F32) ? bf16_spacing(dn) : 0.0;
+                dx_allow[r * N + j] = fabs(rs) * (own + fabs(xh) * flip);
+            }
         }
     }
     return 0;
@@ -368,18 +393,26 @@ int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int64_t M, int64_t N
 /* wt: dtype of the weight (ORC_F32 or ORC_BF16); it selects whether each
  * dw term is rounded to the activation dtype before the sum. */
 int orc_rms_bwd_cols(const void* x, const void* dy, int xt, int wt, int64_t M, int64_t N,
-                     double eps, int mode, double* dw, double* dw_ss)
+                     double eps, int mode, double* dw, double* dw_ss, double* dw_allow)
 {
-    for (int64_t j = 0; j < N; ++j) dw[j] = dw_ss[j] = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        dw[j] = dw_ss[j] = 0.0;
+        if (dw_allow) dw_allow[j] = 0.0;
+    }
     for (int64_t i = 0; i < M; ++i) {
         double rs = rms_r(x, xt, i, N, eps);
         for (int64_t j = 0; j < N; ++j) {
             double n = widen(x, xt, i * N + j) * rs;
-            if (mode == ORC_PARITY) n = round_to(n, xt, NULL);
-            double term = widen(dy, xt, i * N + j) * n;
-            if (mode == ORC_PARITY && wt != ORC_F32) term = round_to(term, xt, NULL);
+            int tie = 0;
+            if (mode == ORC_PARITY) n = round_to(n, xt, &tie);
+            double g = widen(dy, xt, i * N + j);
+            double term = g * n;
+            int round_term = (mode == ORC_PARITY && wt != ORC_F32);
+            if (round_term) term = round_to(term, xt, NULL);
             dw[j] += term;
             dw_ss[j] += term * term;
+            if (dw_allow && tie)
+                dw_allow[j] += fabs(g) * bf16_spacing(n) + (round_term ? bf16_spacing(term) : 0.0);
         }
     }
     return 0;

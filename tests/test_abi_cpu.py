@@ -1,0 +1,123 @@
+"""The C ABI without a GPU: libgbnorm.so builds for sm_103a, loads, exports
+every function include/gbnorm.h declares, and rejects invalid arguments
+with the documented status before touching a device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbnorm.h")
+
+GBN_OK, GBN_EINVAL, GBN_EDTYPE, GBN_EWORKSPACE, GBN_ELAUNCH, GBN_EDEVICE = range(6)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from normalization_layers_fwd_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|void)\s*\**\s*(\w+)\s*\(", text,
+                      flags=re.M)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    assert {"dyt_fwd", "dyt_bwd", "layernorm_fwd", "layernorm_bwd", "rmsnorm_fwd", "rmsnorm_bwd",
+            "gbn_bwd_workspace_bytes", "gbn_status_string"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from normalization_layers_fwd_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_binding_signatures_cover_the_header():
+    from normalization_layers_fwd_gb300 import _lib
+    assert set(declared_functions()) == set(_lib.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.gbn_status_string(s).startswith(b"GBN_")
+    assert lib.gbn_status_string(99) == b"GBN_UNKNOWN"
+
+
+def test_invalid_arguments_are_rejected_before_any_device_use(lib):
+    p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    # bad dtype codes
+    assert lib.dyt_fwd(p, p, p, p, p, 4, 8, 7, 0, None) == GBN_EDTYPE
+    assert lib.rmsnorm_fwd(p, p, p, None, 4, 8, 1e-6, 1, 9, None) == GBN_EDTYPE
+    # bad shapes
+    assert lib.dyt_fwd(p, p, p, p, p, -1, 8, 1, 0, None) == GBN_EINVAL
+    assert lib.dyt_fwd(p, p, p, p, p, 4, 0, 1, 0, None) == GBN_EINVAL
+    assert lib.dyt_fwd(p, p, p, p, p, 4, 1 << 31, 1, 0, None) == GBN_EINVAL
+    assert lib.layernorm_fwd(p, None, None, p, None, None, 1 << 62, 1 << 20, 1e-5, 1, 0,
+                             None) == GBN_EINVAL
+    # required pointers
+    assert lib.dyt_fwd(p, None, p, p, p, 4, 8, 1, 0, None) == GBN_EINVAL
+    assert lib.dyt_fwd(None, p, p, p, p, 4, 8, 1, 0, None) == GBN_EINVAL
+    assert lib.rmsnorm_fwd(p, None, p, None, 4, 8, 1e-6, 1, 1, None) == GBN_EINVAL
+    assert lib.layernorm_bwd(p, p, None, p, None, p, None, None, 4, 8, 1, 0, None, 0,
+                             None) == GBN_EINVAL
+    # eps must be finite and >= 0
+    assert lib.layernorm_fwd(p, None, None, p, None, None, 4, 8, float("nan"), 1, 0,
+                             None) == GBN_EINVAL
+    assert lib.rmsnorm_fwd(p, p, p, None, 4, 8, -1.0, 1, 1, None) == GBN_EINVAL
+    # pointers must be aligned to their element size
+    odd = ctypes.c_void_p(17)
+    assert lib.dyt_fwd(odd, p, p, p, p, 4, 8, 1, 0, None) == GBN_EINVAL
+    assert lib.dyt_fwd(p, ctypes.c_void_p(18), p, p, p, 4, 8, 1, 0, None) == GBN_EINVAL
+    assert lib.rmsnorm_fwd(p, p, p, ctypes.c_void_p(18), 4, 8, 1e-6, 1, 1, None) == GBN_EINVAL
+    # misaligned workspace
+    assert lib.dyt_bwd(p, p, p, p, p, p, p, p, 4, 8, 1, 0, ctypes.c_void_p(18), 1 << 20,
+                       None) == GBN_EINVAL
+
+
+def test_empty_forward_is_a_noop_without_device(lib):
+    p = ctypes.c_void_p(16)
+    assert lib.dyt_fwd(None, p, p, p, None, 0, 8, 1, 0, None) == GBN_OK
+    assert lib.layernorm_fwd(None, None, None, None, None, None, 0, 8, 1e-5, 1, 0, None) == GBN_OK
+    assert lib.rmsnorm_fwd(None, p, None, None, 0, 8, 1e-6, 1, 1, None) == GBN_OK
+
+
+def test_valid_call_without_a_device_reports_edevice(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    p = ctypes.c_void_p(16)
+    assert lib.dyt_fwd(p, p, p, p, p, 4, 8, 1, 0, None) == GBN_EDEVICE
+
+
+def test_workspace_query(lib):
+    from normalization_layers_fwd_gb300._lib import SIZE_MAX
+    assert lib.gbn_bwd_workspace_bytes(5, 10, 10, 1, 0, 0) == SIZE_MAX
+    assert lib.gbn_bwd_workspace_bytes(0, 10, 10, 3, 0, 0) == SIZE_MAX
+    assert lib.gbn_bwd_workspace_bytes(0, -1, 10, 1, 0, 0) == SIZE_MAX
+    assert lib.gbn_bwd_workspace_bytes(0, 0, 10, 1, 0, 0) == 0
+
+
+def test_missing_library_fails_loudly():
+    from normalization_layers_fwd_gb300 import _lib
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _lib.load("/nonexistent/libgbnorm.so")
+
+
+def test_binding_rejects_host_tensors():
+    import torch
+    from normalization_layers_fwd_gb300 import _lib
+    x = torch.zeros(4, 8)
+    with pytest.raises(ValueError):
+        _lib.rmsnorm_fwd(x, torch.ones(8))

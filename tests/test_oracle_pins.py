@@ -341,7 +341,7 @@ def test_rms_width_one(O):
     y, *_ = O.rms_fwd(x, eps, w, O.MATH)
     np.testing.assert_allclose(y[:, 0], w[0] * x[:, 0] / np.sqrt(x[:, 0] ** 2 + eps), rtol=1e-15)
     dy = np.array([[0.7], [-1.1], [2.0], [1.0], [-0.4]])
-    dx, *_ = O.rms_bwd_rows(x, dy, eps, w, O.MATH)
+    dx, *_ = O.rms_bwd_rows(x, dy, eps, w, O.F32, O.MATH)
     dn = dy[:, 0] * w[0]
     want = dn * eps / (x[:, 0] ** 2 + eps) ** 1.5  # the page's closed form
     np.testing.assert_allclose(dx[:, 0], want, rtol=1e-14)
@@ -352,13 +352,13 @@ def test_rms_bwd_closed_form_and_fd(O):
     M, N = 3, 7
     x = rng.standard_normal((M, N)); dy = rng.standard_normal((M, N))
     w = 1 + 0.2 * rng.standard_normal(N); eps = 0.2
-    dx, *_ = O.rms_bwd_rows(x, dy, eps, w, O.MATH)
+    dx, *_ = O.rms_bwd_rows(x, dy, eps, w, O.F32, O.MATH)
     ms = (x * x).mean(axis=1); r = 1 / np.sqrt(ms + eps)
     dn = dy * w
     lhs = (dx * x).sum(axis=1)
     rhs = eps * r * r * (dn * x * r[:, None]).sum(axis=1)
     np.testing.assert_allclose(lhs, rhs, rtol=1e-12, atol=1e-14)
-    dw, _ = O.rms_bwd_cols(x, dy, eps, O.F32, O.MATH)
+    dw, *_ = O.rms_bwd_cols(x, dy, eps, O.F32, O.MATH)
 
     def L(xx, ww):
         y, *_ = O.rms_fwd(xx, eps, ww, O.MATH)
@@ -398,15 +398,15 @@ def test_rms_parity_rounding_points(O):
     # dw: with a bf16 weight each term dy*n is rounded; with unit dy the term
     # is n itself, already a bf16 value, so both weight dtypes agree
     ones = np.full_like(bf, 0x3F80)  # bf16 1.0
-    d_b, _ = O.rms_bwd_cols(bf, ones, eps, O.BF16, O.PARITY)
-    d_f, _ = O.rms_bwd_cols(bf, ones, eps, O.F32, O.PARITY)
+    d_b, *_ = O.rms_bwd_cols(bf, ones, eps, O.BF16, O.PARITY)
+    d_f, *_ = O.rms_bwd_cols(bf, ones, eps, O.F32, O.PARITY)
     np.testing.assert_array_equal(d_b, d_f)
     np.testing.assert_allclose(d_b, y.sum(axis=0), rtol=1e-15)
     # a dy with a 3-bit significand times n (8 bits) needs 11 bits: the bf16
     # weight path rounds each term, the float32 weight path does not
     three = np.full_like(bf, 0x3FE0)  # bf16 1.75
-    t_b, _ = O.rms_bwd_cols(bf, three, eps, O.BF16, O.PARITY)
-    t_f, _ = O.rms_bwd_cols(bf, three, eps, O.F32, O.PARITY)
+    t_b, *_ = O.rms_bwd_cols(bf, three, eps, O.BF16, O.PARITY)
+    t_f, *_ = O.rms_bwd_cols(bf, three, eps, O.F32, O.PARITY)
     np.testing.assert_allclose(t_f, 1.75 * y.sum(axis=0), rtol=1e-15)
     np.testing.assert_allclose(t_b, O.round_bf16_array(1.75 * y).sum(axis=0), rtol=1e-15)
     assert not np.array_equal(t_b, t_f)
@@ -416,6 +416,31 @@ def test_rms_padding_rows(O):
     rng = np.random.default_rng(23)
     x = rng.standard_normal((9, 6)); dy = rng.standard_normal((9, 6))
     xp = np.vstack([x, rng.standard_normal((4, 6))]); dyp = np.vstack([dy, np.zeros((4, 6))])
-    a, _ = O.rms_bwd_cols(x, dy, 1e-6, O.F32, O.MATH)
-    b, _ = O.rms_bwd_cols(xp, dyp, 1e-6, O.F32, O.MATH)
+    a, *_ = O.rms_bwd_cols(x, dy, 1e-6, O.F32, O.MATH)
+    b, *_ = O.rms_bwd_cols(xp, dyp, 1e-6, O.F32, O.MATH)
     np.testing.assert_array_equal(a, b)
+
+
+def test_rms_near_tie_allowance(O):
+    # The allowance is nonzero exactly where the normalized value sits within
+    # 2^-17 (relative) of a bfloat16 midpoint, and equals |w| times the
+    # bfloat16 spacing there.
+    rng = np.random.default_rng(24)
+    x32 = rng.standard_normal((400, 64)).astype(np.float32)
+    bf = (x32.view(np.uint32) >> 16).astype(np.uint16)
+    xv = (bf.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    w = 1 + 0.1 * rng.standard_normal(64)
+    _, _, rs, allow = O.rms_fwd(bf, 1e-6, w, O.PARITY)
+    v = xv * rs[:, None]
+    tie = np.vectorize(O.bf16_near_tie)(v)
+    assert tie.sum() > 0
+    np.testing.assert_array_equal(allow > 0, tie)
+    a = np.abs(v[tie])
+    spacing = 2.0 ** (np.floor(np.log2(a)) - 7)
+    np.testing.assert_allclose(allow[tie], np.abs(np.broadcast_to(w, v.shape)[tie]) * spacing, rtol=0)
+    # a bfloat16 weight makes dy*w exact in float32: no dn allowance
+    dy = bf[::-1].copy()
+    _, _, al_b = O.rms_bwd_rows(bf, dy, 1e-6, w, O.BF16, O.PARITY)
+    assert np.all(al_b == 0)
+    _, _, al_f = O.rms_bwd_rows(bf, dy, 1e-6, w, O.F32, O.PARITY)
+    assert np.any(al_f > 0)

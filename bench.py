@@ -129,6 +129,21 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest `value` over all ranks (the slowest replica's step time)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """Whole-job GB/s: every replica moves the same bytes per step; the job
+    takes as long as its slowest rank."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------ workloads
 
 def alg_bytes(op, direction, M, N, sx, sp):
@@ -220,11 +235,13 @@ class Point:
         return f"{self.wl.op}_{d}[{self.wl.M}x{self.wl.N}]"
 
 
-def workloads(name):
+def workloads(name, ops=None, widths=None):
     from normalization_layers_fwd_gb300 import synth
     if name == "sweep":
-        return synth.sweep_all(), ("sweep: DyT, LayerNorm, RMSNorm fwd+bwd, bf16 x, fp32 params, "
-                                   "N in {16..8192}, M = 2^28 // N")
+        pts = [w for w in synth.sweep_all()
+               if (not ops or w.op in ops) and (not widths or w.N in widths)]
+        return pts, ("sweep: DyT, LayerNorm, RMSNorm fwd+bwd, bf16 x, fp32 params, "
+                     "N in {16..8192}, M = 2^28 // N")
     table = {w.name: w for w in (synth.DYT_F32_SMALL, synth.LN_BWD_TALL, synth.DYT_BF16_TALL,
                                  synth.RMS_BF16)}
     if name not in table:
@@ -264,7 +281,9 @@ def run_ours(args, rank, world, dev):
     from normalization_layers_fwd_gb300 import _lib, build
     build.build()
     lib = _lib.load()
-    wls, wdesc = workloads(args.workload)
+    wls, wdesc = workloads(args.workload, args.ops, args.widths)
+    if args.ops or args.widths:
+        wdesc += f" (subset: ops={args.ops}, widths={args.widths})"
     maxE = max(w.M * w.N for w in wls)
     maxM = max(w.M for w in wls)
     dtype = wls[0].xdtype
@@ -350,15 +369,11 @@ def run_ours(args, rank, world, dev):
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
-    ms_step = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / args.steps, dev)
 
     step_bytes = sum(p.step_bytes() for p in points)
     rows = sum(p.wl.M for p in points)
-    gbs = step_bytes * world / (ms_step * 1e-3) / 1e9
+    gbs = job_throughput(step_bytes, world, ms_step)
     peak, peak_kind = measured_peak()
     dom_bytes = dom_point.bytes[dom_dir]
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
@@ -371,7 +386,7 @@ def run_ours(args, rank, world, dev):
                           "gbs": round(b / (ms * 1e-3) / 1e9, 1),
                           "frac_measured": round(b / (ms * 1e-3) / 1e9 / peak, 3)})
 
-    e2e = run_e2e(lib, points, dev, shared, min(args.steps, 3), world)
+    e2e = None if args.no_e2e else run_e2e(lib, points, dev, shared, min(args.steps, 3), world)
     line = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -488,7 +503,7 @@ def oracle_sample(wls, target_elems):
 
 
 def run_reference(args, rank, world):
-    wls, wdesc = workloads(args.workload)
+    wls, wdesc = workloads(args.workload, args.ops, args.widths)
     target = args.ref_elems
     vals = []
     for i in range(args.warmup + args.steps):
@@ -522,9 +537,14 @@ def main():
     ap.add_argument("--workload", default="sweep")
     ap.add_argument("--ref-elems", type=int, default=1 << 22,
                     help="elements per step of the CPU oracle sample")
-    ap.add_argument("--cpu-baseline-elems", type=int, default=1 << 25,
+    ap.add_argument("--cpu-baseline-elems", type=int, default=1 << 28,
                     help="elements of the CPU oracle sample reported as cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ops", type=lambda v: v.split(","), default=None,
+                    help="restrict the sweep to these layers (profiling runs)")
+    ap.add_argument("--widths", type=lambda v: [int(x) for x in v.split(",")], default=None,
+                    help="restrict the sweep to these widths (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -544,7 +564,8 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     line = run_ours(args, rank, world, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        b, s, desc = oracle_sample(workloads(args.workload)[0], args.cpu_baseline_elems)
+        b, s, desc = oracle_sample(workloads(args.workload, args.ops, args.widths)[0],
+                                   args.cpu_baseline_elems)
         line["cpu_baseline"] = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1,
                                 "kind": "oracle", "sample": desc,
                                 "seconds": round(s, 2)}

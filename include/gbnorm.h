@@ -83,6 +83,23 @@ const char* gbn_status_string(int status);
  * on invalid arguments or when the device cannot be queried. */
 size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int device);
 
+/* Fault word of the current device: bit 0 (GBN_FAULT_WAIT_TIMEOUT) is set
+ * when a kernel's bounded shared-memory barrier wait ran out (about one
+ * second); that kernel then finished without further loads or stores and its
+ * outputs are not valid.  Copies the word to host memory *out (this call
+ * synchronizes with the device) and zeroes it when `clear` is nonzero.  No
+ * counterpart on the pages: it reports the safety bound of the bulk-copy
+ * pipeline. */
+#define GBN_FAULT_WAIT_TIMEOUT 1u
+int gbn_read_faults(unsigned* out, int clear);
+
+/* Self-test of the bounded wait: launches one CTA on `stream` whose barrier
+ * never completes, with a wait limit of `limit_cycles` SM clock cycles
+ * (1..2^32).  The kernel must give up, set GBN_FAULT_WAIT_TIMEOUT and write 0
+ * to *result_device (an int in device memory; 1 would mean the wait
+ * completed).  No counterpart on the pages. */
+int gbn_selftest_wait_timeout(long long limit_cycles, int* result_device, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- DyT
  * dyt_fwd: y[i,j] = gamma[j] * tanh(alpha[0] * x[i,j]) + beta[j].
  *   x, y [M,N] xt; alpha [1], gamma [N], beta [N] pt (all required).

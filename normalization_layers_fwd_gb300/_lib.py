@@ -29,6 +29,8 @@ _P, _I64, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_
 SIGNATURES = {
     "gbn_status_string": ([_I], ctypes.c_char_p),
     "gbn_bwd_workspace_bytes": ([_I, _I64, _I64, _I, _I, _I], _SZ),
+    "gbn_read_faults": ([ctypes.POINTER(ctypes.c_uint), _I], _I),
+    "gbn_selftest_wait_timeout": ([ctypes.c_longlong, _P, _P], _I),
     "dyt_fwd": ([_P, _P, _P, _P, _P, _I64, _I64, _I, _I, _P], _I),
     "dyt_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _I, _P, _SZ, _P], _I),
     "layernorm_fwd": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P], _I),
@@ -133,6 +135,13 @@ def workspace(op: int, M: int, N: int, xt: int, pt: int, device: torch.device):
         buf = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
         _ws_cache[key] = buf
     return buf, n
+
+
+def read_faults(clear: bool = True) -> int:
+    """The current device's fault word (synchronizes); 0 when healthy."""
+    v = ctypes.c_uint(0)
+    _check(load().gbn_read_faults(ctypes.byref(v), int(clear)), "gbn_read_faults")
+    return v.value
 
 
 # ---------------------------------------------------------------------- DyT

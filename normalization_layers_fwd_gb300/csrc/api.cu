@@ -17,6 +17,12 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];  // 0 = not yet queried
 
+// Fault word: bit 0 = a kernel's bounded barrier wait ran out (the kernel then
+// finished without loading or storing; its outputs are not valid).  One per
+// device (a __device__ variable), read and cleared by gbn_read_faults().
+__device__ unsigned int g_fault_word;
+std::atomic<unsigned*> g_fault_ptr[kMaxDevices];
+
 int sm_count(int device)
 {
     if (device < 0 || device >= kMaxDevices) return -1;
@@ -30,14 +36,33 @@ int sm_count(int device)
     return v;
 }
 
-int current_sms()
+int current_device()
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
         return -1;
     }
-    return sm_count(dev);
+    return dev;
+}
+
+int current_sms() { return sm_count(current_device()); }
+
+// Device address of the current device's fault word (cached per device).
+unsigned* fault_ptr()
+{
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    unsigned* p = g_fault_ptr[dev].load(std::memory_order_relaxed);
+    if (p) return p;
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_fault_word) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    p = static_cast<unsigned*>(a);
+    g_fault_ptr[dev].store(p, std::memory_order_relaxed);
+    return p;
 }
 
 bool dtype_ok(int t) { return t == gbn::kF32 || t == gbn::kBF16; }
@@ -74,7 +99,7 @@ int fast_sid(int64_t N, int xt)
 }
 
 // The launch layout of one row-wise kernel.  two_streams: the kernel uses the
-// schedule's UB rows per group (backward kernels, LayerNorm forward).
+// schedule's UB rows per group (the backward kernels read x and dy).
 Launch plan(int64_t M, int64_t N, int xt, bool aligned, int sms, cudaStream_t stream,
             bool two_streams)
 {
@@ -87,7 +112,7 @@ Launch plan(int64_t M, int64_t N, int xt, bool aligned, int sms, cudaStream_t st
         L.fast = 1;
         L.sid = sid;
         L.nblocks = (M + rows_per_block - 1) / rows_per_block;
-        const int64_t cap = (int64_t)sms * e.MINB;
+        const int64_t cap = (int64_t)sms * (two_streams ? e.MINBB : e.MINBF);
         L.grid = (int)(L.nblocks < cap ? L.nblocks : cap);
         L.P = L.grid;
     } else {
@@ -129,9 +154,52 @@ int finish_bwd(cudaStream_t s, const float* ws, int64_t P, int op, int64_t N, in
     return launch_status(gbn::launch_colsum(s, ws, P, rowlen, N, pt, o0, o1, o2));
 }
 
+// A one-CTA kernel whose barrier never completes: it expects bytes that no
+// copy delivers, so its bounded wait must run out, record the timeout in the
+// fault word and return.  It exercises the same wait as the ring kernels.
+__global__ void selftest_wait_kernel(unsigned* fault, long long limit, int* result)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        gbn::mbar_init(&bar, 1);
+        gbn::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) gbn::mbar_expect_tx(&bar, 16);  // 16 bytes that never arrive
+    const bool ok = gbn::mbar_wait(&bar, 0, fault, limit);
+    if (threadIdx.x == 0) *result = ok ? 1 : 0;
+}
+
 }  // namespace
 
 extern "C" {
+
+int gbn_read_faults(unsigned* out, int clear)
+{
+    if (!out) return GBN_EINVAL;
+    if (current_device() < 0) return GBN_EDEVICE;
+    if (cudaMemcpyFromSymbol(out, g_fault_word, sizeof(unsigned)) != cudaSuccess) {
+        cudaGetLastError();
+        return GBN_ELAUNCH;
+    }
+    if (clear) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(unsigned)) != cudaSuccess) {
+            cudaGetLastError();
+            return GBN_ELAUNCH;
+        }
+    }
+    return GBN_OK;
+}
+
+int gbn_selftest_wait_timeout(long long limit_cycles, int* result_device, cudaStream_t stream)
+{
+    if (!result_device || limit_cycles <= 0 || limit_cycles > (1LL << 32)) return GBN_EINVAL;
+    unsigned* f = fault_ptr();
+    if (!f) return GBN_EDEVICE;
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(f, limit_cycles, result_device);
+    return launch_status(cudaGetLastError());
+}
 
 const char* gbn_status_string(int status)
 {
@@ -172,6 +240,7 @@ int dyt_fwd(const void* x, const void* alpha, const void* gamma, const void* bet
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, false);
+    if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (!L.fast) {  // elementwise general path: one thread per element, grid-stride
         const int64_t E = M * N;
         const int64_t blocks = (E + gbn::kGenThreads - 1) / gbn::kGenThreads;
@@ -194,8 +263,9 @@ int dyt_bwd(const void* x, const void* dy, const void* alpha, const void* gamma,
     if (grads && ws && !aligned4(ws)) return GBN_EINVAL;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    const Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
                           true);
+    if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_DYT, L, N))) return GBN_EWORKSPACE;
     float* wsf = grads ? static_cast<float*>(ws) : nullptr;
     if (M > 0) {
@@ -220,7 +290,8 @@ int layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, f
     if (M == 0) return GBN_OK;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    const Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, true);
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, false);
+    if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     return launch_status(
         gbn::launch_ln_fwd(L, xt, pt, x, gamma, beta, y, mean, rstd, M, (int)N, eps));
 }
@@ -239,8 +310,9 @@ int layernorm_bwd(const void* x, const void* dy, const float* mean, const float*
     if (grads && ws && !aligned4(ws)) return GBN_EINVAL;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    const Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
                           true);
+    if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_LAYERNORM, L, N)))
         return GBN_EWORKSPACE;
     float* wsf = grads ? static_cast<float*>(ws) : nullptr;
@@ -265,7 +337,8 @@ int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, i
     if (M == 0) return GBN_OK;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    const Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, false);
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, false);
+    if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     return launch_status(gbn::launch_rms_fwd(L, xt, wt, x, w, y, rstd, M, (int)N, eps));
 }
 
@@ -281,8 +354,9 @@ int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd,
     if (dw && ws && !aligned4(ws)) return GBN_EINVAL;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    const Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
                           true);
+    if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (dw && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_RMSNORM, L, N))) return GBN_EWORKSPACE;
     float* wsf = dw ? static_cast<float*>(ws) : nullptr;
     if (M > 0) {

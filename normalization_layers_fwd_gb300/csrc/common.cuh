@@ -18,24 +18,42 @@ enum DType : int { kF32 = 0, kBF16 = 1 };
 // ------------------------------------------------------------------ schedule
 // One row group = W threads, each holding KV 16-byte vectors of a row
 // (capacity W*KV*VEC columns).  A CTA of T threads holds G = T/W groups; each
-// group handles UF (forward kernels that read one tensor) or UB (kernels
-// that read two tensors, and LayerNorm's two-reduction forward) rows per
-// iteration, so a CTA iteration covers G*U rows ("a row block").  MINB CTAs
+// group handles UF (forward kernels, which read one tensor) or UB (backward
+// kernels, which read two) rows per iteration, so a CTA iteration covers
+// G*U rows ("a row block").  MINB CTAs
 // per SM stay resident; the register budget follows from it through
 // __launch_bounds__.  The per-row summation order depends only on (W, KV),
 // never on U, so a forward and a backward with different U reduce a row
 // identically.
 struct SchedEntry {
-    int max_nvec, W, KV, UF, UB, T, MINB;
+    int max_nvec, W, UF, UB, T, MINBF, MINBB;
 };
 
+// One 16-byte vector per thread per row: a row of nvec vectors takes
+// W = next_pow2(nvec) threads, so register pressure stays flat from N = 8
+// to N = 8192 bf16.  Row blocks of T/W * U rows (8-16 KB per staged tensor)
+// stream through a shared-memory ring filled by the bulk-copy engine.
+// MINBF/MINBB: CTAs per SM the forward/backward are sized for (registers
+// through __launch_bounds__, shared memory through the ring size).
 constexpr int kNumSched = 11;
 constexpr SchedEntry kSched[kNumSched] = {
-    {1, 1, 1, 4, 2, 256, 3},     {2, 2, 1, 4, 2, 256, 3},     {4, 4, 1, 4, 2, 256, 3},
-    {8, 8, 1, 4, 2, 256, 3},     {16, 16, 1, 4, 2, 256, 3},   {32, 32, 1, 4, 2, 256, 3},
-    {64, 32, 2, 2, 2, 256, 2},   {128, 64, 2, 2, 2, 256, 2},  {256, 128, 2, 2, 2, 256, 2},
-    {512, 256, 2, 2, 2, 256, 2}, {1024, 512, 2, 1, 1, 512, 1},
+    {1, 1, 2, 2, 256, 4, 3},        {2, 2, 2, 2, 256, 4, 3},       {4, 4, 2, 2, 256, 4, 3},
+    {8, 8, 2, 2, 256, 4, 3},        {16, 16, 2, 2, 256, 4, 3},     {32, 32, 2, 2, 256, 4, 3},
+    {64, 64, 2, 2, 256, 4, 3},      {128, 128, 2, 2, 256, 4, 3},   {256, 256, 2, 2, 256, 4, 3},
+    {512, 512, 1, 1, 512, 2, 2},    {1024, 1024, 1, 1, 1024, 1, 1},
 };
+constexpr int kStages = 4;  // depth of the shared-memory ring
+
+// Bytes of one ring slot for one staged tensor, and of the whole dynamic
+// shared memory a kernel with NT staged tensors needs (barriers first).
+__host__ __device__ constexpr int slot_bytes(int S, bool bwd)
+{
+    return kSched[S].T * (bwd ? kSched[S].UB : kSched[S].UF) * 16;
+}
+__host__ __device__ constexpr int ring_smem_bytes(int S, bool bwd, int NT)
+{
+    return 128 + kStages * NT * slot_bytes(S, bwd);
+}
 constexpr int kMaxFastVec = 1024;
 
 // Threads per CTA and warps per CTA of the general (any width, any
@@ -132,6 +150,174 @@ __device__ __forceinline__ void st_param(void* p, int pt, int64_t j, float v)
         static_cast<__nv_bfloat16*>(p)[j] = __float2bfloat16_rn(v);
 }
 
+// ---------------------------------------------------- bulk-copy ring (TMA)
+// A CTA streams its row blocks through a ring of kStages shared-memory
+// slots.  Thread 0 issues one 1D bulk copy (cp.async.bulk, the Tensor
+// Memory Accelerator's untiled form) per staged tensor per block, with the
+// slot's mbarrier expecting the bytes; every thread waits on the barrier's
+// phase, reads its vectors from shared memory, and after a __syncthreads
+// thread 0 refills the slot kStages blocks ahead.  Every wait is bounded:
+// after kWaitCycles it records kFaultWaitTimeout in the library's fault
+// word and the CTA finishes its remaining iterations without waiting,
+// loading or storing, then waits (bounded again) for its copies in flight.
+
+constexpr long long kWaitCycles = 1LL << 31;  // ~1 s at 2 GHz
+constexpr unsigned kFaultWaitTimeout = 1u;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for a barrier phase; false (and a fault bit) on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* fault,
+                                          long long limit = kWaitCycles)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > limit) {
+            if (fault) atomicOr(fault, kFaultWaitTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// One 16-byte vector from shared memory, re-read at every use: each pass
+// over a row reads the ring slot again rather than keeping the row in
+// registers across the row reductions (volatile, so it is not merged).
+__device__ __forceinline__ uint4 lds128(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+
+__device__ __forceinline__ uint4 lds128_if(bool ok, const unsigned char* p)
+{
+    return ok ? lds128(p) : make_uint4(0, 0, 0, 0);
+}
+
+// The ring of one CTA.  NT staged tensors, each row `row_bytes` long; row
+// block b covers rows [b*R, min(b*R + R, M)).  Blocks b = blockIdx.x +
+// k*gridDim.x, k = 0..K-1, belong to this CTA.
+template <int NT>
+struct Ring {
+    uint64_t* bar;             // [kStages]
+    unsigned char* buf;        // [kStages][NT][slot]
+    uint32_t slot;             // bytes per tensor per slot
+    const unsigned char* src[NT];
+    int64_t row_bytes, R, M, nblocks;
+    unsigned* fault;
+
+    __device__ int64_t count() const
+    {
+        return nblocks > (int64_t)blockIdx.x ? (nblocks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    }
+    __device__ int64_t block(int64_t k) const { return blockIdx.x + k * (int64_t)gridDim.x; }
+    __device__ const unsigned char* tile(int64_t k, int t) const
+    {
+        return buf + ((k % kStages) * NT + t) * (size_t)slot;
+    }
+    // thread 0 only
+    __device__ void issue(int64_t k)
+    {
+        const int s = (int)(k % kStages);
+        const int64_t r0 = block(k) * R;
+        const int64_t rows = (M - r0) < R ? (M - r0) : R;
+        const uint32_t bytes = (uint32_t)(rows * row_bytes);
+        mbar_expect_tx(&bar[s], NT * bytes);
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            bulk_g2s(buf + (s * NT + t) * (size_t)slot, src[t] + r0 * row_bytes, bytes, &bar[s]);
+    }
+};
+
+// Run `body(b, k, alive)` over this CTA's row blocks with the ring full
+// kStages deep.  `dsm` is the kernel's dynamic shared memory (128-byte
+// aligned).  Every thread makes the same calls (body may __syncthreads).
+template <int NT, class Body>
+__device__ __forceinline__ void ring_loop(Ring<NT>& rg, unsigned char* dsm, Body&& body)
+{
+    rg.bar = reinterpret_cast<uint64_t*>(dsm);
+    rg.buf = dsm + 128;
+    const int64_t K = rg.count();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&rg.bar[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (int64_t k = 0; k < K && k < kStages; ++k) rg.issue(k);
+    bool alive = true;
+    int64_t failed_at = K;
+    for (int64_t k = 0; k < K; ++k) {
+        if (alive) {
+            alive = mbar_wait(&rg.bar[k % kStages], (uint32_t)((k / kStages) & 1), rg.fault);
+            if (!alive) failed_at = k;
+        }
+        body(rg.block(k), k, alive);
+        __syncthreads();  // every thread is done with slot k % kStages
+        if (threadIdx.x == 0 && alive && k + kStages < K) {
+            fence_proxy_async();
+            rg.issue(k + kStages);
+        }
+    }
+    if (!alive) {  // wait, bounded, for copies this thread may have in flight
+        for (int64_t k = failed_at; k < K && k < failed_at + kStages; ++k)
+            mbar_wait(&rg.bar[k % kStages], (uint32_t)((k / kStages) & 1), nullptr, kWaitCycles);
+    }
+    __syncthreads();
+}
+
 // ---------------------------------------------------------------- reductions
 // Sum across the 32 lanes of a warp by an xor butterfly.  Every lane ends
 // with the same bits: at each step a lane adds the same two partial sums as
@@ -152,14 +338,17 @@ template <int W, int T, int NV>
 struct GroupRed {
     static constexpr int kWarps = W / 32;
     static constexpr int kG = T / W;
-    static constexpr int kFloats = (W > 32) ? 2 * kG * kWarps * NV : 1;
+    static constexpr int kFloats = (W > 32) ? 2 * kG * NV * 32 : 1;
 };
 
 // All-reduce NV values over the W threads of a row group.  W <= 32: the
 // group is an aligned slice of a warp and the butterfly stays inside it.
-// W > 32: butterfly per warp, then every thread sums the warps' results in
-// warp order from a double-buffered shared slot (one __syncthreads per call;
-// every thread of the CTA must make the same sequence of calls).
+// W > 32: butterfly per warp; lane 0 of each warp stores its partial into a
+// double-buffered shared slot (one __syncthreads per call); then lane l of
+// every warp loads partial (l mod kWarps) and each aligned run of kWarps
+// lanes runs the same butterfly over the same values in the same positions,
+// so every thread ends with identical bits.  Every thread of the CTA must
+// make the same sequence of calls.
 template <int W, int T, int NV>
 __device__ __forceinline__ void group_allreduce(float (&v)[NV], float* red, int& parity)
 {
@@ -168,23 +357,20 @@ __device__ __forceinline__ void group_allreduce(float (&v)[NV], float* red, int&
     } else {
         constexpr int kWarps = W / 32;
         constexpr int kG = T / W;
+        static_assert(kWarps <= 32, "a row group spans at most 32 warps");
         butterfly<32, NV>(v);
         const int lane = threadIdx.x & 31;
         const int g = threadIdx.x / W;
         const int wig = (threadIdx.x % W) >> 5;
-        float* slot = red + (parity * kG + g) * kWarps * NV;
+        float* slot = red + (parity * kG + g) * NV * 32;  // [NV][32]
         if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < NV; ++k) slot[wig * NV + k] = v[k];
+            for (int k = 0; k < NV; ++k) slot[k * 32 + wig] = v[k];
         }
         __syncthreads();
 #pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            float s = slot[k];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) s += slot[w * NV + k];
-            v[k] = s;
-        }
+        for (int k = 0; k < NV; ++k) v[k] = slot[k * 32 + (lane & (kWarps - 1))];
+        butterfly<kWarps, NV>(v);
         parity ^= 1;
     }
 }
@@ -209,30 +395,27 @@ __device__ __forceinline__ float cta_sum(float v, float* red /* >= T/32 floats *
 }
 
 // Write the CTA's per-column partial sums of one quantity to its workspace
-// row.  acc holds, for this thread, columns (kv*W + l)*VEC + e.  With more
-// than one group per CTA the groups' values are summed in group order
-// through shared memory (buf: G*W*KV*VEC floats); one group writes directly.
-template <int W, int KV, int VEC, int T>
-__device__ __forceinline__ void cta_store_columns(const float (&acc)[KV][VEC], float* buf,
+// row.  acc holds, for this thread, columns l*VEC + e (l = lane in its row
+// group).  With more than one group per CTA the groups' values are summed in
+// group order through shared memory (buf: T*VEC floats); a single group
+// writes directly.
+template <int W, int VEC, int T>
+__device__ __forceinline__ void cta_store_columns(const float (&acc)[VEC], float* buf,
                                                   float* __restrict__ out_row, int N)
 {
     constexpr int kG = T / W;
-    constexpr int kCap = W * KV * VEC;
+    constexpr int kCap = W * VEC;
     const int g = threadIdx.x / W;
     const int l = threadIdx.x % W;
     if constexpr (kG == 1) {
 #pragma unroll
-        for (int kv = 0; kv < KV; ++kv)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const int c = (kv * W + l) * VEC + e;
-                if (c < N) out_row[c] = acc[kv][e];
-            }
+        for (int e = 0; e < VEC; ++e) {
+            const int c = l * VEC + e;
+            if (c < N) out_row[c] = acc[e];
+        }
     } else {
 #pragma unroll
-        for (int kv = 0; kv < KV; ++kv)
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) buf[g * kCap + (kv * W + l) * VEC + e] = acc[kv][e];
+        for (int e = 0; e < VEC; ++e) buf[g * kCap + l * VEC + e] = acc[e];
         __syncthreads();
         for (int c = threadIdx.x; c < kCap && c < N; c += T) {
             float s = buf[c];

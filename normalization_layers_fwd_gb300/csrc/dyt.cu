@@ -17,6 +17,8 @@
 //  * parameter gradients in the parameters' dtype, y and dx in x's dtype.
 // The backward writes one partial row per CTA ([dgamma | dbeta | dalpha],
 // fp32, every row written each launch); colsum.cu reduces the rows.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -38,12 +40,12 @@ __device__ __forceinline__ float rcp_approx(float v)
 }
 
 // tanh and sech^2 in float32, from two identities:
-//  * |z| >= 1/8: with e = exp(-2|z|) = 2^(-2 |z| log2(e)),
+//  * with e = exp(-2|z|) = 2^(-2 |z| log2(e)) (hardware ex2):
 //      tanh|z| = (1 - e) / (1 + e),  sech^2 z = 4e / (1 + e)^2;
-//    neither loses relative accuracy for large |z| (no 1 - tanh^2).
-//  * |z| < 1/8: the Maclaurin series tanh z = z - z^3/3 + 2z^5/15 - 17z^7/315
-//    (the next term is below 2e-10 relative), where (1 - e) would cancel;
-//    there sech^2 = 1 - tanh^2 is at least 63/64 and exact enough.
+//    sech^2 keeps full relative accuracy for every z this way (no
+//    1 - tanh^2 cancellation), so it needs no second branch;
+//  * |z| < 1/8: 1 - e cancels, so tanh takes the Maclaurin series
+//    z - z^3/3 + 2z^5/15 - 17z^7/315 (the next term is below 2e-10 relative).
 // z = +-inf gives tanh = +-1 and sech^2 = 0; NaN propagates.
 constexpr float kM2Log2e = -2.0f * 1.44269504088896340736f;
 constexpr float kSmall = 0.125f;
@@ -68,154 +70,150 @@ __device__ __forceinline__ void dyt_tanh_sech2(float z, float& t, float& s)
     const float a = fabsf(z);
     const float e = ex2_approx(a * kM2Log2e);
     const float q = rcp_approx(1.0f + e);
-    const float ts = tanh_series(z);
-    const bool small = a < kSmall;
-    t = small ? ts : copysignf((1.0f - e) * q, z);
-    s = small ? fmaf(-ts, ts, 1.0f) : 4.0f * e * q * q;
+    t = a < kSmall ? tanh_series(z) : copysignf((1.0f - e) * q, z);
+    s = (4.0f * e) * (q * q);
 }
 
 // ------------------------------------------------------------ fast forward
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINB)
+__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
     dyt_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ alpha,
                  const void* __restrict__ gamma, const void* __restrict__ beta, int pt,
-                 int64_t M, int N, int64_t nblocks)
+                 int64_t M, int N, int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, KV = kSched[S].KV, U = kSched[S].UF, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kSched[S].UF, T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN;
     constexpr int G = T / W;
+    extern __shared__ __align__(128) unsigned char dsm[];
     const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const int nvec = N / VEC;
+    const bool colok = l < N / VEC;
+    const int64_t rb = (int64_t)N * sizeof(TX);
 
     const float a = ld_param(alpha, pt, 0);
-    float gm[KV][VEC], bt[KV][VEC];
+    float gm[VEC], bt[VEC];
 #pragma unroll
-    for (int kv = 0; kv < KV; ++kv) {
-        const int cv = kv * W + l;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            const bool ok = cv < nvec;
-            gm[kv][e] = ok ? ld_param(gamma, pt, cv * VEC + e) : 0.f;
-            bt[kv][e] = ok ? ld_param(beta, pt, cv * VEC + e) : 0.f;
-        }
+    for (int e = 0; e < VEC; ++e) {
+        gm[e] = colok ? ld_param(gamma, pt, l * VEC + e) : 0.f;
+        bt[e] = colok ? ld_param(beta, pt, l * VEC + e) : 0.f;
     }
 
-    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
-        uint4 r[U][KV];
-        int64_t row[U];
+    Ring<1> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.row_bytes = rb;
+    rg.R = G * U;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = slot_bytes(S, false);
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        const unsigned char* tx = rg.tile(k, 0);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            row[u] = b * (G * U) + u * G + g;
-#pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
-                if (row[u] < M && cv < nvec)
-                    r[u][kv] = ld_stream(x + row[u] * N + cv * VEC);
-                else
-                    r[u][kv] = make_uint4(0, 0, 0, 0);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-#pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
+            const int lr = u * G + g;
+            const int64_t row = b * (G * U) + lr;
+            if (alive && colok && row < M) {
                 float f[VEC];
-                unpack(r[u][kv], f);
+                unpack(lds128(tx + lr * rb + l * 16), f);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) f[e] = fmaf(gm[kv][e], dyt_tanh(a * f[e]), bt[kv][e]);
-                if (row[u] < M && cv < nvec) st_stream(y + row[u] * N + cv * VEC, pack(f));
+                for (int e = 0; e < VEC; ++e) f[e] = fmaf(gm[e], dyt_tanh(a * f[e]), bt[e]);
+                st_stream(y + row * N + l * VEC, pack(f));
             }
         }
-    }
+    });
 }
 
 // ----------------------------------------------------------- fast backward
+// x and dy stream through the ring.  Full row blocks run without masking;
+// only the ragged last block masks its padded rows, by a select after the
+// arithmetic (its slots past the last row hold stale data).
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINB)
+__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
     dyt_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy, TX* __restrict__ dx,
                  const void* __restrict__ alpha, const void* __restrict__ gamma, int pt,
-                 float* __restrict__ ws, int64_t M, int N, int64_t nblocks)
+                 float* __restrict__ ws, int64_t M, int N, int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, KV = kSched[S].KV, U = kSched[S].UB, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kSched[S].UB, T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN;
     constexpr int G = T / W;
-    __shared__ float colbuf[G > 1 ? T * KV * VEC : 1];
+    extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[T / 32];
     const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const int nvec = N / VEC;
+    const bool colok = l < N / VEC;
+    const int64_t rb = (int64_t)N * sizeof(TX);
 
     const float a = ld_param(alpha, pt, 0);
-    float gm[KV][VEC], ga[KV][VEC];
+    float gm[VEC], ga[VEC];
 #pragma unroll
-    for (int kv = 0; kv < KV; ++kv) {
-        const int cv = kv * W + l;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            gm[kv][e] = cv < nvec ? ld_param(gamma, pt, cv * VEC + e) : 0.f;
-            ga[kv][e] = gm[kv][e] * a;
-        }
+    for (int e = 0; e < VEC; ++e) {
+        gm[e] = colok ? ld_param(gamma, pt, l * VEC + e) : 0.f;
+        ga[e] = gm[e] * a;
     }
     // Per-column accumulators: sum dy*t, sum dy, sum dy*x*sech^2 (gamma is
     // applied to the last one once, at the end).
-    float acc_g[KV][VEC], acc_b[KV][VEC], acc_a[KV][VEC];
+    float acc_g[VEC], acc_b[VEC], acc_a[VEC];
 #pragma unroll
-    for (int kv = 0; kv < KV; ++kv)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) acc_g[kv][e] = acc_b[kv][e] = acc_a[kv][e] = 0.f;
+    for (int e = 0; e < VEC; ++e) acc_g[e] = acc_b[e] = acc_a[e] = 0.f;
 
-    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
-        uint4 rx[U][KV], rd[U][KV];
-        int64_t row[U];
+    auto rows = [&](int64_t b, const unsigned char* tx, const unsigned char* td, bool alive,
+                    auto masked) {
+        constexpr bool kMask = decltype(masked)::value;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            row[u] = b * (G * U) + u * G + g;
+            const int lr = u * G + g;
+            const int64_t row = b * (G * U) + lr;
+            const bool okr = !kMask || row < M;
+            if (!alive || !colok) continue;
+            float xf[VEC], df[VEC], o[VEC];
+            unpack(lds128(tx + lr * rb + l * 16), xf);
+            unpack(lds128(td + lr * rb + l * 16), df);
 #pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
-                if (row[u] < M && cv < nvec) {
-                    rx[u][kv] = ld_stream(x + row[u] * N + cv * VEC);
-                    rd[u][kv] = ld_stream(dy + row[u] * N + cv * VEC);
+            for (int e = 0; e < VEC; ++e) {
+                float t, s;
+                dyt_tanh_sech2(a * xf[e], t, s);
+                const float ds = df[e] * s;
+                o[e] = ds * ga[e];
+                if constexpr (kMask) {
+                    // padded rows: select after the arithmetic, never a 0/1 multiply
+                    acc_g[e] += okr ? df[e] * t : 0.f;
+                    acc_b[e] += okr ? df[e] : 0.f;
+                    acc_a[e] += okr ? ds * xf[e] : 0.f;
                 } else {
-                    rx[u][kv] = rd[u][kv] = make_uint4(0, 0, 0, 0);
+                    acc_g[e] = fmaf(df[e], t, acc_g[e]);
+                    acc_b[e] += df[e];
+                    acc_a[e] = fmaf(ds, xf[e], acc_a[e]);
                 }
             }
+            if (okr) st_stream(dx + row * N + l * VEC, pack(o));
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-#pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
-                const bool ok = row[u] < M && cv < nvec;
-                float xf[VEC], df[VEC], o[VEC];
-                unpack(rx[u][kv], xf);
-                unpack(rd[u][kv], df);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    float t, s;
-                    dyt_tanh_sech2(a * xf[e], t, s);
-                    const float ds = df[e] * s;
-                    o[e] = ds * ga[kv][e];
-                    // mask after the arithmetic: select, never multiply by 0/1
-                    acc_g[kv][e] += ok ? df[e] * t : 0.f;
-                    acc_b[kv][e] += ok ? df[e] : 0.f;
-                    acc_a[kv][e] += ok ? ds * xf[e] : 0.f;
-                }
-                if (ok) st_stream(dx + row[u] * N + cv * VEC, pack(o));
-            }
-        }
-    }
+    };
+
+    Ring<2> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
+    rg.row_bytes = rb;
+    rg.R = G * U;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = slot_bytes(S, true);
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        if ((b + 1) * (G * U) <= M)
+            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::false_type{});
+        else
+            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::true_type{});
+    });
 
     if (ws == nullptr) return;  // no parameter gradient requested (uniform)
     const int64_t L = 2 * (int64_t)N + 1;
     float* wrow = ws + blockIdx.x * L;
-    cta_store_columns<W, KV, VEC, T>(acc_g, colbuf, wrow, N);
-    cta_store_columns<W, KV, VEC, T>(acc_b, colbuf, wrow + N, N);
+    float* colbuf = reinterpret_cast<float*>(dsm + 128);  // drained ring slots, past the barriers
+    cta_store_columns<W, VEC, T>(acc_g, colbuf, wrow, N);
+    cta_store_columns<W, VEC, T>(acc_b, colbuf, wrow + N, N);
+    // lanes past the row's end hold garbage (tanh(alpha*0) for alpha = inf);
+    // they are never stored above and are excluded here
     float da = 0.f;
 #pragma unroll
-    for (int kv = 0; kv < KV; ++kv)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) da = fmaf(gm[kv][e], acc_a[kv][e], da);
+    for (int e = 0; e < VEC; ++e) da += colok ? gm[e] * acc_a[e] : 0.f;
     const float tot = cta_sum<T>(da, red);
     if (threadIdx.x == 0) wrow[2 * N] = tot;
 }
@@ -285,12 +283,16 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* alp
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                      \
-    case S:                                                                              \
-        dyt_fwd_fast<TX, S><<<L.grid, kSched[S].T, 0, L.stream>>>(xp, yp, alpha, gamma, \
-                                                                  beta, pt, M, N,       \
-                                                                  L.nblocks);           \
-        break;
+#define GBN_CASE(S)                                                                          \
+    case S: {                                                                                \
+        constexpr int smem = ring_smem_bytes(S, false, 1);                                   \
+        auto kern = dyt_fwd_fast<TX, S>;                                                     \
+        if (smem > 48 * 1024)                                                                \
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, alpha, gamma, beta, pt, M, N, \
+                                                       L.nblocks, L.fault);                  \
+        break;                                                                               \
+    }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
 #undef GBN_CASE
@@ -312,11 +314,16 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                           \
-    case S:                                                                                   \
-        dyt_bwd_fast<TX, S><<<L.grid, kSched[S].T, 0, L.stream>>>(xp, dyp, dxp, alpha, gamma, \
-                                                                  pt, ws, M, N, L.nblocks);  \
-        break;
+#define GBN_CASE(S)                                                                          \
+    case S: {                                                                                \
+        constexpr int smem = ring_smem_bytes(S, true, 2);                                    \
+        auto kern = dyt_bwd_fast<TX, S>;                                                     \
+        if (smem > 48 * 1024)                                                                \
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, dyp, dxp, alpha, gamma, pt, ws, M, \
+                                                       N, L.nblocks, L.fault);               \
+        break;                                                                               \
+    }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
 #undef GBN_CASE

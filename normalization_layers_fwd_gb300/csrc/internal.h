@@ -17,6 +17,7 @@ struct Launch {
     int64_t nblocks;    // row blocks of the fast path
     int64_t P;          // partial rows the backward writes into the workspace
     cudaStream_t stream;
+    unsigned* fault;    // the device's fault word (bounded waits that ran out)
 };
 
 // Workspace row length (floats) per layer: the per-column partial sums of

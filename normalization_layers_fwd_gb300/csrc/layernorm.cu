@@ -12,6 +12,8 @@
 // second summation pass.  Here the column partials are accumulated in
 // registers by the same persistent CTAs that compute dx (x and dy are read
 // once), written as one fp32 row per CTA, and summed by colsum.cu.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -19,203 +21,210 @@ namespace gbn {
 namespace {
 
 // ------------------------------------------------------------ fast forward
+// x streams through the ring; two row all-reduces (sum, then the centred sum
+// of squares) per row.  Every thread runs every row (row reductions are
+// collective); loads and stores are predicated.
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINB)
+__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
     ln_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ gamma,
                 const void* __restrict__ beta, int pt, float* __restrict__ mean,
                 float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
-                int64_t nblocks)
+                int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, KV = kSched[S].KV, U = kSched[S].UB, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kSched[S].UF, T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN;
     constexpr int G = T / W;
+    extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
     int parity = 0;
     const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const int nvec = N / VEC;
+    const bool colok = l < N / VEC;
+    const int64_t rb = (int64_t)N * sizeof(TX);
 
-    float gm[KV][VEC], bt[KV][VEC];
+    float gm[VEC], bt[VEC];
 #pragma unroll
-    for (int kv = 0; kv < KV; ++kv) {
-        const int cv = kv * W + l;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            const bool ok = cv < nvec;
-            gm[kv][e] = (ok && gamma) ? ld_param(gamma, pt, cv * VEC + e) : 1.f;
-            bt[kv][e] = (ok && beta) ? ld_param(beta, pt, cv * VEC + e) : 0.f;
-        }
+    for (int e = 0; e < VEC; ++e) {
+        gm[e] = (colok && gamma) ? ld_param(gamma, pt, l * VEC + e) : 1.f;
+        bt[e] = (colok && beta) ? ld_param(beta, pt, l * VEC + e) : 0.f;
     }
 
-    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
-        uint4 r[U][KV];
-        int64_t row[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            row[u] = b * (G * U) + u * G + g;
-#pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
-                if (row[u] < M && cv < nvec)
-                    r[u][kv] = ld_stream(x + row[u] * N + cv * VEC);
-                else
-                    r[u][kv] = make_uint4(0, 0, 0, 0);
-            }
-        }
-        // pass 1: row sums (absent columns were loaded as zeros)
+    Ring<1> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.row_bytes = rb;
+    rg.R = G * U;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = slot_bytes(S, false);
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        const unsigned char* tx = rg.tile(k, 0);
+        bool ok[U];
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const int lr = u * G + g;
+            ok[u] = alive && colok && b * (G * U) + lr < M;
+            float f[VEC];
+            unpack(lds128_if(ok[u], tx + lr * rb + l * 16), f);
             s[u] = 0.f;
 #pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                float f[VEC];
-                unpack(r[u][kv], f);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) s[u] += f[e];
-            }
+            for (int e = 0; e < VEC; ++e) s[u] += f[e];
         }
         group_allreduce<W, T, U>(s, red, parity);
         float mu[U], q[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             mu[u] = s[u] * inv_n;
-            q[u] = 0.f;
+            float f[VEC], qq = 0.f;
+            unpack(lds128_if(ok[u], tx + (u * G + g) * rb + l * 16), f);
 #pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const bool okc = (kv * W + l) < nvec;
-                float f[VEC];
-                unpack(r[u][kv], f);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float d = f[e] - mu[u];
-                    q[u] += okc ? d * d : 0.f;
-                }
+            for (int e = 0; e < VEC; ++e) {
+                const float d = f[e] - mu[u];
+                qq = fmaf(d, d, qq);
             }
+            q[u] = colok ? qq : 0.f;  // a vector past the row's end adds nothing
         }
-        // pass 2: centred sum of squares
         group_allreduce<W, T, U>(q, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const int lr = u * G + g;
+            const int64_t row = b * (G * U) + lr;
             const float rs = rsqrtf(fmaf(q[u], inv_n, eps));
-#pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
+            if (ok[u]) {
                 float f[VEC];
-                unpack(r[u][kv], f);
+                unpack(lds128(tx + lr * rb + l * 16), f);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) f[e] = fmaf((f[e] - mu[u]) * rs, gm[kv][e], bt[kv][e]);
-                if (row[u] < M && cv < nvec) st_stream(y + row[u] * N + cv * VEC, pack(f));
+                for (int e = 0; e < VEC; ++e) f[e] = fmaf((f[e] - mu[u]) * rs, gm[e], bt[e]);
+                st_stream(y + row * N + l * VEC, pack(f));
             }
-            if (l == 0 && row[u] < M) {
-                if (mean) mean[row[u]] = mu[u];
-                if (rstd) rstd[row[u]] = rs;
+            if (alive && l == 0 && row < M) {
+                if (mean) mean[row] = mu[u];
+                if (rstd) rstd[row] = rs;
             }
         }
-    }
+    });
 }
 
 // ----------------------------------------------------------- fast backward
+// x and dy stream through the ring; the saved mean and rstd of the next row
+// block are prefetched into registers while the current one is processed.
+// Full row blocks run without masking; the ragged last block masks its
+// padded rows by a select after the arithmetic.
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINB)
+__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
     ln_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy,
                 const float* __restrict__ mean, const float* __restrict__ rstd,
                 const void* __restrict__ gamma, int pt, TX* __restrict__ dx,
-                float* __restrict__ ws, int64_t M, int N, float inv_n, int64_t nblocks)
+                float* __restrict__ ws, int64_t M, int N, float inv_n, int64_t nblocks,
+                unsigned* fault)
 {
-    constexpr int W = kSched[S].W, KV = kSched[S].KV, U = kSched[S].UB, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kSched[S].UB, T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN;
     constexpr int G = T / W;
-    __shared__ float colbuf[G > 1 ? T * KV * VEC : 1];
+    extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, 2 * U>::kFloats];
     int parity = 0;
     const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const int nvec = N / VEC;
+    const bool colok = l < N / VEC;
+    const int64_t rb = (int64_t)N * sizeof(TX);
 
-    float gm[KV][VEC];
+    float gm[VEC];
 #pragma unroll
-    for (int kv = 0; kv < KV; ++kv) {
-        const int cv = kv * W + l;
+    for (int e = 0; e < VEC; ++e) gm[e] = (colok && gamma) ? ld_param(gamma, pt, l * VEC + e) : 1.f;
+    float acc_g[VEC], acc_b[VEC];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e)
-            gm[kv][e] = (cv < nvec && gamma) ? ld_param(gamma, pt, cv * VEC + e) : 1.f;
-    }
-    float acc_g[KV][VEC], acc_b[KV][VEC];
-#pragma unroll
-    for (int kv = 0; kv < KV; ++kv)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) acc_g[kv][e] = acc_b[kv][e] = 0.f;
+    for (int e = 0; e < VEC; ++e) acc_g[e] = acc_b[e] = 0.f;
 
-    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
-        uint4 rx[U][KV], rd[U][KV];
-        int64_t row[U];
+    // saved statistics of this thread's rows of block b
+    float mu_n[U], rs_n[U];
+    auto load_stats = [&](int64_t b) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t row = b * (G * U) + u * G + g;
+            mu_n[u] = row < M ? __ldcs(mean + row) : 0.f;
+            rs_n[u] = row < M ? __ldcs(rstd + row) : 0.f;
+        }
+    };
+    load_stats(blockIdx.x);
+
+    auto rows = [&](int64_t b, const unsigned char* tx, const unsigned char* td, bool alive,
+                    auto masked) {
+        constexpr bool kMask = decltype(masked)::value;
         float mu[U], rs[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            row[u] = b * (G * U) + u * G + g;
-            const bool okr = row[u] < M;
-            mu[u] = okr ? mean[row[u]] : 0.f;
-            rs[u] = okr ? rstd[row[u]] : 0.f;
-#pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
-                if (okr && cv < nvec) {
-                    rx[u][kv] = ld_stream(x + row[u] * N + cv * VEC);
-                    rd[u][kv] = ld_stream(dy + row[u] * N + cv * VEC);
-                } else {
-                    rx[u][kv] = rd[u][kv] = make_uint4(0, 0, 0, 0);
-                }
-            }
+            mu[u] = mu_n[u];
+            rs[u] = rs_n[u];
         }
-        // one all-reduce of (sum g, sum g*xhat) per row
+        load_stats(b + gridDim.x);  // next block of this CTA (past the end: zeros)
+        bool ok[U];
         float s[2 * U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const int lr = u * G + g;
+            ok[u] = alive && colok && (!kMask || b * (G * U) + lr < M);
+            // (sum g, sum g*xhat); vectors past the row's end hold dy = 0
+            float xf[VEC], df[VEC];
+            unpack(lds128_if(ok[u], tx + lr * rb + l * 16), xf);
+            unpack(lds128_if(ok[u], td + lr * rb + l * 16), df);
             s[2 * u] = s[2 * u + 1] = 0.f;
 #pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const bool okc = (kv * W + l) < nvec;
-                float xf[VEC], df[VEC];
-                unpack(rx[u][kv], xf);
-                unpack(rd[u][kv], df);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float xh = (xf[e] - mu[u]) * rs[u];
-                    const float gg = df[e] * gm[kv][e];
-                    s[2 * u] += gg;
-                    s[2 * u + 1] += okc ? gg * xh : 0.f;
-                }
+            for (int e = 0; e < VEC; ++e) {
+                const float xh = (xf[e] - mu[u]) * rs[u];
+                const float gg = __fmul_rn(df[e], gm[e]);
+                s[2 * u] += gg;
+                s[2 * u + 1] = fmaf(gg, xh, s[2 * u + 1]);
             }
         }
         group_allreduce<W, T, 2 * U>(s, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const int lr = u * G + g;
+            const int64_t row = b * (G * U) + lr;
+            const bool okr = !kMask || row < M;
             const float ma = s[2 * u] * inv_n;
             const float mb = s[2 * u + 1] * inv_n;
-            const bool okr = row[u] < M;
+            float xf[VEC], df[VEC], o[VEC];
+            unpack(lds128_if(ok[u], tx + lr * rb + l * 16), xf);
+            unpack(lds128_if(ok[u], td + lr * rb + l * 16), df);
 #pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
-                const bool ok = okr && cv < nvec;
-                float xf[VEC], df[VEC], o[VEC];
-                unpack(rx[u][kv], xf);
-                unpack(rd[u][kv], df);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float xh = (xf[e] - mu[u]) * rs[u];
-                    const float gg = df[e] * gm[kv][e];
-                    o[e] = rs[u] * (gg - ma - xh * mb);
-                    acc_g[kv][e] += ok ? df[e] * xh : 0.f;
-                    acc_b[kv][e] += ok ? df[e] : 0.f;
+            for (int e = 0; e < VEC; ++e) {
+                const float xh = (xf[e] - mu[u]) * rs[u];
+                const float gg = __fmul_rn(df[e], gm[e]);
+                o[e] = rs[u] * (gg - ma - xh * mb);
+                if constexpr (kMask) {
+                    acc_g[e] += okr ? df[e] * xh : 0.f;
+                    acc_b[e] += okr ? df[e] : 0.f;
+                } else {
+                    acc_g[e] = fmaf(df[e], xh, acc_g[e]);
+                    acc_b[e] += df[e];
                 }
-                if (ok) st_stream(dx + row[u] * N + cv * VEC, pack(o));
             }
+            if (ok[u]) st_stream(dx + row * N + l * VEC, pack(o));
         }
-    }
+    };
+
+    Ring<2> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
+    rg.row_bytes = rb;
+    rg.R = G * U;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = slot_bytes(S, true);
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        if ((b + 1) * (G * U) <= M)
+            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::false_type{});
+        else
+            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::true_type{});
+    });
 
     if (ws == nullptr) return;  // no parameter gradient requested (uniform)
     float* wrow = ws + blockIdx.x * (2 * (int64_t)N);
-    cta_store_columns<W, KV, VEC, T>(acc_g, colbuf, wrow, N);
-    cta_store_columns<W, KV, VEC, T>(acc_b, colbuf, wrow + N, N);
+    float* colbuf = reinterpret_cast<float*>(dsm + 128);  // drained ring slots, past the barriers
+    cta_store_columns<W, VEC, T>(acc_g, colbuf, wrow, N);
+    cta_store_columns<W, VEC, T>(acc_b, colbuf, wrow + N, N);
 }
 
 // ------------------------------------------------------ general (any shape)
@@ -273,7 +282,7 @@ __global__ void __launch_bounds__(kGenThreads)
         float s[2] = {0.f, 0.f};
         for (int c = lane; c < N; c += 32) {
             const float xh = (ld1(xr, c) - mu) * rs;
-            const float gg = ld1(dr, c) * (gamma ? ld_param(gamma, pt, c) : 1.f);
+            const float gg = __fmul_rn(ld1(dr, c), gamma ? ld_param(gamma, pt, c) : 1.f);
             s[0] += gg;
             s[1] += gg * xh;
         }
@@ -282,7 +291,7 @@ __global__ void __launch_bounds__(kGenThreads)
         for (int c = lane; c < N; c += 32) {
             const float xh = (ld1(xr, c) - mu) * rs;
             const float dv = ld1(dr, c);
-            const float gg = dv * (gamma ? ld_param(gamma, pt, c) : 1.f);
+            const float gg = __fmul_rn(dv, gamma ? ld_param(gamma, pt, c) : 1.f);
             st1(dx, r * N + c, rs * (gg - ma - xh * mb));
             if (wrow) {
                 wrow[c] += dv * xh;
@@ -306,12 +315,15 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                            \
-    case S:                                                                                    \
-        ln_fwd_fast<TX, S><<<L.grid, kSched[S].T, 0, L.stream>>>(xp, yp, gamma, beta, pt, mean, \
-                                                                 rstd, M, N, eps, inv_n,       \
-                                                                 L.nblocks);                  \
-        break;
+#define GBN_CASE(S)                                                                          \
+    case S: {                                                                                \
+        constexpr int smem = ring_smem_bytes(S, false, 1);                                  \
+        auto kern = ln_fwd_fast<TX, S>;                                                      \
+        if (smem > 48 * 1024)                                                                \
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault);                              \
+        break;                                                                               \
+    }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
 #undef GBN_CASE
@@ -335,12 +347,15 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                       \
-    case S:                                                                               \
-        ln_bwd_fast<TX, S><<<L.grid, kSched[S].T, 0, L.stream>>>(xp, dyp, mean, rstd,     \
-                                                                 gamma, pt, dxp, ws, M, N, \
-                                                                 inv_n, L.nblocks);       \
-        break;
+#define GBN_CASE(S)                                                                          \
+    case S: {                                                                                \
+        constexpr int smem = ring_smem_bytes(S, true, 2);                                  \
+        auto kern = ln_bwd_fast<TX, S>;                                                      \
+        if (smem > 48 * 1024)                                                                \
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.nblocks, L.fault);                              \
+        break;                                                                               \
+    }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
 #undef GBN_CASE

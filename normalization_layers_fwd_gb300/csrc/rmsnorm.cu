@@ -17,137 +17,140 @@
 // summation order as the forward, so both give identical bits.
 // The PR 8664 narrow-row follow-up computes dx and the weight-gradient
 // partials in one pass over x and dy; every width does that here.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace gbn {
 namespace {
 
-// Sum of squares of one thread's slice of a row (absent columns are zeros).
-template <typename TX, int KV, int VEC>
-__device__ __forceinline__ float slice_sumsq(const uint4 (&r)[KV])
+// Sum of squares of one thread's vector of a row (absent vectors are zeros).
+// The forward and the backward's recomputation share it, so with the same
+// row-group width they reduce a row identically.
+template <int VEC>
+__device__ __forceinline__ float vec_sumsq(uint4 r)
 {
-    float s = 0.f;
+    float f[VEC], s = 0.f;
+    unpack(r, f);
 #pragma unroll
-    for (int kv = 0; kv < KV; ++kv) {
-        float f[VEC];
-        unpack(r[kv], f);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) s = fmaf(f[e], f[e], s);
-    }
+    for (int e = 0; e < VEC; ++e) s = fmaf(f[e], f[e], s);
     return s;
 }
 
 // ------------------------------------------------------------ fast forward
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINB)
+__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
     rms_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ w,
                  int pt, float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
-                 int64_t nblocks)
+                 int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, KV = kSched[S].KV, U = kSched[S].UF, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kSched[S].UF, T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN;
     constexpr int G = T / W;
+    extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
     int parity = 0;
     const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const int nvec = N / VEC;
+    const bool colok = l < N / VEC;
+    const int64_t rb = (int64_t)N * sizeof(TX);
 
-    float wf[KV][VEC];
+    float wf[VEC];
 #pragma unroll
-    for (int kv = 0; kv < KV; ++kv) {
-        const int cv = kv * W + l;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) wf[kv][e] = cv < nvec ? ld_param(w, pt, cv * VEC + e) : 0.f;
-    }
+    for (int e = 0; e < VEC; ++e) wf[e] = colok ? ld_param(w, pt, l * VEC + e) : 0.f;
 
-    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
-        uint4 r[U][KV];
-        int64_t row[U];
+    Ring<1> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.row_bytes = rb;
+    rg.R = G * U;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = slot_bytes(S, false);
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        const unsigned char* tx = rg.tile(k, 0);
+        bool ok[U];
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            row[u] = b * (G * U) + u * G + g;
-#pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
-                if (row[u] < M && cv < nvec)
-                    r[u][kv] = ld_stream(x + row[u] * N + cv * VEC);
-                else
-                    r[u][kv] = make_uint4(0, 0, 0, 0);
-            }
+            const int lr = u * G + g;
+            ok[u] = alive && colok && b * (G * U) + lr < M;
+            s[u] = vec_sumsq<VEC>(lds128_if(ok[u], tx + lr * rb + l * 16));
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) s[u] = slice_sumsq<TX, KV, VEC>(r[u]);
         group_allreduce<W, T, U>(s, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const int lr = u * G + g;
+            const int64_t row = b * (G * U) + lr;
             const float rs = rsqrtf(fmaf(s[u], inv_n, eps));
-#pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
+            if (ok[u]) {
                 float f[VEC];
-                unpack(r[u][kv], f);
+                unpack(lds128(tx + lr * rb + l * 16), f);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) f[e] = wf[kv][e] * round_x<TX>(f[e] * rs);
-                if (row[u] < M && cv < nvec) st_stream(y + row[u] * N + cv * VEC, pack(f));
+                for (int e = 0; e < VEC; ++e) f[e] = wf[e] * round_x<TX>(f[e] * rs);
+                st_stream(y + row * N + l * VEC, pack(f));
             }
-            if (rstd && l == 0 && row[u] < M) rstd[row[u]] = rs;
+            if (rstd && alive && l == 0 && row < M) rstd[row] = rs;
         }
-    }
+    });
 }
 
 // ----------------------------------------------------------- fast backward
+// x and dy stream through the ring; a given rstd of the next row block is
+// prefetched into registers, otherwise r is recomputed with the forward's
+// code.  Full row blocks run without masking; the ragged last block masks its
+// padded rows by a select after the arithmetic.
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINB)
+__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
     rms_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy, const void* __restrict__ w,
                  int pt, const float* __restrict__ rstd, TX* __restrict__ dx,
                  float* __restrict__ ws, int64_t M, int N, float eps, float inv_n,
-                 int64_t nblocks)
+                 int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, KV = kSched[S].KV, U = kSched[S].UB, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kSched[S].UB, T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN;
     constexpr int G = T / W;
-    __shared__ float colbuf[G > 1 ? T * KV * VEC : 1];
+    extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
     int parity = 0;
     const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const int nvec = N / VEC;
+    const bool colok = l < N / VEC;
+    const int64_t rb = (int64_t)N * sizeof(TX);
     const bool round_terms = (pt != kF32);  // weight in x's dtype: round dy*n
 
-    float wf[KV][VEC], acc[KV][VEC];
+    float wf[VEC], acc[VEC];
 #pragma unroll
-    for (int kv = 0; kv < KV; ++kv) {
-        const int cv = kv * W + l;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            wf[kv][e] = cv < nvec ? ld_param(w, pt, cv * VEC + e) : 0.f;
-            acc[kv][e] = 0.f;
-        }
+    for (int e = 0; e < VEC; ++e) {
+        wf[e] = colok ? ld_param(w, pt, l * VEC + e) : 0.f;
+        acc[e] = 0.f;
     }
-
-    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x) {
-        uint4 rx[U][KV], rd[U][KV];
-        int64_t row[U];
-        float rs[U];
+    float rs_n[U];
+    auto load_rstd = [&](int64_t b) {
+        if (rstd) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            row[u] = b * (G * U) + u * G + g;
-            if (rstd) rs[u] = row[u] < M ? rstd[row[u]] : 0.f;
-#pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
-                if (row[u] < M && cv < nvec) {
-                    rx[u][kv] = ld_stream(x + row[u] * N + cv * VEC);
-                    rd[u][kv] = ld_stream(dy + row[u] * N + cv * VEC);
-                } else {
-                    rx[u][kv] = rd[u][kv] = make_uint4(0, 0, 0, 0);
-                }
+            for (int u = 0; u < U; ++u) {
+                const int64_t row = b * (G * U) + u * G + g;
+                rs_n[u] = row < M ? __ldcs(rstd + row) : 0.f;
             }
         }
+    };
+    load_rstd(blockIdx.x);
+
+    auto rows = [&](int64_t b, const unsigned char* tx, const unsigned char* td, bool alive,
+                    auto masked) {
+        constexpr bool kMask = decltype(masked)::value;
+        float rs[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) rs[u] = rs_n[u];
+        load_rstd(b + gridDim.x);
+        bool ok[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            ok[u] = alive && colok && (!kMask || b * (G * U) + u * G + g < M);
         if (!rstd) {  // uniform branch: recompute r exactly as the forward does
 #pragma unroll
-            for (int u = 0; u < U; ++u) rs[u] = slice_sumsq<TX, KV, VEC>(rx[u]);
+            for (int u = 0; u < U; ++u)
+                rs[u] = vec_sumsq<VEC>(lds128_if(ok[u], tx + (u * G + g) * rb + l * 16));
             group_allreduce<W, T, U>(rs, red, parity);
 #pragma unroll
             for (int u = 0; u < U; ++u) rs[u] = rsqrtf(fmaf(rs[u], inv_n, eps));
@@ -155,45 +158,60 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINB)
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const int lr = u * G + g;
+            float xf[VEC], df[VEC];
+            unpack(lds128_if(ok[u], tx + lr * rb + l * 16), xf);
+            unpack(lds128_if(ok[u], td + lr * rb + l * 16), df);
             s[u] = 0.f;
 #pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                float xf[VEC], df[VEC];
-                unpack(rx[u][kv], xf);
-                unpack(rd[u][kv], df);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) s[u] = fmaf(round_x<TX>(df[e] * wf[kv][e]), xf[e] * rs[u], s[u]);
-            }
+            for (int e = 0; e < VEC; ++e)
+                s[u] = fmaf(round_x<TX>(df[e] * wf[e]), xf[e] * rs[u], s[u]);
         }
         group_allreduce<W, T, U>(s, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const int lr = u * G + g;
+            const int64_t row = b * (G * U) + lr;
+            const bool okr = !kMask || row < M;
             const float m = s[u] * inv_n;
-            const bool okr = row[u] < M;
+            float xf[VEC], df[VEC], o[VEC];
+            unpack(lds128_if(ok[u], tx + lr * rb + l * 16), xf);
+            unpack(lds128_if(ok[u], td + lr * rb + l * 16), df);
 #pragma unroll
-            for (int kv = 0; kv < KV; ++kv) {
-                const int cv = kv * W + l;
-                const bool ok = okr && cv < nvec;
-                float xf[VEC], df[VEC], o[VEC];
-                unpack(rx[u][kv], xf);
-                unpack(rd[u][kv], df);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float xh = xf[e] * rs[u];
-                    const float dn = round_x<TX>(df[e] * wf[kv][e]);
-                    o[e] = rs[u] * (dn - xh * m);
-                    float term = df[e] * round_x<TX>(xh);
-                    if (round_terms) term = round_x<TX>(term);
-                    acc[kv][e] += ok ? term : 0.f;
-                }
-                if (ok) st_stream(dx + row[u] * N + cv * VEC, pack(o));
+            for (int e = 0; e < VEC; ++e) {
+                const float xh = xf[e] * rs[u];
+                const float dn = round_x<TX>(df[e] * wf[e]);
+                o[e] = rs[u] * (dn - xh * m);
+                float term = df[e] * round_x<TX>(xh);
+                if (round_terms) term = round_x<TX>(term);
+                if constexpr (kMask)
+                    acc[e] += okr ? term : 0.f;
+                else
+                    acc[e] += term;
             }
+            if (ok[u]) st_stream(dx + row * N + l * VEC, pack(o));
         }
-    }
+    };
+
+    Ring<2> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
+    rg.row_bytes = rb;
+    rg.R = G * U;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = slot_bytes(S, true);
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        if ((b + 1) * (G * U) <= M)
+            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::false_type{});
+        else
+            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::true_type{});
+    });
 
     if (ws == nullptr) return;  // no weight gradient requested (uniform)
     float* wrow = ws + blockIdx.x * (int64_t)N;
-    cta_store_columns<W, KV, VEC, T>(acc, colbuf, wrow, N);
+    cta_store_columns<W, VEC, T>(acc, reinterpret_cast<float*>(dsm + 128), wrow, N);  // drained ring slots
 }
 
 // ------------------------------------------------------ general (any shape)
@@ -276,11 +294,15 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                           \
-    case S:                                                                                   \
-        rms_fwd_fast<TX, S><<<L.grid, kSched[S].T, 0, L.stream>>>(xp, yp, w, pt, rstd, M, N, \
-                                                                  eps, inv_n, L.nblocks);    \
-        break;
+#define GBN_CASE(S)                                                                          \
+    case S: {                                                                                \
+        constexpr int smem = ring_smem_bytes(S, false, 1);                                  \
+        auto kern = rms_fwd_fast<TX, S>;                                                     \
+        if (smem > 48 * 1024)                                                                \
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, w, pt, rstd, M, N, eps, inv_n, L.nblocks, L.fault);                              \
+        break;                                                                               \
+    }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
 #undef GBN_CASE
@@ -303,12 +325,15 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                         \
-    case S:                                                                                 \
-        rms_bwd_fast<TX, S><<<L.grid, kSched[S].T, 0, L.stream>>>(xp, dyp, w, pt, rstd, dxp, \
-                                                                  ws, M, N, eps, inv_n,    \
-                                                                  L.nblocks);              \
-        break;
+#define GBN_CASE(S)                                                                          \
+    case S: {                                                                                \
+        constexpr int smem = ring_smem_bytes(S, true, 2);                                  \
+        auto kern = rms_bwd_fast<TX, S>;                                                     \
+        if (smem > 48 * 1024)                                                                \
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, dyp, w, pt, rstd, dxp, ws, M, N, eps, inv_n, L.nblocks, L.fault);                              \
+        break;                                                                               \
+    }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
 #undef GBN_CASE

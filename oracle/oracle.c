@@ -27,9 +27,12 @@
  *                 the final store, which the caller applies.
  *
  * Outputs are float64 values BEFORE the final rounding to the output
- * dtype, plus a "scale" companion (the sum of the magnitudes of the
- * addends, or the square root of the sum of squared terms for column sums)
- * that the tests use to judge cancellation.
+ * dtype, plus a "scale" companion that the tests use to judge
+ * cancellation: the first-order bound on the rounding error of evaluating
+ * the output in a lower precision, divided by the unit roundoff.  A sum's
+ * error is bounded by the sum of its terms' magnitudes, so inner
+ * reductions (means) enter the scale as means of magnitudes; column sums
+ * come with the sum of their squared terms instead.
  */
 #include <math.h>
 #include <stdint.h>
@@ -231,9 +234,13 @@ int orc_ln_fwd_rows(const void* x, int xt, int64_t M, int64_t N, double eps,
     (void)M;
     for (int64_t r = 0; r < nrows; ++r) {
         int64_t i = row_of(rows, r);
-        double s = 0.0;
-        for (int64_t j = 0; j < N; ++j) s += widen(x, xt, i * N + j);
+        double s = 0.0, sa = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            s += widen(x, xt, i * N + j);
+            sa += fabs(widen(x, xt, i * N + j));
+        }
         double mu = s / (double)N;
+        double mabs = sa / (double)N; /* scale of the mean's rounding error */
         double ss = 0.0;
         for (int64_t j = 0; j < N; ++j) {
             double d = widen(x, xt, i * N + j) - mu;
@@ -248,7 +255,9 @@ int orc_ln_fwd_rows(const void* x, int xt, int64_t M, int64_t N, double eps,
             double g = gamma ? gamma[j] : 1.0;
             double b = beta ? beta[j] : 0.0;
             y[r * N + j] = xh * g + b;
-            if (y_scale) y_scale[r * N + j] = fabs(xh * g) + fabs(b);
+            if (y_scale)
+                y_scale[r * N + j] =
+                    (fabs(widen(x, xt, i * N + j)) + mabs) * rs * fabs(g) + fabs(b);
         }
     }
     return 0;
@@ -262,20 +271,23 @@ int orc_ln_bwd_rows(const void* x, const void* dy, int xt, int64_t M, int64_t N,
     for (int64_t r = 0; r < nrows; ++r) {
         int64_t i = row_of(rows, r);
         double mu = mean[i], rs = rstd[i];
-        double sg = 0.0, sgx = 0.0;
+        double sg = 0.0, sgx = 0.0, sga = 0.0, sgxa = 0.0;
         for (int64_t j = 0; j < N; ++j) {
             double xh = (widen(x, xt, i * N + j) - mu) * rs;
             double g = widen(dy, xt, i * N + j) * (gamma ? gamma[j] : 1.0);
             sg += g;
             sgx += g * xh;
+            sga += fabs(g);
+            sgxa += fabs(g * xh);
         }
         double a = sg / (double)N;
         double b = sgx / (double)N;
+        double aa = sga / (double)N, ba = sgxa / (double)N; /* error scales of a, b */
         for (int64_t j = 0; j < N; ++j) {
             double xh = (widen(x, xt, i * N + j) - mu) * rs;
             double g = widen(dy, xt, i * N + j) * (gamma ? gamma[j] : 1.0);
             dx[r * N + j] = rs * (g - a - xh * b);
-            if (dx_scale) dx_scale[r * N + j] = fabs(rs) * (fabs(g) + fabs(a) + fabs(xh * b));
+            if (dx_scale) dx_scale[r * N + j] = fabs(rs) * (fabs(g) + aa + fabs(xh) * ba);
         }
     }
     return 0;
@@ -363,7 +375,7 @@ int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int wt, int64_t M, i
     for (int64_t r = 0; r < nrows; ++r) {
         int64_t i = row_of(rows, r);
         double rs = rms_r(x, xt, i, N, eps);
-        double s = 0.0, flip = 0.0;
+        double s = 0.0, sa = 0.0, flip = 0.0;
         for (int64_t j = 0; j < N; ++j) {
             double xh = widen(x, xt, i * N + j) * rs;
             double dn = widen(dy, xt, i * N + j) * w[j];
@@ -371,8 +383,10 @@ int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int wt, int64_t M, i
             if (mode == ORC_PARITY) dn = round_to(dn, xt, &tie);
             if (tie && wt == ORC_F32) flip += bf16_spacing(dn) * fabs(xh);
             s += dn * xh;
+            sa += fabs(dn * xh);
         }
         double b = s / (double)N;
+        double ba = sa / (double)N; /* error scale of b */
         flip /= (double)N; /* largest change of b from flipped dn roundings */
         for (int64_t j = 0; j < N; ++j) {
             double xh = widen(x, xt, i * N + j) * rs;
@@ -380,7 +394,7 @@ int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int wt, int64_t M, i
             int tie = 0;
             if (mode == ORC_PARITY) dn = round_to(dn, xt, &tie);
             dx[r * N + j] = rs * (dn - xh * b);
-            if (dx_scale) dx_scale[r * N + j] = fabs(rs) * (fabs(dn) + fabs(xh * b));
+            if (dx_scale) dx_scale[r * N + j] = fabs(rs) * (fabs(dn) + fabs(xh) * ba);
             if (dx_allow) {
                 double own = (tie && wt == ORC_F32) ? bf16_spacing(dn) : 0.0;
                 dx_allow[r * N + j] = fabs(rs) * (own + fabs(xh) * flip);

@@ -101,6 +101,16 @@ def test_valid_call_without_a_device_reports_edevice(lib):
     assert lib.dyt_fwd(p, p, p, p, p, 4, 8, 1, 0, None) == GBN_EDEVICE
 
 
+def test_fault_api_validates_without_device(lib):
+    import torch
+    assert lib.gbn_read_faults(None, 0) == GBN_EINVAL
+    assert lib.gbn_selftest_wait_timeout(0, ctypes.c_void_p(16), None) == GBN_EINVAL
+    assert lib.gbn_selftest_wait_timeout(1 << 40, ctypes.c_void_p(16), None) == GBN_EINVAL
+    if not torch.cuda.is_available():
+        v = ctypes.c_uint(5)
+        assert lib.gbn_read_faults(ctypes.byref(v), 0) == GBN_EDEVICE
+
+
 def test_workspace_query(lib):
     from normalization_layers_fwd_gb300._lib import SIZE_MAX
     assert lib.gbn_bwd_workspace_bytes(5, 10, 10, 1, 0, 0) == SIZE_MAX

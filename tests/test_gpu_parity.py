@@ -283,3 +283,29 @@ def test_autograd_wrappers_match_direct_calls():
         got = [x.grad.view(513, 256)] + [p.grad for p in ps]
         for g, w in zip(got, want):
             assert torch.equal(g, w)
+
+
+def test_bounded_wait_self_test_sets_fault_and_returns():
+    """A barrier that never completes: the kernel's bounded wait must run
+    out (a few milliseconds here), set the fault bit and return, leaving the
+    context usable."""
+    lib = _lib.load()
+    _lib.read_faults(clear=True)
+    res = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert lib.gbn_selftest_wait_timeout(1 << 24, res.data_ptr(), s) == 0
+    torch.cuda.synchronize()
+    assert int(res.item()) == 0
+    assert _lib.read_faults(clear=True) & 1
+    assert _lib.read_faults(clear=False) == 0
+    # the context still works
+    inp = _inputs(333, 128, torch.bfloat16, torch.float32, "after_selftest")
+    _run("rmsnorm", inp)
+
+
+def test_fault_word_clean_after_kernels():
+    _lib.read_faults(clear=True)
+    inp = _inputs(20011, 64, torch.bfloat16, torch.float32, "faultclean")
+    for op in ("dyt", "layernorm", "rmsnorm"):
+        _run(op, inp)
+    assert _lib.read_faults(clear=False) == 0

@@ -37,12 +37,13 @@ struct SchedEntry {
 // through __launch_bounds__, shared memory through the ring size).
 constexpr int kNumSched = 11;
 constexpr SchedEntry kSched[kNumSched] = {
-    {1, 1, 2, 2, 256, 4, 3},        {2, 2, 2, 2, 256, 4, 3},       {4, 4, 2, 2, 256, 4, 3},
-    {8, 8, 2, 2, 256, 4, 3},        {16, 16, 2, 2, 256, 4, 3},     {32, 32, 2, 2, 256, 4, 3},
-    {64, 64, 2, 2, 256, 4, 3},      {128, 128, 2, 2, 256, 4, 3},   {256, 256, 2, 2, 256, 4, 3},
+    {1, 1, 2, 2, 256, 4, 2},        {2, 2, 2, 2, 256, 4, 2},       {4, 4, 2, 2, 256, 4, 2},
+    {8, 8, 2, 2, 256, 4, 2},        {16, 16, 2, 2, 256, 4, 2},     {32, 32, 2, 2, 256, 4, 2},
+    {64, 64, 2, 2, 256, 4, 2},      {128, 128, 2, 2, 256, 4, 2},   {256, 256, 2, 2, 256, 4, 2},
     {512, 512, 1, 1, 512, 2, 2},    {1024, 1024, 1, 1, 1024, 1, 1},
 };
-constexpr int kStages = 4;  // depth of the shared-memory ring
+constexpr int kStagesF = 4;  // ring depth of the forward kernels (one staged tensor)
+constexpr int kStagesB = 4;  // ring depth of the backward kernels (x and dy)
 
 // Bytes of one ring slot for one staged tensor, and of the whole dynamic
 // shared memory a kernel with NT staged tensors needs (barriers first).
@@ -52,7 +53,7 @@ __host__ __device__ constexpr int slot_bytes(int S, bool bwd)
 }
 __host__ __device__ constexpr int ring_smem_bytes(int S, bool bwd, int NT)
 {
-    return 128 + kStages * NT * slot_bytes(S, bwd);
+    return 128 + (bwd ? kStagesB : kStagesF) * NT * slot_bytes(S, bwd);
 }
 constexpr int kMaxFastVec = 1024;
 
@@ -249,7 +250,7 @@ __device__ __forceinline__ uint4 lds128_if(bool ok, const unsigned char* p)
 // The ring of one CTA.  NT staged tensors, each row `row_bytes` long; row
 // block b covers rows [b*R, min(b*R + R, M)).  Blocks b = blockIdx.x +
 // k*gridDim.x, k = 0..K-1, belong to this CTA.
-template <int NT>
+template <int NT, int kStages>
 struct Ring {
     uint64_t* bar;             // [kStages]
     unsigned char* buf;        // [kStages][NT][slot]
@@ -284,8 +285,8 @@ struct Ring {
 // Run `body(b, k, alive)` over this CTA's row blocks with the ring full
 // kStages deep.  `dsm` is the kernel's dynamic shared memory (128-byte
 // aligned).  Every thread makes the same calls (body may __syncthreads).
-template <int NT, class Body>
-__device__ __forceinline__ void ring_loop(Ring<NT>& rg, unsigned char* dsm, Body&& body)
+template <int NT, int kStages, class Body>
+__device__ __forceinline__ void ring_loop(Ring<NT, kStages>& rg, unsigned char* dsm, Body&& body)
 {
     rg.bar = reinterpret_cast<uint64_t*>(dsm);
     rg.buf = dsm + 128;
@@ -316,6 +317,124 @@ __device__ __forceinline__ void ring_loop(Ring<NT>& rg, unsigned char* dsm, Body
             mbar_wait(&rg.bar[k % kStages], (uint32_t)((k / kStages) & 1), nullptr, kWaitCycles);
     }
     __syncthreads();
+}
+
+// ------------------------------------------------------------ paired fp32
+// Two float32 lanes in one 64-bit register pair.  sm_100 and later run add,
+// sub, mul and fma on both lanes in one instruction (the .f32x2 forms), which
+// halves the instruction count of the elementwise arithmetic; these kernels
+// are issue-bound once their loads are staged through shared memory.
+struct f2 {
+    uint64_t v;
+};
+
+__device__ __forceinline__ f2 mk2(float lo, float hi)
+{
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ f2 splat2(float a) { return mk2(a, a); }
+__device__ __forceinline__ float lo2(f2 a)
+{
+    float l, h;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(l), "=f"(h) : "l"(a.v));
+    return l;
+}
+__device__ __forceinline__ float hi2(f2 a)
+{
+    float l, h;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(l), "=f"(h) : "l"(a.v));
+    return h;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b)
+{
+    f2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b)
+{
+    f2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b)
+{
+    f2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c)
+{
+    f2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return r;
+}
+// lane-wise select: c ? a : b
+__device__ __forceinline__ f2 sel2(bool c, f2 a, f2 b)
+{
+    f2 r;
+    r.v = c ? a.v : b.v;
+    return r;
+}
+
+// A bf16 pair (one 32-bit word, element 2k in the low half) as two floats.
+__device__ __forceinline__ f2 bf2_to_f2(uint32_t w)
+{
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "r"(w << 16), "r"(w & 0xffff0000u));
+    return r;
+}
+// Two floats to a bf16 pair, each rounded to nearest even.
+__device__ __forceinline__ uint32_t f2_to_bf2(f2 a)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi2(a)), "f"(lo2(a)));
+    return r;
+}
+
+// One 16-byte vector as pairs: 4 pairs of bf16, or 2 pairs of f32.
+template <typename TX> struct Pairs;
+template <> struct Pairs<__nv_bfloat16> { static constexpr int kP = 4; };
+template <> struct Pairs<float> { static constexpr int kP = 2; };
+
+__device__ __forceinline__ void unpack2(const uint4& u, f2 (&p)[4])
+{
+    p[0] = bf2_to_f2(u.x);
+    p[1] = bf2_to_f2(u.y);
+    p[2] = bf2_to_f2(u.z);
+    p[3] = bf2_to_f2(u.w);
+}
+__device__ __forceinline__ void unpack2(const uint4& u, f2 (&p)[2])
+{
+    asm("mov.b64 %0, {%1, %2};" : "=l"(p[0].v) : "r"(u.x), "r"(u.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(p[1].v) : "r"(u.z), "r"(u.w));
+}
+__device__ __forceinline__ uint4 pack2(const f2 (&p)[4])
+{
+    return make_uint4(f2_to_bf2(p[0]), f2_to_bf2(p[1]), f2_to_bf2(p[2]), f2_to_bf2(p[3]));
+}
+__device__ __forceinline__ uint4 pack2(const f2 (&p)[2])
+{
+    uint4 u;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(u.x), "=r"(u.y) : "l"(p[0].v));
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(u.z), "=r"(u.w) : "l"(p[1].v));
+    return u;
+}
+
+// Round both lanes to the activation dtype's precision (identity for f32).
+template <typename TX> __device__ __forceinline__ f2 round2(f2 a);
+template <> __device__ __forceinline__ f2 round2<float>(f2 a) { return a; }
+template <> __device__ __forceinline__ f2 round2<__nv_bfloat16>(f2 a)
+{
+    return bf2_to_f2(f2_to_bf2(a));
+}
+
+// Parameters of columns c, c+1 as a pair.
+__device__ __forceinline__ f2 ld_param2(const void* p, int pt, int64_t c)
+{
+    return mk2(ld_param(p, pt, c), ld_param(p, pt, c + 1));
 }
 
 // ---------------------------------------------------------------- reductions
@@ -425,6 +544,20 @@ __device__ __forceinline__ void cta_store_columns(const float (&acc)[VEC], float
         }
         __syncthreads();
     }
+}
+
+// Pair form: acc[p] holds columns l*2P + 2p and l*2P + 2p + 1.
+template <int W, int P, int T>
+__device__ __forceinline__ void cta_store_columns2(const f2 (&acc)[P], float* buf,
+                                                   float* __restrict__ out_row, int N)
+{
+    float a[2 * P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        a[2 * p] = lo2(acc[p]);
+        a[2 * p + 1] = hi2(acc[p]);
+    }
+    cta_store_columns<W, 2 * P, T>(a, buf, out_row, N);
 }
 
 }  // namespace gbn

@@ -74,6 +74,42 @@ __device__ __forceinline__ void dyt_tanh_sech2(float z, float& t, float& s)
     s = (4.0f * e) * (q * q);
 }
 
+// The same two identities on a pair of lanes: the exponential and the
+// reciprocal are per lane (MUFU), everything else runs as .f32x2.
+__device__ __forceinline__ f2 tanh_series2(f2 z)
+{
+    const f2 z2 = mul2(z, z);
+    f2 p = fma2(z2, splat2(kT7), splat2(kT5));
+    p = fma2(z2, p, splat2(kT3));
+    p = fma2(z2, p, splat2(1.0f));
+    return mul2(z, p);
+}
+
+__device__ __forceinline__ f2 pick_tanh2(f2 z, f2 ts, f2 tb)
+{
+    const float z0 = lo2(z), z1 = hi2(z);
+    return mk2(fabsf(z0) < kSmall ? lo2(ts) : copysignf(lo2(tb), z0),
+               fabsf(z1) < kSmall ? hi2(ts) : copysignf(hi2(tb), z1));
+}
+
+__device__ __forceinline__ f2 dyt_tanh2(f2 z)
+{
+    const f2 e = mk2(ex2_approx(fabsf(lo2(z)) * kM2Log2e), ex2_approx(fabsf(hi2(z)) * kM2Log2e));
+    const f2 d = add2(e, splat2(1.0f));
+    const f2 q = mk2(rcp_approx(lo2(d)), rcp_approx(hi2(d)));
+    const f2 tb = mul2(sub2(splat2(1.0f), e), q);
+    return pick_tanh2(z, tanh_series2(z), tb);
+}
+
+__device__ __forceinline__ void dyt_tanh_sech2_2(f2 z, f2& t, f2& s)
+{
+    const f2 e = mk2(ex2_approx(fabsf(lo2(z)) * kM2Log2e), ex2_approx(fabsf(hi2(z)) * kM2Log2e));
+    const f2 d = add2(e, splat2(1.0f));
+    const f2 q = mk2(rcp_approx(lo2(d)), rcp_approx(hi2(d)));
+    t = pick_tanh2(z, tanh_series2(z), mul2(sub2(splat2(1.0f), e), q));
+    s = mul2(mul2(e, splat2(4.0f)), mul2(q, q));
+}
+
 // ------------------------------------------------------------ fast forward
 template <typename TX, int S>
 __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
@@ -82,22 +118,22 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
                  int64_t M, int N, int64_t nblocks, unsigned* fault)
 {
     constexpr int W = kSched[S].W, U = kSched[S].UF, T = kSched[S].T;
-    constexpr int VEC = Vec<TX>::kN;
+    constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = T / W;
     extern __shared__ __align__(128) unsigned char dsm[];
     const int g = threadIdx.x / W, l = threadIdx.x % W;
     const bool colok = l < N / VEC;
     const int64_t rb = (int64_t)N * sizeof(TX);
 
-    const float a = ld_param(alpha, pt, 0);
-    float gm[VEC], bt[VEC];
+    const f2 a2 = splat2(ld_param(alpha, pt, 0));
+    f2 gm[P], bt[P];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-        gm[e] = colok ? ld_param(gamma, pt, l * VEC + e) : 0.f;
-        bt[e] = colok ? ld_param(beta, pt, l * VEC + e) : 0.f;
+    for (int p = 0; p < P; ++p) {
+        gm[p] = colok ? ld_param2(gamma, pt, l * VEC + 2 * p) : splat2(0.f);
+        bt[p] = colok ? ld_param2(beta, pt, l * VEC + 2 * p) : splat2(0.f);
     }
 
-    Ring<1> rg;
+    Ring<1, kStagesF> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.row_bytes = rb;
     rg.R = G * U;
@@ -112,11 +148,11 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
             const int lr = u * G + g;
             const int64_t row = b * (G * U) + lr;
             if (alive && colok && row < M) {
-                float f[VEC];
-                unpack(lds128(tx + lr * rb + l * 16), f);
+                f2 v[P];
+                unpack2(lds128(tx + lr * rb + l * 16), v);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) f[e] = fmaf(gm[e], dyt_tanh(a * f[e]), bt[e]);
-                st_stream(y + row * N + l * VEC, pack(f));
+                for (int p = 0; p < P; ++p) v[p] = fma2(gm[p], dyt_tanh2(mul2(a2, v[p])), bt[p]);
+                st_stream(y + row * N + l * VEC, pack2(v));
             }
         }
     });
@@ -133,7 +169,7 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
                  float* __restrict__ ws, int64_t M, int N, int64_t nblocks, unsigned* fault)
 {
     constexpr int W = kSched[S].W, U = kSched[S].UB, T = kSched[S].T;
-    constexpr int VEC = Vec<TX>::kN;
+    constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = T / W;
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[T / 32];
@@ -142,17 +178,18 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
     const int64_t rb = (int64_t)N * sizeof(TX);
 
     const float a = ld_param(alpha, pt, 0);
-    float gm[VEC], ga[VEC];
+    const f2 a2 = splat2(a);
+    f2 gm[P], ga[P];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-        gm[e] = colok ? ld_param(gamma, pt, l * VEC + e) : 0.f;
-        ga[e] = gm[e] * a;
+    for (int p = 0; p < P; ++p) {
+        gm[p] = colok ? ld_param2(gamma, pt, l * VEC + 2 * p) : splat2(0.f);
+        ga[p] = mul2(gm[p], a2);
     }
     // Per-column accumulators: sum dy*t, sum dy, sum dy*x*sech^2 (gamma is
     // applied to the last one once, at the end).
-    float acc_g[VEC], acc_b[VEC], acc_a[VEC];
+    f2 acc_g[P], acc_b[P], acc_a[P];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) acc_g[e] = acc_b[e] = acc_a[e] = 0.f;
+    for (int p = 0; p < P; ++p) acc_g[p] = acc_b[p] = acc_a[p] = splat2(0.f);
 
     auto rows = [&](int64_t b, const unsigned char* tx, const unsigned char* td, bool alive,
                     auto masked) {
@@ -163,31 +200,32 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
             const int64_t row = b * (G * U) + lr;
             const bool okr = !kMask || row < M;
             if (!alive || !colok) continue;
-            float xf[VEC], df[VEC], o[VEC];
-            unpack(lds128(tx + lr * rb + l * 16), xf);
-            unpack(lds128(td + lr * rb + l * 16), df);
+            f2 xv[P], dv[P], o[P];
+            unpack2(lds128(tx + lr * rb + l * 16), xv);
+            unpack2(lds128(td + lr * rb + l * 16), dv);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                float t, s;
-                dyt_tanh_sech2(a * xf[e], t, s);
-                const float ds = df[e] * s;
-                o[e] = ds * ga[e];
+            for (int p = 0; p < P; ++p) {
+                f2 t, s;
+                dyt_tanh_sech2_2(mul2(a2, xv[p]), t, s);
+                const f2 ds = mul2(dv[p], s);
+                o[p] = mul2(ds, ga[p]);
                 if constexpr (kMask) {
                     // padded rows: select after the arithmetic, never a 0/1 multiply
-                    acc_g[e] += okr ? df[e] * t : 0.f;
-                    acc_b[e] += okr ? df[e] : 0.f;
-                    acc_a[e] += okr ? ds * xf[e] : 0.f;
+                    const f2 z = splat2(0.f);
+                    acc_g[p] = add2(acc_g[p], sel2(okr, mul2(dv[p], t), z));
+                    acc_b[p] = add2(acc_b[p], sel2(okr, dv[p], z));
+                    acc_a[p] = add2(acc_a[p], sel2(okr, mul2(ds, xv[p]), z));
                 } else {
-                    acc_g[e] = fmaf(df[e], t, acc_g[e]);
-                    acc_b[e] += df[e];
-                    acc_a[e] = fmaf(ds, xf[e], acc_a[e]);
+                    acc_g[p] = fma2(dv[p], t, acc_g[p]);
+                    acc_b[p] = add2(acc_b[p], dv[p]);
+                    acc_a[p] = fma2(ds, xv[p], acc_a[p]);
                 }
             }
-            if (okr) st_stream(dx + row * N + l * VEC, pack(o));
+            if (okr) st_stream(dx + row * N + l * VEC, pack2(o));
         }
     };
 
-    Ring<2> rg;
+    Ring<2, kStagesB> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     rg.row_bytes = rb;
@@ -207,13 +245,18 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
     const int64_t L = 2 * (int64_t)N + 1;
     float* wrow = ws + blockIdx.x * L;
     float* colbuf = reinterpret_cast<float*>(dsm + 128);  // drained ring slots, past the barriers
-    cta_store_columns<W, VEC, T>(acc_g, colbuf, wrow, N);
-    cta_store_columns<W, VEC, T>(acc_b, colbuf, wrow + N, N);
+    cta_store_columns2<W, P, T>(acc_g, colbuf, wrow, N);
+    cta_store_columns2<W, P, T>(acc_b, colbuf, wrow + N, N);
     // lanes past the row's end hold garbage (tanh(alpha*0) for alpha = inf);
     // they are never stored above and are excluded here
     float da = 0.f;
+    if (colok) {
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) da += colok ? gm[e] * acc_a[e] : 0.f;
+        for (int p = 0; p < P; ++p) {
+            const f2 q = mul2(gm[p], acc_a[p]);
+            da += lo2(q) + hi2(q);
+        }
+    }
     const float tot = cta_sum<T>(da, red);
     if (threadIdx.x == 0) wrow[2 * N] = tot;
 }

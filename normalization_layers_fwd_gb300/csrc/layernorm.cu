@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
                 int64_t nblocks, unsigned* fault)
 {
     constexpr int W = kSched[S].W, U = kSched[S].UF, T = kSched[S].T;
-    constexpr int VEC = Vec<TX>::kN;
+    constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = T / W;
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
@@ -41,14 +41,14 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
     const bool colok = l < N / VEC;
     const int64_t rb = (int64_t)N * sizeof(TX);
 
-    float gm[VEC], bt[VEC];
+    f2 gm[P], bt[P];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-        gm[e] = (colok && gamma) ? ld_param(gamma, pt, l * VEC + e) : 1.f;
-        bt[e] = (colok && beta) ? ld_param(beta, pt, l * VEC + e) : 0.f;
+    for (int p = 0; p < P; ++p) {
+        gm[p] = (colok && gamma) ? ld_param2(gamma, pt, l * VEC + 2 * p) : splat2(1.f);
+        bt[p] = (colok && beta) ? ld_param2(beta, pt, l * VEC + 2 * p) : splat2(0.f);
     }
 
-    Ring<1> rg;
+    Ring<1, kStagesF> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.row_bytes = rb;
     rg.R = G * U;
@@ -59,43 +59,43 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* tx = rg.tile(k, 0);
         bool ok[U];
+        f2 xv[U][P];
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int lr = u * G + g;
             ok[u] = alive && colok && b * (G * U) + lr < M;
-            float f[VEC];
-            unpack(lds128_if(ok[u], tx + lr * rb + l * 16), f);
-            s[u] = 0.f;
+            unpack2(lds128_if(ok[u], tx + lr * rb + l * 16), xv[u]);
+            f2 a2 = xv[u][0];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) s[u] += f[e];
+            for (int p = 1; p < P; ++p) a2 = add2(a2, xv[u][p]);
+            s[u] = lo2(a2) + hi2(a2);
         }
         group_allreduce<W, T, U>(s, red, parity);
         float mu[U], q[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             mu[u] = s[u] * inv_n;
-            float f[VEC], qq = 0.f;
-            unpack(lds128_if(ok[u], tx + (u * G + g) * rb + l * 16), f);
+            const f2 m2 = splat2(mu[u]);
+            f2 q2 = splat2(0.f);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float d = f[e] - mu[u];
-                qq = fmaf(d, d, qq);
+            for (int p = 0; p < P; ++p) {
+                const f2 d = sub2(xv[u][p], m2);
+                q2 = fma2(d, d, q2);
             }
-            q[u] = colok ? qq : 0.f;  // a vector past the row's end adds nothing
+            q[u] = colok ? lo2(q2) + hi2(q2) : 0.f;  // a vector past the row's end adds nothing
         }
         group_allreduce<W, T, U>(q, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int lr = u * G + g;
-            const int64_t row = b * (G * U) + lr;
+            const int64_t row = b * (G * U) + u * G + g;
             const float rs = rsqrtf(fmaf(q[u], inv_n, eps));
             if (ok[u]) {
-                float f[VEC];
-                unpack(lds128(tx + lr * rb + l * 16), f);
+                const f2 m2 = splat2(mu[u]), r2 = splat2(rs);
+                f2 o[P];
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) f[e] = fmaf((f[e] - mu[u]) * rs, gm[e], bt[e]);
-                st_stream(y + row * N + l * VEC, pack(f));
+                for (int p = 0; p < P; ++p) o[p] = fma2(mul2(sub2(xv[u][p], m2), r2), gm[p], bt[p]);
+                st_stream(y + row * N + l * VEC, pack2(o));
             }
             if (alive && l == 0 && row < M) {
                 if (mean) mean[row] = mu[u];
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
                 unsigned* fault)
 {
     constexpr int W = kSched[S].W, U = kSched[S].UB, T = kSched[S].T;
-    constexpr int VEC = Vec<TX>::kN;
+    constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = T / W;
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, 2 * U>::kFloats];
@@ -128,12 +128,13 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
     const bool colok = l < N / VEC;
     const int64_t rb = (int64_t)N * sizeof(TX);
 
-    float gm[VEC];
+    f2 gm[P];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) gm[e] = (colok && gamma) ? ld_param(gamma, pt, l * VEC + e) : 1.f;
-    float acc_g[VEC], acc_b[VEC];
+    for (int p = 0; p < P; ++p)
+        gm[p] = (colok && gamma) ? ld_param2(gamma, pt, l * VEC + 2 * p) : splat2(1.f);
+    f2 acc_g[P], acc_b[P];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) acc_g[e] = acc_b[e] = 0.f;
+    for (int p = 0; p < P; ++p) acc_g[p] = acc_b[p] = splat2(0.f);
 
     // saved statistics of this thread's rows of block b
     float mu_n[U], rs_n[U];
@@ -150,61 +151,59 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
     auto rows = [&](int64_t b, const unsigned char* tx, const unsigned char* td, bool alive,
                     auto masked) {
         constexpr bool kMask = decltype(masked)::value;
-        float mu[U], rs[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            mu[u] = mu_n[u];
-            rs[u] = rs_n[u];
-        }
-        load_stats(b + gridDim.x);  // next block of this CTA (past the end: zeros)
+        float rs[U];
+        f2 xh[U][P], dv[U][P];
         bool ok[U];
         float s[2 * U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int lr = u * G + g;
             ok[u] = alive && colok && (!kMask || b * (G * U) + lr < M);
+            const f2 m2 = splat2(mu_n[u]), r2 = splat2(rs_n[u]);
+            rs[u] = rs_n[u];
+            unpack2(lds128_if(ok[u], tx + lr * rb + l * 16), xh[u]);
+            unpack2(lds128_if(ok[u], td + lr * rb + l * 16), dv[u]);
             // (sum g, sum g*xhat); vectors past the row's end hold dy = 0
-            float xf[VEC], df[VEC];
-            unpack(lds128_if(ok[u], tx + lr * rb + l * 16), xf);
-            unpack(lds128_if(ok[u], td + lr * rb + l * 16), df);
-            s[2 * u] = s[2 * u + 1] = 0.f;
+            f2 s1 = splat2(0.f), s2 = splat2(0.f);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float xh = (xf[e] - mu[u]) * rs[u];
-                const float gg = __fmul_rn(df[e], gm[e]);
-                s[2 * u] += gg;
-                s[2 * u + 1] = fmaf(gg, xh, s[2 * u + 1]);
+            for (int p = 0; p < P; ++p) {
+                xh[u][p] = mul2(sub2(xh[u][p], m2), r2);
+                const f2 gg = mul2(dv[u][p], gm[p]);
+                s1 = add2(s1, gg);
+                s2 = fma2(gg, xh[u][p], s2);
             }
+            s[2 * u] = lo2(s1) + hi2(s1);
+            s[2 * u + 1] = lo2(s2) + hi2(s2);
         }
+        load_stats(b + gridDim.x);  // next block of this CTA (past the end: zeros)
         group_allreduce<W, T, 2 * U>(s, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int lr = u * G + g;
-            const int64_t row = b * (G * U) + lr;
+            const int64_t row = b * (G * U) + u * G + g;
             const bool okr = !kMask || row < M;
-            const float ma = s[2 * u] * inv_n;
-            const float mb = s[2 * u + 1] * inv_n;
-            float xf[VEC], df[VEC], o[VEC];
-            unpack(lds128_if(ok[u], tx + lr * rb + l * 16), xf);
-            unpack(lds128_if(ok[u], td + lr * rb + l * 16), df);
+            const f2 ma = splat2(s[2 * u] * inv_n), nmb = splat2(-(s[2 * u + 1] * inv_n));
+            const f2 r2 = splat2(rs[u]);
+            f2 o[P];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float xh = (xf[e] - mu[u]) * rs[u];
-                const float gg = __fmul_rn(df[e], gm[e]);
-                o[e] = rs[u] * (gg - ma - xh * mb);
+            for (int p = 0; p < P; ++p) {
+                // rstd * (g - mean(g) - xhat * mean(g xhat)); g - mean(g) first,
+                // so a width-one row gives exactly zero
+                const f2 gg = mul2(dv[u][p], gm[p]);
+                o[p] = mul2(r2, fma2(xh[u][p], nmb, sub2(gg, ma)));
                 if constexpr (kMask) {
-                    acc_g[e] += okr ? df[e] * xh : 0.f;
-                    acc_b[e] += okr ? df[e] : 0.f;
+                    const f2 z = splat2(0.f);
+                    acc_g[p] = add2(acc_g[p], sel2(okr, mul2(dv[u][p], xh[u][p]), z));
+                    acc_b[p] = add2(acc_b[p], sel2(okr, dv[u][p], z));
                 } else {
-                    acc_g[e] = fmaf(df[e], xh, acc_g[e]);
-                    acc_b[e] += df[e];
+                    acc_g[p] = fma2(dv[u][p], xh[u][p], acc_g[p]);
+                    acc_b[p] = add2(acc_b[p], dv[u][p]);
                 }
             }
-            if (ok[u]) st_stream(dx + row * N + l * VEC, pack(o));
+            if (ok[u]) st_stream(dx + row * N + l * VEC, pack2(o));
         }
     };
 
-    Ring<2> rg;
+    Ring<2, kStagesB> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     rg.row_bytes = rb;
@@ -223,8 +222,8 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
     if (ws == nullptr) return;  // no parameter gradient requested (uniform)
     float* wrow = ws + blockIdx.x * (2 * (int64_t)N);
     float* colbuf = reinterpret_cast<float*>(dsm + 128);  // drained ring slots, past the barriers
-    cta_store_columns<W, VEC, T>(acc_g, colbuf, wrow, N);
-    cta_store_columns<W, VEC, T>(acc_b, colbuf, wrow + N, N);
+    cta_store_columns2<W, P, T>(acc_g, colbuf, wrow, N);
+    cta_store_columns2<W, P, T>(acc_b, colbuf, wrow + N, N);
 }
 
 // ------------------------------------------------------ general (any shape)

@@ -25,17 +25,17 @@
 namespace gbn {
 namespace {
 
-// Sum of squares of one thread's vector of a row (absent vectors are zeros).
-// The forward and the backward's recomputation share it, so with the same
-// row-group width they reduce a row identically.
-template <int VEC>
-__device__ __forceinline__ float vec_sumsq(uint4 r)
+// Sum of squares of one thread's vector of a row (absent vectors are zeros):
+// pairwise fma into two lanes, then the lanes added.  The forward and the
+// backward's recomputation share it, so with the same row-group width they
+// reduce a row identically.
+template <int P>
+__device__ __forceinline__ float vec_sumsq2(const f2 (&v)[P])
 {
-    float f[VEC], s = 0.f;
-    unpack(r, f);
+    f2 s = splat2(0.f);
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) s = fmaf(f[e], f[e], s);
-    return s;
+    for (int p = 0; p < P; ++p) s = fma2(v[p], v[p], s);
+    return lo2(s) + hi2(s);
 }
 
 // ------------------------------------------------------------ fast forward
@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
                  int64_t nblocks, unsigned* fault)
 {
     constexpr int W = kSched[S].W, U = kSched[S].UF, T = kSched[S].T;
-    constexpr int VEC = Vec<TX>::kN;
+    constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = T / W;
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
@@ -55,11 +55,11 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
     const bool colok = l < N / VEC;
     const int64_t rb = (int64_t)N * sizeof(TX);
 
-    float wf[VEC];
+    f2 wf[P];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) wf[e] = colok ? ld_param(w, pt, l * VEC + e) : 0.f;
+    for (int p = 0; p < P; ++p) wf[p] = colok ? ld_param2(w, pt, l * VEC + 2 * p) : splat2(0.f);
 
-    Ring<1> rg;
+    Ring<1, kStagesF> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.row_bytes = rb;
     rg.R = G * U;
@@ -70,25 +70,26 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* tx = rg.tile(k, 0);
         bool ok[U];
+        f2 xv[U][P];
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int lr = u * G + g;
             ok[u] = alive && colok && b * (G * U) + lr < M;
-            s[u] = vec_sumsq<VEC>(lds128_if(ok[u], tx + lr * rb + l * 16));
+            unpack2(lds128_if(ok[u], tx + lr * rb + l * 16), xv[u]);
+            s[u] = vec_sumsq2<P>(xv[u]);
         }
         group_allreduce<W, T, U>(s, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int lr = u * G + g;
-            const int64_t row = b * (G * U) + lr;
+            const int64_t row = b * (G * U) + u * G + g;
             const float rs = rsqrtf(fmaf(s[u], inv_n, eps));
             if (ok[u]) {
-                float f[VEC];
-                unpack(lds128(tx + lr * rb + l * 16), f);
+                const f2 r2 = splat2(rs);
+                f2 o[P];
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) f[e] = wf[e] * round_x<TX>(f[e] * rs);
-                st_stream(y + row * N + l * VEC, pack(f));
+                for (int p = 0; p < P; ++p) o[p] = mul2(wf[p], round2<TX>(mul2(xv[u][p], r2)));
+                st_stream(y + row * N + l * VEC, pack2(o));
             }
             if (rstd && alive && l == 0 && row < M) rstd[row] = rs;
         }
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
                  int64_t nblocks, unsigned* fault)
 {
     constexpr int W = kSched[S].W, U = kSched[S].UB, T = kSched[S].T;
-    constexpr int VEC = Vec<TX>::kN;
+    constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = T / W;
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
@@ -118,11 +119,11 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
     const int64_t rb = (int64_t)N * sizeof(TX);
     const bool round_terms = (pt != kF32);  // weight in x's dtype: round dy*n
 
-    float wf[VEC], acc[VEC];
+    f2 wf[P], acc[P];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-        wf[e] = colok ? ld_param(w, pt, l * VEC + e) : 0.f;
-        acc[e] = 0.f;
+    for (int p = 0; p < P; ++p) {
+        wf[p] = colok ? ld_param2(w, pt, l * VEC + 2 * p) : splat2(0.f);
+        acc[p] = splat2(0.f);
     }
     float rs_n[U];
     auto load_rstd = [&](int64_t b) {
@@ -140,17 +141,20 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
                     auto masked) {
         constexpr bool kMask = decltype(masked)::value;
         float rs[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) rs[u] = rs_n[u];
-        load_rstd(b + gridDim.x);
         bool ok[U];
+        f2 xv[U][P], dv[U][P];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            ok[u] = alive && colok && (!kMask || b * (G * U) + u * G + g < M);
+        for (int u = 0; u < U; ++u) {
+            const int lr = u * G + g;
+            ok[u] = alive && colok && (!kMask || b * (G * U) + lr < M);
+            unpack2(lds128_if(ok[u], tx + lr * rb + l * 16), xv[u]);
+            unpack2(lds128_if(ok[u], td + lr * rb + l * 16), dv[u]);
+            rs[u] = rs_n[u];
+        }
+        load_rstd(b + gridDim.x);
         if (!rstd) {  // uniform branch: recompute r exactly as the forward does
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                rs[u] = vec_sumsq<VEC>(lds128_if(ok[u], tx + (u * G + g) * rb + l * 16));
+            for (int u = 0; u < U; ++u) rs[u] = vec_sumsq2<P>(xv[u]);
             group_allreduce<W, T, U>(rs, red, parity);
 #pragma unroll
             for (int u = 0; u < U; ++u) rs[u] = rsqrtf(fmaf(rs[u], inv_n, eps));
@@ -158,42 +162,37 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int lr = u * G + g;
-            float xf[VEC], df[VEC];
-            unpack(lds128_if(ok[u], tx + lr * rb + l * 16), xf);
-            unpack(lds128_if(ok[u], td + lr * rb + l * 16), df);
-            s[u] = 0.f;
+            const f2 r2 = splat2(rs[u]);
+            f2 a2 = splat2(0.f);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e)
-                s[u] = fmaf(round_x<TX>(df[e] * wf[e]), xf[e] * rs[u], s[u]);
+            for (int p = 0; p < P; ++p)
+                a2 = fma2(round2<TX>(mul2(dv[u][p], wf[p])), mul2(xv[u][p], r2), a2);
+            s[u] = lo2(a2) + hi2(a2);
         }
         group_allreduce<W, T, U>(s, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int lr = u * G + g;
-            const int64_t row = b * (G * U) + lr;
+            const int64_t row = b * (G * U) + u * G + g;
             const bool okr = !kMask || row < M;
-            const float m = s[u] * inv_n;
-            float xf[VEC], df[VEC], o[VEC];
-            unpack(lds128_if(ok[u], tx + lr * rb + l * 16), xf);
-            unpack(lds128_if(ok[u], td + lr * rb + l * 16), df);
+            const f2 r2 = splat2(rs[u]), nm = splat2(-(s[u] * inv_n));
+            f2 o[P];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-                const float xh = xf[e] * rs[u];
-                const float dn = round_x<TX>(df[e] * wf[e]);
-                o[e] = rs[u] * (dn - xh * m);
-                float term = df[e] * round_x<TX>(xh);
-                if (round_terms) term = round_x<TX>(term);
+            for (int p = 0; p < P; ++p) {
+                const f2 xh = mul2(xv[u][p], r2);
+                const f2 dn = round2<TX>(mul2(dv[u][p], wf[p]));
+                o[p] = mul2(r2, fma2(xh, nm, dn));
+                f2 term = mul2(dv[u][p], round2<TX>(xh));
+                if (round_terms) term = round2<TX>(term);
                 if constexpr (kMask)
-                    acc[e] += okr ? term : 0.f;
+                    acc[p] = add2(acc[p], sel2(okr, term, splat2(0.f)));
                 else
-                    acc[e] += term;
+                    acc[p] = add2(acc[p], term);
             }
-            if (ok[u]) st_stream(dx + row * N + l * VEC, pack(o));
+            if (ok[u]) st_stream(dx + row * N + l * VEC, pack2(o));
         }
     };
 
-    Ring<2> rg;
+    Ring<2, kStagesB> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     rg.row_bytes = rb;
@@ -211,7 +210,7 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
 
     if (ws == nullptr) return;  // no weight gradient requested (uniform)
     float* wrow = ws + blockIdx.x * (int64_t)N;
-    cta_store_columns<W, VEC, T>(acc, reinterpret_cast<float*>(dsm + 128), wrow, N);  // drained ring slots
+    cta_store_columns2<W, P, T>(acc, reinterpret_cast<float*>(dsm + 128), wrow, N);  // drained ring slots
 }
 
 // ------------------------------------------------------ general (any shape)

@@ -26,7 +26,8 @@ LIB = os.path.join(OUT, "libgbnorm.so")
 SOURCES = ["api.cu", "colsum.cu", "dyt.cu", "layernorm.cu", "rmsnorm.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
+                     "-I", INCLUDE,
                      "-I", CSRC]
 
 

@@ -98,21 +98,21 @@ int fast_sid(int64_t N, int xt)
     return -1;
 }
 
-// The launch layout of one row-wise kernel.  two_streams: the kernel uses the
-// schedule's UB rows per group (the backward kernels read x and dy).
-Launch plan(int64_t M, int64_t N, int xt, bool aligned, int sms, cudaStream_t stream,
-            bool two_streams)
+// The launch layout of one row-wise kernel of the given kind (gbn::kFwdDyT,
+// gbn::kFwdNorm or gbn::kBwd).
+Launch plan(int64_t M, int64_t N, int xt, bool aligned, int sms, cudaStream_t stream, int kind)
 {
     Launch L{};
     L.stream = stream;
     const int sid = aligned ? fast_sid(N, xt) : -1;
     if (sid >= 0) {
         const gbn::SchedEntry& e = gbn::kSched[sid];
-        const int64_t rows_per_block = (int64_t)(e.T / e.W) * (two_streams ? e.UB : e.UF);
+        const int64_t rows_per_block =
+            (int64_t)gbn::groups_per_cta(e.W, e.T) * gbn::kind_U(sid, kind);
         L.fast = 1;
         L.sid = sid;
         L.nblocks = (M + rows_per_block - 1) / rows_per_block;
-        const int64_t cap = (int64_t)sms * (two_streams ? e.MINBB : e.MINBF);
+        const int64_t cap = (int64_t)sms * gbn::kind_minb(sid, kind);
         L.grid = (int)(L.nblocks < cap ? L.nblocks : cap);
         L.P = L.grid;
     } else {
@@ -222,8 +222,9 @@ size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int
     if (M == 0) return 0;
     const int sms = sm_count(device);
     if (sms <= 0) return (size_t)-1;
-    const Launch a = plan(M, N, xt, true, sms, nullptr, true);
-    const Launch b = plan(M, N, xt, false, sms, nullptr, true);
+    const Launch a =
+        plan(M, N, xt, true, sms, nullptr, op == GBN_OP_DYT ? gbn::kBwdDyT : gbn::kBwd);
+    const Launch b = plan(M, N, xt, false, sms, nullptr, gbn::kBwd);
     const size_t need = ws_needed(op, a.P > b.P ? a : b, N);
     return (need + 255) & ~(size_t)255;
 }
@@ -239,7 +240,7 @@ int dyt_fwd(const void* x, const void* alpha, const void* gamma, const void* bet
     if (M == 0) return GBN_OK;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, false);
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, gbn::kFwdDyT);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (!L.fast) {  // elementwise general path: one thread per element, grid-stride
         const int64_t E = M * N;
@@ -264,7 +265,7 @@ int dyt_bwd(const void* x, const void* dy, const void* alpha, const void* gamma,
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                          true);
+                    gbn::kBwdDyT);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_DYT, L, N))) return GBN_EWORKSPACE;
     float* wsf = grads ? static_cast<float*>(ws) : nullptr;
@@ -290,7 +291,8 @@ int layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, f
     if (M == 0) return GBN_OK;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, false);
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream,
+                    gbn::kFwdNorm);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     return launch_status(
         gbn::launch_ln_fwd(L, xt, pt, x, gamma, beta, y, mean, rstd, M, (int)N, eps));
@@ -311,7 +313,7 @@ int layernorm_bwd(const void* x, const void* dy, const float* mean, const float*
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                          true);
+                    gbn::kBwd);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_LAYERNORM, L, N)))
         return GBN_EWORKSPACE;
@@ -337,7 +339,8 @@ int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, i
     if (M == 0) return GBN_OK;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, false);
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream,
+                    gbn::kFwdNorm);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     return launch_status(gbn::launch_rms_fwd(L, xt, wt, x, w, y, rstd, M, (int)N, eps));
 }
@@ -355,7 +358,7 @@ int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd,
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                          true);
+                    gbn::kBwd);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (dw && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_RMSNORM, L, N))) return GBN_EWORKSPACE;
     float* wsf = dw ? static_cast<float*>(ws) : nullptr;

@@ -26,36 +26,95 @@ enum DType : int { kF32 = 0, kBF16 = 1 };
 // never on U, so a forward and a backward with different U reduce a row
 // identically.
 struct SchedEntry {
-    int max_nvec, W, UF, UB, T, MINBF, MINBB;
+    int max_nvec, W, T;
 };
 
 // One 16-byte vector per thread per row: a row of nvec vectors takes
 // W = next_pow2(nvec) threads, so register pressure stays flat from N = 8
-// to N = 8192 bf16.  Row blocks of T/W * U rows (8-16 KB per staged tensor)
-// stream through a shared-memory ring filled by the bulk-copy engine.
-// MINBF/MINBB: CTAs per SM the forward/backward are sized for (registers
-// through __launch_bounds__, shared memory through the ring size).
-constexpr int kNumSched = 11;
+// to N = 8192 bf16.  A CTA has T = max(256, W) threads.
+// Rows of exactly 3 vectors (bf16 N = 24, the tall-narrow LayerNorm of the
+// torch-xpu-ops page) take segmented groups of W = 3 lanes, 10 per warp,
+// instead of 4-lane groups with a lane idle.
+constexpr int kNumSched = 12;
 constexpr SchedEntry kSched[kNumSched] = {
-    {1, 1, 2, 2, 256, 4, 2},        {2, 2, 2, 2, 256, 4, 2},       {4, 4, 2, 2, 256, 4, 2},
-    {8, 8, 2, 2, 256, 4, 2},        {16, 16, 2, 2, 256, 4, 2},     {32, 32, 2, 2, 256, 4, 2},
-    {64, 64, 2, 2, 256, 4, 2},      {128, 128, 2, 2, 256, 4, 2},   {256, 256, 2, 2, 256, 4, 2},
-    {512, 512, 1, 1, 512, 2, 2},    {1024, 1024, 1, 1, 1024, 1, 1},
+    {1, 1, 256},     {2, 2, 256},     {3, 3, 256},     {4, 4, 256},
+    {8, 8, 256},     {16, 16, 256},   {32, 32, 256},   {64, 64, 256},
+    {128, 128, 256}, {256, 256, 256}, {512, 512, 512}, {1024, 1024, 1024},
 };
-constexpr int kStagesF = 4;  // ring depth of the forward kernels (one staged tensor)
-constexpr int kStagesB = 4;  // ring depth of the backward kernels (x and dy)
+constexpr int kMaxFastVec = 1024;
+
+// Row groups of a power-of-two width tile the CTA; a width that is not a
+// power of two packs floor(32/W) groups per warp and leaves the rest of the
+// warp's lanes idle.
+constexpr bool seg_groups(int W) { return (W & (W - 1)) != 0; }
+constexpr int groups_per_cta(int W, int T) { return seg_groups(W) ? (T / 32) * (32 / W) : T / W; }
+
+template <int W>
+__device__ __forceinline__ int grp()
+{
+    if constexpr (seg_groups(W))
+        return (threadIdx.x >> 5) * (32 / W) + (threadIdx.x & 31) / W;
+    else
+        return threadIdx.x / W;
+}
+template <int W>
+__device__ __forceinline__ int lan()
+{
+    if constexpr (seg_groups(W))
+        return (threadIdx.x & 31) % W;
+    else
+        return threadIdx.x % W;
+}
+// false for the idle lanes of a segmented warp
+template <int W>
+__device__ __forceinline__ bool in_group()
+{
+    if constexpr (seg_groups(W))
+        return (threadIdx.x & 31) < (32 / W) * W;
+    else
+        return true;
+}
+
+// Launch traits per kernel kind: U rows per thread per row block, CTAs per
+// SM (registers through __launch_bounds__, shared memory through the ring),
+// and ring depth.  Row blocks of T/W * U rows are 8-32 KB per staged tensor.
+// DyT's kernels have no row reduction and the most arithmetic per byte, so
+// they take the largest blocks; the backward kernels stage two tensors and
+// keep more per-row state, so they run 2 CTAs per SM.  At the widest rows
+// (512 threads at 2 CTAs per SM, 64 registers) the backwards keep one row
+// per thread: two spill.
+enum KernelKind : int { kFwdDyT = 0, kFwdNorm = 1, kBwd = 2, kBwdDyT = 3 };
+
+constexpr int kind_U(int S, int kind)
+{
+    return kind == kBwd      ? (kSched[S].T == 256 ? 2 : 1)
+           : kind == kBwdDyT ? (kSched[S].T == 512 ? 1 : 2)
+           : kind == kFwdDyT && kSched[S].T == 256 ? 4
+                                                   : 2;
+}
+constexpr int kind_minb(int S, int kind)
+{
+    return kSched[S].T == 1024 ? 1
+           : kSched[S].T == 512 ? 2
+           : kind == kBwd || kind == kBwdDyT ? 2
+           : kind == kFwdDyT                 ? 3
+                                             : 4;
+}
+constexpr int kind_stages(int S, int kind)
+{
+    return kind == kBwdDyT && kSched[S].T == 1024 ? 3 : 4;
+}
 
 // Bytes of one ring slot for one staged tensor, and of the whole dynamic
 // shared memory a kernel with NT staged tensors needs (barriers first).
-__host__ __device__ constexpr int slot_bytes(int S, bool bwd)
+constexpr int slot_bytes(int S, int kind)
 {
-    return kSched[S].T * (bwd ? kSched[S].UB : kSched[S].UF) * 16;
+    return groups_per_cta(kSched[S].W, kSched[S].T) * kSched[S].W * kind_U(S, kind) * 16;
 }
-__host__ __device__ constexpr int ring_smem_bytes(int S, bool bwd, int NT)
+constexpr int ring_smem_bytes(int S, int kind, int NT)
 {
-    return 128 + (bwd ? kStagesB : kStagesF) * NT * slot_bytes(S, bwd);
+    return 128 + kind_stages(S, kind) * NT * slot_bytes(S, kind);
 }
-constexpr int kMaxFastVec = 1024;
 
 // Threads per CTA and warps per CTA of the general (any width, any
 // alignment) kernels, which give every warp one row at a time.
@@ -423,6 +482,37 @@ __device__ __forceinline__ uint4 pack2(const f2 (&p)[2])
     return u;
 }
 
+// acc + a*b for bf16 a, b (the low or high halves of packed pairs): one
+// instruction, the exact product added with one rounding to float32.
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float acc)
+{
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+    return acc;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float acc)
+{
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+    return acc;
+}
+
+// Two bf16 products of bf16 pairs, each rounded once to bf16 (the exact
+// product of two bf16 values fits in float32, so this equals rounding the
+// float32 product).
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // Round both lanes to the activation dtype's precision (identity for f32).
 template <typename TX> __device__ __forceinline__ f2 round2(f2 a);
 template <> __device__ __forceinline__ f2 round2<float>(f2 a) { return a; }
@@ -471,7 +561,17 @@ struct GroupRed {
 template <int W, int T, int NV>
 __device__ __forceinline__ void group_allreduce(float (&v)[NV], float* red, int& parity)
 {
-    if constexpr (W <= 32) {
+    if constexpr (seg_groups(W)) {
+        // gather the group's W values in lane order: the same sum on every lane
+        const int base = ((threadIdx.x & 31) / W) * W;
+#pragma unroll
+        for (int k = 0; k < NV; ++k) {
+            float sum = __shfl_sync(0xffffffffu, v[k], base);
+#pragma unroll
+            for (int j = 1; j < W; ++j) sum += __shfl_sync(0xffffffffu, v[k], base + j);
+            v[k] = sum;
+        }
+    } else if constexpr (W <= 32) {
         butterfly<W, NV>(v);
     } else {
         constexpr int kWarps = W / 32;
@@ -522,10 +622,10 @@ template <int W, int VEC, int T>
 __device__ __forceinline__ void cta_store_columns(const float (&acc)[VEC], float* buf,
                                                   float* __restrict__ out_row, int N)
 {
-    constexpr int kG = T / W;
+    constexpr int kG = groups_per_cta(W, T);
     constexpr int kCap = W * VEC;
-    const int g = threadIdx.x / W;
-    const int l = threadIdx.x % W;
+    const int g = grp<W>();
+    const int l = lan<W>();
     if constexpr (kG == 1) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
@@ -533,8 +633,10 @@ __device__ __forceinline__ void cta_store_columns(const float (&acc)[VEC], float
             if (c < N) out_row[c] = acc[e];
         }
     } else {
+        if (in_group<W>()) {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) buf[g * kCap + l * VEC + e] = acc[e];
+            for (int e = 0; e < VEC; ++e) buf[g * kCap + l * VEC + e] = acc[e];
+        }
         __syncthreads();
         for (int c = threadIdx.x; c < kCap && c < N; c += T) {
             float s = buf[c];

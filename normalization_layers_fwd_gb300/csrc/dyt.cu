@@ -111,19 +111,23 @@ __device__ __forceinline__ void dyt_tanh_sech2_2(f2 z, f2& t, f2& s)
 }
 
 // ------------------------------------------------------------ fast forward
+// Addressing: a thread's vector of row u of a block sits at soff + u*srow in
+// the ring slot and at row0*N + l*VEC + u*grow in HBM (row0 = the block's
+// first row + g); only the ragged last block compares rows against M.
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
+__global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
     dyt_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ alpha,
                  const void* __restrict__ gamma, const void* __restrict__ beta, int pt,
                  int64_t M, int N, int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kSched[S].UF, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kFwdDyT), T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
-    constexpr int G = T / W;
+    constexpr int G = groups_per_cta(W, T);
     extern __shared__ __align__(128) unsigned char dsm[];
-    const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const bool colok = l < N / VEC;
-    const int64_t rb = (int64_t)N * sizeof(TX);
+    const int g = grp<W>(), l = lan<W>();
+    const bool colok = in_group<W>() && l < N / VEC;
+    const int rb = N * (int)sizeof(TX);
+    const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
 
     const f2 a2 = splat2(ld_param(alpha, pt, 0));
     f2 gm[P], bt[P];
@@ -133,26 +137,28 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
         bt[p] = colok ? ld_param2(beta, pt, l * VEC + 2 * p) : splat2(0.f);
     }
 
-    Ring<1, kStagesF> rg;
+    Ring<1, kind_stages(S, kFwdDyT)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = slot_bytes(S, false);
+    rg.slot = slot_bytes(S, kFwdDyT);
     rg.fault = fault;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
-        const unsigned char* tx = rg.tile(k, 0);
+        if (!alive || !colok) return;  // nothing collective in this kernel
+        const unsigned char* xs = rg.tile(k, 0) + soff;
+        const int64_t row0 = b * (G * U) + g;
+        const bool full = (b + 1) * (G * U) <= M;
+        TX* yb = y + row0 * N + l * VEC;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int lr = u * G + g;
-            const int64_t row = b * (G * U) + lr;
-            if (alive && colok && row < M) {
+            if (full || row0 + u * G < M) {
                 f2 v[P];
-                unpack2(lds128(tx + lr * rb + l * 16), v);
+                unpack2(lds128(xs + u * srow), v);
 #pragma unroll
                 for (int p = 0; p < P; ++p) v[p] = fma2(gm[p], dyt_tanh2(mul2(a2, v[p])), bt[p]);
-                st_stream(y + row * N + l * VEC, pack2(v));
+                st_stream(yb + u * grow, pack2(v));
             }
         }
     });
@@ -163,22 +169,22 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
 // only the ragged last block masks its padded rows, by a select after the
 // arithmetic (its slots past the last row hold stale data).
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
+__global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     dyt_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy, TX* __restrict__ dx,
                  const void* __restrict__ alpha, const void* __restrict__ gamma, int pt,
                  float* __restrict__ ws, int64_t M, int N, int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kSched[S].UB, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kBwdDyT), T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
-    constexpr int G = T / W;
+    constexpr int G = groups_per_cta(W, T);
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[T / 32];
-    const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const bool colok = l < N / VEC;
-    const int64_t rb = (int64_t)N * sizeof(TX);
+    const int g = grp<W>(), l = lan<W>();
+    const bool colok = in_group<W>() && l < N / VEC;
+    const int rb = N * (int)sizeof(TX);
+    const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
 
-    const float a = ld_param(alpha, pt, 0);
-    const f2 a2 = splat2(a);
+    const f2 a2 = splat2(ld_param(alpha, pt, 0));
     f2 gm[P], ga[P];
 #pragma unroll
     for (int p = 0; p < P; ++p) {
@@ -191,54 +197,56 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
 #pragma unroll
     for (int p = 0; p < P; ++p) acc_g[p] = acc_b[p] = acc_a[p] = splat2(0.f);
 
-    auto rows = [&](int64_t b, const unsigned char* tx, const unsigned char* td, bool alive,
+    auto rows = [&](const unsigned char* xs, const unsigned char* ds, TX* dxb, int64_t row0,
                     auto masked) {
         constexpr bool kMask = decltype(masked)::value;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int lr = u * G + g;
-            const int64_t row = b * (G * U) + lr;
-            const bool okr = !kMask || row < M;
-            if (!alive || !colok) continue;
+            const bool okr = !kMask || row0 + u * G < M;
             f2 xv[P], dv[P], o[P];
-            unpack2(lds128(tx + lr * rb + l * 16), xv);
-            unpack2(lds128(td + lr * rb + l * 16), dv);
+            unpack2(lds128(xs + u * srow), xv);
+            unpack2(lds128(ds + u * srow), dv);
 #pragma unroll
             for (int p = 0; p < P; ++p) {
                 f2 t, s;
                 dyt_tanh_sech2_2(mul2(a2, xv[p]), t, s);
-                const f2 ds = mul2(dv[p], s);
-                o[p] = mul2(ds, ga[p]);
+                const f2 dsd = mul2(dv[p], s);
+                o[p] = mul2(dsd, ga[p]);
                 if constexpr (kMask) {
                     // padded rows: select after the arithmetic, never a 0/1 multiply
                     const f2 z = splat2(0.f);
                     acc_g[p] = add2(acc_g[p], sel2(okr, mul2(dv[p], t), z));
                     acc_b[p] = add2(acc_b[p], sel2(okr, dv[p], z));
-                    acc_a[p] = add2(acc_a[p], sel2(okr, mul2(ds, xv[p]), z));
+                    acc_a[p] = add2(acc_a[p], sel2(okr, mul2(dsd, xv[p]), z));
                 } else {
                     acc_g[p] = fma2(dv[p], t, acc_g[p]);
                     acc_b[p] = add2(acc_b[p], dv[p]);
-                    acc_a[p] = fma2(ds, xv[p], acc_a[p]);
+                    acc_a[p] = fma2(dsd, xv[p], acc_a[p]);
                 }
             }
-            if (okr) st_stream(dx + row * N + l * VEC, pack2(o));
+            if (okr) st_stream(dxb + u * grow, pack2(o));
         }
     };
 
-    Ring<2, kStagesB> rg;
+    Ring<2, kind_stages(S, kBwdDyT)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = slot_bytes(S, true);
+    rg.slot = slot_bytes(S, kBwdDyT);
     rg.fault = fault;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        if (!alive || !colok) return;  // nothing collective in this kernel
+        const int64_t row0 = b * (G * U) + g;
+        TX* dxb = dx + row0 * N + l * VEC;
+        const unsigned char* xs = rg.tile(k, 0) + soff;
+        const unsigned char* ds = rg.tile(k, 1) + soff;
         if ((b + 1) * (G * U) <= M)
-            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::false_type{});
+            rows(xs, ds, dxb, row0, std::false_type{});
         else
-            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::true_type{});
+            rows(xs, ds, dxb, row0, std::true_type{});
     });
 
     if (ws == nullptr) return;  // no parameter gradient requested (uniform)
@@ -328,16 +336,17 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* alp
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, false, 1);                                   \
+        constexpr int smem = ring_smem_bytes(S, kFwdDyT, 1);                                   \
         auto kern = dyt_fwd_fast<TX, S>;                                                     \
-        if (smem > 48 * 1024)                                                                \
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,          \
+                             cudaSharedmemCarveoutMaxShared);                               \
         kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, alpha, gamma, beta, pt, M, N, \
                                                        L.nblocks, L.fault);                  \
         break;                                                                               \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
-        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
+        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }
@@ -359,16 +368,17 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, true, 2);                                    \
+        constexpr int smem = ring_smem_bytes(S, kBwdDyT, 2);                                    \
         auto kern = dyt_bwd_fast<TX, S>;                                                     \
-        if (smem > 48 * 1024)                                                                \
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,          \
+                             cudaSharedmemCarveoutMaxShared);                               \
         kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, dyp, dxp, alpha, gamma, pt, ws, M, \
                                                        N, L.nblocks, L.fault);               \
         break;                                                                               \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
-        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
+        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }

@@ -23,23 +23,25 @@ namespace {
 // ------------------------------------------------------------ fast forward
 // x streams through the ring; two row all-reduces (sum, then the centred sum
 // of squares) per row.  Every thread runs every row (row reductions are
-// collective); loads and stores are predicated.
+// collective); loads and stores are predicated, and only the ragged last
+// block compares rows against M.
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
+__global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
     ln_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ gamma,
                 const void* __restrict__ beta, int pt, float* __restrict__ mean,
                 float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
                 int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kSched[S].UF, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kFwdNorm), T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
-    constexpr int G = T / W;
+    constexpr int G = groups_per_cta(W, T);
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
     int parity = 0;
-    const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const bool colok = l < N / VEC;
-    const int64_t rb = (int64_t)N * sizeof(TX);
+    const int g = grp<W>(), l = lan<W>();
+    const bool colok = in_group<W>() && l < N / VEC;
+    const int rb = N * (int)sizeof(TX);
+    const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
 
     f2 gm[P], bt[P];
 #pragma unroll
@@ -48,24 +50,26 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
         bt[p] = (colok && beta) ? ld_param2(beta, pt, l * VEC + 2 * p) : splat2(0.f);
     }
 
-    Ring<1, kStagesF> rg;
+    Ring<1, kind_stages(S, kFwdNorm)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = slot_bytes(S, false);
+    rg.slot = slot_bytes(S, kFwdNorm);
     rg.fault = fault;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
-        const unsigned char* tx = rg.tile(k, 0);
-        bool ok[U];
+        const unsigned char* xs = rg.tile(k, 0) + soff;
+        const int64_t row0 = b * (G * U) + g;
+        const bool full = (b + 1) * (G * U) <= M;
+        bool okr[U], ok[U];
         f2 xv[U][P];
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int lr = u * G + g;
-            ok[u] = alive && colok && b * (G * U) + lr < M;
-            unpack2(lds128_if(ok[u], tx + lr * rb + l * 16), xv[u]);
+            okr[u] = alive && (full || row0 + u * G < M);
+            ok[u] = okr[u] && colok;
+            unpack2(lds128_if(ok[u], xs + u * srow), xv[u]);
             f2 a2 = xv[u][0];
 #pragma unroll
             for (int p = 1; p < P; ++p) a2 = add2(a2, xv[u][p]);
@@ -86,20 +90,20 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
             q[u] = colok ? lo2(q2) + hi2(q2) : 0.f;  // a vector past the row's end adds nothing
         }
         group_allreduce<W, T, U>(q, red, parity);
+        TX* yb = y + row0 * N + l * VEC;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t row = b * (G * U) + u * G + g;
             const float rs = rsqrtf(fmaf(q[u], inv_n, eps));
             if (ok[u]) {
                 const f2 m2 = splat2(mu[u]), r2 = splat2(rs);
                 f2 o[P];
 #pragma unroll
                 for (int p = 0; p < P; ++p) o[p] = fma2(mul2(sub2(xv[u][p], m2), r2), gm[p], bt[p]);
-                st_stream(y + row * N + l * VEC, pack2(o));
+                st_stream(yb + u * grow, pack2(o));
             }
-            if (alive && l == 0 && row < M) {
-                if (mean) mean[row] = mu[u];
-                if (rstd) rstd[row] = rs;
+            if (okr[u] && l == 0 && in_group<W>()) {
+                if (mean) mean[row0 + u * G] = mu[u];
+                if (rstd) rstd[row0 + u * G] = rs;
             }
         }
     });
@@ -111,22 +115,23 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
 // Full row blocks run without masking; the ragged last block masks its
 // padded rows by a select after the arithmetic.
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
+__global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwd))
     ln_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy,
                 const float* __restrict__ mean, const float* __restrict__ rstd,
                 const void* __restrict__ gamma, int pt, TX* __restrict__ dx,
                 float* __restrict__ ws, int64_t M, int N, float inv_n, int64_t nblocks,
                 unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kSched[S].UB, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kBwd), T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
-    constexpr int G = T / W;
+    constexpr int G = groups_per_cta(W, T);
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, 2 * U>::kFloats];
     int parity = 0;
-    const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const bool colok = l < N / VEC;
-    const int64_t rb = (int64_t)N * sizeof(TX);
+    const int g = grp<W>(), l = lan<W>();
+    const bool colok = in_group<W>() && l < N / VEC;
+    const int rb = N * (int)sizeof(TX);
+    const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
 
     f2 gm[P];
 #pragma unroll
@@ -136,87 +141,90 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
 #pragma unroll
     for (int p = 0; p < P; ++p) acc_g[p] = acc_b[p] = splat2(0.f);
 
-    // saved statistics of this thread's rows of block b
+    // saved statistics of this thread's rows of the block starting at row0
     float mu_n[U], rs_n[U];
-    auto load_stats = [&](int64_t b) {
+    auto load_stats = [&](int64_t row0) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t row = b * (G * U) + u * G + g;
+            const int64_t row = row0 + u * G;
             mu_n[u] = row < M ? __ldcs(mean + row) : 0.f;
             rs_n[u] = row < M ? __ldcs(rstd + row) : 0.f;
         }
     };
-    load_stats(blockIdx.x);
+    load_stats((int64_t)blockIdx.x * (G * U) + g);
 
-    auto rows = [&](int64_t b, const unsigned char* tx, const unsigned char* td, bool alive,
-                    auto masked) {
+    // Pass 1 (before the row reduction) also accumulates the parameter
+    // gradients, which do not depend on it; pass 2 keeps only xhat and g.
+    auto rows = [&](const unsigned char* xs, const unsigned char* ds, TX* dxb, int64_t row0,
+                    bool alive, auto masked) {
         constexpr bool kMask = decltype(masked)::value;
         float rs[U];
-        f2 xh[U][P], dv[U][P];
+        f2 xh[U][P], gg[U][P];
         bool ok[U];
         float s[2 * U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int lr = u * G + g;
-            ok[u] = alive && colok && (!kMask || b * (G * U) + lr < M);
+            ok[u] = alive && colok && (!kMask || row0 + u * G < M);
+            const bool okr = !kMask || row0 + u * G < M;
             const f2 m2 = splat2(mu_n[u]), r2 = splat2(rs_n[u]);
             rs[u] = rs_n[u];
-            unpack2(lds128_if(ok[u], tx + lr * rb + l * 16), xh[u]);
-            unpack2(lds128_if(ok[u], td + lr * rb + l * 16), dv[u]);
+            f2 dv[P];
+            unpack2(lds128_if(ok[u], xs + u * srow), xh[u]);
+            unpack2(lds128_if(ok[u], ds + u * srow), dv);
             // (sum g, sum g*xhat); vectors past the row's end hold dy = 0
             f2 s1 = splat2(0.f), s2 = splat2(0.f);
 #pragma unroll
             for (int p = 0; p < P; ++p) {
                 xh[u][p] = mul2(sub2(xh[u][p], m2), r2);
-                const f2 gg = mul2(dv[u][p], gm[p]);
-                s1 = add2(s1, gg);
-                s2 = fma2(gg, xh[u][p], s2);
+                gg[u][p] = mul2(dv[p], gm[p]);
+                s1 = add2(s1, gg[u][p]);
+                s2 = fma2(gg[u][p], xh[u][p], s2);
+                if constexpr (kMask) {
+                    // padded rows: select after the arithmetic, never a 0/1 multiply
+                    const f2 z = splat2(0.f);
+                    acc_g[p] = add2(acc_g[p], sel2(okr, mul2(dv[p], xh[u][p]), z));
+                    acc_b[p] = add2(acc_b[p], sel2(okr, dv[p], z));
+                } else {
+                    acc_g[p] = fma2(dv[p], xh[u][p], acc_g[p]);
+                    acc_b[p] = add2(acc_b[p], dv[p]);
+                }
             }
             s[2 * u] = lo2(s1) + hi2(s1);
             s[2 * u + 1] = lo2(s2) + hi2(s2);
         }
-        load_stats(b + gridDim.x);  // next block of this CTA (past the end: zeros)
+        load_stats(row0 + (int64_t)gridDim.x * (G * U));  // next block of this CTA
         group_allreduce<W, T, 2 * U>(s, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t row = b * (G * U) + u * G + g;
-            const bool okr = !kMask || row < M;
             const f2 ma = splat2(s[2 * u] * inv_n), nmb = splat2(-(s[2 * u + 1] * inv_n));
             const f2 r2 = splat2(rs[u]);
             f2 o[P];
+            // rstd * (g - mean(g) - xhat * mean(g xhat)); g - mean(g) first,
+            // so a width-one row gives exactly zero
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                // rstd * (g - mean(g) - xhat * mean(g xhat)); g - mean(g) first,
-                // so a width-one row gives exactly zero
-                const f2 gg = mul2(dv[u][p], gm[p]);
-                o[p] = mul2(r2, fma2(xh[u][p], nmb, sub2(gg, ma)));
-                if constexpr (kMask) {
-                    const f2 z = splat2(0.f);
-                    acc_g[p] = add2(acc_g[p], sel2(okr, mul2(dv[u][p], xh[u][p]), z));
-                    acc_b[p] = add2(acc_b[p], sel2(okr, dv[u][p], z));
-                } else {
-                    acc_g[p] = fma2(dv[u][p], xh[u][p], acc_g[p]);
-                    acc_b[p] = add2(acc_b[p], dv[u][p]);
-                }
-            }
-            if (ok[u]) st_stream(dx + row * N + l * VEC, pack2(o));
+            for (int p = 0; p < P; ++p) o[p] = mul2(r2, fma2(xh[u][p], nmb, sub2(gg[u][p], ma)));
+            if (ok[u]) st_stream(dxb + u * grow, pack2(o));
         }
     };
 
-    Ring<2, kStagesB> rg;
+    Ring<2, kind_stages(S, kBwd)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = slot_bytes(S, true);
+    rg.slot = slot_bytes(S, kBwd);
     rg.fault = fault;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        const int64_t row0 = b * (G * U) + g;
+        TX* dxb = dx + row0 * N + l * VEC;
+        const unsigned char* xs = rg.tile(k, 0) + soff;
+        const unsigned char* ds = rg.tile(k, 1) + soff;
         if ((b + 1) * (G * U) <= M)
-            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::false_type{});
+            rows(xs, ds, dxb, row0, alive, std::false_type{});
         else
-            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::true_type{});
+            rows(xs, ds, dxb, row0, alive, std::true_type{});
     });
 
     if (ws == nullptr) return;  // no parameter gradient requested (uniform)
@@ -316,15 +324,16 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, false, 1);                                  \
+        constexpr int smem = ring_smem_bytes(S, kFwdNorm, 1);                                  \
         auto kern = ln_fwd_fast<TX, S>;                                                      \
-        if (smem > 48 * 1024)                                                                \
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,          \
+                             cudaSharedmemCarveoutMaxShared);                               \
         kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault);                              \
         break;                                                                               \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
-        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
+        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }
@@ -348,15 +357,16 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, true, 2);                                  \
+        constexpr int smem = ring_smem_bytes(S, kBwd, 2);                                  \
         auto kern = ln_bwd_fast<TX, S>;                                                      \
-        if (smem > 48 * 1024)                                                                \
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,          \
+                             cudaSharedmemCarveoutMaxShared);                               \
         kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.nblocks, L.fault);                              \
         break;                                                                               \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
-        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
+        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }

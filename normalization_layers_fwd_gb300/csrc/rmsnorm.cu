@@ -38,60 +38,96 @@ __device__ __forceinline__ float vec_sumsq2(const f2 (&v)[P])
     return lo2(s) + hi2(s);
 }
 
+// Words of one 16-byte vector (4 bf16 pairs, or 2 f32 pairs' worth).
+__device__ __forceinline__ uint32_t word(const uint4& v, int p)
+{
+    return p == 0 ? v.x : p == 1 ? v.y : p == 2 ? v.z : v.w;
+}
+
+// With bf16 activations and a bf16 weight, the products w*n (forward), dy*w
+// and dy*n (backward) are products of two bf16 values, exact in float32 and
+// rounded once to bf16 by the rounding points above; mul.rn.bf16x2 computes
+// exactly that on a packed pair.  Other dtype pairs take float32 pairs.
+template <typename TX>
+__device__ __forceinline__ constexpr bool is_bf16()
+{
+    return std::is_same<TX, __nv_bfloat16>::value;
+}
+
 // ------------------------------------------------------------ fast forward
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
+__global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
     rms_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ w,
                  int pt, float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
                  int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kSched[S].UF, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kFwdNorm), T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
-    constexpr int G = T / W;
+    constexpr int G = groups_per_cta(W, T);
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
     int parity = 0;
-    const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const bool colok = l < N / VEC;
-    const int64_t rb = (int64_t)N * sizeof(TX);
+    const int g = grp<W>(), l = lan<W>();
+    const bool colok = in_group<W>() && l < N / VEC;
+    const int rb = N * (int)sizeof(TX);
+    const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
+    const bool wbf = is_bf16<TX>() && pt == kBF16;
 
     f2 wf[P];
+    uint32_t wpk[P];  // the bf16 weight pair, packed (used when wbf)
 #pragma unroll
-    for (int p = 0; p < P; ++p) wf[p] = colok ? ld_param2(w, pt, l * VEC + 2 * p) : splat2(0.f);
+    for (int p = 0; p < P; ++p) {
+        wf[p] = colok ? ld_param2(w, pt, l * VEC + 2 * p) : splat2(0.f);
+        wpk[p] = (wbf && colok) ? static_cast<const uint32_t*>(w)[(l * VEC) / 2 + p] : 0u;
+    }
 
-    Ring<1, kStagesF> rg;
+    Ring<1, kind_stages(S, kFwdNorm)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = slot_bytes(S, false);
+    rg.slot = slot_bytes(S, kFwdNorm);
     rg.fault = fault;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
-        const unsigned char* tx = rg.tile(k, 0);
-        bool ok[U];
+        const unsigned char* xs = rg.tile(k, 0) + soff;
+        const int64_t row0 = b * (G * U) + g;
+        const bool full = (b + 1) * (G * U) <= M;
+        bool okr[U], ok[U];
         f2 xv[U][P];
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int lr = u * G + g;
-            ok[u] = alive && colok && b * (G * U) + lr < M;
-            unpack2(lds128_if(ok[u], tx + lr * rb + l * 16), xv[u]);
+            okr[u] = alive && (full || row0 + u * G < M);
+            ok[u] = okr[u] && colok;
+            unpack2(lds128_if(ok[u], xs + u * srow), xv[u]);
             s[u] = vec_sumsq2<P>(xv[u]);
         }
         group_allreduce<W, T, U>(s, red, parity);
+        TX* yb = y + row0 * N + l * VEC;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t row = b * (G * U) + u * G + g;
             const float rs = rsqrtf(fmaf(s[u], inv_n, eps));
             if (ok[u]) {
                 const f2 r2 = splat2(rs);
-                f2 o[P];
+                uint4 out;
+                if constexpr (is_bf16<TX>()) {
+                    uint32_t o[4];
 #pragma unroll
-                for (int p = 0; p < P; ++p) o[p] = mul2(wf[p], round2<TX>(mul2(xv[u][p], r2)));
-                st_stream(y + row * N + l * VEC, pack2(o));
+                    for (int p = 0; p < P; ++p) {
+                        const uint32_t npk = f2_to_bf2(mul2(xv[u][p], r2));  // n = round_x(x r)
+                        o[p] = wbf ? bmul2(wpk[p], npk) : f2_to_bf2(mul2(wf[p], bf2_to_f2(npk)));
+                    }
+                    out = make_uint4(o[0], o[1], o[2], o[3]);
+                } else {
+                    f2 o[P];
+#pragma unroll
+                    for (int p = 0; p < P; ++p) o[p] = mul2(wf[p], mul2(xv[u][p], r2));
+                    out = pack2(o);
+                }
+                st_stream(yb + u * grow, out);
             }
-            if (rstd && alive && l == 0 && row < M) rstd[row] = rs;
+            if (rstd && okr[u] && l == 0 && in_group<W>()) rstd[row0 + u * G] = rs;
         }
     });
 }
@@ -102,59 +138,65 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBF)
 // code.  Full row blocks run without masking; the ragged last block masks its
 // padded rows by a select after the arithmetic.
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
+__global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwd))
     rms_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy, const void* __restrict__ w,
                  int pt, const float* __restrict__ rstd, TX* __restrict__ dx,
                  float* __restrict__ ws, int64_t M, int N, float eps, float inv_n,
                  int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kSched[S].UB, T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kBwd), T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
-    constexpr int G = T / W;
+    constexpr int G = groups_per_cta(W, T);
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
     int parity = 0;
-    const int g = threadIdx.x / W, l = threadIdx.x % W;
-    const bool colok = l < N / VEC;
-    const int64_t rb = (int64_t)N * sizeof(TX);
-    const bool round_terms = (pt != kF32);  // weight in x's dtype: round dy*n
+    const int g = grp<W>(), l = lan<W>();
+    const bool colok = in_group<W>() && l < N / VEC;
+    const int rb = N * (int)sizeof(TX);
+    const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
+    // a weight in x's dtype: each dy*n is rounded to x's dtype (bf16 pairs
+    // then multiply in bf16); a float32 weight keeps the float32 product
+    const bool wbf = is_bf16<TX>() && pt == kBF16;
 
     f2 wf[P], acc[P];
+    uint32_t wpk[P];
 #pragma unroll
     for (int p = 0; p < P; ++p) {
         wf[p] = colok ? ld_param2(w, pt, l * VEC + 2 * p) : splat2(0.f);
+        wpk[p] = (wbf && colok) ? static_cast<const uint32_t*>(w)[(l * VEC) / 2 + p] : 0u;
         acc[p] = splat2(0.f);
     }
     float rs_n[U];
-    auto load_rstd = [&](int64_t b) {
+    auto load_rstd = [&](int64_t row0) {
         if (rstd) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int64_t row = b * (G * U) + u * G + g;
+                const int64_t row = row0 + u * G;
                 rs_n[u] = row < M ? __ldcs(rstd + row) : 0.f;
             }
         }
     };
-    load_rstd(blockIdx.x);
+    load_rstd((int64_t)blockIdx.x * (G * U) + g);
 
-    auto rows = [&](int64_t b, const unsigned char* tx, const unsigned char* td, bool alive,
-                    auto masked) {
+    // Pass 1 (after r is known) computes dn and xhat, the reduction term and
+    // the weight-gradient term (independent of the row reduction); pass 2
+    // keeps only xhat and dn.
+    auto rows = [&](const unsigned char* xs, const unsigned char* ds, TX* dxb, int64_t row0,
+                    bool alive, auto masked) {
         constexpr bool kMask = decltype(masked)::value;
         float rs[U];
         bool ok[U];
-        f2 xv[U][P], dv[U][P];
+        f2 xh[U][P], dn[U][P];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int lr = u * G + g;
-            ok[u] = alive && colok && (!kMask || b * (G * U) + lr < M);
-            unpack2(lds128_if(ok[u], tx + lr * rb + l * 16), xv[u]);
-            unpack2(lds128_if(ok[u], td + lr * rb + l * 16), dv[u]);
+            ok[u] = alive && colok && (!kMask || row0 + u * G < M);
+            unpack2(lds128_if(ok[u], xs + u * srow), xh[u]);  // x, scaled by r below
             rs[u] = rs_n[u];
         }
-        load_rstd(b + gridDim.x);
+        load_rstd(row0 + (int64_t)gridDim.x * (G * U));
         if (!rstd) {  // uniform branch: recompute r exactly as the forward does
 #pragma unroll
-            for (int u = 0; u < U; ++u) rs[u] = vec_sumsq2<P>(xv[u]);
+            for (int u = 0; u < U; ++u) rs[u] = vec_sumsq2<P>(xh[u]);
             group_allreduce<W, T, U>(rs, red, parity);
 #pragma unroll
             for (int u = 0; u < U; ++u) rs[u] = rsqrtf(fmaf(rs[u], inv_n, eps));
@@ -162,50 +204,66 @@ __global__ void __launch_bounds__(kSched[S].T, kSched[S].MINBB)
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const bool okr = !kMask || row0 + u * G < M;
             const f2 r2 = splat2(rs[u]);
+            const uint4 dr = lds128_if(ok[u], ds + u * srow);
+            f2 dv[P];
+            unpack2(dr, dv);
             f2 a2 = splat2(0.f);
 #pragma unroll
-            for (int p = 0; p < P; ++p)
-                a2 = fma2(round2<TX>(mul2(dv[u][p], wf[p])), mul2(xv[u][p], r2), a2);
+            for (int p = 0; p < P; ++p) {
+                xh[u][p] = mul2(xh[u][p], r2);
+                f2 nxt;  // the accumulator with this row's dw term added
+                if constexpr (is_bf16<TX>()) {
+                    const uint32_t npk = f2_to_bf2(xh[u][p]);  // n = round_x(xhat)
+                    if (wbf) {
+                        dn[u][p] = bf2_to_f2(bmul2(word(dr, p), wpk[p]));
+                        nxt = add2(acc[p], bf2_to_f2(bmul2(word(dr, p), npk)));
+                    } else {
+                        // float32 weight: dy*n unrounded, exact product of two bf16
+                        dn[u][p] = round2<TX>(mul2(dv[p], wf[p]));
+                        nxt = mk2(fma_bf16_lo(word(dr, p), npk, lo2(acc[p])),
+                                  fma_bf16_hi(word(dr, p), npk, hi2(acc[p])));
+                    }
+                } else {
+                    dn[u][p] = mul2(dv[p], wf[p]);
+                    nxt = fma2(dv[p], xh[u][p], acc[p]);
+                }
+                a2 = fma2(dn[u][p], xh[u][p], a2);
+                // padded rows: keep the old sum, a select after the arithmetic
+                acc[p] = (!kMask || okr) ? nxt : acc[p];
+            }
             s[u] = lo2(a2) + hi2(a2);
         }
         group_allreduce<W, T, U>(s, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t row = b * (G * U) + u * G + g;
-            const bool okr = !kMask || row < M;
             const f2 r2 = splat2(rs[u]), nm = splat2(-(s[u] * inv_n));
             f2 o[P];
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const f2 xh = mul2(xv[u][p], r2);
-                const f2 dn = round2<TX>(mul2(dv[u][p], wf[p]));
-                o[p] = mul2(r2, fma2(xh, nm, dn));
-                f2 term = mul2(dv[u][p], round2<TX>(xh));
-                if (round_terms) term = round2<TX>(term);
-                if constexpr (kMask)
-                    acc[p] = add2(acc[p], sel2(okr, term, splat2(0.f)));
-                else
-                    acc[p] = add2(acc[p], term);
-            }
-            if (ok[u]) st_stream(dx + row * N + l * VEC, pack2(o));
+            for (int p = 0; p < P; ++p) o[p] = mul2(r2, fma2(xh[u][p], nm, dn[u][p]));
+            if (ok[u]) st_stream(dxb + u * grow, pack2(o));
         }
     };
 
-    Ring<2, kStagesB> rg;
+    Ring<2, kind_stages(S, kBwd)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = slot_bytes(S, true);
+    rg.slot = slot_bytes(S, kBwd);
     rg.fault = fault;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        const int64_t row0 = b * (G * U) + g;
+        TX* dxb = dx + row0 * N + l * VEC;
+        const unsigned char* xs = rg.tile(k, 0) + soff;
+        const unsigned char* ds = rg.tile(k, 1) + soff;
         if ((b + 1) * (G * U) <= M)
-            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::false_type{});
+            rows(xs, ds, dxb, row0, alive, std::false_type{});
         else
-            rows(b, rg.tile(k, 0), rg.tile(k, 1), alive, std::true_type{});
+            rows(xs, ds, dxb, row0, alive, std::true_type{});
     });
 
     if (ws == nullptr) return;  // no weight gradient requested (uniform)
@@ -295,15 +353,16 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, false, 1);                                  \
+        constexpr int smem = ring_smem_bytes(S, kFwdNorm, 1);                                  \
         auto kern = rms_fwd_fast<TX, S>;                                                     \
-        if (smem > 48 * 1024)                                                                \
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,          \
+                             cudaSharedmemCarveoutMaxShared);                               \
         kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, w, pt, rstd, M, N, eps, inv_n, L.nblocks, L.fault);                              \
         break;                                                                               \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
-        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
+        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }
@@ -326,15 +385,16 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, true, 2);                                  \
+        constexpr int smem = ring_smem_bytes(S, kBwd, 2);                                  \
         auto kern = rms_bwd_fast<TX, S>;                                                     \
-        if (smem > 48 * 1024)                                                                \
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);   \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,          \
+                             cudaSharedmemCarveoutMaxShared);                               \
         kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, dyp, w, pt, rstd, dxp, ws, M, N, eps, inv_n, L.nblocks, L.fault);                              \
         break;                                                                               \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
-        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10)
+        GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }

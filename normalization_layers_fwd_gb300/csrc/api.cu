@@ -98,8 +98,7 @@ int fast_sid(int64_t N, int xt)
     return -1;
 }
 
-// The launch layout of one row-wise kernel of the given kind (gbn::kFwdDyT,
-// gbn::kFwdNorm or gbn::kBwd).
+// The launch layout of one row-wise kernel of the given kind (gbn::KernelKind).
 Launch plan(int64_t M, int64_t N, int xt, bool aligned, int sms, cudaStream_t stream, int kind)
 {
     Launch L{};
@@ -223,8 +222,9 @@ size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int
     const int sms = sm_count(device);
     if (sms <= 0) return (size_t)-1;
     const Launch a =
-        plan(M, N, xt, true, sms, nullptr, op == GBN_OP_DYT ? gbn::kBwdDyT : gbn::kBwd);
-    const Launch b = plan(M, N, xt, false, sms, nullptr, gbn::kBwd);
+        plan(M, N, xt, true, sms, nullptr,
+             op == GBN_OP_DYT ? gbn::kBwdDyT : op == GBN_OP_LAYERNORM ? gbn::kBwdLN : gbn::kBwdRms);
+    const Launch b = plan(M, N, xt, false, sms, nullptr, gbn::kBwdLN);
     const size_t need = ws_needed(op, a.P > b.P ? a : b, N);
     return (need + 255) & ~(size_t)255;
 }
@@ -313,7 +313,7 @@ int layernorm_bwd(const void* x, const void* dy, const float* mean, const float*
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                    gbn::kBwd);
+                    gbn::kBwdLN);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_LAYERNORM, L, N)))
         return GBN_EWORKSPACE;
@@ -358,7 +358,7 @@ int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd,
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                    gbn::kBwd);
+                    gbn::kBwdRms);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (dw && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_RMSNORM, L, N))) return GBN_EWORKSPACE;
     float* wsf = dw ? static_cast<float*>(ws) : nullptr;

@@ -27,7 +27,16 @@ __global__ void __launch_bounds__(kCols * kSlices)
     const int64_t c = blockIdx.x * (int64_t)kCols + tx;
     float s = 0.f;
     if (c < rowlen) {
-        for (int64_t p = ty; p < P; p += kSlices) s += ws[p * rowlen + c];
+        // batches of 8 independent loads (all in flight), added in row order
+        int64_t p = ty;
+        for (; p + 7 * kSlices < P; p += 8 * kSlices) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = ws[(p + i * kSlices) * rowlen + c];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s += v[i];
+        }
+        for (; p < P; p += kSlices) s += ws[p * rowlen + c];
     }
     part[ty][tx] = s;
     __syncthreads();

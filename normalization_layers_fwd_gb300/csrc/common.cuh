@@ -83,22 +83,27 @@ __device__ __forceinline__ bool in_group()
 // keep more per-row state, so they run 2 CTAs per SM.  At the widest rows
 // (512 threads at 2 CTAs per SM, 64 registers) the backwards keep one row
 // per thread: two spill.
-enum KernelKind : int { kFwdDyT = 0, kFwdNorm = 1, kBwd = 2, kBwdDyT = 3 };
+enum KernelKind : int { kFwdDyT = 0, kFwdNorm = 1, kBwdLN = 2, kBwdDyT = 3, kBwdRms = 4 };
+
+constexpr bool is_bwd(int kind) { return kind >= kBwdLN; }
 
 constexpr int kind_U(int S, int kind)
 {
-    return kind == kBwd      ? (kSched[S].T == 256 ? 2 : 1)
-           : kind == kBwdDyT ? (kSched[S].T == 512 ? 1 : 2)
+    return kind == kBwdDyT ? (kSched[S].T == 512 ? 1 : 2)
+           : is_bwd(kind)  ? (kSched[S].T == 256 ? 2 : 1)
            : kind == kFwdDyT && kSched[S].T == 256 ? 4
                                                    : 2;
 }
+// RMSNorm's backward keeps the least per-row state (84 registers), so it
+// fits 3 CTAs per SM and more bytes in flight.
 constexpr int kind_minb(int S, int kind)
 {
     return kSched[S].T == 1024 ? 1
            : kSched[S].T == 512 ? 2
-           : kind == kBwd || kind == kBwdDyT ? 2
-           : kind == kFwdDyT                 ? 3
-                                             : 4;
+           : kind == kBwdRms    ? 3
+           : is_bwd(kind)       ? 2
+           : kind == kFwdDyT    ? 3
+                                : 4;
 }
 constexpr int kind_stages(int S, int kind)
 {
@@ -660,6 +665,23 @@ __device__ __forceinline__ void cta_store_columns2(const f2 (&acc)[P], float* bu
         a[2 * p + 1] = hi2(acc[p]);
     }
     cta_store_columns<W, 2 * P, T>(a, buf, out_row, N);
+}
+
+// Raise a kernel's dynamic shared-memory limit and prefer the maximum
+// shared-memory carve-out, once per kernel per device (host side).  The
+// template parameter is the kernel itself, so every kernel has its own flag.
+template <auto Kernel>
+inline void ring_attributes(int smem)
+{
+    static unsigned long long done = 0;  // bit d: device d configured
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+    const unsigned long long bit = 1ull << dev;
+    if (__atomic_load_n(&done, __ATOMIC_RELAXED) & bit) return;
+    cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(Kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    __atomic_fetch_or(&done, bit, __ATOMIC_RELAXED);
 }
 
 }  // namespace gbn

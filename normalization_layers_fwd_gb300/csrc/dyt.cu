@@ -338,9 +338,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* alp
     case S: {                                                                                \
         constexpr int smem = ring_smem_bytes(S, kFwdDyT, 1);                                   \
         auto kern = dyt_fwd_fast<TX, S>;                                                     \
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,          \
-                             cudaSharedmemCarveoutMaxShared);                               \
+        ring_attributes<dyt_fwd_fast<TX, S>>(smem);                                                         \
         kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, alpha, gamma, beta, pt, M, N, \
                                                        L.nblocks, L.fault);                  \
         break;                                                                               \
@@ -370,9 +368,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     case S: {                                                                                \
         constexpr int smem = ring_smem_bytes(S, kBwdDyT, 2);                                    \
         auto kern = dyt_bwd_fast<TX, S>;                                                     \
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,          \
-                             cudaSharedmemCarveoutMaxShared);                               \
+        ring_attributes<dyt_bwd_fast<TX, S>>(smem);                                                         \
         kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, dyp, dxp, alpha, gamma, pt, ws, M, \
                                                        N, L.nblocks, L.fault);               \
         break;                                                                               \

@@ -138,13 +138,13 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
 // code.  Full row blocks run without masking; the ragged last block masks its
 // padded rows by a select after the arithmetic.
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwd))
+__global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
     rms_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy, const void* __restrict__ w,
                  int pt, const float* __restrict__ rstd, TX* __restrict__ dx,
                  float* __restrict__ ws, int64_t M, int N, float eps, float inv_n,
                  int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kind_U(S, kBwd), T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kBwdRms), T = kSched[S].T;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
     extern __shared__ __align__(128) unsigned char dsm[];
@@ -246,14 +246,14 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwd))
         }
     };
 
-    Ring<2, kind_stages(S, kBwd)> rg;
+    Ring<2, kind_stages(S, kBwdRms)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = slot_bytes(S, kBwd);
+    rg.slot = slot_bytes(S, kBwdRms);
     rg.fault = fault;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const int64_t row0 = b * (G * U) + g;
@@ -355,9 +355,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
     case S: {                                                                                \
         constexpr int smem = ring_smem_bytes(S, kFwdNorm, 1);                                  \
         auto kern = rms_fwd_fast<TX, S>;                                                     \
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,          \
-                             cudaSharedmemCarveoutMaxShared);                               \
+        ring_attributes<rms_fwd_fast<TX, S>>(smem);                                                         \
         kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, w, pt, rstd, M, N, eps, inv_n, L.nblocks, L.fault);                              \
         break;                                                                               \
     }
@@ -385,11 +383,9 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, kBwd, 2);                                  \
+        constexpr int smem = ring_smem_bytes(S, kBwdRms, 2);                                  \
         auto kern = rms_bwd_fast<TX, S>;                                                     \
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);       \
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,          \
-                             cudaSharedmemCarveoutMaxShared);                               \
+        ring_attributes<rms_bwd_fast<TX, S>>(smem);                                                         \
         kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, dyp, w, pt, rstd, dxp, ws, M, N, eps, inv_n, L.nblocks, L.fault);                              \
         break;                                                                               \
     }

@@ -68,7 +68,9 @@ typedef enum {
     GBN_EDTYPE = 2,     /* dtype code not in gbn_dtype */
     GBN_EWORKSPACE = 3, /* ws_bytes smaller than the call needs */
     GBN_ELAUNCH = 4,    /* a kernel launch failed (cudaGetLastError after the launch) */
-    GBN_EDEVICE = 5     /* the current device could not be queried */
+    GBN_EDEVICE = 5,    /* the current device could not be queried */
+    GBN_ESCRATCH = 6    /* rmsnorm_bwd_static_ws: the call needs more scratch than
+                           GBN_STATIC_WS_BYTES */
 } gbn_status;
 
 /* Layer selector of gbn_bwd_workspace_bytes. */
@@ -147,6 +149,35 @@ int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, i
 int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd, void* dx,
                 void* dw, int64_t M, int64_t N, float eps, int xt, int wt, void* ws,
                 size_t ws_bytes, cudaStream_t stream);
+
+/* rmsnorm_bwd_static_ws: rmsnorm_bwd without a caller workspace.  The pages
+ *   have no counterpart; it exists for callers that cannot allocate device
+ *   memory (a host program with no device allocator of its own, code under a
+ *   pool that already holds the device's memory, a loop that must not call
+ *   cudaMalloc/cudaFree because they can synchronize the device).  Arguments,
+ *   kernels, launch layout and results are those of rmsnorm_bwd; the partial
+ *   column sums of dw go to a static device array of GBN_STATIC_WS_BYTES
+ *   (8 MiB) inside the library, held by every device that loads the library
+ *   until the process exits.  The call allocates nothing.
+ *   Limit: a call with dw non-null and M > 0 whose partial sums need more than
+ *   GBN_STATIC_WS_BYTES returns GBN_ESCRATCH before launching anything.  The
+ *   need is (rows of partials) x N x 4 bytes; at most 5 MB for 16-byte aligned
+ *   activations with N a multiple of 8 (bf16) or 4 (f32) up to N = 8192 (bf16)
+ *   or 4096 (f32) on 152 SMs, and about 2.4 KB x N on the general path.
+ *   gbn_bwd_workspace_bytes(GBN_OP_RMSNORM, ...) <= GBN_STATIC_WS_BYTES is a
+ *   sufficient check ahead of a call.  With dw null the array is not used.
+ *   Set-up: the first call on a device (made current) looks up the array's
+ *   device address with cudaGetSymbolAddress; make that first call before
+ *   any stream capture.  Returns GBN_EDEVICE when the lookup fails.
+ *   Sharing: every call on a device uses the same array, which keeps the last
+ *   call's contents (nothing in it needs to start at zero: each call writes
+ *   every partial row before reading it).  Calls that may overlap on the GPU
+ *   (different streams, or host threads without ordering) race on the array
+ *   and give wrong dw. */
+#define GBN_STATIC_WS_BYTES (8u << 20)
+int rmsnorm_bwd_static_ws(const void* x, const void* dy, const void* w, const float* rstd,
+                          void* dx, void* dw, int64_t M, int64_t N, float eps, int xt, int wt,
+                          cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -20,6 +20,8 @@ from . import build as _build
 GBN_F32, GBN_BF16 = 0, 1
 GBN_OP_DYT, GBN_OP_LAYERNORM, GBN_OP_RMSNORM = 0, 1, 2
 GBN_OK = 0
+GBN_ESCRATCH = 6
+GBN_STATIC_WS_BYTES = 8 << 20  # size of the library's static scratch array
 SIZE_MAX = ctypes.c_size_t(-1).value
 
 _DTYPES = {torch.float32: GBN_F32, torch.bfloat16: GBN_BF16}
@@ -37,6 +39,7 @@ SIGNATURES = {
     "layernorm_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _I, _P, _SZ, _P], _I),
     "rmsnorm_fwd": ([_P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P], _I),
     "rmsnorm_bwd": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P, _SZ, _P], _I),
+    "rmsnorm_bwd_static_ws": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P], _I),
 }
 
 _lock = threading.Lock()
@@ -247,4 +250,23 @@ def rmsnorm_bwd(x, dy, w, rstd=None, eps=1e-6, need_dw=True):
     _check(load().rmsnorm_bwd(_ptr(x), _ptr(dy), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw), M, N,
                               float(eps), _code(x), _code(w), _ptr(ws), nbytes, _stream(x.device)),
            "rmsnorm_bwd")
+    return dx, dw
+
+
+def rmsnorm_bwd_static_ws(x, dy, w, rstd=None, eps=1e-6, need_dw=True):
+    """(dx, dw) like rmsnorm_bwd, with the library's static scratch array in
+    place of a workspace allocated here: for callers that cannot allocate
+    device memory.  Raises GbnError (GBN_ESCRATCH) when the shape needs more
+    scratch than GBN_STATIC_WS_BYTES."""
+    x, M, N = _rows(x)
+    dy = dy.contiguous()
+    if dy.shape != x.shape or dy.dtype != x.dtype:
+        raise ValueError("dy must match x in shape and dtype")
+    w = _param(w, x, N, "w")
+    rstd = _param(rstd, x, M, "rstd", required=False)
+    dx = torch.empty_like(x)
+    dw = torch.empty(N, dtype=w.dtype, device=x.device) if need_dw else None
+    _check(load().rmsnorm_bwd_static_ws(_ptr(x), _ptr(dy), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw),
+                                        M, N, float(eps), _code(x), _code(w), _stream(x.device)),
+           "rmsnorm_bwd_static_ws")
     return dx, dw

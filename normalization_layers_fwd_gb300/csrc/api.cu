@@ -209,6 +209,9 @@ const char* gbn_status_string(int status)
         case GBN_EWORKSPACE: return "GBN_EWORKSPACE: workspace too small";
         case GBN_ELAUNCH: return "GBN_ELAUNCH: kernel launch failed";
         case GBN_EDEVICE: return "GBN_EDEVICE: cannot query the CUDA device";
+        case GBN_ESCRATCH:
+            return "GBN_ESCRATCH: the call needs more scratch than the static array "
+                   "(GBN_STATIC_WS_BYTES) holds";
         default: return "GBN_UNKNOWN";
     }
 }

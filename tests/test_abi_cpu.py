@@ -50,7 +50,7 @@ def test_binding_signatures_cover_the_header():
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert lib.gbn_status_string(s).startswith(b"GBN_")
     assert lib.gbn_status_string(99) == b"GBN_UNKNOWN"
 

@@ -95,11 +95,13 @@ constexpr int kind_U(int S, int kind)
                                                    : 2;
 }
 // RMSNorm's backward keeps the least per-row state (84 registers), so it
-// fits 3 CTAs per SM and more bytes in flight.
+// fits 3 CTAs per SM and more bytes in flight.  DyT's backward at 512
+// threads needs about 80 registers (three column accumulators besides the
+// row), so it runs one CTA per SM rather than spill at two.
 constexpr int kind_minb(int S, int kind)
 {
     return kSched[S].T == 1024 ? 1
-           : kSched[S].T == 512 ? 2
+           : kSched[S].T == 512 ? (kind == kBwdDyT ? 1 : 2)
            : kind == kBwdRms    ? 3
            : is_bwd(kind)       ? 2
            : kind == kFwdDyT    ? 3
@@ -138,6 +140,23 @@ __device__ __forceinline__ uint4 ld_stream(const void* p)
 __device__ __forceinline__ void st_stream(void* p, const uint4& v)
 {
     __stcs(static_cast<uint4*>(p), v);
+}
+
+// Predicated stores: every lane issues one instruction and the predicate
+// decides, so a per-lane condition costs no divergent branch.
+__device__ __forceinline__ void st_stream_if(bool p, void* addr, const uint4& v)
+{
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t"
+        "@q st.global.cs.v4.b32 [%1], {%2, %3, %4, %5};\n\t}" ::"r"((int)p),
+        "l"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+__device__ __forceinline__ void st_f32_if(bool p, float* addr, float v)
+{
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %0, 0;\n\t@q st.global.f32 [%1], %2;\n\t}" ::"r"(
+            (int)p),
+        "l"(addr), "f"(v));
 }
 
 __device__ __forceinline__ void unpack(const uint4& u, float (&f)[4])

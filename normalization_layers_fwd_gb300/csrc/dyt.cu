@@ -145,22 +145,24 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
     rg.nblocks = nblocks;
     rg.slot = slot_bytes(S, kFwdDyT);
     rg.fault = fault;
+    const int64_t nfull = M / (G * U);  // blocks without padded rows
+    const int64_t rstride = (int64_t)gridDim.x * (G * U);
+    int64_t row0 = (int64_t)blockIdx.x * (G * U) + g;  // this thread's first row
+    TX* yb = y + row0 * N + l * VEC;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
-        if (!alive || !colok) return;  // nothing collective in this kernel
         const unsigned char* xs = rg.tile(k, 0) + soff;
-        const int64_t row0 = b * (G * U) + g;
-        const bool full = (b + 1) * (G * U) <= M;
-        TX* yb = y + row0 * N + l * VEC;
+        const bool full = b < nfull;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            if (full || row0 + u * G < M) {
-                f2 v[P];
-                unpack2(lds128(xs + u * srow), v);
+            const bool ok = alive && colok && (full || row0 + u * G < M);
+            f2 v[P];
+            unpack2(lds128_if(ok, xs + u * srow), v);
 #pragma unroll
-                for (int p = 0; p < P; ++p) v[p] = fma2(gm[p], dyt_tanh2(mul2(a2, v[p])), bt[p]);
-                st_stream(yb + u * grow, pack2(v));
-            }
+            for (int p = 0; p < P; ++p) v[p] = fma2(gm[p], dyt_tanh2(mul2(a2, v[p])), bt[p]);
+            st_stream_if(ok, yb + u * grow, pack2(v));
         }
+        row0 += rstride;
+        yb += rstride * N;
     });
 }
 
@@ -198,14 +200,15 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     for (int p = 0; p < P; ++p) acc_g[p] = acc_b[p] = acc_a[p] = splat2(0.f);
 
     auto rows = [&](const unsigned char* xs, const unsigned char* ds, TX* dxb, int64_t row0,
-                    auto masked) {
+                    bool alive, auto masked) {
         constexpr bool kMask = decltype(masked)::value;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const bool okr = !kMask || row0 + u * G < M;
+            const bool ok = alive && colok && okr;
             f2 xv[P], dv[P], o[P];
-            unpack2(lds128(xs + u * srow), xv);
-            unpack2(lds128(ds + u * srow), dv);
+            unpack2(lds128_if(ok, xs + u * srow), xv);
+            unpack2(lds128_if(ok, ds + u * srow), dv);
 #pragma unroll
             for (int p = 0; p < P; ++p) {
                 f2 t, s;
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
                     acc_a[p] = fma2(dsd, xv[p], acc_a[p]);
                 }
             }
-            if (okr) st_stream(dxb + u * grow, pack2(o));
+            st_stream_if(ok, dxb + u * grow, pack2(o));
         }
     };
 
@@ -237,16 +240,19 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     rg.nblocks = nblocks;
     rg.slot = slot_bytes(S, kBwdDyT);
     rg.fault = fault;
+    const int64_t nfull = M / (G * U);  // blocks without padded rows
+    const int64_t rstride = (int64_t)gridDim.x * (G * U);
+    int64_t row0 = (int64_t)blockIdx.x * (G * U) + g;  // this thread's first row
+    TX* dxb = dx + row0 * N + l * VEC;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
-        if (!alive || !colok) return;  // nothing collective in this kernel
-        const int64_t row0 = b * (G * U) + g;
-        TX* dxb = dx + row0 * N + l * VEC;
         const unsigned char* xs = rg.tile(k, 0) + soff;
         const unsigned char* ds = rg.tile(k, 1) + soff;
-        if ((b + 1) * (G * U) <= M)
-            rows(xs, ds, dxb, row0, std::false_type{});
+        if (b < nfull)
+            rows(xs, ds, dxb, row0, alive, std::false_type{});
         else
-            rows(xs, ds, dxb, row0, std::true_type{});
+            rows(xs, ds, dxb, row0, alive, std::true_type{});
+        row0 += rstride;
+        dxb += rstride * N;
     });
 
     if (ws == nullptr) return;  // no parameter gradient requested (uniform)

@@ -58,10 +58,16 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
     rg.nblocks = nblocks;
     rg.slot = slot_bytes(S, kFwdNorm);
     rg.fault = fault;
+    // Row positions advance by a fixed stride from one of this CTA's blocks
+    // to the next; blocks below nfull hold no padded rows.
+    const int64_t nfull = M / (G * U);
+    const int64_t rstride = (int64_t)gridDim.x * (G * U);
+    int64_t row0 = (int64_t)blockIdx.x * (G * U) + g;  // this thread's first row
+    TX* yb = y + row0 * N + l * VEC;
+    const bool lead = l == 0 && in_group<W>();  // stores the row statistics
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* xs = rg.tile(k, 0) + soff;
-        const int64_t row0 = b * (G * U) + g;
-        const bool full = (b + 1) * (G * U) <= M;
+        const bool full = b < nfull;
         bool okr[U], ok[U];
         f2 xv[U][P];
         float s[U];
@@ -84,28 +90,25 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
             f2 q2 = splat2(0.f);
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-                const f2 d = sub2(xv[u][p], m2);
-                q2 = fma2(d, d, q2);
+                xv[u][p] = sub2(xv[u][p], m2);  // x - mu, kept for the output
+                q2 = fma2(xv[u][p], xv[u][p], q2);
             }
             q[u] = colok ? lo2(q2) + hi2(q2) : 0.f;  // a vector past the row's end adds nothing
         }
         group_allreduce<W, T, U>(q, red, parity);
-        TX* yb = y + row0 * N + l * VEC;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const float rs = rsqrtf(fmaf(q[u], inv_n, eps));
-            if (ok[u]) {
-                const f2 m2 = splat2(mu[u]), r2 = splat2(rs);
-                f2 o[P];
+            const f2 r2 = splat2(rs);
+            f2 o[P];
 #pragma unroll
-                for (int p = 0; p < P; ++p) o[p] = fma2(mul2(sub2(xv[u][p], m2), r2), gm[p], bt[p]);
-                st_stream(yb + u * grow, pack2(o));
-            }
-            if (okr[u] && l == 0 && in_group<W>()) {
-                if (mean) mean[row0 + u * G] = mu[u];
-                if (rstd) rstd[row0 + u * G] = rs;
-            }
+            for (int p = 0; p < P; ++p) o[p] = fma2(mul2(xv[u][p], r2), gm[p], bt[p]);
+            st_stream_if(ok[u], yb + u * grow, pack2(o));
+            if (mean) st_f32_if(lead && okr[u], mean + (row0 + u * G), mu[u]);
+            if (rstd) st_f32_if(lead && okr[u], rstd + (row0 + u * G), rs);
         }
+        row0 += rstride;
+        yb += rstride * N;
     });
 }
 
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
             // so a width-one row gives exactly zero
 #pragma unroll
             for (int p = 0; p < P; ++p) o[p] = mul2(r2, fma2(xh[u][p], nmb, sub2(gg[u][p], ma)));
-            if (ok[u]) st_stream(dxb + u * grow, pack2(o));
+            st_stream_if(ok[u], dxb + u * grow, pack2(o));
         }
     };
 
@@ -216,15 +219,19 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     rg.nblocks = nblocks;
     rg.slot = slot_bytes(S, kBwdLN);
     rg.fault = fault;
+    const int64_t nfull = M / (G * U);  // blocks without padded rows
+    const int64_t rstride = (int64_t)gridDim.x * (G * U);
+    int64_t row0 = (int64_t)blockIdx.x * (G * U) + g;  // this thread's first row
+    TX* dxb = dx + row0 * N + l * VEC;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
-        const int64_t row0 = b * (G * U) + g;
-        TX* dxb = dx + row0 * N + l * VEC;
         const unsigned char* xs = rg.tile(k, 0) + soff;
         const unsigned char* ds = rg.tile(k, 1) + soff;
-        if ((b + 1) * (G * U) <= M)
+        if (b < nfull)
             rows(xs, ds, dxb, row0, alive, std::false_type{});
         else
             rows(xs, ds, dxb, row0, alive, std::true_type{});
+        row0 += rstride;
+        dxb += rstride * N;
     });
 
     if (ws == nullptr) return;  // no parameter gradient requested (uniform)

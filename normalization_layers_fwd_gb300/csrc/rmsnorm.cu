@@ -89,10 +89,14 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
     rg.nblocks = nblocks;
     rg.slot = slot_bytes(S, kFwdNorm);
     rg.fault = fault;
+    const int64_t nfull = M / (G * U);  // blocks without padded rows
+    const int64_t rstride = (int64_t)gridDim.x * (G * U);
+    int64_t row0 = (int64_t)blockIdx.x * (G * U) + g;  // this thread's first row
+    TX* yb = y + row0 * N + l * VEC;
+    const bool lead = l == 0 && in_group<W>();  // stores rstd
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* xs = rg.tile(k, 0) + soff;
-        const int64_t row0 = b * (G * U) + g;
-        const bool full = (b + 1) * (G * U) <= M;
+        const bool full = b < nfull;
         bool okr[U], ok[U];
         f2 xv[U][P];
         float s[U];
@@ -104,31 +108,30 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
             s[u] = vec_sumsq2<P>(xv[u]);
         }
         group_allreduce<W, T, U>(s, red, parity);
-        TX* yb = y + row0 * N + l * VEC;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const float rs = rsqrtf(fmaf(s[u], inv_n, eps));
-            if (ok[u]) {
-                const f2 r2 = splat2(rs);
-                uint4 out;
-                if constexpr (is_bf16<TX>()) {
-                    uint32_t o[4];
+            const f2 r2 = splat2(rs);
+            uint4 out;
+            if constexpr (is_bf16<TX>()) {
+                uint32_t o[4];
 #pragma unroll
-                    for (int p = 0; p < P; ++p) {
-                        const uint32_t npk = f2_to_bf2(mul2(xv[u][p], r2));  // n = round_x(x r)
-                        o[p] = wbf ? bmul2(wpk[p], npk) : f2_to_bf2(mul2(wf[p], bf2_to_f2(npk)));
-                    }
-                    out = make_uint4(o[0], o[1], o[2], o[3]);
-                } else {
-                    f2 o[P];
-#pragma unroll
-                    for (int p = 0; p < P; ++p) o[p] = mul2(wf[p], mul2(xv[u][p], r2));
-                    out = pack2(o);
+                for (int p = 0; p < P; ++p) {
+                    const uint32_t npk = f2_to_bf2(mul2(xv[u][p], r2));  // n = round_x(x r)
+                    o[p] = wbf ? bmul2(wpk[p], npk) : f2_to_bf2(mul2(wf[p], bf2_to_f2(npk)));
                 }
-                st_stream(yb + u * grow, out);
+                out = make_uint4(o[0], o[1], o[2], o[3]);
+            } else {
+                f2 o[P];
+#pragma unroll
+                for (int p = 0; p < P; ++p) o[p] = mul2(wf[p], mul2(xv[u][p], r2));
+                out = pack2(o);
             }
-            if (rstd && okr[u] && l == 0 && in_group<W>()) rstd[row0 + u * G] = rs;
+            st_stream_if(ok[u], yb + u * grow, out);
+            if (rstd) st_f32_if(lead && okr[u], rstd + (row0 + u * G), rs);
         }
+        row0 += rstride;
+        yb += rstride * N;
     });
 }
 
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
             f2 o[P];
 #pragma unroll
             for (int p = 0; p < P; ++p) o[p] = mul2(r2, fma2(xh[u][p], nm, dn[u][p]));
-            if (ok[u]) st_stream(dxb + u * grow, pack2(o));
+            st_stream_if(ok[u], dxb + u * grow, pack2(o));
         }
     };
 
@@ -255,15 +258,19 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
     rg.nblocks = nblocks;
     rg.slot = slot_bytes(S, kBwdRms);
     rg.fault = fault;
+    const int64_t nfull = M / (G * U);  // blocks without padded rows
+    const int64_t rstride = (int64_t)gridDim.x * (G * U);
+    int64_t row0 = (int64_t)blockIdx.x * (G * U) + g;  // this thread's first row
+    TX* dxb = dx + row0 * N + l * VEC;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
-        const int64_t row0 = b * (G * U) + g;
-        TX* dxb = dx + row0 * N + l * VEC;
         const unsigned char* xs = rg.tile(k, 0) + soff;
         const unsigned char* ds = rg.tile(k, 1) + soff;
-        if ((b + 1) * (G * U) <= M)
+        if (b < nfull)
             rows(xs, ds, dxb, row0, alive, std::false_type{});
         else
             rows(xs, ds, dxb, row0, alive, std::true_type{});
+        row0 += rstride;
+        dxb += rstride * N;
     });
 
     if (ws == nullptr) return;  // no weight gradient requested (uniform)

@@ -107,9 +107,17 @@ constexpr int kind_minb(int S, int kind)
            : kind == kFwdDyT    ? 3
                                 : 4;
 }
+// Ring depth.  Every SM keeps (CTAs x stages) row blocks of loads in
+// flight.  The forward kernels at 256 threads (4 or 3 CTAs per SM) stream
+// best with 2 stages: at 4 the whole GPU holds about 20 MB of outstanding
+// bulk copies and the forward sweep loses 5-15%.  The backward kernels,
+// which spend longer per block, want 3 (RMSNorm) or 4.
 constexpr int kind_stages(int S, int kind)
 {
-    return kind == kBwdDyT && kSched[S].T == 1024 ? 3 : 4;
+    return !is_bwd(kind) ? (kSched[S].T == 256 ? 2 : 4)
+           : kind == kBwdRms ? 3
+           : kind == kBwdDyT && kSched[S].T == 1024 ? 3
+                                                    : 4;
 }
 
 // Bytes of one ring slot for one staged tensor, and of the whole dynamic

@@ -88,22 +88,31 @@ int64_t general_warps(int64_t M, int sms) { return M < 4LL * sms ? M : 4LL * sms
 
 // Whether [M, N] of dtype xt can take the 16-byte vector path (alignment
 // aside), and its schedule index.
-int fast_sid(int64_t N, int xt)
+// Kernels given kv_max > 1 take the multi-vector schedules (up to kv_max
+// vectors per thread) for rows of more than 256 vectors: only kernels whose
+// row summation order no other kernel has to reproduce, within their
+// register budget.
+int fast_sid(int64_t N, int xt, int kv_max)
 {
     const int vec = 16 / elem_bytes(xt);
     if (N % vec != 0) return -1;
     const int64_t nvec = N / vec;
-    for (int s = 0; s < gbn::kNumSched; ++s)
+    if (nvec > 256) {
+        for (int s = gbn::kNumSched1; s < gbn::kNumSched; ++s)
+            if (gbn::kSched[s].KV <= kv_max && nvec <= gbn::kSched[s].max_nvec) return s;
+    }
+    for (int s = 0; s < gbn::kNumSched1; ++s)
         if (nvec <= gbn::kSched[s].max_nvec) return s;
     return -1;
 }
 
 // The launch layout of one row-wise kernel of the given kind (gbn::KernelKind).
-Launch plan(int64_t M, int64_t N, int xt, bool aligned, int sms, cudaStream_t stream, int kind)
+Launch plan(int64_t M, int64_t N, int xt, bool aligned, int sms, cudaStream_t stream, int kind,
+            int kv_max = 1)
 {
     Launch L{};
     L.stream = stream;
-    const int sid = aligned ? fast_sid(N, xt) : -1;
+    const int sid = aligned ? fast_sid(N, xt, kv_max) : -1;
     if (sid >= 0) {
         const gbn::SchedEntry& e = gbn::kSched[sid];
         const int64_t rows_per_block =
@@ -226,7 +235,8 @@ size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int
     if (sms <= 0) return (size_t)-1;
     const Launch a =
         plan(M, N, xt, true, sms, nullptr,
-             op == GBN_OP_DYT ? gbn::kBwdDyT : op == GBN_OP_LAYERNORM ? gbn::kBwdLN : gbn::kBwdRms);
+             op == GBN_OP_DYT ? gbn::kBwdDyT : op == GBN_OP_LAYERNORM ? gbn::kBwdLN : gbn::kBwdRms,
+            op == GBN_OP_LAYERNORM ? 2 : 1);
     const Launch b = plan(M, N, xt, false, sms, nullptr, gbn::kBwdLN);
     const size_t need = ws_needed(op, a.P > b.P ? a : b, N);
     return (need + 255) & ~(size_t)255;
@@ -243,7 +253,7 @@ int dyt_fwd(const void* x, const void* alpha, const void* gamma, const void* bet
     if (M == 0) return GBN_OK;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, gbn::kFwdDyT);
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, gbn::kFwdDyT, 4);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (!L.fast) {  // elementwise general path: one thread per element, grid-stride
         const int64_t E = M * N;
@@ -295,7 +305,7 @@ int layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, f
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream,
-                    gbn::kFwdNorm);
+                    gbn::kFwdNorm, 4);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     return launch_status(
         gbn::launch_ln_fwd(L, xt, pt, x, gamma, beta, y, mean, rstd, M, (int)N, eps));
@@ -316,7 +326,7 @@ int layernorm_bwd(const void* x, const void* dy, const float* mean, const float*
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                    gbn::kBwdLN);
+                    gbn::kBwdLN, 2);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_LAYERNORM, L, N)))
         return GBN_EWORKSPACE;

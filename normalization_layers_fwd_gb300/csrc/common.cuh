@@ -26,20 +26,27 @@ enum DType : int { kF32 = 0, kBF16 = 1 };
 // never on U, so a forward and a backward with different U reduce a row
 // identically.
 struct SchedEntry {
-    int max_nvec, W, T;
+    int max_nvec, W, T, KV;
 };
 
-// One 16-byte vector per thread per row: a row of nvec vectors takes
-// W = next_pow2(nvec) threads, so register pressure stays flat from N = 8
-// to N = 8192 bf16.  A CTA has T = max(256, W) threads.
+// Schedules 0-11: one 16-byte vector per thread per row: a row of nvec
+// vectors takes W = next_pow2(nvec) threads, so register pressure stays flat
+// from N = 8 to N = 8192 bf16.  A CTA has T = max(256, W) threads.
 // Rows of exactly 3 vectors (bf16 N = 24, the tall-narrow LayerNorm of the
 // torch-xpu-ops page) take segmented groups of W = 3 lanes, 10 per warp,
 // instead of 4-lane groups with a lane idle.
-constexpr int kNumSched = 12;
+// Schedules 12-13: wide rows (257-1024 vectors) held by 256 threads with
+// KV = 2 or 4 vectors each (vector l + j*W for j < KV), one row per CTA of
+// 256 threads.  Against schedules 10-11 they divide the per-row reduction
+// and barrier cost by KV and let two independent CTAs share an SM.  Only
+// kernels whose summation order nothing else has to reproduce take them.
+constexpr int kNumSched = 14;
+constexpr int kNumSched1 = 12;  // the one-vector schedules
 constexpr SchedEntry kSched[kNumSched] = {
-    {1, 1, 256},     {2, 2, 256},     {3, 3, 256},     {4, 4, 256},
-    {8, 8, 256},     {16, 16, 256},   {32, 32, 256},   {64, 64, 256},
-    {128, 128, 256}, {256, 256, 256}, {512, 512, 512}, {1024, 1024, 1024},
+    {1, 1, 256, 1},     {2, 2, 256, 1},     {3, 3, 256, 1},     {4, 4, 256, 1},
+    {8, 8, 256, 1},     {16, 16, 256, 1},   {32, 32, 256, 1},   {64, 64, 256, 1},
+    {128, 128, 256, 1}, {256, 256, 256, 1}, {512, 512, 512, 1}, {1024, 1024, 1024, 1},
+    {512, 256, 256, 2}, {1024, 256, 256, 4},
 };
 constexpr int kMaxFastVec = 1024;
 
@@ -87,12 +94,17 @@ enum KernelKind : int { kFwdDyT = 0, kFwdNorm = 1, kBwdLN = 2, kBwdDyT = 3, kBwd
 
 constexpr bool is_bwd(int kind) { return kind >= kBwdLN; }
 
-constexpr int kind_U(int S, int kind)
+constexpr int kind_U1(int S, int kind)
 {
     return kind == kBwdDyT ? (kSched[S].T == 512 ? 1 : 2)
            : is_bwd(kind)  ? (kSched[S].T == 256 ? 2 : 1)
            : kind == kFwdDyT && kSched[S].T == 256 ? 4
                                                    : 2;
+}
+// Several vectors per thread take proportionally fewer rows.
+constexpr int kind_U(int S, int kind)
+{
+    return kind_U1(S, kind) / kSched[S].KV > 1 ? kind_U1(S, kind) / kSched[S].KV : 1;
 }
 // RMSNorm's backward keeps the least per-row state (84 registers), so it
 // fits 3 CTAs per SM and more bytes in flight.  DyT's backward at 512
@@ -100,7 +112,8 @@ constexpr int kind_U(int S, int kind)
 // row), so it runs one CTA per SM rather than spill at two.
 constexpr int kind_minb(int S, int kind)
 {
-    return kSched[S].T == 1024 ? 1
+    return kSched[S].KV > 1 ? 2
+           : kSched[S].T == 1024 ? 1
            : kSched[S].T == 512 ? (kind == kBwdDyT ? 1 : 2)
            : kind == kBwdRms    ? 3
            : is_bwd(kind)       ? 2
@@ -108,13 +121,17 @@ constexpr int kind_minb(int S, int kind)
                                 : 4;
 }
 // Ring depth.  Every SM keeps (CTAs x stages) row blocks of loads in
-// flight.  The forward kernels at 256 threads (4 or 3 CTAs per SM) stream
-// best with 2 stages: at 4 the whole GPU holds about 20 MB of outstanding
-// bulk copies and the forward sweep loses 5-15%.  The backward kernels,
+// flight.  The one-vector forward kernels at 256 threads (4 or 3 CTAs per
+// SM) stream best with 2 stages: at 4 the whole GPU holds about 20 MB of
+// outstanding bulk copies and the forward sweep loses 5-15%.  The wide-row
+// forwards of schedules 12-13 (two CTAs of one row each) want 4, except the
+// LayerNorm forward at 4 vectors per thread (2).  The backward kernels,
 // which spend longer per block, want 3 (RMSNorm) or 4.
 constexpr int kind_stages(int S, int kind)
 {
-    return !is_bwd(kind) ? (kSched[S].T == 256 ? 2 : 4)
+    return !is_bwd(kind) ? (kSched[S].KV == 1 ? (kSched[S].T == 256 ? 2 : 4)
+                            : kSched[S].KV == 4 && kind == kFwdNorm ? 2
+                                                                    : 4)
            : kind == kBwdRms ? 3
            : kind == kBwdDyT && kSched[S].T == 1024 ? 3
                                                     : 4;
@@ -124,7 +141,8 @@ constexpr int kind_stages(int S, int kind)
 // shared memory a kernel with NT staged tensors needs (barriers first).
 constexpr int slot_bytes(int S, int kind)
 {
-    return groups_per_cta(kSched[S].W, kSched[S].T) * kSched[S].W * kind_U(S, kind) * 16;
+    return groups_per_cta(kSched[S].W, kSched[S].T) * kSched[S].W * kSched[S].KV *
+           kind_U(S, kind) * 16;
 }
 constexpr int ring_smem_bytes(int S, int kind, int NT)
 {
@@ -692,6 +710,30 @@ __device__ __forceinline__ void cta_store_columns2(const f2 (&acc)[P], float* bu
         a[2 * p + 1] = hi2(acc[p]);
     }
     cta_store_columns<W, 2 * P, T>(a, buf, out_row, N);
+}
+
+// KV vectors per thread (vector l + j*W holds columns (l + j*W)*VEC ...).
+// With one vector this is cta_store_columns2; the multi-vector schedules
+// have one row group per CTA, so each thread writes its own columns.
+template <int W, int KV, int P, int T>
+__device__ __forceinline__ void cta_store_columns_kv(const f2 (&acc)[KV][P], float* buf,
+                                                     float* __restrict__ out_row, int N)
+{
+    if constexpr (KV == 1) {
+        cta_store_columns2<W, P, T>(acc[0], buf, out_row, N);
+    } else {
+        static_assert(groups_per_cta(W, T) == 1, "multi-vector schedules hold one group per CTA");
+        const int l = lan<W>();
+#pragma unroll
+        for (int j = 0; j < KV; ++j) {
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const int c = (l + j * W) * 2 * P + 2 * p;
+                if (c < N) out_row[c] = lo2(acc[j][p]);
+                if (c + 1 < N) out_row[c + 1] = hi2(acc[j][p]);
+            }
+        }
+    }
 }
 
 // Raise a kernel's dynamic shared-memory limit and prefer the maximum

@@ -120,21 +120,28 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
                  const void* __restrict__ gamma, const void* __restrict__ beta, int pt,
                  int64_t M, int N, int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kind_U(S, kFwdDyT), T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kFwdDyT), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
     extern __shared__ __align__(128) unsigned char dsm[];
     const int g = grp<W>(), l = lan<W>();
-    const bool colok = in_group<W>() && l < N / VEC;
+    // vector j of a row is vector l + j*W: in shared memory at +j*W*16 bytes
+    bool colok[KV];
+#pragma unroll
+    for (int j = 0; j < KV; ++j) colok[j] = in_group<W>() && l + j * W < N / VEC;
     const int rb = N * (int)sizeof(TX);
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
 
     const f2 a2 = splat2(ld_param(alpha, pt, 0));
-    f2 gm[P], bt[P];
+    f2 gm[KV][P], bt[KV][P];
 #pragma unroll
-    for (int p = 0; p < P; ++p) {
-        gm[p] = colok ? ld_param2(gamma, pt, l * VEC + 2 * p) : splat2(0.f);
-        bt[p] = colok ? ld_param2(beta, pt, l * VEC + 2 * p) : splat2(0.f);
+    for (int j = 0; j < KV; ++j) {
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            const int c = (l + j * W) * VEC + 2 * p;
+            gm[j][p] = colok[j] ? ld_param2(gamma, pt, c) : splat2(0.f);
+            bt[j][p] = colok[j] ? ld_param2(beta, pt, c) : splat2(0.f);
+        }
     }
 
     Ring<1, kind_stages(S, kFwdDyT)> rg;
@@ -154,12 +161,17 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
         const bool full = b < nfull;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const bool ok = alive && colok && (full || row0 + u * G < M);
-            f2 v[P];
-            unpack2(lds128_if(ok, xs + u * srow), v);
+            const bool okr = alive && (full || row0 + u * G < M);
 #pragma unroll
-            for (int p = 0; p < P; ++p) v[p] = fma2(gm[p], dyt_tanh2(mul2(a2, v[p])), bt[p]);
-            st_stream_if(ok, yb + u * grow, pack2(v));
+            for (int j = 0; j < KV; ++j) {
+                const bool ok = okr && colok[j];
+                f2 v[P];
+                unpack2(lds128_if(ok, xs + u * srow + j * W * 16), v);
+#pragma unroll
+                for (int p = 0; p < P; ++p)
+                    v[p] = fma2(gm[j][p], dyt_tanh2(mul2(a2, v[p])), bt[j][p]);
+                st_stream_if(ok, yb + u * grow + j * W * VEC, pack2(v));
+            }
         }
         row0 += rstride;
         yb += rstride * N;
@@ -351,6 +363,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* alp
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
+        GBN_CASE(12) GBN_CASE(13)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }

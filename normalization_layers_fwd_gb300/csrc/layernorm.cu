@@ -32,22 +32,29 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
                 float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
                 int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kind_U(S, kFwdNorm), T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kFwdNorm), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
     int parity = 0;
     const int g = grp<W>(), l = lan<W>();
-    const bool colok = in_group<W>() && l < N / VEC;
+    // vector j of a row is vector l + j*W: in shared memory at +j*W*16 bytes
+    bool colok[KV];
+#pragma unroll
+    for (int j = 0; j < KV; ++j) colok[j] = in_group<W>() && l + j * W < N / VEC;
     const int rb = N * (int)sizeof(TX);
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
 
-    f2 gm[P], bt[P];
+    f2 gm[KV][P], bt[KV][P];
 #pragma unroll
-    for (int p = 0; p < P; ++p) {
-        gm[p] = (colok && gamma) ? ld_param2(gamma, pt, l * VEC + 2 * p) : splat2(1.f);
-        bt[p] = (colok && beta) ? ld_param2(beta, pt, l * VEC + 2 * p) : splat2(0.f);
+    for (int j = 0; j < KV; ++j) {
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            const int c = (l + j * W) * VEC + 2 * p;
+            gm[j][p] = (colok[j] && gamma) ? ld_param2(gamma, pt, c) : splat2(1.f);
+            bt[j][p] = (colok[j] && beta) ? ld_param2(beta, pt, c) : splat2(0.f);
+        }
     }
 
     Ring<1, kind_stages(S, kFwdNorm)> rg;
@@ -68,18 +75,21 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* xs = rg.tile(k, 0) + soff;
         const bool full = b < nfull;
-        bool okr[U], ok[U];
-        f2 xv[U][P];
+        bool okr[U];
+        f2 xv[U][KV][P];
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             okr[u] = alive && (full || row0 + u * G < M);
-            ok[u] = okr[u] && colok;
-            unpack2(lds128_if(ok[u], xs + u * srow), xv[u]);
-            f2 a2 = xv[u][0];
+            s[u] = 0.f;
 #pragma unroll
-            for (int p = 1; p < P; ++p) a2 = add2(a2, xv[u][p]);
-            s[u] = lo2(a2) + hi2(a2);
+            for (int j = 0; j < KV; ++j) {
+                unpack2(lds128_if(okr[u] && colok[j], xs + u * srow + j * W * 16), xv[u][j]);
+                f2 a2 = xv[u][j][0];
+#pragma unroll
+                for (int p = 1; p < P; ++p) a2 = add2(a2, xv[u][j][p]);
+                s[u] += lo2(a2) + hi2(a2);
+            }
         }
         group_allreduce<W, T, U>(s, red, parity);
         float mu[U], q[U];
@@ -87,23 +97,30 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
         for (int u = 0; u < U; ++u) {
             mu[u] = s[u] * inv_n;
             const f2 m2 = splat2(mu[u]);
-            f2 q2 = splat2(0.f);
+            q[u] = 0.f;
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                xv[u][p] = sub2(xv[u][p], m2);  // x - mu, kept for the output
-                q2 = fma2(xv[u][p], xv[u][p], q2);
+            for (int j = 0; j < KV; ++j) {
+                f2 q2 = splat2(0.f);
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    xv[u][j][p] = sub2(xv[u][j][p], m2);  // x - mu, kept for the output
+                    q2 = fma2(xv[u][j][p], xv[u][j][p], q2);
+                }
+                q[u] += colok[j] ? lo2(q2) + hi2(q2) : 0.f;  // vectors past the row's end add nothing
             }
-            q[u] = colok ? lo2(q2) + hi2(q2) : 0.f;  // a vector past the row's end adds nothing
         }
         group_allreduce<W, T, U>(q, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const float rs = rsqrtf(fmaf(q[u], inv_n, eps));
             const f2 r2 = splat2(rs);
-            f2 o[P];
 #pragma unroll
-            for (int p = 0; p < P; ++p) o[p] = fma2(mul2(xv[u][p], r2), gm[p], bt[p]);
-            st_stream_if(ok[u], yb + u * grow, pack2(o));
+            for (int j = 0; j < KV; ++j) {
+                f2 o[P];
+#pragma unroll
+                for (int p = 0; p < P; ++p) o[p] = fma2(mul2(xv[u][j][p], r2), gm[j][p], bt[j][p]);
+                st_stream_if(okr[u] && colok[j], yb + u * grow + j * W * VEC, pack2(o));
+            }
             if (mean) st_f32_if(lead && okr[u], mean + (row0 + u * G), mu[u]);
             if (rstd) st_f32_if(lead && okr[u], rstd + (row0 + u * G), rs);
         }
@@ -125,24 +142,34 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
                 float* __restrict__ ws, int64_t M, int N, float inv_n, int64_t nblocks,
                 unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kind_U(S, kBwdLN), T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kBwdLN), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
+    // xhat and g of every vector stay in registers across the row reduction;
+    // with the column accumulators that caps this kernel at 2 vectors per
+    // thread (4 spill).
+    static_assert(KV <= 2, "the LayerNorm backward takes at most 2 vectors per thread");
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, 2 * U>::kFloats];
     int parity = 0;
     const int g = grp<W>(), l = lan<W>();
-    const bool colok = in_group<W>() && l < N / VEC;
+    // vector j of a row is vector l + j*W: in shared memory at +j*W*16 bytes
+    bool colok[KV];
+#pragma unroll
+    for (int j = 0; j < KV; ++j) colok[j] = in_group<W>() && l + j * W < N / VEC;
     const int rb = N * (int)sizeof(TX);
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
 
-    f2 gm[P];
+    f2 gm[KV][P], acc_g[KV][P], acc_b[KV][P];
 #pragma unroll
-    for (int p = 0; p < P; ++p)
-        gm[p] = (colok && gamma) ? ld_param2(gamma, pt, l * VEC + 2 * p) : splat2(1.f);
-    f2 acc_g[P], acc_b[P];
+    for (int j = 0; j < KV; ++j) {
 #pragma unroll
-    for (int p = 0; p < P; ++p) acc_g[p] = acc_b[p] = splat2(0.f);
+        for (int p = 0; p < P; ++p) {
+            gm[j][p] = (colok[j] && gamma) ? ld_param2(gamma, pt, (l + j * W) * VEC + 2 * p)
+                                           : splat2(1.f);
+            acc_g[j][p] = acc_b[j][p] = splat2(0.f);
+        }
+    }
 
     // saved statistics of this thread's rows of the block starting at row0
     float mu_n[U], rs_n[U];
@@ -157,39 +184,44 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     load_stats((int64_t)blockIdx.x * (G * U) + g);
 
     // Pass 1 (before the row reduction) also accumulates the parameter
-    // gradients, which do not depend on it; pass 2 keeps only xhat and g.
+    // gradients, which do not depend on it; pass 2 needs only xhat and g.
     auto rows = [&](const unsigned char* xs, const unsigned char* ds, TX* dxb, int64_t row0,
                     bool alive, auto masked) {
         constexpr bool kMask = decltype(masked)::value;
         float rs[U];
-        f2 xh[U][P], gg[U][P];
-        bool ok[U];
+        f2 xh[U][KV][P], gg[U][KV][P];
+        bool okr[U];
         float s[2 * U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            ok[u] = alive && colok && (!kMask || row0 + u * G < M);
-            const bool okr = !kMask || row0 + u * G < M;
-            const f2 m2 = splat2(mu_n[u]), r2 = splat2(rs_n[u]);
+            okr[u] = !kMask || row0 + u * G < M;
             rs[u] = rs_n[u];
-            f2 dv[P];
-            unpack2(lds128_if(ok[u], xs + u * srow), xh[u]);
-            unpack2(lds128_if(ok[u], ds + u * srow), dv);
+            const f2 m2 = splat2(mu_n[u]), r2 = splat2(rs[u]);
             // (sum g, sum g*xhat); vectors past the row's end hold dy = 0
             f2 s1 = splat2(0.f), s2 = splat2(0.f);
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                xh[u][p] = mul2(sub2(xh[u][p], m2), r2);
-                gg[u][p] = mul2(dv[p], gm[p]);
-                s1 = add2(s1, gg[u][p]);
-                s2 = fma2(gg[u][p], xh[u][p], s2);
-                if constexpr (kMask) {
-                    // padded rows: select after the arithmetic, never a 0/1 multiply
-                    const f2 z = splat2(0.f);
-                    acc_g[p] = add2(acc_g[p], sel2(okr, mul2(dv[p], xh[u][p]), z));
-                    acc_b[p] = add2(acc_b[p], sel2(okr, dv[p], z));
-                } else {
-                    acc_g[p] = fma2(dv[p], xh[u][p], acc_g[p]);
-                    acc_b[p] = add2(acc_b[p], dv[p]);
+            for (int j = 0; j < KV; ++j) {
+                const bool ok = alive && colok[j] && okr[u];
+                f2 xv[P], dv[P];
+                unpack2(lds128_if(ok, xs + u * srow + j * W * 16), xv);
+                unpack2(lds128_if(ok, ds + u * srow + j * W * 16), dv);
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    const f2 xhv = mul2(sub2(xv[p], m2), r2);
+                    const f2 ggv = mul2(dv[p], gm[j][p]);
+                    s1 = add2(s1, ggv);
+                    s2 = fma2(ggv, xhv, s2);
+                    if constexpr (kMask) {
+                        // padded rows: select after the arithmetic, never a 0/1 multiply
+                        const f2 z = splat2(0.f);
+                        acc_g[j][p] = add2(acc_g[j][p], sel2(okr[u], mul2(dv[p], xhv), z));
+                        acc_b[j][p] = add2(acc_b[j][p], sel2(okr[u], dv[p], z));
+                    } else {
+                        acc_g[j][p] = fma2(dv[p], xhv, acc_g[j][p]);
+                        acc_b[j][p] = add2(acc_b[j][p], dv[p]);
+                    }
+                    xh[u][j][p] = xhv;
+                    gg[u][j][p] = ggv;
                 }
             }
             s[2 * u] = lo2(s1) + hi2(s1);
@@ -201,12 +233,17 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
         for (int u = 0; u < U; ++u) {
             const f2 ma = splat2(s[2 * u] * inv_n), nmb = splat2(-(s[2 * u + 1] * inv_n));
             const f2 r2 = splat2(rs[u]);
-            f2 o[P];
-            // rstd * (g - mean(g) - xhat * mean(g xhat)); g - mean(g) first,
-            // so a width-one row gives exactly zero
 #pragma unroll
-            for (int p = 0; p < P; ++p) o[p] = mul2(r2, fma2(xh[u][p], nmb, sub2(gg[u][p], ma)));
-            st_stream_if(ok[u], dxb + u * grow, pack2(o));
+            for (int j = 0; j < KV; ++j) {
+                const bool ok = alive && colok[j] && okr[u];
+                // rstd * (g - mean(g) - xhat * mean(g xhat)); g - mean(g) first,
+                // so a width-one row gives exactly zero
+                f2 o[P];
+#pragma unroll
+                for (int p = 0; p < P; ++p)
+                    o[p] = mul2(r2, fma2(xh[u][j][p], nmb, sub2(gg[u][j][p], ma)));
+                st_stream_if(ok, dxb + u * grow + j * W * VEC, pack2(o));
+            }
         }
     };
 
@@ -237,8 +274,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     if (ws == nullptr) return;  // no parameter gradient requested (uniform)
     float* wrow = ws + blockIdx.x * (2 * (int64_t)N);
     float* colbuf = reinterpret_cast<float*>(dsm + 128);  // drained ring slots, past the barriers
-    cta_store_columns2<W, P, T>(acc_g, colbuf, wrow, N);
-    cta_store_columns2<W, P, T>(acc_b, colbuf, wrow + N, N);
+    cta_store_columns_kv<W, KV, P, T>(acc_g, colbuf, wrow, N);
+    cta_store_columns_kv<W, KV, P, T>(acc_b, colbuf, wrow + N, N);
 }
 
 // ------------------------------------------------------ general (any shape)
@@ -339,6 +376,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
+        GBN_CASE(12) GBN_CASE(13)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }
@@ -370,6 +408,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
+        GBN_CASE(12)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }

@@ -55,7 +55,7 @@ DTYPES = [(torch.bfloat16, torch.float32), (torch.bfloat16, torch.bfloat16),
 CASES = []
 for xdt, pdt in DTYPES:
     for N in (BF16_WIDTHS if xdt == torch.bfloat16 else F32_WIDTHS):
-        if pdt != torch.float32 and N not in (24, 128, 2048):
+        if pdt != torch.float32 and N not in (24, 128, 2048, 3072, 8192):
             continue
         for op in ("dyt", "layernorm", "rmsnorm"):
             CASES.append((op, xdt, pdt, N))

@@ -88,18 +88,23 @@ int64_t general_warps(int64_t M, int sms) { return M < 4LL * sms ? M : 4LL * sms
 
 // Whether [M, N] of dtype xt can take the 16-byte vector path (alignment
 // aside), and its schedule index.
-// Kernels given kv_max > 1 take the multi-vector schedules (up to kv_max
-// vectors per thread) for rows of more than 256 vectors: only kernels whose
-// row summation order no other kernel has to reproduce, within their
-// register budget.
-int fast_sid(int64_t N, int xt, int kv_max)
+// Multi-vector schedules a kernel may take for rows of more than 256
+// vectors, as a set (bit s - kNumSched1 for schedule s), chosen per kernel
+// within its register budget and by measurement: the DyT and LayerNorm
+// forwards 12-13, the LayerNorm backward 12 and 14, the DyT backward 12,
+// the RMSNorm forward and backward 12 (the same set, so the backward's
+// recomputed rstd reduces a row in the forward's order).  Other rows, and
+// kernels with an empty set, take the one-vector schedules.
+constexpr unsigned kWide12 = 1u, kWide13 = 2u, kWide14 = 4u;
+
+int fast_sid(int64_t N, int xt, unsigned wide)
 {
     const int vec = 16 / elem_bytes(xt);
     if (N % vec != 0) return -1;
     const int64_t nvec = N / vec;
     if (nvec > 256) {
         for (int s = gbn::kNumSched1; s < gbn::kNumSched; ++s)
-            if (gbn::kSched[s].KV <= kv_max && nvec <= gbn::kSched[s].max_nvec) return s;
+            if (((wide >> (s - gbn::kNumSched1)) & 1u) && nvec <= gbn::kSched[s].max_nvec) return s;
     }
     for (int s = 0; s < gbn::kNumSched1; ++s)
         if (nvec <= gbn::kSched[s].max_nvec) return s;
@@ -108,11 +113,11 @@ int fast_sid(int64_t N, int xt, int kv_max)
 
 // The launch layout of one row-wise kernel of the given kind (gbn::KernelKind).
 Launch plan(int64_t M, int64_t N, int xt, bool aligned, int sms, cudaStream_t stream, int kind,
-            int kv_max = 1)
+            unsigned wide = 0)
 {
     Launch L{};
     L.stream = stream;
-    const int sid = aligned ? fast_sid(N, xt, kv_max) : -1;
+    const int sid = aligned ? fast_sid(N, xt, wide) : -1;
     if (sid >= 0) {
         const gbn::SchedEntry& e = gbn::kSched[sid];
         const int64_t rows_per_block =
@@ -236,7 +241,7 @@ size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int
     const Launch a =
         plan(M, N, xt, true, sms, nullptr,
              op == GBN_OP_DYT ? gbn::kBwdDyT : op == GBN_OP_LAYERNORM ? gbn::kBwdLN : gbn::kBwdRms,
-            op == GBN_OP_LAYERNORM ? 2 : 1);
+             op == GBN_OP_LAYERNORM ? kWide12 | kWide14 : kWide12);
     const Launch b = plan(M, N, xt, false, sms, nullptr, gbn::kBwdLN);
     const size_t need = ws_needed(op, a.P > b.P ? a : b, N);
     return (need + 255) & ~(size_t)255;
@@ -253,7 +258,8 @@ int dyt_fwd(const void* x, const void* alpha, const void* gamma, const void* bet
     if (M == 0) return GBN_OK;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, gbn::kFwdDyT, 4);
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, gbn::kFwdDyT,
+                    kWide12 | kWide13);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (!L.fast) {  // elementwise general path: one thread per element, grid-stride
         const int64_t E = M * N;
@@ -278,7 +284,7 @@ int dyt_bwd(const void* x, const void* dy, const void* alpha, const void* gamma,
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                    gbn::kBwdDyT);
+                    gbn::kBwdDyT, kWide12);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_DYT, L, N))) return GBN_EWORKSPACE;
     float* wsf = grads ? static_cast<float*>(ws) : nullptr;
@@ -305,7 +311,7 @@ int layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, f
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream,
-                    gbn::kFwdNorm, 4);
+                    gbn::kFwdLN, kWide12 | kWide13);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     return launch_status(
         gbn::launch_ln_fwd(L, xt, pt, x, gamma, beta, y, mean, rstd, M, (int)N, eps));
@@ -326,7 +332,7 @@ int layernorm_bwd(const void* x, const void* dy, const float* mean, const float*
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                    gbn::kBwdLN, 2);
+                    gbn::kBwdLN, kWide12 | kWide14);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_LAYERNORM, L, N)))
         return GBN_EWORKSPACE;
@@ -353,7 +359,7 @@ int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, i
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream,
-                    gbn::kFwdNorm);
+                    gbn::kFwdNorm, kWide12);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     return launch_status(gbn::launch_rms_fwd(L, xt, wt, x, w, y, rstd, M, (int)N, eps));
 }
@@ -371,7 +377,7 @@ int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd,
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                    gbn::kBwdRms);
+                    gbn::kBwdRms, kWide12);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     if (dw && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_RMSNORM, L, N))) return GBN_EWORKSPACE;
     float* wsf = dw ? static_cast<float*>(ws) : nullptr;

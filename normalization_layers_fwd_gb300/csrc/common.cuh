@@ -35,18 +35,19 @@ struct SchedEntry {
 // Rows of exactly 3 vectors (bf16 N = 24, the tall-narrow LayerNorm of the
 // torch-xpu-ops page) take segmented groups of W = 3 lanes, 10 per warp,
 // instead of 4-lane groups with a lane idle.
-// Schedules 12-13: wide rows (257-1024 vectors) held by 256 threads with
-// KV = 2 or 4 vectors each (vector l + j*W for j < KV), one row per CTA of
-// 256 threads.  Against schedules 10-11 they divide the per-row reduction
-// and barrier cost by KV and let two independent CTAs share an SM.  Only
-// kernels whose summation order nothing else has to reproduce take them.
-constexpr int kNumSched = 14;
+// Schedules 12-14: wide rows (257-1024 vectors) held by 256 or 512 threads
+// with KV = 2 or 4 vectors each (vector l + j*W for j < KV), one row per
+// CTA.  Against schedules 10-11 they divide the per-row reduction and
+// barrier cost by KV; at 256 threads two independent CTAs share an SM.
+// Which kernel takes which is decided per kernel by the planner (api.cu),
+// within each kernel's register budget.
+constexpr int kNumSched = 15;
 constexpr int kNumSched1 = 12;  // the one-vector schedules
 constexpr SchedEntry kSched[kNumSched] = {
     {1, 1, 256, 1},     {2, 2, 256, 1},     {3, 3, 256, 1},     {4, 4, 256, 1},
     {8, 8, 256, 1},     {16, 16, 256, 1},   {32, 32, 256, 1},   {64, 64, 256, 1},
     {128, 128, 256, 1}, {256, 256, 256, 1}, {512, 512, 512, 1}, {1024, 1024, 1024, 1},
-    {512, 256, 256, 2}, {1024, 256, 256, 4},
+    {512, 256, 256, 2}, {1024, 256, 256, 4}, {1024, 512, 512, 2},
 };
 constexpr int kMaxFastVec = 1024;
 
@@ -90,7 +91,11 @@ __device__ __forceinline__ bool in_group()
 // keep more per-row state, so they run 2 CTAs per SM.  At the widest rows
 // (512 threads at 2 CTAs per SM, 64 registers) the backwards keep one row
 // per thread: two spill.
-enum KernelKind : int { kFwdDyT = 0, kFwdNorm = 1, kBwdLN = 2, kBwdDyT = 3, kBwdRms = 4 };
+// kFwdNorm is the RMSNorm forward; the LayerNorm forward (kFwdLN) shares its
+// traits except at 2 vectors per thread, where it runs 3 CTAs per SM.
+enum KernelKind : int {
+    kFwdDyT = 0, kFwdNorm = 1, kFwdLN = 2, kBwdLN = 3, kBwdDyT = 4, kBwdRms = 5
+};
 
 constexpr bool is_bwd(int kind) { return kind >= kBwdLN; }
 
@@ -112,7 +117,7 @@ constexpr int kind_U(int S, int kind)
 // row), so it runs one CTA per SM rather than spill at two.
 constexpr int kind_minb(int S, int kind)
 {
-    return kSched[S].KV > 1 ? 2
+    return kSched[S].KV > 1 ? (kSched[S].T == 512 ? 1 : kind == kFwdLN && kSched[S].KV == 2 ? 3 : 2)
            : kSched[S].T == 1024 ? 1
            : kSched[S].T == 512 ? (kind == kBwdDyT ? 1 : 2)
            : kind == kBwdRms    ? 3
@@ -130,7 +135,7 @@ constexpr int kind_minb(int S, int kind)
 constexpr int kind_stages(int S, int kind)
 {
     return !is_bwd(kind) ? (kSched[S].KV == 1 ? (kSched[S].T == 256 ? 2 : 4)
-                            : kSched[S].KV == 4 && kind == kFwdNorm ? 2
+                            : kSched[S].KV == 4 && kind == kFwdLN ? 2
                                                                     : 4)
            : kind == kBwdRms ? 3
            : kind == kBwdDyT && kSched[S].T == 1024 ? 3

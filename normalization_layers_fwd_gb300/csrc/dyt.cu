@@ -188,28 +188,38 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
                  const void* __restrict__ alpha, const void* __restrict__ gamma, int pt,
                  float* __restrict__ ws, int64_t M, int N, int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kind_U(S, kBwdDyT), T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kBwdDyT), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
+    static_assert(KV <= 2, "the DyT backward takes at most 2 vectors per thread");
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[T / 32];
     const int g = grp<W>(), l = lan<W>();
-    const bool colok = in_group<W>() && l < N / VEC;
+    // vector j of a row is vector l + j*W: in shared memory at +j*W*16 bytes
+    bool colok[KV];
+#pragma unroll
+    for (int j = 0; j < KV; ++j) colok[j] = in_group<W>() && l + j * W < N / VEC;
     const int rb = N * (int)sizeof(TX);
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
 
     const f2 a2 = splat2(ld_param(alpha, pt, 0));
-    f2 gm[P], ga[P];
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-        gm[p] = colok ? ld_param2(gamma, pt, l * VEC + 2 * p) : splat2(0.f);
-        ga[p] = mul2(gm[p], a2);
-    }
+    f2 gm[KV][P];
+    // gamma*alpha: precomputed with one vector per thread; with two it is
+    // recomputed at each use (the same product, so the same bits), which
+    // keeps the kernel within 128 registers
+    f2 ga[KV == 1 ? P : 1];
     // Per-column accumulators: sum dy*t, sum dy, sum dy*x*sech^2 (gamma is
     // applied to the last one once, at the end).
-    f2 acc_g[P], acc_b[P], acc_a[P];
+    f2 acc_g[KV][P], acc_b[KV][P], acc_a[KV][P];
 #pragma unroll
-    for (int p = 0; p < P; ++p) acc_g[p] = acc_b[p] = acc_a[p] = splat2(0.f);
+    for (int j = 0; j < KV; ++j) {
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            gm[j][p] = colok[j] ? ld_param2(gamma, pt, (l + j * W) * VEC + 2 * p) : splat2(0.f);
+            if constexpr (KV == 1) ga[p] = mul2(gm[0][p], a2);
+            acc_g[j][p] = acc_b[j][p] = acc_a[j][p] = splat2(0.f);
+        }
+    }
 
     auto rows = [&](const unsigned char* xs, const unsigned char* ds, TX* dxb, int64_t row0,
                     bool alive, auto masked) {
@@ -217,29 +227,35 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const bool okr = !kMask || row0 + u * G < M;
-            const bool ok = alive && colok && okr;
-            f2 xv[P], dv[P], o[P];
-            unpack2(lds128_if(ok, xs + u * srow), xv);
-            unpack2(lds128_if(ok, ds + u * srow), dv);
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                f2 t, s;
-                dyt_tanh_sech2_2(mul2(a2, xv[p]), t, s);
-                const f2 dsd = mul2(dv[p], s);
-                o[p] = mul2(dsd, ga[p]);
-                if constexpr (kMask) {
-                    // padded rows: select after the arithmetic, never a 0/1 multiply
-                    const f2 z = splat2(0.f);
-                    acc_g[p] = add2(acc_g[p], sel2(okr, mul2(dv[p], t), z));
-                    acc_b[p] = add2(acc_b[p], sel2(okr, dv[p], z));
-                    acc_a[p] = add2(acc_a[p], sel2(okr, mul2(dsd, xv[p]), z));
-                } else {
-                    acc_g[p] = fma2(dv[p], t, acc_g[p]);
-                    acc_b[p] = add2(acc_b[p], dv[p]);
-                    acc_a[p] = fma2(dsd, xv[p], acc_a[p]);
+            for (int j = 0; j < KV; ++j) {
+                const bool ok = alive && colok[j] && okr;
+                f2 xv[P], dv[P], o[P];
+                unpack2(lds128_if(ok, xs + u * srow + j * W * 16), xv);
+                unpack2(lds128_if(ok, ds + u * srow + j * W * 16), dv);
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    f2 t, s;
+                    dyt_tanh_sech2_2(mul2(a2, xv[p]), t, s);
+                    const f2 dsd = mul2(dv[p], s);
+                    if constexpr (KV == 1)
+                        o[p] = mul2(dsd, ga[p]);
+                    else
+                        o[p] = mul2(dsd, mul2(gm[j][p], a2));
+                    if constexpr (kMask) {
+                        // padded rows: select after the arithmetic, never a 0/1 multiply
+                        const f2 z = splat2(0.f);
+                        acc_g[j][p] = add2(acc_g[j][p], sel2(okr, mul2(dv[p], t), z));
+                        acc_b[j][p] = add2(acc_b[j][p], sel2(okr, dv[p], z));
+                        acc_a[j][p] = add2(acc_a[j][p], sel2(okr, mul2(dsd, xv[p]), z));
+                    } else {
+                        acc_g[j][p] = fma2(dv[p], t, acc_g[j][p]);
+                        acc_b[j][p] = add2(acc_b[j][p], dv[p]);
+                        acc_a[j][p] = fma2(dsd, xv[p], acc_a[j][p]);
+                    }
                 }
+                st_stream_if(ok, dxb + u * grow + j * W * VEC, pack2(o));
             }
-            st_stream_if(ok, dxb + u * grow, pack2(o));
         }
     };
 
@@ -271,16 +287,19 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     const int64_t L = 2 * (int64_t)N + 1;
     float* wrow = ws + blockIdx.x * L;
     float* colbuf = reinterpret_cast<float*>(dsm + 128);  // drained ring slots, past the barriers
-    cta_store_columns2<W, P, T>(acc_g, colbuf, wrow, N);
-    cta_store_columns2<W, P, T>(acc_b, colbuf, wrow + N, N);
+    cta_store_columns_kv<W, KV, P, T>(acc_g, colbuf, wrow, N);
+    cta_store_columns_kv<W, KV, P, T>(acc_b, colbuf, wrow + N, N);
     // lanes past the row's end hold garbage (tanh(alpha*0) for alpha = inf);
     // they are never stored above and are excluded here
     float da = 0.f;
-    if (colok) {
 #pragma unroll
-        for (int p = 0; p < P; ++p) {
-            const f2 q = mul2(gm[p], acc_a[p]);
-            da += lo2(q) + hi2(q);
+    for (int j = 0; j < KV; ++j) {
+        if (colok[j]) {
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const f2 q = mul2(gm[j][p], acc_a[j][p]);
+                da += lo2(q) + hi2(q);
+            }
         }
     }
     const float tot = cta_sum<T>(da, red);
@@ -394,6 +413,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
+        GBN_CASE(12)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }

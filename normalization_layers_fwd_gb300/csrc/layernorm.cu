@@ -26,13 +26,13 @@ namespace {
 // collective); loads and stores are predicated, and only the ragged last
 // block compares rows against M.
 template <typename TX, int S>
-__global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
+__global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
     ln_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ gamma,
                 const void* __restrict__ beta, int pt, float* __restrict__ mean,
                 float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
                 int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kind_U(S, kFwdNorm), T = kSched[S].T, KV = kSched[S].KV;
+    constexpr int W = kSched[S].W, U = kind_U(S, kFwdLN), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
     extern __shared__ __align__(128) unsigned char dsm[];
@@ -57,13 +57,13 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
         }
     }
 
-    Ring<1, kind_stages(S, kFwdNorm)> rg;
+    Ring<1, kind_stages(S, kFwdLN)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = slot_bytes(S, kFwdNorm);
+    rg.slot = slot_bytes(S, kFwdLN);
     rg.fault = fault;
     // Row positions advance by a fixed stride from one of this CTA's blocks
     // to the next; blocks below nfull hold no padded rows.
@@ -368,7 +368,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, kFwdNorm, 1);                                  \
+        constexpr int smem = ring_smem_bytes(S, kFwdLN, 1);                                    \
         auto kern = ln_fwd_fast<TX, S>;                                                      \
         ring_attributes<ln_fwd_fast<TX, S>>(smem);                                                         \
         kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault);                              \
@@ -408,7 +408,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
-        GBN_CASE(12)
+        GBN_CASE(12) GBN_CASE(14)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }

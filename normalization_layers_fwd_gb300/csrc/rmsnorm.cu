@@ -61,24 +61,31 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
                  int pt, float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
                  int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kind_U(S, kFwdNorm), T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kFwdNorm), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
     int parity = 0;
     const int g = grp<W>(), l = lan<W>();
-    const bool colok = in_group<W>() && l < N / VEC;
+    // vector j of a row is vector l + j*W: in shared memory at +j*W*16 bytes
+    bool colok[KV];
+#pragma unroll
+    for (int j = 0; j < KV; ++j) colok[j] = in_group<W>() && l + j * W < N / VEC;
     const int rb = N * (int)sizeof(TX);
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
     const bool wbf = is_bf16<TX>() && pt == kBF16;
 
-    f2 wf[P];
-    uint32_t wpk[P];  // the bf16 weight pair, packed (used when wbf)
+    f2 wf[KV][P];
+    uint32_t wpk[KV][P];  // the bf16 weight pair, packed (used when wbf)
 #pragma unroll
-    for (int p = 0; p < P; ++p) {
-        wf[p] = colok ? ld_param2(w, pt, l * VEC + 2 * p) : splat2(0.f);
-        wpk[p] = (wbf && colok) ? static_cast<const uint32_t*>(w)[(l * VEC) / 2 + p] : 0u;
+    for (int j = 0; j < KV; ++j) {
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            const int c = (l + j * W) * VEC + 2 * p;
+            wf[j][p] = colok[j] ? ld_param2(w, pt, c) : splat2(0.f);
+            wpk[j][p] = (wbf && colok[j]) ? static_cast<const uint32_t*>(w)[c / 2] : 0u;
+        }
     }
 
     Ring<1, kind_stages(S, kFwdNorm)> rg;
@@ -97,37 +104,44 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* xs = rg.tile(k, 0) + soff;
         const bool full = b < nfull;
-        bool okr[U], ok[U];
-        f2 xv[U][P];
+        bool okr[U];
+        f2 xv[U][KV][P];
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             okr[u] = alive && (full || row0 + u * G < M);
-            ok[u] = okr[u] && colok;
-            unpack2(lds128_if(ok[u], xs + u * srow), xv[u]);
-            s[u] = vec_sumsq2<P>(xv[u]);
+            s[u] = 0.f;
+#pragma unroll
+            for (int j = 0; j < KV; ++j) {
+                unpack2(lds128_if(okr[u] && colok[j], xs + u * srow + j * W * 16), xv[u][j]);
+                s[u] += vec_sumsq2<P>(xv[u][j]);
+            }
         }
         group_allreduce<W, T, U>(s, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const float rs = rsqrtf(fmaf(s[u], inv_n, eps));
             const f2 r2 = splat2(rs);
-            uint4 out;
-            if constexpr (is_bf16<TX>()) {
-                uint32_t o[4];
 #pragma unroll
-                for (int p = 0; p < P; ++p) {
-                    const uint32_t npk = f2_to_bf2(mul2(xv[u][p], r2));  // n = round_x(x r)
-                    o[p] = wbf ? bmul2(wpk[p], npk) : f2_to_bf2(mul2(wf[p], bf2_to_f2(npk)));
+            for (int j = 0; j < KV; ++j) {
+                uint4 out;
+                if constexpr (is_bf16<TX>()) {
+                    uint32_t o[4];
+#pragma unroll
+                    for (int p = 0; p < P; ++p) {
+                        const uint32_t npk = f2_to_bf2(mul2(xv[u][j][p], r2));  // n = round_x(x r)
+                        o[p] = wbf ? bmul2(wpk[j][p], npk)
+                                   : f2_to_bf2(mul2(wf[j][p], bf2_to_f2(npk)));
+                    }
+                    out = make_uint4(o[0], o[1], o[2], o[3]);
+                } else {
+                    f2 o[P];
+#pragma unroll
+                    for (int p = 0; p < P; ++p) o[p] = mul2(wf[j][p], mul2(xv[u][j][p], r2));
+                    out = pack2(o);
                 }
-                out = make_uint4(o[0], o[1], o[2], o[3]);
-            } else {
-                f2 o[P];
-#pragma unroll
-                for (int p = 0; p < P; ++p) o[p] = mul2(wf[p], mul2(xv[u][p], r2));
-                out = pack2(o);
+                st_stream_if(okr[u] && colok[j], yb + u * grow + j * W * VEC, out);
             }
-            st_stream_if(ok[u], yb + u * grow, out);
             if (rstd) st_f32_if(lead && okr[u], rstd + (row0 + u * G), rs);
         }
         row0 += rstride;
@@ -147,27 +161,35 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
                  float* __restrict__ ws, int64_t M, int N, float eps, float inv_n,
                  int64_t nblocks, unsigned* fault)
 {
-    constexpr int W = kSched[S].W, U = kind_U(S, kBwdRms), T = kSched[S].T;
+    constexpr int W = kSched[S].W, U = kind_U(S, kBwdRms), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
+    static_assert(KV <= 2, "the RMSNorm backward takes at most 2 vectors per thread");
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
     int parity = 0;
     const int g = grp<W>(), l = lan<W>();
-    const bool colok = in_group<W>() && l < N / VEC;
+    // vector j of a row is vector l + j*W: in shared memory at +j*W*16 bytes
+    bool colok[KV];
+#pragma unroll
+    for (int j = 0; j < KV; ++j) colok[j] = in_group<W>() && l + j * W < N / VEC;
     const int rb = N * (int)sizeof(TX);
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
     // a weight in x's dtype: each dy*n is rounded to x's dtype (bf16 pairs
     // then multiply in bf16); a float32 weight keeps the float32 product
     const bool wbf = is_bf16<TX>() && pt == kBF16;
 
-    f2 wf[P], acc[P];
-    uint32_t wpk[P];
+    f2 wf[KV][P], acc[KV][P];
+    uint32_t wpk[KV][P];
 #pragma unroll
-    for (int p = 0; p < P; ++p) {
-        wf[p] = colok ? ld_param2(w, pt, l * VEC + 2 * p) : splat2(0.f);
-        wpk[p] = (wbf && colok) ? static_cast<const uint32_t*>(w)[(l * VEC) / 2 + p] : 0u;
-        acc[p] = splat2(0.f);
+    for (int j = 0; j < KV; ++j) {
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            const int c = (l + j * W) * VEC + 2 * p;
+            wf[j][p] = colok[j] ? ld_param2(w, pt, c) : splat2(0.f);
+            wpk[j][p] = (wbf && colok[j]) ? static_cast<const uint32_t*>(w)[c / 2] : 0u;
+            acc[j][p] = splat2(0.f);
+        }
     }
     float rs_n[U];
     auto load_rstd = [&](int64_t row0) {
@@ -188,18 +210,25 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
                     bool alive, auto masked) {
         constexpr bool kMask = decltype(masked)::value;
         float rs[U];
-        bool ok[U];
-        f2 xh[U][P], dn[U][P];
+        bool okr[U];
+        f2 xh[U][KV][P], dn[U][KV][P];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            ok[u] = alive && colok && (!kMask || row0 + u * G < M);
-            unpack2(lds128_if(ok[u], xs + u * srow), xh[u]);  // x, scaled by r below
+            okr[u] = !kMask || row0 + u * G < M;
+#pragma unroll
+            for (int j = 0; j < KV; ++j)  // x, scaled by r below
+                unpack2(lds128_if(alive && okr[u] && colok[j], xs + u * srow + j * W * 16),
+                        xh[u][j]);
             rs[u] = rs_n[u];
         }
         load_rstd(row0 + (int64_t)gridDim.x * (G * U));
         if (!rstd) {  // uniform branch: recompute r exactly as the forward does
 #pragma unroll
-            for (int u = 0; u < U; ++u) rs[u] = vec_sumsq2<P>(xh[u]);
+            for (int u = 0; u < U; ++u) {
+                rs[u] = 0.f;
+#pragma unroll
+                for (int j = 0; j < KV; ++j) rs[u] += vec_sumsq2<P>(xh[u][j]);
+            }
             group_allreduce<W, T, U>(rs, red, parity);
 #pragma unroll
             for (int u = 0; u < U; ++u) rs[u] = rsqrtf(fmaf(rs[u], inv_n, eps));
@@ -207,34 +236,36 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const bool okr = !kMask || row0 + u * G < M;
             const f2 r2 = splat2(rs[u]);
-            const uint4 dr = lds128_if(ok[u], ds + u * srow);
-            f2 dv[P];
-            unpack2(dr, dv);
             f2 a2 = splat2(0.f);
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                xh[u][p] = mul2(xh[u][p], r2);
-                f2 nxt;  // the accumulator with this row's dw term added
-                if constexpr (is_bf16<TX>()) {
-                    const uint32_t npk = f2_to_bf2(xh[u][p]);  // n = round_x(xhat)
-                    if (wbf) {
-                        dn[u][p] = bf2_to_f2(bmul2(word(dr, p), wpk[p]));
-                        nxt = add2(acc[p], bf2_to_f2(bmul2(word(dr, p), npk)));
+            for (int j = 0; j < KV; ++j) {
+                const uint4 dr = lds128_if(alive && okr[u] && colok[j], ds + u * srow + j * W * 16);
+                f2 dv[P];
+                unpack2(dr, dv);
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    xh[u][j][p] = mul2(xh[u][j][p], r2);
+                    f2 nxt;  // the accumulator with this row's dw term added
+                    if constexpr (is_bf16<TX>()) {
+                        const uint32_t npk = f2_to_bf2(xh[u][j][p]);  // n = round_x(xhat)
+                        if (wbf) {
+                            dn[u][j][p] = bf2_to_f2(bmul2(word(dr, p), wpk[j][p]));
+                            nxt = add2(acc[j][p], bf2_to_f2(bmul2(word(dr, p), npk)));
+                        } else {
+                            // float32 weight: dy*n unrounded, exact product of two bf16
+                            dn[u][j][p] = round2<TX>(mul2(dv[p], wf[j][p]));
+                            nxt = mk2(fma_bf16_lo(word(dr, p), npk, lo2(acc[j][p])),
+                                      fma_bf16_hi(word(dr, p), npk, hi2(acc[j][p])));
+                        }
                     } else {
-                        // float32 weight: dy*n unrounded, exact product of two bf16
-                        dn[u][p] = round2<TX>(mul2(dv[p], wf[p]));
-                        nxt = mk2(fma_bf16_lo(word(dr, p), npk, lo2(acc[p])),
-                                  fma_bf16_hi(word(dr, p), npk, hi2(acc[p])));
+                        dn[u][j][p] = mul2(dv[p], wf[j][p]);
+                        nxt = fma2(dv[p], xh[u][j][p], acc[j][p]);
                     }
-                } else {
-                    dn[u][p] = mul2(dv[p], wf[p]);
-                    nxt = fma2(dv[p], xh[u][p], acc[p]);
+                    a2 = fma2(dn[u][j][p], xh[u][j][p], a2);
+                    // padded rows: keep the old sum, a select after the arithmetic
+                    acc[j][p] = (!kMask || okr[u]) ? nxt : acc[j][p];
                 }
-                a2 = fma2(dn[u][p], xh[u][p], a2);
-                // padded rows: keep the old sum, a select after the arithmetic
-                acc[p] = (!kMask || okr) ? nxt : acc[p];
             }
             s[u] = lo2(a2) + hi2(a2);
         }
@@ -242,10 +273,13 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const f2 r2 = splat2(rs[u]), nm = splat2(-(s[u] * inv_n));
-            f2 o[P];
 #pragma unroll
-            for (int p = 0; p < P; ++p) o[p] = mul2(r2, fma2(xh[u][p], nm, dn[u][p]));
-            st_stream_if(ok[u], dxb + u * grow, pack2(o));
+            for (int j = 0; j < KV; ++j) {
+                f2 o[P];
+#pragma unroll
+                for (int p = 0; p < P; ++p) o[p] = mul2(r2, fma2(xh[u][j][p], nm, dn[u][j][p]));
+                st_stream_if(alive && okr[u] && colok[j], dxb + u * grow + j * W * VEC, pack2(o));
+            }
         }
     };
 
@@ -275,7 +309,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
 
     if (ws == nullptr) return;  // no weight gradient requested (uniform)
     float* wrow = ws + blockIdx.x * (int64_t)N;
-    cta_store_columns2<W, P, T>(acc, reinterpret_cast<float*>(dsm + 128), wrow, N);  // drained ring slots
+    cta_store_columns_kv<W, KV, P, T>(acc, reinterpret_cast<float*>(dsm + 128), wrow, N);  // drained ring slots
 }
 
 // ------------------------------------------------------ general (any shape)
@@ -368,6 +402,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
+        GBN_CASE(12)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }
@@ -398,6 +433,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(10) GBN_CASE(11)
+        GBN_CASE(12)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }

@@ -48,8 +48,8 @@ def _run(op, inp, eps=1e-5, rows=None):
 
 
 BF16_WIDTHS = [1, 5, 8, 16, 24, 40, 64, 128, 129, 136, 256, 264, 512, 520, 1000, 1024, 2048,
-               3072, 4096, 8192, 8200]
-F32_WIDTHS = [1, 3, 4, 12, 64, 100, 256, 1024, 2048, 4096, 4100]
+               3072, 4096, 6000, 8192, 8200]
+F32_WIDTHS = [1, 3, 4, 12, 64, 100, 256, 1024, 2048, 3000, 4096, 4100]
 DTYPES = [(torch.bfloat16, torch.float32), (torch.bfloat16, torch.bfloat16),
           (torch.float32, torch.float32), (torch.float32, torch.bfloat16)]
 CASES = []

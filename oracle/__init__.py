@@ -6,8 +6,8 @@ never does.  The arithmetic lives in ``oracle.c`` (plain C, float64, serial
 sums in index order); this module only builds that file with gcc, marshals
 numpy arrays to it and returns numpy arrays.
 
-Inputs are numpy arrays: ``float32``, ``float64`` or ``uint16`` (raw
-bfloat16 bit patterns).  They are widened exactly inside the C code.
+Inputs are numpy arrays: ``float32``, ``float64``, ``float16`` or
+``uint16`` (raw bfloat16 bit patterns).  They are widened exactly inside the C code.
 Parameters (gamma, beta, weight) are passed as float64 arrays holding the
 exact values of the stored parameters.
 
@@ -23,7 +23,7 @@ import threading
 
 import numpy as np
 
-F32, BF16, F64 = 0, 1, 2
+F32, BF16, F64, F16 = 0, 1, 2, 3
 MATH, PARITY = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -63,6 +63,8 @@ def _lib():
             "orc_round_bf16": ([D], D),
             "orc_bf16_near_tie": ([D], I),
             "orc_round_bf16_array": ([P, P, I64], None),
+            "orc_round_f16": ([D], D),
+            "orc_round_f16_array": ([P, P, I64], None),
             "orc_dyt_fwd_rows": ([P, I, I64, I64, D, P, P, P, I64, P, P], I),
             "orc_dyt_bwd_rows": ([P, P, I, I64, I64, D, P, P, I64, P], I),
             "orc_dyt_bwd_cols": ([P, P, I, I64, I64, D, P, P, P, P, P, P, P], I),
@@ -89,7 +91,7 @@ def _act(a: np.ndarray):
     if a.ndim != 2:
         raise ValueError("activations must be 2-D [M, N]")
     code = {np.dtype(np.float32): F32, np.dtype(np.uint16): BF16,
-            np.dtype(np.float64): F64}.get(a.dtype)
+            np.dtype(np.float64): F64, np.dtype(np.float16): F16}.get(a.dtype)
     if code is None:
         raise TypeError(f"unsupported activation dtype {a.dtype}")
     return a, code, a.shape[0], a.shape[1]
@@ -136,6 +138,19 @@ def round_bf16_array(a) -> np.ndarray:
 
 def bf16_near_tie(v: float) -> bool:
     return bool(_lib().orc_bf16_near_tie(float(v)))
+
+
+def round_f16(v: float) -> float:
+    """float64 -> nearest IEEE binary16 value (ties to even), as float."""
+    return _lib().orc_round_f16(float(v))
+
+
+def round_f16_array(a) -> np.ndarray:
+    """Elementwise float64 -> nearest binary16 value, as float64."""
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    out = np.empty_like(a)
+    _lib().orc_round_f16_array(_ptr(a), _ptr(out), a.size)
+    return out
 
 
 # ------------------------------------------------------------------- DyT
@@ -233,7 +248,7 @@ def rms_fwd(x, eps, w, mode=PARITY, rows=None):
 
 
 def rms_bwd_rows(x, dy, eps, w, w_dtype_code=F32, mode=PARITY, rows=None):
-    """(dx, dx_scale, dx_allow); w_dtype_code is F32 or BF16."""
+    """(dx, dx_scale, dx_allow); w_dtype_code is F32 or the activation's 16-bit code."""
     x, xt, M, N = _act(x)
     dy, dt, _, _ = _act(dy)
     assert dt == xt and dy.shape == x.shape
@@ -247,7 +262,8 @@ def rms_bwd_rows(x, dy, eps, w, w_dtype_code=F32, mode=PARITY, rows=None):
 
 
 def rms_bwd_cols(x, dy, eps, w_dtype_code, mode=PARITY):
-    """(dw, dw_ss, dw_allow); w_dtype_code is F32 or BF16 (selects the term rounding)."""
+    """(dw, dw_ss, dw_allow); w_dtype_code is F32 or the activation's 16-bit code
+    (selects the term rounding)."""
     x, xt, M, N = _act(x)
     dy, dt, _, _ = _act(dy)
     assert dt == xt and dy.shape == x.shape

@@ -11,8 +11,8 @@
  *
  * Every computation is the textbook definition written out in float64,
  * row by row, with serial sums in index order and no blocking or
- * reordering.  Inputs arrive as raw float32, bfloat16 (raw 16-bit
- * patterns) or float64 arrays and are widened exactly to float64.
+ * reordering.  Inputs arrive as raw float32, bfloat16 or float16 (raw
+ * 16-bit patterns) or float64 arrays and are widened exactly to float64.
  *
  * Two modes:
  *   ORC_MATH   -- pure float64, no intermediate rounding (closed-form,
@@ -39,11 +39,13 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2, ORC_F16 = 3 };
 enum { ORC_MATH = 0, ORC_PARITY = 1 };
 
 /* Largest finite bfloat16: significand 0xFF (8 bits) times 2^(127-7). */
 #define BF16_MAX_FINITE (255.0 * 1329227995784915872903807060280344576.0 /* 2^120 */)
+/* Largest finite IEEE binary16: significand 0x7FF (11 bits) times 2^(15-10). */
+#define F16_MAX_FINITE 65504.0
 
 /* Relative distance to a bfloat16 rounding midpoint below which a value
  * computed in float32 elsewhere may legitimately round the other way. */
@@ -51,10 +53,27 @@ enum { ORC_MATH = 0, ORC_PARITY = 1 };
 
 /* ---------------------------------------------------------------- inputs */
 
+/* IEEE binary16 bit pattern to its exact value: 1 sign bit, 5 exponent
+ * bits (bias 15), 10 fraction bits; exponent 0 holds zero and the
+ * subnormals (fraction * 2^-24), exponent 31 infinity and NaN. */
+static double f16_value(uint16_t h)
+{
+    int e = (h >> 10) & 0x1f, f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f | 0x400), e - 25);
+    return (h & 0x8000) ? -v : v;
+}
+
 static double widen(const void* p, int dt, int64_t i)
 {
     if (dt == ORC_F64) return ((const double*)p)[i];
     if (dt == ORC_F32) return (double)((const float*)p)[i];
+    if (dt == ORC_F16) return f16_value(((const uint16_t*)p)[i]);
     /* bfloat16 is the upper half of a float32 bit pattern. */
     uint32_t u = (uint32_t)((const uint16_t*)p)[i] << 16;
     float f;
@@ -93,26 +112,58 @@ static double round_bf16(double v, int* near_tie)
     return copysign(r, v);
 }
 
-/* Round to the activation dtype: bfloat16 as above, float32 by the C
- * conversion (round to nearest even), float64 unchanged. */
+/*
+ * Round a float64 to the nearest IEEE binary16, ties to even, directly.
+ * binary16 keeps 11 significant bits; a normal value a in [2^(k-1), 2^k)
+ * is a multiple of 2^(k-11), and below the normal range (2^-14) the
+ * spacing stays 2^-24.  Results above the largest finite value (65504,
+ * i.e. inputs from 65520 up) become infinity.  *near_tie as for bfloat16.
+ */
+static double round_f16(double v, int* near_tie)
+{
+    if (near_tie) *near_tie = 0;
+    if (isnan(v) || isinf(v) || v == 0.0) return v;
+    double a = fabs(v);
+    int k;
+    (void)frexp(a, &k);
+    int qe = k - 11;
+    if (qe < -24) qe = -24;
+    double m = ldexp(a, -qe);
+    double mr = nearbyint(m);
+    if (near_tie) {
+        double frac = m - floor(m);
+        if (fabs(frac - 0.5) < NEAR_TIE_REL * m) *near_tie = 1;
+    }
+    double r = ldexp(mr, qe);
+    if (r > F16_MAX_FINITE) r = INFINITY;
+    return copysign(r, v);
+}
+
+/* Round to the activation dtype: bfloat16 and binary16 as above, float32 by
+ * the C conversion (round to nearest even), float64 unchanged. */
 static double round_to(double v, int dt, int* near_tie)
 {
     if (dt == ORC_BF16) return round_bf16(v, near_tie);
+    if (dt == ORC_F16) return round_f16(v, near_tie);
     if (near_tie) *near_tie = 0;
     if (dt == ORC_F32) return (double)(float)v;
     return v;
 }
 
-/* Spacing of bfloat16 at |v|: the gap between the two neighbours that a
- * near-tie rounding of v chooses between. */
-static double bf16_spacing(double v)
+/* Spacing of the activation dtype at |v|: the gap between the two
+ * neighbours that a near-tie rounding of v chooses between (bfloat16: 8
+ * significant bits down to 2^-133; binary16: 11 bits down to 2^-24;
+ * float32: 24 bits down to 2^-149). */
+static double spacing(double v, int dt)
 {
+    int bits = dt == ORC_BF16 ? 8 : dt == ORC_F16 ? 11 : 24;
+    int lo = dt == ORC_BF16 ? -133 : dt == ORC_F16 ? -24 : -149;
     double a = fabs(v);
-    if (a == 0.0 || isnan(a) || isinf(a)) return ldexp(1.0, -133);
+    if (a == 0.0 || isnan(a) || isinf(a)) return ldexp(1.0, lo);
     int k;
     (void)frexp(a, &k);
-    int qe = k - 8;
-    if (qe < -133) qe = -133;
+    int qe = k - bits;
+    if (qe < lo) qe = lo;
     return ldexp(1.0, qe);
 }
 
@@ -127,6 +178,12 @@ int orc_bf16_near_tie(double v)
     int t;
     (void)round_bf16(v, &t);
     return t;
+}
+
+double orc_round_f16(double v) { return round_f16(v, NULL); }
+void orc_round_f16_array(const double* in, double* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = round_f16(in[i], NULL);
 }
 
 static int64_t row_of(const int64_t* rows, int64_t r) { return rows ? rows[r] : r; }
@@ -327,13 +384,13 @@ int orc_ln_bwd_cols(const void* x, const void* dy, int xt, int64_t M, int64_t N,
  * GPU path, not part of the definition.  At width one the input derivative
  * is dn eps / (x^2 + eps)^(3/2) (the PR 8664 page, "Numerics").
  *
- * Near-tie allowances (parity mode, bfloat16 activations): where a value
- * reaches a bfloat16 rounding point within NEAR_TIE_REL of a midpoint, an
+ * Near-tie allowances (parity mode, 16-bit activations): where a value
+ * reaches a bfloat16 or binary16 rounding point within NEAR_TIE_REL of a midpoint, an
  * implementation that computes it in float32 may round it to the other
  * neighbour.  The *_allow outputs give, per output, the largest change such
  * a flip can cause (zero where no rounding is near a tie).  dy*w is exact
- * in float32 when both are bfloat16, so it is only flagged for a float32
- * weight.
+ * in float32 when both are 16-bit (8 or 11 significant bits each), so it
+ * is only flagged for a float32 weight.
  */
 
 static double rms_r(const void* x, int xt, int64_t i, int64_t N, double eps)
@@ -361,7 +418,7 @@ int orc_rms_fwd_rows(const void* x, int xt, int64_t M, int64_t N, double eps,
             if (mode == ORC_PARITY) v = round_to(v, xt, &tie);
             y[r * N + j] = w[j] * v;
             if (y_scale) y_scale[r * N + j] = fabs(w[j] * v);
-            if (y_allow) y_allow[r * N + j] = tie ? fabs(w[j]) * bf16_spacing(v) : 0.0;
+            if (y_allow) y_allow[r * N + j] = tie ? fabs(w[j]) * spacing(v, xt) : 0.0;
         }
     }
     return 0;
@@ -381,7 +438,7 @@ int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int wt, int64_t M, i
             double dn = widen(dy, xt, i * N + j) * w[j];
             int tie = 0;
             if (mode == ORC_PARITY) dn = round_to(dn, xt, &tie);
-            if (tie && wt == ORC_F32) flip += bf16_spacing(dn) * fabs(xh);
+            if (tie && wt == ORC_F32) flip += spacing(dn, xt) * fabs(xh);
             s += dn * xh;
             sa += fabs(dn * xh);
         }
@@ -396,7 +453,7 @@ int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int wt, int64_t M, i
             dx[r * N + j] = rs * (dn - xh * b);
             if (dx_scale) dx_scale[r * N + j] = fabs(rs) * (fabs(dn) + fabs(xh) * ba);
             if (dx_allow) {
-                double own = (tie && wt == ORC_F32) ? bf16_spacing(dn) : 0.0;
+                double own = (tie && wt == ORC_F32) ? spacing(dn, xt) : 0.0;
                 dx_allow[r * N + j] = fabs(rs) * (own + fabs(xh) * flip);
             }
         }
@@ -404,8 +461,9 @@ int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int wt, int64_t M, i
     return 0;
 }
 
-/* wt: dtype of the weight (ORC_F32 or ORC_BF16); it selects whether each
- * dw term is rounded to the activation dtype before the sum. */
+/* wt: dtype of the weight (ORC_F32, or a 16-bit code equal to xt); it
+ * selects whether each dw term is rounded to the activation dtype before
+ * the sum. */
 int orc_rms_bwd_cols(const void* x, const void* dy, int xt, int wt, int64_t M, int64_t N,
                      double eps, int mode, double* dw, double* dw_ss, double* dw_allow)
 {
@@ -426,7 +484,7 @@ int orc_rms_bwd_cols(const void* x, const void* dy, int xt, int wt, int64_t M, i
             dw[j] += term;
             dw_ss[j] += term * term;
             if (dw_allow && tie)
-                dw_allow[j] += fabs(g) * bf16_spacing(n) + (round_term ? bf16_spacing(term) : 0.0);
+                dw_allow[j] += fabs(g) * spacing(n, xt) + (round_term ? spacing(term, xt) : 0.0);
         }
     }
     return 0;

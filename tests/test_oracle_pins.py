@@ -83,6 +83,87 @@ def test_bf16_rounding_matches_brute_force(O):
     assert math.isnan(O.round_bf16(math.nan))
 
 
+# ------------------------------------------------------- binary16 rounding
+
+def _f16_table():
+    """All finite non-negative IEEE binary16 values, ascending, by enumeration
+    of the bit patterns (decoded from the format's definition, not a library)."""
+    vals = []
+    for bits in range(0, 0x7C00):  # 0x7C00 is +inf
+        e, f = bits >> 10, bits & 0x3FF
+        v = math.ldexp(f, -24) if e == 0 else math.ldexp(f | 0x400, e - 25)
+        vals.append((v, bits))
+    return vals
+
+
+def _brute_round_f16(v, table):
+    if v == 0.0:
+        return v
+    fa = Fraction(abs(v))
+    maxv = table[-1][0]
+    if fa >= Fraction(maxv) + (Fraction(2) ** 16 - Fraction(maxv)) / 2:
+        return math.copysign(math.inf, v)
+    lo, hi = 0, len(table) - 1
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if Fraction(table[mid][0]) <= fa:
+            lo = mid
+        else:
+            hi = mid
+    best = min([table[lo], table[hi]], key=lambda c: (abs(Fraction(c[0]) - fa), c[1] & 1))
+    return math.copysign(best[0], v)
+
+
+def test_f16_rounding_matches_brute_force(O):
+    table = _f16_table()
+    assert table[-1][0] == 65504.0 and table[1][0] == 2.0 ** -24
+    rng = np.random.default_rng(11)
+    vals = []
+    for e in range(-27, 17):
+        vals += list(rng.uniform(0.5, 1.0, 6) * 2.0 ** e)
+    # exact midpoints and neighbours: normal, subnormal, binade edges, overflow
+    for bits in list(range(0x3C00, 0x3C10)) + [0x0000, 0x0001, 0x0002, 0x03FF, 0x0400, 0x7BFE]:
+        lo = table[bits][0]
+        hi = table[bits + 1][0]
+        midv = (lo + hi) / 2
+        vals += [midv, math.nextafter(midv, 0), math.nextafter(midv, math.inf)]
+    vals += [65504.0, 65519.99, 65520.0, 65536.0, 1e-9, 2.0 ** -25, 3 * 2.0 ** -26, 1e300]
+    vals += [-v for v in vals[::4]]
+    for v in vals:
+        want = _brute_round_f16(v, table)
+        got = O.round_f16(v)
+        assert got == want or (math.isinf(want) and math.isinf(got) and (got > 0) == (want > 0)), \
+            (v, got, want)
+    assert math.isnan(O.round_f16(math.nan))
+
+
+def test_f16_rounding_matches_numpy(O):
+    """Against a library routine: numpy's float64 -> float16 conversion."""
+    rng = np.random.default_rng(12)
+    v = rng.standard_normal(200000) * np.exp(rng.uniform(-20, 11.5, 200000))
+    with np.errstate(over="ignore"):
+        want = v.astype(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(O.round_f16_array(v), want)
+
+
+def test_f16_inputs_widen_exactly(O):
+    """A binary16 activation array gives the same results as the float64
+    array of the same values (decoding is exact)."""
+    rng = np.random.default_rng(13)
+    xh = (rng.standard_normal((5, 12)) * 3).astype(np.float16)
+    xh[0, 0] = np.float16(2.0 ** -24)  # a subnormal
+    dyh = rng.standard_normal((5, 12)).astype(np.float16)
+    x64, dy64 = xh.astype(np.float64), dyh.astype(np.float64)
+    g, b = rng.standard_normal(12), rng.standard_normal(12)
+    for fn in (lambda x: O.ln_fwd(x, 1e-5, g, b)[0], lambda x: O.dyt_fwd(x, 0.7, g, b)[0],
+               lambda x: O.rms_fwd(x, 1e-6, g, O.MATH)[0]):
+        np.testing.assert_array_equal(fn(xh), fn(x64))
+    ch = O.ln_bwd_cols(xh, dyh, *O.ln_fwd(xh, 1e-5, g, b)[2:4])
+    c64 = O.ln_bwd_cols(x64, dy64, *O.ln_fwd(x64, 1e-5, g, b)[2:4])
+    for k in ch:
+        np.testing.assert_array_equal(ch[k], c64[k])
+
+
 def test_bf16_array_matches_scalar(O):
     v = np.random.default_rng(3).standard_normal(1000) * 10
     a = O.round_bf16_array(v)
@@ -410,6 +491,32 @@ def test_rms_parity_rounding_points(O):
     np.testing.assert_allclose(t_f, 1.75 * y.sum(axis=0), rtol=1e-15)
     np.testing.assert_allclose(t_b, O.round_bf16_array(1.75 * y).sum(axis=0), rtol=1e-15)
     assert not np.array_equal(t_b, t_f)
+
+
+def test_rms_parity_rounding_points_f16(O):
+    """The same rounding points with binary16 activations: n rounds to
+    binary16, and a binary16 weight rounds each dw term."""
+    rng = np.random.default_rng(24)
+    xh = rng.standard_normal((6, 16)).astype(np.float16)
+    eps = 1e-6
+    y, *_ = O.rms_fwd(xh, eps, np.ones(16), O.PARITY)
+    ym, *_ = O.rms_fwd(xh, eps, np.ones(16), O.MATH)
+    np.testing.assert_array_equal(y, O.round_f16_array(ym))
+    assert not np.array_equal(y, ym)
+    # dy = 1.75 has a 3-bit significand; n has 11: each product needs 13 bits
+    three = np.full((6, 16), 1.75, dtype=np.float16)
+    t_h, *_ = O.rms_bwd_cols(xh, three, eps, O.F16, O.PARITY)
+    t_f, *_ = O.rms_bwd_cols(xh, three, eps, O.F32, O.PARITY)
+    np.testing.assert_allclose(t_f, 1.75 * y.sum(axis=0), rtol=1e-15)
+    np.testing.assert_allclose(t_h, O.round_f16_array(1.75 * y).sum(axis=0), rtol=1e-15)
+    assert not np.array_equal(t_h, t_f)
+    # dn = round(dy w) in binary16
+    w = rng.standard_normal(16)
+    dyh = rng.standard_normal((6, 16)).astype(np.float16)
+    dx, *_ = O.rms_bwd_rows(xh, dyh, eps, w, O.F32, O.PARITY)
+    dxm, *_ = O.rms_bwd_rows(xh, dyh, eps, w, O.F32, O.MATH)
+    assert not np.array_equal(dx, dxm)
+    np.testing.assert_allclose(dx, dxm, rtol=0, atol=2.0 ** -8 * np.abs(dxm).max())
 
 
 def test_rms_padding_rows(O):

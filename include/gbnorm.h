@@ -57,15 +57,16 @@
 extern "C" {
 #endif
 
-/* Element types. */
-typedef enum { GBN_F32 = 0, GBN_BF16 = 1 } gbn_dtype;
+/* Element types: float32, bfloat16, IEEE binary16. */
+typedef enum { GBN_F32 = 0, GBN_BF16 = 1, GBN_F16 = 2 } gbn_dtype;
 
 /* Return codes. */
 typedef enum {
     GBN_OK = 0,
     GBN_EINVAL = 1,     /* null required pointer, M < 0, N < 1, N > INT32_MAX, bad eps, a pointer
                            not aligned to its element size, misaligned ws */
-    GBN_EDTYPE = 2,     /* dtype code not in gbn_dtype */
+    GBN_EDTYPE = 2,     /* dtype code not in gbn_dtype, or an RMSNorm dtype pair without
+                           defined rounding (see rmsnorm_fwd) */
     GBN_EWORKSPACE = 3, /* ws_bytes smaller than the call needs */
     GBN_ELAUNCH = 4,    /* a kernel launch failed (cudaGetLastError after the launch) */
     GBN_EDEVICE = 5,    /* the current device could not be queried */
@@ -141,7 +142,9 @@ int layernorm_bwd(const void* x, const void* dy, const float* mean, const float*
  * rmsnorm_bwd: xhat = x r, dn = round_x(dy w),
  *   dx = round_x(r (dn - xhat mean_j(dn xhat))),
  *   dw[j] = sum_i round_x(dy n) when wt == xt, sum_i dy n when wt is f32
- *   (DeepSpeed PR 8645 quoted in PR 8664, "Semantics").  rstd nullable:
+ *   (DeepSpeed PR 8645 quoted in PR 8664, "Semantics").  With 16-bit
+ *   activations (bf16 or f16) the weight is f32 or of the activation dtype;
+ *   any other pair returns GBN_EDTYPE.  rstd nullable:
  *   when null r is recomputed with the forward's exact arithmetic, so the
  *   result is bit-identical either way.  dw nullable.  eps >= 0, finite. */
 int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,

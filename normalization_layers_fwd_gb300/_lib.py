@@ -17,14 +17,14 @@ import torch
 
 from . import build as _build
 
-GBN_F32, GBN_BF16 = 0, 1
+GBN_F32, GBN_BF16, GBN_F16 = 0, 1, 2
 GBN_OP_DYT, GBN_OP_LAYERNORM, GBN_OP_RMSNORM = 0, 1, 2
 GBN_OK = 0
 GBN_ESCRATCH = 6
 GBN_STATIC_WS_BYTES = 8 << 20  # size of the library's static scratch array
 SIZE_MAX = ctypes.c_size_t(-1).value
 
-_DTYPES = {torch.float32: GBN_F32, torch.bfloat16: GBN_BF16}
+_DTYPES = {torch.float32: GBN_F32, torch.bfloat16: GBN_BF16, torch.float16: GBN_F16}
 
 # The entry points the header declares, with their ctypes signatures.
 _P, _I64, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t

@@ -65,7 +65,7 @@ unsigned* fault_ptr()
     return p;
 }
 
-bool dtype_ok(int t) { return t == gbn::kF32 || t == gbn::kBF16; }
+bool dtype_ok(int t) { return t == gbn::kF32 || t == gbn::kBF16 || t == gbn::kF16; }
 int elem_bytes(int t) { return t == gbn::kF32 ? 4 : 2; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -347,10 +347,18 @@ int layernorm_bwd(const void* x, const void* dy, const float* mean, const float*
 }
 
 // ------------------------------------------------------------------ RMSNorm
+// RMSNorm rounds w*n, dy*w and dy*n to the activation dtype; with 16-bit
+// activations the weight is float32 or of the activation dtype (a bf16 x
+// with an f16 weight, or the reverse, has no defined rounding point).
+bool rms_dtypes_ok(int xt, int wt)
+{
+    return dtype_ok(xt) && dtype_ok(wt) && (xt == GBN_F32 || wt == GBN_F32 || wt == xt);
+}
+
 int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
                 float eps, int xt, int wt, cudaStream_t stream)
 {
-    if (!dtype_ok(xt) || !dtype_ok(wt)) return GBN_EDTYPE;
+    if (!rms_dtypes_ok(xt, wt)) return GBN_EDTYPE;
     if (!shape_ok(M, N) || !eps_ok(eps) || !w) return GBN_EINVAL;
     if (M > 0 && (!x || !y)) return GBN_EINVAL;
     if (!all_aligned(xt, {x, y}) || !all_aligned(wt, {w}) || !all_aligned(GBN_F32, {rstd}))
@@ -368,7 +376,7 @@ int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd,
                 void* dw, int64_t M, int64_t N, float eps, int xt, int wt, void* ws,
                 size_t ws_bytes, cudaStream_t stream)
 {
-    if (!dtype_ok(xt) || !dtype_ok(wt)) return GBN_EDTYPE;
+    if (!rms_dtypes_ok(xt, wt)) return GBN_EDTYPE;
     if (!shape_ok(M, N) || !eps_ok(eps) || !w) return GBN_EINVAL;
     if (M > 0 && (!x || !dy || !dx)) return GBN_EINVAL;
     if (!all_aligned(xt, {x, dy, dx}) || !all_aligned(wt, {w, dw}) || !all_aligned(GBN_F32, {rstd}))

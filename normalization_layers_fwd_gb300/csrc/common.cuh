@@ -1,6 +1,6 @@
 // common.cuh -- device helpers shared by the DyT, LayerNorm and RMSNorm kernels.
 //
-// Data movement: every hot kernel streams 16-byte vectors (8 bf16 or 4 f32)
+// Data movement: every hot kernel streams 16-byte vectors (8 bf16 or f16, or 4 f32)
 // with evict-first cache hints (each activation byte is touched once), keeps
 // a row (or a few rows) in registers, and reduces within a "row group" of W
 // threads: warp shuffles when W <= 32, shuffles plus one shared-memory step
@@ -8,12 +8,15 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace gbn {
 
-enum DType : int { kF32 = 0, kBF16 = 1 };
+enum DType : int { kF32 = 0, kBF16 = 1, kF16 = 2 };
 
 // ------------------------------------------------------------------ schedule
 // One row group = W threads, each holding KV 16-byte vectors of a row
@@ -163,6 +166,19 @@ constexpr int kGenWarps = kGenThreads / 32;
 template <typename TX> struct Vec;
 template <> struct Vec<float> { static constexpr int kN = 4; };
 template <> struct Vec<__nv_bfloat16> { static constexpr int kN = 8; };
+template <> struct Vec<__half> { static constexpr int kN = 8; };
+
+// The dtype code of an activation type, and whether it is a 16-bit type.
+template <typename TX>
+constexpr int dtype_code()
+{
+    return std::is_same<TX, float>::value ? kF32 : std::is_same<TX, __half>::value ? kF16 : kBF16;
+}
+template <typename TX>
+constexpr bool is16()
+{
+    return !std::is_same<TX, float>::value;
+}
 
 __device__ __forceinline__ uint4 ld_stream(const void* p)
 {
@@ -190,56 +206,24 @@ __device__ __forceinline__ void st_f32_if(bool p, float* addr, float v)
         "l"(addr), "f"(v));
 }
 
-__device__ __forceinline__ void unpack(const uint4& u, float (&f)[4])
-{
-    f[0] = __uint_as_float(u.x);
-    f[1] = __uint_as_float(u.y);
-    f[2] = __uint_as_float(u.z);
-    f[3] = __uint_as_float(u.w);
-}
-
-// bfloat16 is the upper half of a float32; element 2k sits in the low half
-// of 32-bit word k.
-__device__ __forceinline__ void unpack(const uint4& u, float (&f)[8])
-{
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        f[2 * k] = __uint_as_float(w[k] << 16);
-        f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-    }
-}
-
-__device__ __forceinline__ uint4 pack(const float (&f)[4])
-{
-    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
-                      __float_as_uint(f[3]));
-}
-
-__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi)
-{
-    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
-    uint32_t r;
-    memcpy(&r, &h, sizeof r);
-    return r;
-}
-
-__device__ __forceinline__ uint4 pack(const float (&f)[8])
-{
-    return make_uint4(pack2_bf16(f[0], f[1]), pack2_bf16(f[2], f[3]), pack2_bf16(f[4], f[5]),
-                      pack2_bf16(f[6], f[7]));
-}
-
 // Scalar access (general path).
 __device__ __forceinline__ float ld1(const float* p, int64_t i) { return __ldcs(p + i); }
 __device__ __forceinline__ float ld1(const __nv_bfloat16* p, int64_t i)
 {
     return __bfloat162float(__ldcs(p + i));
 }
+__device__ __forceinline__ float ld1(const __half* p, int64_t i)
+{
+    return __half2float(__ldcs(p + i));
+}
 __device__ __forceinline__ void st1(float* p, int64_t i, float v) { __stcs(p + i, v); }
 __device__ __forceinline__ void st1(__nv_bfloat16* p, int64_t i, float v)
 {
     __stcs(p + i, __float2bfloat16_rn(v));
+}
+__device__ __forceinline__ void st1(__half* p, int64_t i, float v)
+{
+    __stcs(p + i, __float2half_rn(v));
 }
 
 // Round a float32 value to the activation dtype's precision (identity for f32).
@@ -249,20 +233,28 @@ template <> __device__ __forceinline__ float round_x<__nv_bfloat16>(float v)
 {
     return __bfloat162float(__float2bfloat16_rn(v));
 }
+template <> __device__ __forceinline__ float round_x<__half>(float v)
+{
+    return __half2float(__float2half_rn(v));
+}
 
-// Parameters (gamma, beta, alpha, weight) are f32 or bf16 per a runtime code.
+// Parameters (gamma, beta, alpha, weight) are f32, bf16 or f16 per a
+// runtime code.
 __device__ __forceinline__ float ld_param(const void* p, int pt, int64_t j)
 {
     if (pt == kF32) return static_cast<const float*>(p)[j];
-    return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[j]);
+    if (pt == kBF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[j]);
+    return __half2float(static_cast<const __half*>(p)[j]);
 }
 
 __device__ __forceinline__ void st_param(void* p, int pt, int64_t j, float v)
 {
     if (pt == kF32)
         static_cast<float*>(p)[j] = v;
-    else
+    else if (pt == kBF16)
         static_cast<__nv_bfloat16*>(p)[j] = __float2bfloat16_rn(v);
+    else
+        static_cast<__half*>(p)[j] = __float2half_rn(v);
 }
 
 // ---------------------------------------------------- bulk-copy ring (TMA)
@@ -508,34 +500,11 @@ __device__ __forceinline__ uint32_t f2_to_bf2(f2 a)
     return r;
 }
 
-// One 16-byte vector as pairs: 4 pairs of bf16, or 2 pairs of f32.
+// One 16-byte vector as pairs: 4 pairs of bf16 or f16, or 2 pairs of f32.
 template <typename TX> struct Pairs;
 template <> struct Pairs<__nv_bfloat16> { static constexpr int kP = 4; };
+template <> struct Pairs<__half> { static constexpr int kP = 4; };
 template <> struct Pairs<float> { static constexpr int kP = 2; };
-
-__device__ __forceinline__ void unpack2(const uint4& u, f2 (&p)[4])
-{
-    p[0] = bf2_to_f2(u.x);
-    p[1] = bf2_to_f2(u.y);
-    p[2] = bf2_to_f2(u.z);
-    p[3] = bf2_to_f2(u.w);
-}
-__device__ __forceinline__ void unpack2(const uint4& u, f2 (&p)[2])
-{
-    asm("mov.b64 %0, {%1, %2};" : "=l"(p[0].v) : "r"(u.x), "r"(u.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(p[1].v) : "r"(u.z), "r"(u.w));
-}
-__device__ __forceinline__ uint4 pack2(const f2 (&p)[4])
-{
-    return make_uint4(f2_to_bf2(p[0]), f2_to_bf2(p[1]), f2_to_bf2(p[2]), f2_to_bf2(p[3]));
-}
-__device__ __forceinline__ uint4 pack2(const f2 (&p)[2])
-{
-    uint4 u;
-    asm("mov.b64 {%0, %1}, %2;" : "=r"(u.x), "=r"(u.y) : "l"(p[0].v));
-    asm("mov.b64 {%0, %1}, %2;" : "=r"(u.z), "=r"(u.w) : "l"(p[1].v));
-    return u;
-}
 
 // acc + a*b for bf16 a, b (the low or high halves of packed pairs): one
 // instruction, the exact product added with one rounding to float32.
@@ -568,12 +537,114 @@ __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b)
     return r;
 }
 
-// Round both lanes to the activation dtype's precision (identity for f32).
-template <typename TX> __device__ __forceinline__ f2 round2(f2 a);
-template <> __device__ __forceinline__ f2 round2<float>(f2 a) { return a; }
-template <> __device__ __forceinline__ f2 round2<__nv_bfloat16>(f2 a)
+// The same operations for IEEE binary16 pairs: f16 -> f32 is exact, f32 ->
+// f16 rounds to nearest even, and an f16 x f16 product (at most 22
+// significant bits) is exact in float32 before its one rounding.
+__device__ __forceinline__ f2 h2_to_f2(uint32_t w)
 {
-    return bf2_to_f2(f2_to_bf2(a));
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+    return mk2(lo, hi);
+}
+__device__ __forceinline__ uint32_t f2_to_h2(f2 a)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi2(a)), "f"(lo2(a)));
+    return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ float fma_f16_lo(uint32_t a, uint32_t b, float acc)
+{
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+    return acc;
+}
+__device__ __forceinline__ float fma_f16_hi(uint32_t a, uint32_t b, float acc)
+{
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+    return acc;
+}
+
+// Packed-pair operations of a 16-bit activation type.
+template <typename TX> struct P16;
+template <> struct P16<__nv_bfloat16> {
+    static __device__ __forceinline__ f2 to_f2(uint32_t w) { return bf2_to_f2(w); }
+    static __device__ __forceinline__ uint32_t from_f2(f2 a) { return f2_to_bf2(a); }
+    static __device__ __forceinline__ uint32_t mul(uint32_t a, uint32_t b) { return bmul2(a, b); }
+    static __device__ __forceinline__ float fma_lo(uint32_t a, uint32_t b, float c)
+    {
+        return fma_bf16_lo(a, b, c);
+    }
+    static __device__ __forceinline__ float fma_hi(uint32_t a, uint32_t b, float c)
+    {
+        return fma_bf16_hi(a, b, c);
+    }
+};
+template <> struct P16<__half> {
+    static __device__ __forceinline__ f2 to_f2(uint32_t w) { return h2_to_f2(w); }
+    static __device__ __forceinline__ uint32_t from_f2(f2 a) { return f2_to_h2(a); }
+    static __device__ __forceinline__ uint32_t mul(uint32_t a, uint32_t b) { return hmul2(a, b); }
+    static __device__ __forceinline__ float fma_lo(uint32_t a, uint32_t b, float c)
+    {
+        return fma_f16_lo(a, b, c);
+    }
+    static __device__ __forceinline__ float fma_hi(uint32_t a, uint32_t b, float c)
+    {
+        return fma_f16_hi(a, b, c);
+    }
+};
+
+// One 16-byte vector of activations <-> its float32 pairs.
+template <typename TX>
+__device__ __forceinline__ void unpack2(const uint4& u, f2 (&p)[Pairs<TX>::kP])
+{
+    if constexpr (is16<TX>()) {
+        p[0] = P16<TX>::to_f2(u.x);
+        p[1] = P16<TX>::to_f2(u.y);
+        p[2] = P16<TX>::to_f2(u.z);
+        p[3] = P16<TX>::to_f2(u.w);
+    } else {
+        asm("mov.b64 %0, {%1, %2};" : "=l"(p[0].v) : "r"(u.x), "r"(u.y));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(p[1].v) : "r"(u.z), "r"(u.w));
+    }
+}
+template <typename TX>
+__device__ __forceinline__ uint4 pack2(const f2 (&p)[Pairs<TX>::kP])
+{
+    if constexpr (is16<TX>()) {
+        return make_uint4(P16<TX>::from_f2(p[0]), P16<TX>::from_f2(p[1]), P16<TX>::from_f2(p[2]),
+                          P16<TX>::from_f2(p[3]));
+    } else {
+        uint4 u;
+        asm("mov.b64 {%0, %1}, %2;" : "=r"(u.x), "=r"(u.y) : "l"(p[0].v));
+        asm("mov.b64 {%0, %1}, %2;" : "=r"(u.z), "=r"(u.w) : "l"(p[1].v));
+        return u;
+    }
+}
+
+// Round both lanes to the activation dtype's precision (identity for f32).
+template <typename TX>
+__device__ __forceinline__ f2 round2(f2 a)
+{
+    if constexpr (is16<TX>())
+        return P16<TX>::to_f2(P16<TX>::from_f2(a));
+    else
+        return a;
 }
 
 // Parameters of columns c, c+1 as a pair.

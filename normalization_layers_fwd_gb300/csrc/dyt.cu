@@ -166,11 +166,11 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
             for (int j = 0; j < KV; ++j) {
                 const bool ok = okr && colok[j];
                 f2 v[P];
-                unpack2(lds128_if(ok, xs + u * srow + j * W * 16), v);
+                unpack2<TX>(lds128_if(ok, xs + u * srow + j * W * 16), v);
 #pragma unroll
                 for (int p = 0; p < P; ++p)
                     v[p] = fma2(gm[j][p], dyt_tanh2(mul2(a2, v[p])), bt[j][p]);
-                st_stream_if(ok, yb + u * grow + j * W * VEC, pack2(v));
+                st_stream_if(ok, yb + u * grow + j * W * VEC, pack2<TX>(v));
             }
         }
         row0 += rstride;
@@ -231,8 +231,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
             for (int j = 0; j < KV; ++j) {
                 const bool ok = alive && colok[j] && okr;
                 f2 xv[P], dv[P], o[P];
-                unpack2(lds128_if(ok, xs + u * srow + j * W * 16), xv);
-                unpack2(lds128_if(ok, ds + u * srow + j * W * 16), dv);
+                unpack2<TX>(lds128_if(ok, xs + u * srow + j * W * 16), xv);
+                unpack2<TX>(lds128_if(ok, ds + u * srow + j * W * 16), dv);
 #pragma unroll
                 for (int p = 0; p < P; ++p) {
                     f2 t, s;
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
                         acc_a[j][p] = fma2(dsd, xv[p], acc_a[j][p]);
                     }
                 }
-                st_stream_if(ok, dxb + u * grow + j * W * VEC, pack2(o));
+                st_stream_if(ok, dxb + u * grow + j * W * VEC, pack2<TX>(o));
             }
         }
     };
@@ -426,6 +426,7 @@ cudaError_t launch_dyt_fwd(const Launch& L, int xt, int pt, const void* x, const
                            const void* gamma, const void* beta, void* y, int64_t M, int N)
 {
     if (xt == kF32) return fwd_dispatch<float>(L, pt, x, alpha, gamma, beta, y, M, N);
+    if (xt == kF16) return fwd_dispatch<__half>(L, pt, x, alpha, gamma, beta, y, M, N);
     return fwd_dispatch<__nv_bfloat16>(L, pt, x, alpha, gamma, beta, y, M, N);
 }
 
@@ -434,6 +435,7 @@ cudaError_t launch_dyt_bwd(const Launch& L, int xt, int pt, const void* x, const
                            int N)
 {
     if (xt == kF32) return bwd_dispatch<float>(L, pt, x, dy, alpha, gamma, dx, ws, M, N);
+    if (xt == kF16) return bwd_dispatch<__half>(L, pt, x, dy, alpha, gamma, dx, ws, M, N);
     return bwd_dispatch<__nv_bfloat16>(L, pt, x, dy, alpha, gamma, dx, ws, M, N);
 }
 

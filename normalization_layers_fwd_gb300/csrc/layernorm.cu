@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
             s[u] = 0.f;
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
-                unpack2(lds128_if(okr[u] && colok[j], xs + u * srow + j * W * 16), xv[u][j]);
+                unpack2<TX>(lds128_if(okr[u] && colok[j], xs + u * srow + j * W * 16), xv[u][j]);
                 f2 a2 = xv[u][j][0];
 #pragma unroll
                 for (int p = 1; p < P; ++p) a2 = add2(a2, xv[u][j][p]);
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
                 f2 o[P];
 #pragma unroll
                 for (int p = 0; p < P; ++p) o[p] = fma2(mul2(xv[u][j][p], r2), gm[j][p], bt[j][p]);
-                st_stream_if(okr[u] && colok[j], yb + u * grow + j * W * VEC, pack2(o));
+                st_stream_if(okr[u] && colok[j], yb + u * grow + j * W * VEC, pack2<TX>(o));
             }
             if (mean) st_f32_if(lead && okr[u], mean + (row0 + u * G), mu[u]);
             if (rstd) st_f32_if(lead && okr[u], rstd + (row0 + u * G), rs);
@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
             for (int j = 0; j < KV; ++j) {
                 const bool ok = alive && colok[j] && okr[u];
                 f2 xv[P], dv[P];
-                unpack2(lds128_if(ok, xs + u * srow + j * W * 16), xv);
-                unpack2(lds128_if(ok, ds + u * srow + j * W * 16), dv);
+                unpack2<TX>(lds128_if(ok, xs + u * srow + j * W * 16), xv);
+                unpack2<TX>(lds128_if(ok, ds + u * srow + j * W * 16), dv);
 #pragma unroll
                 for (int p = 0; p < P; ++p) {
                     const f2 xhv = mul2(sub2(xv[p], m2), r2);
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
 #pragma unroll
                 for (int p = 0; p < P; ++p)
                     o[p] = mul2(r2, fma2(xh[u][j][p], nmb, sub2(gg[u][j][p], ma)));
-                st_stream_if(ok, dxb + u * grow + j * W * VEC, pack2(o));
+                st_stream_if(ok, dxb + u * grow + j * W * VEC, pack2<TX>(o));
             }
         }
     };
@@ -422,6 +422,7 @@ cudaError_t launch_ln_fwd(const Launch& L, int xt, int pt, const void* x, const 
                           float eps)
 {
     if (xt == kF32) return fwd_dispatch<float>(L, pt, x, gamma, beta, y, mean, rstd, M, N, eps);
+    if (xt == kF16) return fwd_dispatch<__half>(L, pt, x, gamma, beta, y, mean, rstd, M, N, eps);
     return fwd_dispatch<__nv_bfloat16>(L, pt, x, gamma, beta, y, mean, rstd, M, N, eps);
 }
 
@@ -430,6 +431,7 @@ cudaError_t launch_ln_bwd(const Launch& L, int xt, int pt, const void* x, const 
                           float* ws, int64_t M, int N)
 {
     if (xt == kF32) return bwd_dispatch<float>(L, pt, x, dy, mean, rstd, gamma, dx, ws, M, N);
+    if (xt == kF16) return bwd_dispatch<__half>(L, pt, x, dy, mean, rstd, gamma, dx, ws, M, N);
     return bwd_dispatch<__nv_bfloat16>(L, pt, x, dy, mean, rstd, gamma, dx, ws, M, N);
 }
 

@@ -44,15 +44,11 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int p)
     return p == 0 ? v.x : p == 1 ? v.y : p == 2 ? v.z : v.w;
 }
 
-// With bf16 activations and a bf16 weight, the products w*n (forward), dy*w
-// and dy*n (backward) are products of two bf16 values, exact in float32 and
-// rounded once to bf16 by the rounding points above; mul.rn.bf16x2 computes
-// exactly that on a packed pair.  Other dtype pairs take float32 pairs.
-template <typename TX>
-__device__ __forceinline__ constexpr bool is_bf16()
-{
-    return std::is_same<TX, __nv_bfloat16>::value;
-}
+// With 16-bit activations and a weight of the same type, the products w*n
+// (forward), dy*w and dy*n (backward) are products of two 16-bit values,
+// exact in float32 and rounded once to the activation type by the rounding
+// points above; mul.rn.bf16x2 / mul.rn.f16x2 compute exactly that on a
+// packed pair.  Other dtype pairs take float32 pairs.
 
 // ------------------------------------------------------------ fast forward
 template <typename TX, int S>
@@ -74,17 +70,17 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
     for (int j = 0; j < KV; ++j) colok[j] = in_group<W>() && l + j * W < N / VEC;
     const int rb = N * (int)sizeof(TX);
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
-    const bool wbf = is_bf16<TX>() && pt == kBF16;
+    const bool w16 = is16<TX>() && pt == dtype_code<TX>();
 
     f2 wf[KV][P];
-    uint32_t wpk[KV][P];  // the bf16 weight pair, packed (used when wbf)
+    uint32_t wpk[KV][P];  // the 16-bit weight pair, packed (used when w16)
 #pragma unroll
     for (int j = 0; j < KV; ++j) {
 #pragma unroll
         for (int p = 0; p < P; ++p) {
             const int c = (l + j * W) * VEC + 2 * p;
             wf[j][p] = colok[j] ? ld_param2(w, pt, c) : splat2(0.f);
-            wpk[j][p] = (wbf && colok[j]) ? static_cast<const uint32_t*>(w)[c / 2] : 0u;
+            wpk[j][p] = (w16 && colok[j]) ? static_cast<const uint32_t*>(w)[c / 2] : 0u;
         }
     }
 
@@ -113,7 +109,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
             s[u] = 0.f;
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
-                unpack2(lds128_if(okr[u] && colok[j], xs + u * srow + j * W * 16), xv[u][j]);
+                unpack2<TX>(lds128_if(okr[u] && colok[j], xs + u * srow + j * W * 16), xv[u][j]);
                 s[u] += vec_sumsq2<P>(xv[u][j]);
             }
         }
@@ -125,20 +121,21 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
                 uint4 out;
-                if constexpr (is_bf16<TX>()) {
+                if constexpr (is16<TX>()) {
                     uint32_t o[4];
 #pragma unroll
                     for (int p = 0; p < P; ++p) {
-                        const uint32_t npk = f2_to_bf2(mul2(xv[u][j][p], r2));  // n = round_x(x r)
-                        o[p] = wbf ? bmul2(wpk[j][p], npk)
-                                   : f2_to_bf2(mul2(wf[j][p], bf2_to_f2(npk)));
+                        // n = round_x(x r)
+                        const uint32_t npk = P16<TX>::from_f2(mul2(xv[u][j][p], r2));
+                        o[p] = w16 ? P16<TX>::mul(wpk[j][p], npk)
+                                   : P16<TX>::from_f2(mul2(wf[j][p], P16<TX>::to_f2(npk)));
                     }
                     out = make_uint4(o[0], o[1], o[2], o[3]);
                 } else {
                     f2 o[P];
 #pragma unroll
                     for (int p = 0; p < P; ++p) o[p] = mul2(wf[j][p], mul2(xv[u][j][p], r2));
-                    out = pack2(o);
+                    out = pack2<TX>(o);
                 }
                 st_stream_if(okr[u] && colok[j], yb + u * grow + j * W * VEC, out);
             }
@@ -177,7 +174,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
     // a weight in x's dtype: each dy*n is rounded to x's dtype (bf16 pairs
     // then multiply in bf16); a float32 weight keeps the float32 product
-    const bool wbf = is_bf16<TX>() && pt == kBF16;
+    const bool w16 = is16<TX>() && pt == dtype_code<TX>();
 
     f2 wf[KV][P], acc[KV][P];
     uint32_t wpk[KV][P];
@@ -187,7 +184,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
         for (int p = 0; p < P; ++p) {
             const int c = (l + j * W) * VEC + 2 * p;
             wf[j][p] = colok[j] ? ld_param2(w, pt, c) : splat2(0.f);
-            wpk[j][p] = (wbf && colok[j]) ? static_cast<const uint32_t*>(w)[c / 2] : 0u;
+            wpk[j][p] = (w16 && colok[j]) ? static_cast<const uint32_t*>(w)[c / 2] : 0u;
             acc[j][p] = splat2(0.f);
         }
     }
@@ -217,7 +214,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
             okr[u] = !kMask || row0 + u * G < M;
 #pragma unroll
             for (int j = 0; j < KV; ++j)  // x, scaled by r below
-                unpack2(lds128_if(alive && okr[u] && colok[j], xs + u * srow + j * W * 16),
+                unpack2<TX>(lds128_if(alive && okr[u] && colok[j], xs + u * srow + j * W * 16),
                         xh[u][j]);
             rs[u] = rs_n[u];
         }
@@ -242,21 +239,21 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
             for (int j = 0; j < KV; ++j) {
                 const uint4 dr = lds128_if(alive && okr[u] && colok[j], ds + u * srow + j * W * 16);
                 f2 dv[P];
-                unpack2(dr, dv);
+                unpack2<TX>(dr, dv);
 #pragma unroll
                 for (int p = 0; p < P; ++p) {
                     xh[u][j][p] = mul2(xh[u][j][p], r2);
                     f2 nxt;  // the accumulator with this row's dw term added
-                    if constexpr (is_bf16<TX>()) {
-                        const uint32_t npk = f2_to_bf2(xh[u][j][p]);  // n = round_x(xhat)
-                        if (wbf) {
-                            dn[u][j][p] = bf2_to_f2(bmul2(word(dr, p), wpk[j][p]));
-                            nxt = add2(acc[j][p], bf2_to_f2(bmul2(word(dr, p), npk)));
+                    if constexpr (is16<TX>()) {
+                        const uint32_t npk = P16<TX>::from_f2(xh[u][j][p]);  // n = round_x(xhat)
+                        if (w16) {
+                            dn[u][j][p] = P16<TX>::to_f2(P16<TX>::mul(word(dr, p), wpk[j][p]));
+                            nxt = add2(acc[j][p], P16<TX>::to_f2(P16<TX>::mul(word(dr, p), npk)));
                         } else {
-                            // float32 weight: dy*n unrounded, exact product of two bf16
+                            // float32 weight: dy*n unrounded, exact product of two 16-bit values
                             dn[u][j][p] = round2<TX>(mul2(dv[p], wf[j][p]));
-                            nxt = mk2(fma_bf16_lo(word(dr, p), npk, lo2(acc[j][p])),
-                                      fma_bf16_hi(word(dr, p), npk, hi2(acc[j][p])));
+                            nxt = mk2(P16<TX>::fma_lo(word(dr, p), npk, lo2(acc[j][p])),
+                                      P16<TX>::fma_hi(word(dr, p), npk, hi2(acc[j][p])));
                         }
                     } else {
                         dn[u][j][p] = mul2(dv[p], wf[j][p]);
@@ -278,7 +275,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
                 f2 o[P];
 #pragma unroll
                 for (int p = 0; p < P; ++p) o[p] = mul2(r2, fma2(xh[u][j][p], nm, dn[u][j][p]));
-                st_stream_if(alive && okr[u] && colok[j], dxb + u * grow + j * W * VEC, pack2(o));
+                st_stream_if(alive && okr[u] && colok[j], dxb + u * grow + j * W * VEC, pack2<TX>(o));
             }
         }
     };
@@ -446,6 +443,7 @@ cudaError_t launch_rms_fwd(const Launch& L, int xt, int pt, const void* x, const
                            float* rstd, int64_t M, int N, float eps)
 {
     if (xt == kF32) return fwd_dispatch<float>(L, pt, x, w, y, rstd, M, N, eps);
+    if (xt == kF16) return fwd_dispatch<__half>(L, pt, x, w, y, rstd, M, N, eps);
     return fwd_dispatch<__nv_bfloat16>(L, pt, x, w, y, rstd, M, N, eps);
 }
 
@@ -454,6 +452,7 @@ cudaError_t launch_rms_bwd(const Launch& L, int xt, int pt, const void* x, const
                            int N, float eps)
 {
     if (xt == kF32) return bwd_dispatch<float>(L, pt, x, dy, w, rstd, dx, ws, M, N, eps);
+    if (xt == kF16) return bwd_dispatch<__half>(L, pt, x, dy, w, rstd, dx, ws, M, N, eps);
     return bwd_dispatch<__nv_bfloat16>(L, pt, x, dy, w, rstd, dx, ws, M, N, eps);
 }
 

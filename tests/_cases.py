@@ -23,7 +23,7 @@ def _sel(t, rows):
 
 
 def _pcode(t):
-    return oracle.BF16 if t.dtype == torch.bfloat16 else oracle.F32
+    return {torch.bfloat16: oracle.BF16, torch.float16: oracle.F16}.get(t.dtype, oracle.F32)
 
 
 def dyt_case(x, dy, alpha, gamma, beta, rows=None, cols=True):
@@ -83,10 +83,10 @@ def rmsnorm_case(x, dy, w, eps, rows=None, cols=True):
     dx2, dw2 = _lib.rmsnorm_bwd(x, dy, w, None, eps)
     torch.cuda.synchronize()
     # the saved rstd is a cache: recomputing it must give identical bits
-    assert torch.equal(dx.view(torch.int16) if dx.dtype == torch.bfloat16 else dx.view(torch.int32),
-                       dx2.view(torch.int16) if dx2.dtype == torch.bfloat16 else dx2.view(torch.int32))
-    assert torch.equal(dw.view(torch.int16) if dw.dtype == torch.bfloat16 else dw.view(torch.int32),
-                       dw2.view(torch.int16) if dw2.dtype == torch.bfloat16 else dw2.view(torch.int32))
+    def bits(t):
+        return t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)
+    assert torch.equal(bits(dx), bits(dx2))
+    assert torch.equal(bits(dw), bits(dw2))
     xo, dyo = to_oracle(x), to_oracle(dy)
     w64 = f64(w)
     yo, ys, rso, yal = oracle.rms_fwd(xo, eps, w64, oracle.PARITY, rows)

@@ -2,7 +2,8 @@
 
 Tolerances (each rule names the arithmetic it comes from):
 
-* bfloat16 outputs must lie within 1 bfloat16 ULP of bf16(o), o being the
+* bfloat16 (and IEEE binary16) outputs must lie within 1 ULP of the
+  nearest bf16 (f16) value to o, o being the
   oracle's float64 value before the final rounding.  The ULP distance is
   taken from ordered bit patterns, as the fused-RMSNorm page measures it
   (DeepSpeed PR 8645 quoted in PR 8664, "Correctness evidence (1)").
@@ -43,7 +44,7 @@ def to_oracle(t: torch.Tensor) -> np.ndarray:
     t = t.detach().cpu().contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16).reshape(t.shape)
-    if t.dtype == torch.float32:
+    if t.dtype in (torch.float32, torch.float16):
         return t.numpy()
     raise TypeError(t.dtype)
 
@@ -57,9 +58,13 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def bits_of_f64(v: np.ndarray) -> np.ndarray:
-    """Bit patterns of float64 values that are exactly bfloat16-representable."""
-    return (np.asarray(v, dtype=np.float64).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+def bits_of_f64(v: np.ndarray, fmt: str = "bf16") -> np.ndarray:
+    """Bit patterns of float64 values exactly representable in fmt (bf16/f16)."""
+    v = np.asarray(v, dtype=np.float64)
+    if fmt == "f16":
+        with np.errstate(over="ignore"):
+            return v.astype(np.float16).view(np.uint16)
+    return (v.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
 
 
 def ordered(bits: np.ndarray) -> np.ndarray:
@@ -71,13 +76,22 @@ def ulp_distance_bf16(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
     return np.abs(ordered(a_bits) - ordered(b_bits))
 
 
-def bf16_ulp(v: np.ndarray) -> np.ndarray:
-    """Spacing of bfloat16 at |v| (v bfloat16-representable)."""
+def bf16_ulp(v: np.ndarray, fmt: str = "bf16") -> np.ndarray:
+    """Spacing of fmt at |v| (v representable): bfloat16 keeps 8 significant
+    bits down to 2^-126, binary16 11 bits down to 2^-14."""
+    bits, emin = (11, -14.0) if fmt == "f16" else (8, -126.0)
     a = np.abs(np.asarray(v, dtype=np.float64))
     with np.errstate(divide="ignore"):
         e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    e = np.maximum(e, -126.0)
-    return np.where(np.isfinite(a), 2.0 ** (e - 7), np.inf)
+    e = np.maximum(e, emin)
+    return np.where(np.isfinite(a), 2.0 ** (e - (bits - 1)), np.inf)
+
+
+_ROUND = {"bf16": lambda v: oracle.round_bf16_array(v), "f16": lambda v: oracle.round_f16_array(v)}
+
+
+def fmt_of(t: torch.Tensor):
+    return {torch.bfloat16: "bf16", torch.float16: "f16"}.get(t.dtype)
 
 
 # ------------------------------------------------------------------ checks
@@ -102,16 +116,18 @@ def check_nan(name, g, o):
 
 
 def check_bf16(name, g_t: torch.Tensor, o, scale, allow=None) -> Report:
-    """bfloat16 output vs oracle value o (float64, before rounding).
+    """16-bit (bfloat16 or binary16) output vs oracle value o (float64,
+    before rounding).
 
     The cap on counted exceptions does not apply at width one, where the
     input gradient is (nearly) all cancellation: DeepSpeed PR 8664 notes
     that a width-one norm's computed input gradient is rounding noise."""
+    fmt = fmt_of(g_t)
     gb = bf16_bits(g_t).reshape(o.shape)
     g = f64(g_t).reshape(o.shape)
     nan = check_nan(name, g, o)
-    ref = oracle.round_bf16_array(np.where(nan, 0.0, o))
-    rb = bits_of_f64(ref)
+    ref = _ROUND[fmt](np.where(nan, 0.0, o))
+    rb = bits_of_f64(ref, fmt)
     d = ulp_distance_bf16(gb, rb)
     d = np.where(nan, 0, d)
     both_inf = np.isinf(g) & np.isinf(ref) & (np.sign(g) == np.sign(ref))
@@ -120,7 +136,7 @@ def check_bf16(name, g_t: torch.Tensor, o, scale, allow=None) -> Report:
         err = np.abs(g - o)
     ok1 = d <= 1
     okc = err <= np.maximum(CANCEL_REL * scale, TINY)
-    oka = np.zeros_like(ok1) if allow is None else ((allow > 0) & (err <= allow + bf16_ulp(ref)))
+    oka = np.zeros_like(ok1) if allow is None else ((allow > 0) & (err <= allow + bf16_ulp(ref, fmt)))
     bad = ~(ok1 | okc | oka | nan)
     if bad.any():
         _fail(name, bad, g, o, f"(max ulp {int(d[bad].max())})")
@@ -162,9 +178,10 @@ def check_reduced(name, g_t: torch.Tensor, o, ss, allow=None) -> Report:
     if allow is not None:
         tol = tol + np.asarray(allow, dtype=np.float64).reshape(-1)
     ok = err <= tol
-    if g_t.dtype == torch.bfloat16:
-        ref = oracle.round_bf16_array(np.where(nan, 0.0, o))
-        d = ulp_distance_bf16(bf16_bits(g_t).reshape(-1), bits_of_f64(ref))
+    fmt = fmt_of(g_t)
+    if fmt:
+        ref = _ROUND[fmt](np.where(nan, 0.0, o))
+        d = ulp_distance_bf16(bf16_bits(g_t).reshape(-1), bits_of_f64(ref, fmt))
         ok = ok | (d <= 1)
     bad = ~ok & ~nan
     if bad.any():
@@ -175,6 +192,6 @@ def check_reduced(name, g_t: torch.Tensor, o, ss, allow=None) -> Report:
 
 
 def check_out(name, g_t, o, scale, allow=None):
-    if g_t.dtype == torch.bfloat16:
+    if fmt_of(g_t):
         return check_bf16(name, g_t, o, scale, allow)
     return check_f32(name, g_t, o, scale, allow)

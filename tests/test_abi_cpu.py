@@ -60,6 +60,9 @@ def test_invalid_arguments_are_rejected_before_any_device_use(lib):
     # bad dtype codes
     assert lib.dyt_fwd(p, p, p, p, p, 4, 8, 7, 0, None) == GBN_EDTYPE
     assert lib.rmsnorm_fwd(p, p, p, None, 4, 8, 1e-6, 1, 9, None) == GBN_EDTYPE
+    # RMSNorm with a 16-bit weight of the other 16-bit type has no rounding point
+    assert lib.rmsnorm_fwd(p, p, p, None, 4, 8, 1e-6, 1, 2, None) == GBN_EDTYPE
+    assert lib.rmsnorm_bwd(p, p, p, None, p, p, 4, 8, 1e-6, 2, 1, None, 0, None) == GBN_EDTYPE
     # bad shapes
     assert lib.dyt_fwd(p, p, p, p, p, -1, 8, 1, 0, None) == GBN_EINVAL
     assert lib.dyt_fwd(p, p, p, p, p, 4, 0, 1, 0, None) == GBN_EINVAL
@@ -91,6 +94,20 @@ def test_empty_forward_is_a_noop_without_device(lib):
     assert lib.dyt_fwd(None, p, p, p, None, 0, 8, 1, 0, None) == GBN_OK
     assert lib.layernorm_fwd(None, None, None, None, None, None, 0, 8, 1e-5, 1, 0, None) == GBN_OK
     assert lib.rmsnorm_fwd(None, p, None, None, 0, 8, 1e-6, 1, 1, None) == GBN_OK
+
+
+def test_f16_codes_are_accepted(lib):
+    """binary16 (code 2) passes the dtype checks: without a device the call
+    gets as far as the device query."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    size_max = ctypes.c_size_t(-1).value
+    p = ctypes.c_void_p(16)
+    for xt, pt in ((2, 2), (2, 0), (0, 2)):
+        assert lib.dyt_fwd(p, p, p, p, p, 4, 8, xt, pt, None) == GBN_EDEVICE
+        assert lib.rmsnorm_fwd(p, p, p, None, 4, 8, 1e-6, xt, pt, None) == GBN_EDEVICE
+    assert lib.gbn_bwd_workspace_bytes(2, 10, 10, 2, 2, 0) == size_max  # no device here
 
 
 def test_valid_call_without_a_device_reports_edevice(lib):

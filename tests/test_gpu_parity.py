@@ -50,11 +50,14 @@ def _run(op, inp, eps=1e-5, rows=None):
 BF16_WIDTHS = [1, 5, 8, 16, 24, 40, 64, 128, 129, 136, 256, 264, 512, 520, 1000, 1024, 2048,
                3072, 4096, 6000, 8192, 8200]
 F32_WIDTHS = [1, 3, 4, 12, 64, 100, 256, 1024, 2048, 3000, 4096, 4100]
+F16_WIDTHS = [1, 8, 16, 24, 40, 64, 128, 264, 1000, 2048, 3072, 4096, 6000, 8192, 8200]
 DTYPES = [(torch.bfloat16, torch.float32), (torch.bfloat16, torch.bfloat16),
-          (torch.float32, torch.float32), (torch.float32, torch.bfloat16)]
+          (torch.float32, torch.float32), (torch.float32, torch.bfloat16),
+          (torch.float16, torch.float32), (torch.float16, torch.float16)]
+WIDTHS = {torch.bfloat16: BF16_WIDTHS, torch.float32: F32_WIDTHS, torch.float16: F16_WIDTHS}
 CASES = []
 for xdt, pdt in DTYPES:
-    for N in (BF16_WIDTHS if xdt == torch.bfloat16 else F32_WIDTHS):
+    for N in WIDTHS[xdt]:
         if pdt != torch.float32 and N not in (24, 128, 2048, 3072, 8192):
             continue
         for op in ("dyt", "layernorm", "rmsnorm"):

@@ -1,7 +1,7 @@
 """Benchmark of the row-normalization hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload sweep|dyt_f32_4096x64|layernorm_bwd_401408x24|
+                    [--workload sweep|sweep_f16|dyt_f32_4096x64|layernorm_bwd_401408x24|
                                 dyt_bf16_1048576x128|rmsnorm_bf16_16384x2048]
 
 A step is one pass of the whole hot path over one batch of synthetic input:
@@ -238,10 +238,11 @@ class Point:
 
 def workloads(name, ops=None, widths=None):
     from normalization_layers_fwd_gb300 import synth
-    if name == "sweep":
-        pts = [w for w in synth.sweep_all()
+    if name in ("sweep", "sweep_f16"):
+        xd = torch.bfloat16 if name == "sweep" else torch.float16
+        pts = [w for w in synth.sweep_all(xd)
                if (not ops or w.op in ops) and (not widths or w.N in widths)]
-        return pts, ("sweep: DyT, LayerNorm, RMSNorm fwd+bwd, bf16 x, fp32 params, "
+        return pts, (f"{name}: DyT, LayerNorm, RMSNorm fwd+bwd, {str(xd)[6:]} x, fp32 params, "
                      "N in {16..8192}, M = 2^28 // N")
     table = {w.name: w for w in (synth.DYT_F32_SMALL, synth.LN_BWD_TALL, synth.DYT_BF16_TALL,
                                  synth.RMS_BF16)}
@@ -421,8 +422,9 @@ def run_ours(args, rank, world, dev):
     line = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
-        if dtype == torch.bfloat16 else "f32", "data": "synthetic (seeded, generated on the GPU)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {torch.bfloat16: "bf16", torch.float16: "f16"}.get(dtype, "f32"),
+        "data": "synthetic (seeded, generated on the GPU)",
         "config": {"workload": wdesc, "points": len(points), "rows_per_step": rows,
                    "x_dtype": str(dtype)[6:], "param_dtype": str(wls[0].pdtype)[6:],
                    "l2": "inputs larger than L2" if big else "L2 flushed (512 MiB write) before every step",
@@ -508,7 +510,7 @@ def oracle_sample(wls, target_elems):
         def arr(t):
             if t.dtype == torch.bfloat16:
                 return t.contiguous().view(torch.int16).numpy().view(np.uint16)
-            return t.contiguous().numpy()
+            return t.contiguous().numpy()  # float32 and float16 directly
         x, dy = arr(inp["x"]), arr(inp["dy"])
         t0 = time.perf_counter()
         if w.op == "dyt":
@@ -524,7 +526,8 @@ def oracle_sample(wls, target_elems):
             oracle.ln_bwd_cols(x, dy, mu, rs)
         else:
             wt = inp["weight"].double().numpy()
-            code = oracle.BF16 if inp["weight"].dtype == torch.bfloat16 else oracle.F32
+            code = {torch.bfloat16: oracle.BF16, torch.float16: oracle.F16}.get(
+                inp["weight"].dtype, oracle.F32)
             oracle.rms_fwd(x, w.eps, wt)
             oracle.rms_bwd_rows(x, dy, w.eps, wt, code)
             oracle.rms_bwd_cols(x, dy, w.eps, code)

@@ -108,8 +108,9 @@ RMS_BF16 = Workload("rmsnorm_bf16_16384x2048", 4, "rmsnorm", 16384, 2048, torch.
                     param_dist={"weight": (1.0, 0.05)})
 
 
-def sweep(op: str, N: int) -> Workload:
-    """Workload 5: bf16 activations, fp32 parameters ~ N(1, 0.1), M = 2^28 // N."""
+def sweep(op: str, N: int, xdtype: torch.dtype = torch.bfloat16) -> Workload:
+    """Workload 5: bf16 activations (or xdtype), fp32 parameters ~ N(1, 0.1),
+    M = 2^28 // N."""
     M = SWEEP_ELEMS // N
     if op == "dyt":
         params = {"alpha": (1.0, 0.1), "gamma": (1.0, 0.1), "beta": (1.0, 0.1)}
@@ -120,12 +121,13 @@ def sweep(op: str, N: int) -> Workload:
     else:
         params = {"weight": (1.0, 0.1)}
         eps = 1e-6
-    return Workload(f"sweep_{op}_{M}x{N}", 5, op, M, N, torch.bfloat16, torch.float32, eps=eps,
+    tag = "" if xdtype == torch.bfloat16 else "_" + str(xdtype)[6:]
+    return Workload(f"sweep{tag}_{op}_{M}x{N}", 5, op, M, N, xdtype, torch.float32, eps=eps,
                     param_dist=params)
 
 
-def sweep_all():
-    return [sweep(op, n) for n in SWEEP_WIDTHS for op in ("dyt", "layernorm", "rmsnorm")]
+def sweep_all(xdtype: torch.dtype = torch.bfloat16):
+    return [sweep(op, n, xdtype) for n in SWEEP_WIDTHS for op in ("dyt", "layernorm", "rmsnorm")]
 
 
 def scaled(w: Workload, M: int) -> Workload:

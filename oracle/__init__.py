@@ -25,6 +25,9 @@ import numpy as np
 
 F32, BF16, F64, F16 = 0, 1, 2, 3
 MATH, PARITY = 0, 1
+# RMSNorm expression variants: weight after the cast (Llama), weight before
+# the cast, and Gemma's (1 + weight) before the cast.
+RMS_CAST_FIRST, RMS_WEIGHT_FIRST, RMS_GEMMA = 0, 1, 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
@@ -71,9 +74,9 @@ def _lib():
             "orc_ln_fwd_rows": ([P, I, I64, I64, D, P, P, P, I64, P, P, P, P], I),
             "orc_ln_bwd_rows": ([P, P, I, I64, I64, P, P, P, P, I64, P, P], I),
             "orc_ln_bwd_cols": ([P, P, I, I64, I64, P, P, P, P, P, P], I),
-            "orc_rms_fwd_rows": ([P, I, I64, I64, D, P, I, P, I64, P, P, P, P], I),
-            "orc_rms_bwd_rows": ([P, P, I, I, I64, I64, D, P, I, P, I64, P, P, P], I),
-            "orc_rms_bwd_cols": ([P, P, I, I, I64, I64, D, I, P, P, P], I),
+            "orc_rms_fwd_rows": ([P, I, I64, I64, D, P, I, I, P, I64, P, P, P, P], I),
+            "orc_rms_bwd_rows": ([P, P, I, I, I64, I64, D, P, I, I, P, I64, P, P, P], I),
+            "orc_rms_bwd_cols": ([P, P, I, I, I64, I64, D, I, I, P, P, P], I),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -234,7 +237,7 @@ def ln_bwd_cols(x, dy, mean, rstd):
 
 # --------------------------------------------------------------- RMSNorm
 
-def rms_fwd(x, eps, w, mode=PARITY, rows=None):
+def rms_fwd(x, eps, w, mode=PARITY, rows=None, variant=RMS_CAST_FIRST):
     """(y, y_scale, rstd, y_allow).  y_allow: largest change of y that a
     float32 implementation may legitimately show where the rounding of the
     normalized value is near a bfloat16 tie (zero elsewhere)."""
@@ -242,12 +245,14 @@ def rms_fwd(x, eps, w, mode=PARITY, rows=None):
     wv = _f64(w)
     r, nr = _rows(rows, M)
     y = np.empty((nr, N)); ys = np.empty((nr, N)); rs = np.empty(nr); al = np.empty((nr, N))
-    _check(_lib().orc_rms_fwd_rows(_ptr(x), xt, M, N, float(eps), _ptr(wv), int(mode), _ptr(r),
-                                   nr, _ptr(y), _ptr(ys), _ptr(rs), _ptr(al)), "rms_fwd")
+    _check(_lib().orc_rms_fwd_rows(_ptr(x), xt, M, N, float(eps), _ptr(wv), int(mode),
+                                   int(variant), _ptr(r), nr, _ptr(y), _ptr(ys), _ptr(rs),
+                                   _ptr(al)), "rms_fwd")
     return y, ys, rs, al
 
 
-def rms_bwd_rows(x, dy, eps, w, w_dtype_code=F32, mode=PARITY, rows=None):
+def rms_bwd_rows(x, dy, eps, w, w_dtype_code=F32, mode=PARITY, rows=None,
+                 variant=RMS_CAST_FIRST):
     """(dx, dx_scale, dx_allow); w_dtype_code is F32 or the activation's 16-bit code."""
     x, xt, M, N = _act(x)
     dy, dt, _, _ = _act(dy)
@@ -256,12 +261,13 @@ def rms_bwd_rows(x, dy, eps, w, w_dtype_code=F32, mode=PARITY, rows=None):
     r, nr = _rows(rows, M)
     dx = np.empty((nr, N)); dxs = np.empty((nr, N)); al = np.empty((nr, N))
     _check(_lib().orc_rms_bwd_rows(_ptr(x), _ptr(dy), xt, int(w_dtype_code), M, N, float(eps),
-                                   _ptr(wv), int(mode), _ptr(r), nr, _ptr(dx), _ptr(dxs), _ptr(al)),
+                                   _ptr(wv), int(mode), int(variant), _ptr(r), nr, _ptr(dx),
+                                   _ptr(dxs), _ptr(al)),
            "rms_bwd_rows")
     return dx, dxs, al
 
 
-def rms_bwd_cols(x, dy, eps, w_dtype_code, mode=PARITY):
+def rms_bwd_cols(x, dy, eps, w_dtype_code, mode=PARITY, variant=RMS_CAST_FIRST):
     """(dw, dw_ss, dw_allow); w_dtype_code is F32 or the activation's 16-bit code
     (selects the term rounding)."""
     x, xt, M, N = _act(x)
@@ -269,5 +275,6 @@ def rms_bwd_cols(x, dy, eps, w_dtype_code, mode=PARITY):
     assert dt == xt and dy.shape == x.shape
     dw = np.empty(N); ss = np.empty(N); al = np.empty(N)
     _check(_lib().orc_rms_bwd_cols(_ptr(x), _ptr(dy), xt, int(w_dtype_code), M, N, float(eps),
-                                   int(mode), _ptr(dw), _ptr(ss), _ptr(al)), "rms_bwd_cols")
+                                   int(mode), int(variant), _ptr(dw), _ptr(ss), _ptr(al)),
+           "rms_bwd_cols")
     return dw, ss, al

@@ -384,6 +384,18 @@ int orc_ln_bwd_cols(const void* x, const void* dy, int xt, int64_t M, int64_t N,
  * GPU path, not part of the definition.  At width one the input derivative
  * is dn eps / (x^2 + eps)^(3/2) (the PR 8664 page, "Numerics").
  *
+ * Expression variants (the same page, "Which modules are replaced" and "Not
+ * covered": classes that multiply by the weight before the cast, and the
+ * Gemma family's (1 + weight)), selected by `variant`:
+ *   ORC_RMS_CAST_FIRST  (0)  the expression above;
+ *   ORC_RMS_WEIGHT_FIRST (1) y = w * (x r), one rounding at the output: the
+ *                         weight multiplies the float32 normalized value;
+ *   ORC_RMS_GEMMA       (2)  y = (x r) * (1 + w), with 1 + w formed in
+ *                         float32 (a rounding point in parity mode).
+ * Their backward, by the same autograd reading, has no intermediate
+ * rounding: dn = dy * w' (w' = w or 1 + w), dx = r (dn - xhat mean_j(dn xhat)),
+ * dw_j = sum_i dy xhat (d w'/d w = 1).
+ *
  * Near-tie allowances (parity mode, 16-bit activations): where a value
  * reaches a bfloat16 or binary16 rounding point within NEAR_TIE_REL of a midpoint, an
  * implementation that computes it in float32 may round it to the other
@@ -392,6 +404,16 @@ int orc_ln_bwd_cols(const void* x, const void* dy, int xt, int64_t M, int64_t N,
  * in float32 when both are 16-bit (8 or 11 significant bits each), so it
  * is only flagged for a float32 weight.
  */
+
+enum { ORC_RMS_CAST_FIRST = 0, ORC_RMS_WEIGHT_FIRST = 1, ORC_RMS_GEMMA = 2 };
+
+/* The weight the variant multiplies by: w, or 1 + w (rounded to float32 in
+ * parity mode, where eager forms it as a float32 sum). */
+static double rms_weight(double w, int variant, int mode)
+{
+    if (variant != ORC_RMS_GEMMA) return w;
+    return mode == ORC_PARITY ? (double)(float)(1.0 + w) : 1.0 + w;
+}
 
 static double rms_r(const void* x, int xt, int64_t i, int64_t N, double eps)
 {
@@ -404,8 +426,8 @@ static double rms_r(const void* x, int xt, int64_t i, int64_t N, double eps)
 }
 
 int orc_rms_fwd_rows(const void* x, int xt, int64_t M, int64_t N, double eps,
-                     const double* w, int mode, const int64_t* rows, int64_t nrows,
-                     double* y, double* y_scale, double* rstd, double* y_allow)
+                     const double* w, int mode, int variant, const int64_t* rows,
+                     int64_t nrows, double* y, double* y_scale, double* rstd, double* y_allow)
 {
     (void)M;
     for (int64_t r = 0; r < nrows; ++r) {
@@ -414,30 +436,32 @@ int orc_rms_fwd_rows(const void* x, int xt, int64_t M, int64_t N, double eps,
         if (rstd) rstd[r] = rs;
         for (int64_t j = 0; j < N; ++j) {
             double v = widen(x, xt, i * N + j) * rs;
+            double wj = rms_weight(w[j], variant, mode);
             int tie = 0;
-            if (mode == ORC_PARITY) v = round_to(v, xt, &tie);
-            y[r * N + j] = w[j] * v;
-            if (y_scale) y_scale[r * N + j] = fabs(w[j] * v);
-            if (y_allow) y_allow[r * N + j] = tie ? fabs(w[j]) * spacing(v, xt) : 0.0;
+            if (mode == ORC_PARITY && variant == ORC_RMS_CAST_FIRST) v = round_to(v, xt, &tie);
+            y[r * N + j] = wj * v;
+            if (y_scale) y_scale[r * N + j] = fabs(wj * v);
+            if (y_allow) y_allow[r * N + j] = tie ? fabs(wj) * spacing(v, xt) : 0.0;
         }
     }
     return 0;
 }
 
 int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int wt, int64_t M, int64_t N,
-                     double eps, const double* w, int mode, const int64_t* rows,
+                     double eps, const double* w, int mode, int variant, const int64_t* rows,
                      int64_t nrows, double* dx, double* dx_scale, double* dx_allow)
 {
     (void)M;
+    const int round_dn = mode == ORC_PARITY && variant == ORC_RMS_CAST_FIRST;
     for (int64_t r = 0; r < nrows; ++r) {
         int64_t i = row_of(rows, r);
         double rs = rms_r(x, xt, i, N, eps);
         double s = 0.0, sa = 0.0, flip = 0.0;
         for (int64_t j = 0; j < N; ++j) {
             double xh = widen(x, xt, i * N + j) * rs;
-            double dn = widen(dy, xt, i * N + j) * w[j];
+            double dn = widen(dy, xt, i * N + j) * rms_weight(w[j], variant, mode);
             int tie = 0;
-            if (mode == ORC_PARITY) dn = round_to(dn, xt, &tie);
+            if (round_dn) dn = round_to(dn, xt, &tie);
             if (tie && wt == ORC_F32) flip += spacing(dn, xt) * fabs(xh);
             s += dn * xh;
             sa += fabs(dn * xh);
@@ -447,9 +471,9 @@ int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int wt, int64_t M, i
         flip /= (double)N; /* largest change of b from flipped dn roundings */
         for (int64_t j = 0; j < N; ++j) {
             double xh = widen(x, xt, i * N + j) * rs;
-            double dn = widen(dy, xt, i * N + j) * w[j];
+            double dn = widen(dy, xt, i * N + j) * rms_weight(w[j], variant, mode);
             int tie = 0;
-            if (mode == ORC_PARITY) dn = round_to(dn, xt, &tie);
+            if (round_dn) dn = round_to(dn, xt, &tie);
             dx[r * N + j] = rs * (dn - xh * b);
             if (dx_scale) dx_scale[r * N + j] = fabs(rs) * (fabs(dn) + fabs(xh) * ba);
             if (dx_allow) {
@@ -465,8 +489,10 @@ int orc_rms_bwd_rows(const void* x, const void* dy, int xt, int wt, int64_t M, i
  * selects whether each dw term is rounded to the activation dtype before
  * the sum. */
 int orc_rms_bwd_cols(const void* x, const void* dy, int xt, int wt, int64_t M, int64_t N,
-                     double eps, int mode, double* dw, double* dw_ss, double* dw_allow)
+                     double eps, int mode, int variant, double* dw, double* dw_ss,
+                     double* dw_allow)
 {
+    const int cast_first = variant == ORC_RMS_CAST_FIRST;
     for (int64_t j = 0; j < N; ++j) {
         dw[j] = dw_ss[j] = 0.0;
         if (dw_allow) dw_allow[j] = 0.0;
@@ -476,10 +502,10 @@ int orc_rms_bwd_cols(const void* x, const void* dy, int xt, int wt, int64_t M, i
         for (int64_t j = 0; j < N; ++j) {
             double n = widen(x, xt, i * N + j) * rs;
             int tie = 0;
-            if (mode == ORC_PARITY) n = round_to(n, xt, &tie);
+            if (mode == ORC_PARITY && cast_first) n = round_to(n, xt, &tie);
             double g = widen(dy, xt, i * N + j);
             double term = g * n;
-            int round_term = (mode == ORC_PARITY && wt != ORC_F32);
+            int round_term = (mode == ORC_PARITY && cast_first && wt != ORC_F32);
             if (round_term) term = round_to(term, xt, NULL);
             dw[j] += term;
             dw_ss[j] += term * term;

@@ -519,6 +519,83 @@ def test_rms_parity_rounding_points_f16(O):
     np.testing.assert_allclose(dx, dxm, rtol=0, atol=2.0 ** -8 * np.abs(dxm).max())
 
 
+def test_rms_variants_math_and_fd(O):
+    """In math mode the weight-first expression is the Llama one (only the
+    rounding points differ), and Gemma's is the Llama one with w -> 1 + w;
+    Gemma's gradients also match central finite differences."""
+    rng = np.random.default_rng(25)
+    M, N = 3, 7
+    x = rng.standard_normal((M, N)); dy = rng.standard_normal((M, N))
+    w = 0.2 * rng.standard_normal(N); eps = 0.2
+    V0, V1, V2 = O.RMS_CAST_FIRST, O.RMS_WEIGHT_FIRST, O.RMS_GEMMA
+    y0, *_ = O.rms_fwd(x, eps, w, O.MATH, variant=V0)
+    y1, *_ = O.rms_fwd(x, eps, w, O.MATH, variant=V1)
+    y2, *_ = O.rms_fwd(x, eps, w, O.MATH, variant=V2)
+    y0p, *_ = O.rms_fwd(x, eps, 1 + w, O.MATH, variant=V0)
+    np.testing.assert_array_equal(y1, y0)
+    np.testing.assert_array_equal(y2, y0p)
+    dx2, *_ = O.rms_bwd_rows(x, dy, eps, w, O.F32, O.MATH, variant=V2)
+    dx0p, *_ = O.rms_bwd_rows(x, dy, eps, 1 + w, O.F32, O.MATH, variant=V0)
+    np.testing.assert_array_equal(dx2, dx0p)
+    dw2, *_ = O.rms_bwd_cols(x, dy, eps, O.F32, O.MATH, variant=V2)
+    dw0, *_ = O.rms_bwd_cols(x, dy, eps, O.F32, O.MATH, variant=V0)
+    np.testing.assert_array_equal(dw2, dw0)  # d(1 + w)/dw = 1
+
+    def L(xx, ww):
+        y, *_ = O.rms_fwd(xx, eps, ww, O.MATH, variant=V2)
+        return float(np.sum(dy * y))
+
+    def fd(f, v):
+        h = 1e-6 * max(1.0, abs(v))
+        return (f(v + h) - f(v - h)) / (2 * h)
+
+    for i in range(M):
+        for j in range(N):
+            def f(v, i=i, j=j):
+                xx = x.copy(); xx[i, j] = v
+                return L(xx, w)
+            assert abs(fd(f, x[i, j]) - dx2[i, j]) <= 1e-7 * max(1, abs(dx2[i, j]))
+    for j in range(N):
+        def fw(v, j=j):
+            ww = w.copy(); ww[j] = v
+            return L(x, ww)
+        assert abs(fd(fw, w[j]) - dw2[j]) <= 1e-7 * max(1, abs(dw2[j]))
+
+
+def test_rms_variants_rounding_points(O):
+    """Weight-first and Gemma round only at the outputs, except Gemma's
+    float32 1 + w."""
+    rng = np.random.default_rng(26)
+    x32 = rng.standard_normal((5, 16)).astype(np.float32)
+    bf = (x32.view(np.uint32) >> 16).astype(np.uint16)
+    dyb = (rng.standard_normal((5, 16)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    eps = 1e-6
+    w = 1 + 0.1 * rng.standard_normal(16)
+    for v in (O.RMS_WEIGHT_FIRST, O.RMS_GEMMA):
+        wv = w - 1 if v == O.RMS_GEMMA else w
+        wv = wv.astype(np.float32).astype(np.float64)
+        yp, *_ = O.rms_fwd(bf, eps, wv, O.PARITY, variant=v)
+        ym, *_ = O.rms_fwd(bf, eps, wv, O.MATH, variant=v)
+        # no rounding of the normalized value: parity differs from math only
+        # through Gemma's float32 1 + w
+        if v == O.RMS_WEIGHT_FIRST:
+            np.testing.assert_array_equal(yp, ym)
+        dxp, *_ = O.rms_bwd_rows(bf, dyb, eps, wv, O.BF16, O.PARITY, variant=v)
+        dxm, *_ = O.rms_bwd_rows(bf, dyb, eps, wv, O.BF16, O.MATH, variant=v)
+        dwp, *_ = O.rms_bwd_cols(bf, dyb, eps, O.BF16, O.PARITY, variant=v)
+        dwm, *_ = O.rms_bwd_cols(bf, dyb, eps, O.BF16, O.MATH, variant=v)
+        np.testing.assert_array_equal(dwp, dwm)  # no per-term rounding
+        if v == O.RMS_WEIGHT_FIRST:
+            np.testing.assert_array_equal(dxp, dxm)
+    # Gemma: 1 + w in float32 swallows a weight below float32's resolution
+    tiny = np.full(16, 2.0 ** -30)
+    yg, *_ = O.rms_fwd(bf, eps, tiny, O.PARITY, variant=O.RMS_GEMMA)
+    yg1, *_ = O.rms_fwd(bf, eps, np.zeros(16), O.PARITY, variant=O.RMS_GEMMA)
+    ygm, *_ = O.rms_fwd(bf, eps, tiny, O.MATH, variant=O.RMS_GEMMA)
+    np.testing.assert_array_equal(yg, yg1)
+    assert not np.array_equal(yg, ygm)
+
+
 def test_rms_padding_rows(O):
     rng = np.random.default_rng(23)
     x = rng.standard_normal((9, 6)); dy = rng.standard_normal((9, 6))

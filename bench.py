@@ -163,7 +163,7 @@ class Point:
     """One (layer, shape) of a workload with its device buffers and the C-ABI
     argument tuples of its forward and backward calls."""
 
-    def __init__(self, lib, wl, dev, shared, fwd=True):
+    def __init__(self, lib, wl, dev, shared, fwd=True, rms_variant=0):
         from normalization_layers_fwd_gb300 import _lib
         self.wl, self.lib, self.fwd_enabled = wl, lib, fwd and not wl.bwd_only
         M, N = wl.M, wl.N
@@ -202,9 +202,10 @@ class Point:
                                                  nws, s))
         else:
             W = P(inp["weight"])
-            self.fwd_call = (lib.rmsnorm_fwd, (X, W, Y, P(self.rstd), M, N, wl.eps, xt, pt, s))
-            self.bwd_call = (lib.rmsnorm_bwd, (X, DY, W, P(self.rstd), DX, P(self.g1), M, N,
-                                               wl.eps, xt, pt, P(self.ws), nws, s))
+            v = rms_variant
+            self.fwd_call = (lib.rmsnorm_fwd_ex, (X, W, Y, P(self.rstd), M, N, wl.eps, xt, pt, v, s))
+            self.bwd_call = (lib.rmsnorm_bwd_ex, (X, DY, W, P(self.rstd), DX, P(self.g1), M, N,
+                                                  wl.eps, xt, pt, v, P(self.ws), nws, s))
         if wl.bwd_only:
             # saved statistics for the backward-only workload come from one
             # forward, outside the timed region
@@ -314,6 +315,8 @@ def run_ours(args, rank, world, dev):
     wls, wdesc = workloads(args.workload, args.ops, args.widths)
     if args.ops or args.widths:
         wdesc += f" (subset: ops={args.ops}, widths={args.widths})"
+    if args.rms_variant:
+        wdesc += f" (RMSNorm expression {['cast first', 'weight first', 'gemma'][args.rms_variant]})"
     maxE = max(w.M * w.N for w in wls)
     maxM = max(w.M for w in wls)
     dtype = wls[0].xdtype
@@ -321,7 +324,7 @@ def run_ours(args, rank, world, dev):
               "dx": torch.empty(maxE, dtype=dtype, device=dev),
               "mean": torch.empty(maxM, dtype=torch.float32, device=dev),
               "rstd": torch.empty(maxM, dtype=torch.float32, device=dev)}
-    points = [Point(lib, w, dev, shared) for w in wls]
+    points = [Point(lib, w, dev, shared, rms_variant=args.rms_variant) for w in wls]
     torch.cuda.synchronize(dev)
     per_tensor = min(w.M * w.N * w.xdtype.itemsize for w in wls)
     big = per_tensor > 2 * L2_BYTES
@@ -583,6 +586,8 @@ def main():
                     help="restrict the sweep to these layers (profiling runs)")
     ap.add_argument("--widths", type=lambda v: [int(x) for x in v.split(",")], default=None,
                     help="restrict the sweep to these widths (profiling runs)")
+    ap.add_argument("--rms-variant", type=int, choices=[0, 1, 2], default=0,
+                    help="RMSNorm expression: 0 Llama (default), 1 weight first, 2 Gemma")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

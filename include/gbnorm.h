@@ -153,6 +153,33 @@ int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd,
                 void* dw, int64_t M, int64_t N, float eps, int xt, int wt, void* ws,
                 size_t ws_bytes, cudaStream_t stream);
 
+/* RMSNorm expression variants (the fused-RMSNorm page, DeepSpeed PR 8645
+ * quoted in PR 8664, "Which modules are replaced" and "Not covered"):
+ *   GBN_RMS_CAST_FIRST   y = w * (x r).to(x.dtype): the Llama expression of
+ *                        rmsnorm_fwd / rmsnorm_bwd above;
+ *   GBN_RMS_WEIGHT_FIRST y = (w * (x r)).to(x.dtype): the weight multiplies
+ *                        the float32 normalized value (GptOss, OLMo 2/3
+ *                        style);
+ *   GBN_RMS_GEMMA        y = ((x r) * (1 + w)).to(x.dtype), 1 + w in float32.
+ * The weight-first forms round only their outputs; their backward is
+ *   dn = dy w' (float32, w' = w or 1 + w), dx = round_x(r (dn - xhat
+ *   mean_j(dn xhat))), dw[j] = sum_i dy xhat (float32, one final rounding).
+ * They accept any weight dtype. */
+typedef enum {
+    GBN_RMS_CAST_FIRST = 0,
+    GBN_RMS_WEIGHT_FIRST = 1,
+    GBN_RMS_GEMMA = 2
+} gbn_rms_variant;
+
+/* rmsnorm_fwd / rmsnorm_bwd with an expression variant (gbn_rms_variant;
+ * anything else returns GBN_EINVAL).  Arguments otherwise as above; the
+ * backward's rstd recomputation (rstd null) is the same in every variant. */
+int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
+                   float eps, int xt, int wt, int variant, cudaStream_t stream);
+int rmsnorm_bwd_ex(const void* x, const void* dy, const void* w, const float* rstd, void* dx,
+                   void* dw, int64_t M, int64_t N, float eps, int xt, int wt, int variant,
+                   void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* rmsnorm_bwd_static_ws: rmsnorm_bwd without a caller workspace.  The pages
  *   have no counterpart; it exists for callers that cannot allocate device
  *   memory (a host program with no device allocator of its own, code under a

@@ -20,6 +20,8 @@ from . import build as _build
 GBN_F32, GBN_BF16, GBN_F16 = 0, 1, 2
 GBN_OP_DYT, GBN_OP_LAYERNORM, GBN_OP_RMSNORM = 0, 1, 2
 GBN_OK = 0
+# RMSNorm expressions: Llama (weight after the cast), weight before the cast, Gemma (1 + w)
+GBN_RMS_CAST_FIRST, GBN_RMS_WEIGHT_FIRST, GBN_RMS_GEMMA = 0, 1, 2
 GBN_ESCRATCH = 6
 GBN_STATIC_WS_BYTES = 8 << 20  # size of the library's static scratch array
 SIZE_MAX = ctypes.c_size_t(-1).value
@@ -39,6 +41,8 @@ SIGNATURES = {
     "layernorm_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I, _I, _P, _SZ, _P], _I),
     "rmsnorm_fwd": ([_P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P], _I),
     "rmsnorm_bwd": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P, _SZ, _P], _I),
+    "rmsnorm_fwd_ex": ([_P, _P, _P, _P, _I64, _I64, _F, _I, _I, _I, _P], _I),
+    "rmsnorm_bwd_ex": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _I, _P, _SZ, _P], _I),
     "rmsnorm_bwd_static_ws": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _I, _I, _P], _I),
 }
 
@@ -225,18 +229,20 @@ def layernorm_bwd(x, dy, mean, rstd, gamma=None, need_dgamma=True, need_dbeta=Tr
 
 # ------------------------------------------------------------------ RMSNorm
 
-def rmsnorm_fwd(x, w, eps=1e-6, save_rstd=True):
-    """(y, rstd): weight * (x.float() * rsqrt(mean(x^2) + eps)).to(x.dtype)."""
+def rmsnorm_fwd(x, w, eps=1e-6, save_rstd=True, variant=GBN_RMS_CAST_FIRST):
+    """(y, rstd): weight * (x.float() * rsqrt(mean(x^2) + eps)).to(x.dtype), or
+    the weight-first / Gemma expression (variant, gbn_rms_variant)."""
     x, M, N = _rows(x)
     w = _param(w, x, N, "w")
     y = torch.empty_like(x)
     rstd = torch.empty(M, dtype=torch.float32, device=x.device) if save_rstd else None
-    _check(load().rmsnorm_fwd(_ptr(x), _ptr(w), _ptr(y), _ptr(rstd), M, N, float(eps), _code(x),
-                              _code(w), _stream(x.device)), "rmsnorm_fwd")
+    _check(load().rmsnorm_fwd_ex(_ptr(x), _ptr(w), _ptr(y), _ptr(rstd), M, N, float(eps),
+                                 _code(x), _code(w), int(variant), _stream(x.device)),
+           "rmsnorm_fwd_ex")
     return y, rstd
 
 
-def rmsnorm_bwd(x, dy, w, rstd=None, eps=1e-6, need_dw=True):
+def rmsnorm_bwd(x, dy, w, rstd=None, eps=1e-6, need_dw=True, variant=GBN_RMS_CAST_FIRST):
     """(dx, dw); rstd None recomputes it exactly as the forward does."""
     x, M, N = _rows(x)
     dy = dy.contiguous()
@@ -247,9 +253,9 @@ def rmsnorm_bwd(x, dy, w, rstd=None, eps=1e-6, need_dw=True):
     dx = torch.empty_like(x)
     dw = torch.empty(N, dtype=w.dtype, device=x.device) if need_dw else None
     ws, nbytes = workspace(GBN_OP_RMSNORM, M, N, _code(x), _code(w), x.device)
-    _check(load().rmsnorm_bwd(_ptr(x), _ptr(dy), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw), M, N,
-                              float(eps), _code(x), _code(w), _ptr(ws), nbytes, _stream(x.device)),
-           "rmsnorm_bwd")
+    _check(load().rmsnorm_bwd_ex(_ptr(x), _ptr(dy), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw), M,
+                                 N, float(eps), _code(x), _code(w), int(variant), _ptr(ws),
+                                 nbytes, _stream(x.device)), "rmsnorm_bwd_ex")
     return dx, dw
 
 

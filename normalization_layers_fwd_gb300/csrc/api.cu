@@ -347,18 +347,24 @@ int layernorm_bwd(const void* x, const void* dy, const float* mean, const float*
 }
 
 // ------------------------------------------------------------------ RMSNorm
-// RMSNorm rounds w*n, dy*w and dy*n to the activation dtype; with 16-bit
-// activations the weight is float32 or of the activation dtype (a bf16 x
-// with an f16 weight, or the reverse, has no defined rounding point).
-bool rms_dtypes_ok(int xt, int wt)
+// The Llama expression (variant 0) rounds w*n, dy*w and dy*n to the
+// activation dtype; with 16-bit activations its weight is float32 or of the
+// activation dtype (a bf16 x with an f16 weight, or the reverse, has no
+// defined rounding point).  The weight-first variants round only their
+// outputs and take any weight dtype.
+bool rms_dtypes_ok(int xt, int wt, int variant)
 {
-    return dtype_ok(xt) && dtype_ok(wt) && (xt == GBN_F32 || wt == GBN_F32 || wt == xt);
+    if (!dtype_ok(xt) || !dtype_ok(wt)) return false;
+    return variant != GBN_RMS_CAST_FIRST || xt == GBN_F32 || wt == GBN_F32 || wt == xt;
 }
 
-int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
-                float eps, int xt, int wt, cudaStream_t stream)
+bool rms_variant_ok(int v) { return v >= GBN_RMS_CAST_FIRST && v <= GBN_RMS_GEMMA; }
+
+int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
+                   float eps, int xt, int wt, int variant, cudaStream_t stream)
 {
-    if (!rms_dtypes_ok(xt, wt)) return GBN_EDTYPE;
+    if (!rms_variant_ok(variant)) return GBN_EINVAL;
+    if (!rms_dtypes_ok(xt, wt, variant)) return GBN_EDTYPE;
     if (!shape_ok(M, N) || !eps_ok(eps) || !w) return GBN_EINVAL;
     if (M > 0 && (!x || !y)) return GBN_EINVAL;
     if (!all_aligned(xt, {x, y}) || !all_aligned(wt, {w}) || !all_aligned(GBN_F32, {rstd}))
@@ -369,14 +375,15 @@ int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, i
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream,
                     gbn::kFwdNorm, kWide12);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
-    return launch_status(gbn::launch_rms_fwd(L, xt, wt, x, w, y, rstd, M, (int)N, eps));
+    return launch_status(gbn::launch_rms_fwd(L, xt, wt, x, w, y, rstd, M, (int)N, eps, variant));
 }
 
-int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd, void* dx,
-                void* dw, int64_t M, int64_t N, float eps, int xt, int wt, void* ws,
-                size_t ws_bytes, cudaStream_t stream)
+int rmsnorm_bwd_ex(const void* x, const void* dy, const void* w, const float* rstd, void* dx,
+                   void* dw, int64_t M, int64_t N, float eps, int xt, int wt, int variant,
+                   void* ws, size_t ws_bytes, cudaStream_t stream)
 {
-    if (!rms_dtypes_ok(xt, wt)) return GBN_EDTYPE;
+    if (!rms_variant_ok(variant)) return GBN_EINVAL;
+    if (!rms_dtypes_ok(xt, wt, variant)) return GBN_EDTYPE;
     if (!shape_ok(M, N) || !eps_ok(eps) || !w) return GBN_EINVAL;
     if (M > 0 && (!x || !dy || !dx)) return GBN_EINVAL;
     if (!all_aligned(xt, {x, dy, dx}) || !all_aligned(wt, {w, dw}) || !all_aligned(GBN_F32, {rstd}))
@@ -391,10 +398,24 @@ int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd,
     float* wsf = dw ? static_cast<float*>(ws) : nullptr;
     if (M > 0) {
         const int rc = launch_status(
-            gbn::launch_rms_bwd(L, xt, wt, x, dy, w, rstd, dx, wsf, M, (int)N, eps));
+            gbn::launch_rms_bwd(L, xt, wt, x, dy, w, rstd, dx, wsf, M, (int)N, eps, variant));
         if (rc != GBN_OK) return rc;
     }
     return finish_bwd(stream, wsf, M > 0 ? L.P : 0, GBN_OP_RMSNORM, N, wt, dw, nullptr, nullptr);
+}
+
+int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
+                float eps, int xt, int wt, cudaStream_t stream)
+{
+    return rmsnorm_fwd_ex(x, w, y, rstd, M, N, eps, xt, wt, GBN_RMS_CAST_FIRST, stream);
+}
+
+int rmsnorm_bwd(const void* x, const void* dy, const void* w, const float* rstd, void* dx,
+                void* dw, int64_t M, int64_t N, float eps, int xt, int wt, void* ws,
+                size_t ws_bytes, cudaStream_t stream)
+{
+    return rmsnorm_bwd_ex(x, dy, w, rstd, dx, dw, M, N, eps, xt, wt, GBN_RMS_CAST_FIRST, ws,
+                          ws_bytes, stream);
 }
 
 }  // extern "C"

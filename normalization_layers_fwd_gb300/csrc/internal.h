@@ -40,11 +40,13 @@ cudaError_t launch_ln_bwd(const Launch& L, int xt, int pt, const void* x, const 
                           const float* mean, const float* rstd, const void* gamma, void* dx,
                           float* ws, int64_t M, int N);
 
+// variant: the RMSNorm expression (0 cast then weight, 1 weight then cast,
+// 2 Gemma's (1 + weight) then cast), as gbn_rms_variant in gbnorm.h.
 cudaError_t launch_rms_fwd(const Launch& L, int xt, int pt, const void* x, const void* w,
-                           void* y, float* rstd, int64_t M, int N, float eps);
+                           void* y, float* rstd, int64_t M, int N, float eps, int variant);
 cudaError_t launch_rms_bwd(const Launch& L, int xt, int pt, const void* x, const void* dy,
                            const void* w, const float* rstd, void* dx, float* ws, int64_t M,
-                           int N, float eps);
+                           int N, float eps, int variant);
 
 // Second stage of the parameter-gradient reduction: out[c] = sum over the P
 // workspace rows of column c, in a fixed order, written in the parameter

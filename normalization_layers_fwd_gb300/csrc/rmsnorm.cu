@@ -51,11 +51,11 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int p)
 // packed pair.  Other dtype pairs take float32 pairs.
 
 // ------------------------------------------------------------ fast forward
-template <typename TX, int S>
+template <typename TX, int S, bool kWF>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
     rms_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ w,
                  int pt, float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
-                 int64_t nblocks, unsigned* fault)
+                 int64_t nblocks, unsigned* fault, int gemma)
 {
     constexpr int W = kSched[S].W, U = kind_U(S, kFwdNorm), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
@@ -70,7 +70,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
     for (int j = 0; j < KV; ++j) colok[j] = in_group<W>() && l + j * W < N / VEC;
     const int rb = N * (int)sizeof(TX);
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
-    const bool w16 = is16<TX>() && pt == dtype_code<TX>();
+    // the Llama expression's packed 16-bit product (weight of x's dtype)
+    const bool w16 = !kWF && is16<TX>() && pt == dtype_code<TX>();
 
     f2 wf[KV][P];
     uint32_t wpk[KV][P];  // the 16-bit weight pair, packed (used when w16)
@@ -80,6 +81,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
         for (int p = 0; p < P; ++p) {
             const int c = (l + j * W) * VEC + 2 * p;
             wf[j][p] = colok[j] ? ld_param2(w, pt, c) : splat2(0.f);
+            if (gemma) wf[j][p] = add2(splat2(1.f), wf[j][p]);  // 1 + w in float32
             wpk[j][p] = (w16 && colok[j]) ? static_cast<const uint32_t*>(w)[c / 2] : 0u;
         }
     }
@@ -121,7 +123,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
                 uint4 out;
-                if constexpr (is16<TX>()) {
+                if constexpr (is16<TX>() && !kWF) {
                     uint32_t o[4];
 #pragma unroll
                     for (int p = 0; p < P; ++p) {
@@ -151,12 +153,12 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
 // prefetched into registers, otherwise r is recomputed with the forward's
 // code.  Full row blocks run without masking; the ragged last block masks its
 // padded rows by a select after the arithmetic.
-template <typename TX, int S>
+template <typename TX, int S, bool kWF>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
     rms_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy, const void* __restrict__ w,
                  int pt, const float* __restrict__ rstd, TX* __restrict__ dx,
                  float* __restrict__ ws, int64_t M, int N, float eps, float inv_n,
-                 int64_t nblocks, unsigned* fault)
+                 int64_t nblocks, unsigned* fault, int gemma)
 {
     constexpr int W = kSched[S].W, U = kind_U(S, kBwdRms), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
     // a weight in x's dtype: each dy*n is rounded to x's dtype (bf16 pairs
     // then multiply in bf16); a float32 weight keeps the float32 product
-    const bool w16 = is16<TX>() && pt == dtype_code<TX>();
+    const bool w16 = !kWF && is16<TX>() && pt == dtype_code<TX>();
 
     f2 wf[KV][P], acc[KV][P];
     uint32_t wpk[KV][P];
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
         for (int p = 0; p < P; ++p) {
             const int c = (l + j * W) * VEC + 2 * p;
             wf[j][p] = colok[j] ? ld_param2(w, pt, c) : splat2(0.f);
+            if (gemma) wf[j][p] = add2(splat2(1.f), wf[j][p]);  // 1 + w in float32
             wpk[j][p] = (w16 && colok[j]) ? static_cast<const uint32_t*>(w)[c / 2] : 0u;
             acc[j][p] = splat2(0.f);
         }
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
                 for (int p = 0; p < P; ++p) {
                     xh[u][j][p] = mul2(xh[u][j][p], r2);
                     f2 nxt;  // the accumulator with this row's dw term added
-                    if constexpr (is16<TX>()) {
+                    if constexpr (is16<TX>() && !kWF) {
                         const uint32_t npk = P16<TX>::from_f2(xh[u][j][p]);  // n = round_x(xhat)
                         if (w16) {
                             dn[u][j][p] = P16<TX>::to_f2(P16<TX>::mul(word(dr, p), wpk[j][p]));
@@ -310,6 +313,14 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
 }
 
 // ------------------------------------------------------ general (any shape)
+// The weight of column c as the expression variant uses it: w, or Gemma's
+// 1 + w formed in float32.
+__device__ __forceinline__ float rms_weight(const void* w, int pt, int c, int variant)
+{
+    const float v = ld_param(w, pt, c);
+    return variant == 2 ? 1.f + v : v;
+}
+
 template <typename TX>
 __device__ __forceinline__ float warp_row_rstd(const TX* xr, int N, int lane, float eps,
                                                float inv_n)
@@ -326,15 +337,18 @@ __device__ __forceinline__ float warp_row_rstd(const TX* xr, int N, int lane, fl
 template <typename TX>
 __global__ void __launch_bounds__(kGenThreads)
     rms_fwd_general(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ w,
-                    int pt, float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n)
+                    int pt, float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
+                    int variant)
 {
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * kGenWarps;
     for (int64_t r = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5); r < M; r += nw) {
         const TX* xr = x + r * N;
         const float rs = warp_row_rstd(xr, N, lane, eps, inv_n);
-        for (int c = lane; c < N; c += 32)
-            st1(y, r * N + c, ld_param(w, pt, c) * round_x<TX>(ld1(xr, c) * rs));
+        for (int c = lane; c < N; c += 32) {
+            const float xh = ld1(xr, c) * rs;
+            st1(y, r * N + c, rms_weight(w, pt, c, variant) * (variant == 0 ? round_x<TX>(xh) : xh));
+        }
         if (rstd && lane == 0) rstd[r] = rs;
     }
 }
@@ -344,12 +358,13 @@ __global__ void __launch_bounds__(kGenThreads)
     rms_bwd_general(const TX* __restrict__ x, const TX* __restrict__ dy,
                     const void* __restrict__ w, int pt, const float* __restrict__ rstd,
                     TX* __restrict__ dx, float* __restrict__ ws, int64_t M, int N, float eps,
-                    float inv_n)
+                    float inv_n, int variant)
 {
     const int lane = threadIdx.x & 31;
     const int64_t wi = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5);
     const int64_t nw = (int64_t)gridDim.x * kGenWarps;
-    const bool round_terms = (pt != kF32);
+    const bool cast_first = variant == 0;  // the Llama expression's rounding points
+    const bool round_terms = cast_first && pt != kF32;
     float* wrow = ws ? ws + wi * (int64_t)N : nullptr;
     if (wrow)
         for (int c = lane; c < N; c += 32) wrow[c] = 0.f;
@@ -359,7 +374,8 @@ __global__ void __launch_bounds__(kGenThreads)
         const float rs = rstd ? rstd[r] : warp_row_rstd(xr, N, lane, eps, inv_n);
         float s[1] = {0.f};
         for (int c = lane; c < N; c += 32) {
-            const float dn = round_x<TX>(ld1(dr, c) * ld_param(w, pt, c));
+            float dn = ld1(dr, c) * rms_weight(w, pt, c, variant);
+            if (cast_first) dn = round_x<TX>(dn);
             s[0] = fmaf(dn, ld1(xr, c) * rs, s[0]);
         }
         butterfly<32, 1>(s);
@@ -367,35 +383,52 @@ __global__ void __launch_bounds__(kGenThreads)
         for (int c = lane; c < N; c += 32) {
             const float dv = ld1(dr, c);
             const float xh = ld1(xr, c) * rs;
-            const float dn = round_x<TX>(dv * ld_param(w, pt, c));
+            float dn = dv * rms_weight(w, pt, c, variant);
+            if (cast_first) dn = round_x<TX>(dn);
             st1(dx, r * N + c, rs * (dn - xh * m));
-            float term = dv * round_x<TX>(xh);
+            float term = dv * (cast_first ? round_x<TX>(xh) : xh);
             if (round_terms) term = round_x<TX>(term);
             if (wrow) wrow[c] += term;
         }
     }
 }
 
+// Launch schedule S of a fast kernel: the weight-first instance (kWF) for
+// the weight-first and Gemma expressions with 16-bit activations; with
+// float32 activations both expressions are the same float32 arithmetic.
+#define GBN_RMS_LAUNCH(KERNEL, S, SMEM, ...)                                                       \
+    do {                                                                                           \
+        if constexpr (is16<TX>()) {                                                                \
+            if (variant != 0) {                                                                    \
+                ring_attributes<KERNEL<TX, S, true>>(SMEM);                                        \
+                KERNEL<TX, S, true><<<L.grid, kSched[S].T, SMEM, L.stream>>>(__VA_ARGS__);         \
+                break;                                                                             \
+            }                                                                                      \
+        }                                                                                          \
+        ring_attributes<KERNEL<TX, S, false>>(SMEM);                                               \
+        KERNEL<TX, S, false><<<L.grid, kSched[S].T, SMEM, L.stream>>>(__VA_ARGS__);                \
+    } while (0)
+
 template <typename TX>
 cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, void* y,
-                         float* rstd, int64_t M, int N, float eps)
+                         float* rstd, int64_t M, int N, float eps, int variant)
 {
     const TX* xp = static_cast<const TX*>(x);
     TX* yp = static_cast<TX*>(y);
     const float inv_n = (float)(1.0 / (double)N);
+    const int gemma = variant == 2;
     if (!L.fast) {
         rms_fwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, yp, w, pt, rstd, M, N, eps,
-                                                                  inv_n);
+                                                                  inv_n, variant);
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                          \
-    case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, kFwdNorm, 1);                                  \
-        auto kern = rms_fwd_fast<TX, S>;                                                     \
-        ring_attributes<rms_fwd_fast<TX, S>>(smem);                                                         \
-        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, w, pt, rstd, M, N, eps, inv_n, L.nblocks, L.fault);                              \
-        break;                                                                               \
+#define GBN_CASE(S)                                                                                \
+    case S: {                                                                                      \
+        constexpr int smem = ring_smem_bytes(S, kFwdNorm, 1);                                      \
+        GBN_RMS_LAUNCH(rms_fwd_fast, S, smem, xp, yp, w, pt, rstd, M, N, eps, inv_n, L.nblocks,    \
+                       L.fault, gemma);                                                            \
+        break;                                                                                     \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(11)
@@ -408,25 +441,26 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
 
 template <typename TX>
 cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy, const void* w,
-                         const float* rstd, void* dx, float* ws, int64_t M, int N, float eps)
+                         const float* rstd, void* dx, float* ws, int64_t M, int N, float eps,
+                         int variant)
 {
     const TX* xp = static_cast<const TX*>(x);
     const TX* dyp = static_cast<const TX*>(dy);
     TX* dxp = static_cast<TX*>(dx);
     const float inv_n = (float)(1.0 / (double)N);
+    const int gemma = variant == 2;
     if (!L.fast) {
         rms_bwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, dyp, w, pt, rstd, dxp, ws,
-                                                                  M, N, eps, inv_n);
+                                                                  M, N, eps, inv_n, variant);
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                          \
-    case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, kBwdRms, 2);                                  \
-        auto kern = rms_bwd_fast<TX, S>;                                                     \
-        ring_attributes<rms_bwd_fast<TX, S>>(smem);                                                         \
-        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, dyp, w, pt, rstd, dxp, ws, M, N, eps, inv_n, L.nblocks, L.fault);                              \
-        break;                                                                               \
+#define GBN_CASE(S)                                                                                \
+    case S: {                                                                                      \
+        constexpr int smem = ring_smem_bytes(S, kBwdRms, 2);                                       \
+        GBN_RMS_LAUNCH(rms_bwd_fast, S, smem, xp, dyp, w, pt, rstd, dxp, ws, M, N, eps, inv_n,     \
+                       L.nblocks, L.fault, gemma);                                                 \
+        break;                                                                                     \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(11)
@@ -436,24 +470,25 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     }
     return cudaGetLastError();
 }
+#undef GBN_RMS_LAUNCH
 
 }  // namespace
 
 cudaError_t launch_rms_fwd(const Launch& L, int xt, int pt, const void* x, const void* w, void* y,
-                           float* rstd, int64_t M, int N, float eps)
+                           float* rstd, int64_t M, int N, float eps, int variant)
 {
-    if (xt == kF32) return fwd_dispatch<float>(L, pt, x, w, y, rstd, M, N, eps);
-    if (xt == kF16) return fwd_dispatch<__half>(L, pt, x, w, y, rstd, M, N, eps);
-    return fwd_dispatch<__nv_bfloat16>(L, pt, x, w, y, rstd, M, N, eps);
+    if (xt == kF32) return fwd_dispatch<float>(L, pt, x, w, y, rstd, M, N, eps, variant);
+    if (xt == kF16) return fwd_dispatch<__half>(L, pt, x, w, y, rstd, M, N, eps, variant);
+    return fwd_dispatch<__nv_bfloat16>(L, pt, x, w, y, rstd, M, N, eps, variant);
 }
 
 cudaError_t launch_rms_bwd(const Launch& L, int xt, int pt, const void* x, const void* dy,
                            const void* w, const float* rstd, void* dx, float* ws, int64_t M,
-                           int N, float eps)
+                           int N, float eps, int variant)
 {
-    if (xt == kF32) return bwd_dispatch<float>(L, pt, x, dy, w, rstd, dx, ws, M, N, eps);
-    if (xt == kF16) return bwd_dispatch<__half>(L, pt, x, dy, w, rstd, dx, ws, M, N, eps);
-    return bwd_dispatch<__nv_bfloat16>(L, pt, x, dy, w, rstd, dx, ws, M, N, eps);
+    if (xt == kF32) return bwd_dispatch<float>(L, pt, x, dy, w, rstd, dx, ws, M, N, eps, variant);
+    if (xt == kF16) return bwd_dispatch<__half>(L, pt, x, dy, w, rstd, dx, ws, M, N, eps, variant);
+    return bwd_dispatch<__nv_bfloat16>(L, pt, x, dy, w, rstd, dx, ws, M, N, eps, variant);
 }
 
 }  // namespace gbn

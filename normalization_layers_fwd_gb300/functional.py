@@ -44,18 +44,19 @@ class _LayerNorm(torch.autograd.Function):
 
 class _RMSNorm(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, x, w, eps):
-        y, rstd = _lib.rmsnorm_fwd(x, w, eps)
+    def forward(ctx, x, w, eps, variant):
+        y, rstd = _lib.rmsnorm_fwd(x, w, eps, variant=variant)
         ctx.save_for_backward(x, w, rstd)
-        ctx.eps = eps
+        ctx.eps, ctx.variant = eps, variant
         return y.view(x.shape)
 
     @staticmethod
     @once_differentiable
     def backward(ctx, dy):
         x, w, rstd = ctx.saved_tensors
-        dx, dw = _lib.rmsnorm_bwd(x, dy, w, rstd, ctx.eps, ctx.needs_input_grad[1])
-        return dx.view(x.shape), dw, None
+        dx, dw = _lib.rmsnorm_bwd(x, dy, w, rstd, ctx.eps, ctx.needs_input_grad[1],
+                                  variant=ctx.variant)
+        return dx.view(x.shape), dw, None, None
 
 
 def dyt(x, alpha, gamma, beta):
@@ -68,6 +69,9 @@ def layer_norm(x, gamma=None, beta=None, eps=1e-5):
     return _LayerNorm.apply(x, gamma, beta, eps)
 
 
-def rms_norm(x, weight, eps=1e-6):
-    """Llama-style RMSNorm: weight * (x.float() * rsqrt(mean(x^2) + eps)).to(x.dtype)."""
-    return _RMSNorm.apply(x, weight, eps)
+def rms_norm(x, weight, eps=1e-6, variant=_lib.GBN_RMS_CAST_FIRST):
+    """RMSNorm over the last dimension.  variant 0 (default) is the Llama
+    expression weight * (x.float() * rsqrt(mean(x^2) + eps)).to(x.dtype);
+    1 multiplies by the weight before the cast; 2 is Gemma's (1 + weight)
+    before the cast."""
+    return _RMSNorm.apply(x, weight, eps, variant)

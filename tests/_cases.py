@@ -76,11 +76,14 @@ def layernorm_case(x, dy, gamma, beta, eps, rows=None, cols=True, stats=None):
     return reps, out
 
 
-def rmsnorm_case(x, dy, w, eps, rows=None, cols=True):
+def rmsnorm_case(x, dy, w, eps, rows=None, cols=True, variant=0):
+    """variant: the library's RMSNorm expression code (0 Llama, 1 weight
+    first, 2 Gemma), compared with the oracle's expression of that name."""
     reps = []
-    y, rstd = _lib.rmsnorm_fwd(x, w, eps)
-    dx, dw = _lib.rmsnorm_bwd(x, dy, w, rstd, eps)
-    dx2, dw2 = _lib.rmsnorm_bwd(x, dy, w, None, eps)
+    ov = {0: oracle.RMS_CAST_FIRST, 1: oracle.RMS_WEIGHT_FIRST, 2: oracle.RMS_GEMMA}[variant]
+    y, rstd = _lib.rmsnorm_fwd(x, w, eps, variant=variant)
+    dx, dw = _lib.rmsnorm_bwd(x, dy, w, rstd, eps, variant=variant)
+    dx2, dw2 = _lib.rmsnorm_bwd(x, dy, w, None, eps, variant=variant)
     torch.cuda.synchronize()
     # the saved rstd is a cache: recomputing it must give identical bits
     def bits(t):
@@ -89,13 +92,14 @@ def rmsnorm_case(x, dy, w, eps, rows=None, cols=True):
     assert torch.equal(bits(dw), bits(dw2))
     xo, dyo = to_oracle(x), to_oracle(dy)
     w64 = f64(w)
-    yo, ys, rso, yal = oracle.rms_fwd(xo, eps, w64, oracle.PARITY, rows)
+    yo, ys, rso, yal = oracle.rms_fwd(xo, eps, w64, oracle.PARITY, rows, variant=ov)
     reps.append(check_out("rms y", _sel(y, rows), yo, ys, yal))
     reps.append(check_f32("rms rstd", _sel(rstd, rows), rso, np.abs(rso)))
-    dxo, dxs, dxal = oracle.rms_bwd_rows(xo, dyo, eps, w64, _pcode(w), oracle.PARITY, rows)
+    dxo, dxs, dxal = oracle.rms_bwd_rows(xo, dyo, eps, w64, _pcode(w), oracle.PARITY, rows,
+                                         variant=ov)
     reps.append(check_out("rms dx", _sel(dx, rows), dxo, dxs, dxal))
     if cols:
-        dwo, ss, al = oracle.rms_bwd_cols(xo, dyo, eps, _pcode(w), oracle.PARITY)
+        dwo, ss, al = oracle.rms_bwd_cols(xo, dyo, eps, _pcode(w), oracle.PARITY, variant=ov)
         reps.append(check_reduced("rms dw", dw, dwo, ss, al))
     return reps, dict(y=y, rstd=rstd, dx=dx, dw=dw)
 

@@ -63,6 +63,11 @@ def test_invalid_arguments_are_rejected_before_any_device_use(lib):
     # RMSNorm with a 16-bit weight of the other 16-bit type has no rounding point
     assert lib.rmsnorm_fwd(p, p, p, None, 4, 8, 1e-6, 1, 2, None) == GBN_EDTYPE
     assert lib.rmsnorm_bwd(p, p, p, None, p, p, 4, 8, 1e-6, 2, 1, None, 0, None) == GBN_EDTYPE
+    # ... in the Llama expression only; unknown expression codes are rejected
+    assert lib.rmsnorm_fwd_ex(p, p, p, None, 4, 8, 1e-6, 1, 2, 0, None) == GBN_EDTYPE
+    assert lib.rmsnorm_fwd_ex(p, p, p, None, 4, 8, 1e-6, 1, 1, 3, None) == GBN_EINVAL
+    assert lib.rmsnorm_bwd_ex(p, p, p, None, p, p, 4, 8, 1e-6, 1, 1, -1, None, 0, None) == \
+        GBN_EINVAL
     # bad shapes
     assert lib.dyt_fwd(p, p, p, p, p, -1, 8, 1, 0, None) == GBN_EINVAL
     assert lib.dyt_fwd(p, p, p, p, p, 4, 0, 1, 0, None) == GBN_EINVAL

@@ -78,6 +78,24 @@ def test_parity_small(case):
         print(r.line())
 
 
+@pytest.mark.parametrize("variant", [1, 2], ids=["weight_first", "gemma"])
+@pytest.mark.parametrize("xdt,pdt", [(torch.bfloat16, torch.float32),
+                                     (torch.bfloat16, torch.bfloat16),
+                                     (torch.float16, torch.float16),
+                                     (torch.bfloat16, torch.float16),
+                                     (torch.float32, torch.float32)],
+                         ids=["bf16-f32", "bf16-bf16", "f16-f16", "bf16-f16", "f32-f32"])
+@pytest.mark.parametrize("N", [8, 24, 128, 1000, 2048, 4096, 8192, 8200])
+def test_rms_variants(variant, xdt, pdt, N):
+    """The weight-first and Gemma RMSNorm expressions against the oracle
+    (vector, multi-vector and general paths; rstd recomputation bit-exact)."""
+    M = max(3, min(3001, (1 << 20) // N))
+    inp = _inputs(M, N, xdt, pdt, f"rmsv{variant}{N}{xdt}{pdt}")
+    reps, _ = rmsnorm_case(inp["x"], inp["dy"], inp["gamma"], 1e-6, variant=variant)
+    for r in reps:
+        print(r.line())
+
+
 @pytest.mark.parametrize("op", ["dyt", "layernorm", "rmsnorm"])
 @pytest.mark.parametrize("N", [16, 24, 64])
 def test_persistent_loop(op, N):

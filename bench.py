@@ -1,8 +1,9 @@
 """Benchmark of the row-normalization hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload sweep|sweep_f16|dyt_f32_4096x64|layernorm_bwd_401408x24|
-                                dyt_bf16_1048576x128|rmsnorm_bf16_16384x2048]
+                    [--workload sweep|sweep_f16|headmajor|dyt_f32_4096x64|
+                                layernorm_bwd_401408x24|dyt_bf16_1048576x128|
+                                rmsnorm_bf16_16384x2048]
 
 A step is one pass of the whole hot path over one batch of synthetic input:
 for the default "sweep" workload, DyT, LayerNorm and RMSNorm forward +
@@ -19,6 +20,11 @@ the slowest rank's time.
 
 `--impl reference` times the float64 CPU oracle (the correctness
 reference) on a bounded sample of the same workload instead.
+
+The "headmajor" workload runs the three layers per head over head-major
+[B, H, S, D] activations and upstream gradients read in place as
+[B, S, H, D] rows (the gbn_rows entry points), to compare with the sweep's
+contiguous rows of the same width (`--widths 128`).
 """
 from __future__ import annotations
 
@@ -39,6 +45,7 @@ METRIC = "fwd+bwd achieved HBM GB/s and % of GB300 8 TB/s roofline, per op and [
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
+HEAD_MAJOR = (8, 32, 8192, 128)  # B, H, S, D of the head-major workload (2^28 elements)
 
 
 # ------------------------------------------------------------------ helpers
@@ -170,6 +177,8 @@ class Point:
         inp = wl.inputs(device=dev)
         self.inp = inp
         self.x, self.dy = inp["x"], inp["dy"]
+        # contiguous storage behind x and dy (what a host copy fills)
+        self.xs, self.dys = inp.get("x_storage", self.x), inp.get("dy_storage", self.dy)
         E = M * N
         self.y = shared["y"][:E].view(M, N)
         self.dx = shared["dx"][:E].view(M, N)
@@ -188,7 +197,33 @@ class Point:
         s = torch.cuda.current_stream(dev).cuda_stream
         P = lambda t: None if t is None else t.data_ptr()  # noqa: E731
         X, DY, Y, DX = P(self.x), P(self.dy), P(self.y), P(self.dx)
-        if wl.op == "dyt":
+        if wl.lead is not None:
+            # rows read in place through gbn_rows layouts
+            self.layouts = [_lib.fold_rows(tuple(t.shape), tuple(t.stride()))
+                            for t in (self.x, self.dy)]
+            XL, DYL = (ctypes.byref(lay) for lay in self.layouts)
+            if wl.op == "dyt":
+                A, G, B = P(inp["alpha"]), P(inp["gamma"]), P(inp["beta"])
+                self.fwd_call = (lib.dyt_fwd_rows, (X, XL, A, G, B, Y, M, N, xt, pt, s))
+                self.bwd_call = (lib.dyt_bwd_rows, (X, XL, DY, DYL, A, G, DX, P(self.g3),
+                                                    P(self.g1), P(self.g2), M, N, xt, pt,
+                                                    P(self.ws), nws, s))
+            elif wl.op == "layernorm":
+                G, B = P(inp["gamma"]), P(inp["beta"])
+                self.fwd_call = (lib.layernorm_fwd_rows, (X, XL, G, B, Y, P(self.mean),
+                                                          P(self.rstd), M, N, wl.eps, xt, pt, s))
+                self.bwd_call = (lib.layernorm_bwd_rows, (X, XL, DY, DYL, P(self.mean),
+                                                          P(self.rstd), G, DX, P(self.g1),
+                                                          P(self.g2), M, N, xt, pt, P(self.ws),
+                                                          nws, s))
+            else:
+                W, v = P(inp["weight"]), rms_variant
+                self.fwd_call = (lib.rmsnorm_fwd_rows, (X, XL, W, Y, P(self.rstd), M, N, wl.eps,
+                                                        xt, pt, v, s))
+                self.bwd_call = (lib.rmsnorm_bwd_rows, (X, XL, DY, DYL, W, P(self.rstd), DX,
+                                                        P(self.g1), M, N, wl.eps, xt, pt, v,
+                                                        P(self.ws), nws, s))
+        elif wl.op == "dyt":
             A, G, B = P(inp["alpha"]), P(inp["gamma"]), P(inp["beta"])
             self.fwd_call = (lib.dyt_fwd, (X, A, G, B, Y, M, N, xt, pt, s))
             self.bwd_call = (lib.dyt_bwd, (X, DY, A, G, DX, P(self.g3), P(self.g1), P(self.g2), M,
@@ -245,6 +280,12 @@ def workloads(name, ops=None, widths=None):
                if (not ops or w.op in ops) and (not widths or w.N in widths)]
         return pts, (f"{name}: DyT, LayerNorm, RMSNorm fwd+bwd, {str(xd)[6:]} x, fp32 params, "
                      "N in {16..8192}, M = 2^28 // N")
+    if name == "headmajor":
+        B, H, S, D = HEAD_MAJOR
+        pts = [synth.head_major(op, B, H, S, D) for op in ("dyt", "layernorm", "rmsnorm")
+               if not ops or op in ops]
+        return pts, (f"headmajor: DyT, LayerNorm, RMSNorm fwd+bwd per head over head-major bf16 "
+                     f"[B={B}, H={H}, S={S}, D={D}] read in place as [B, S, H, D], fp32 params")
     table = {w.name: w for w in (synth.DYT_F32_SMALL, synth.LN_BWD_TALL, synth.DYT_BF16_TALL,
                                  synth.RMS_BF16)}
     if name not in table:
@@ -463,8 +504,8 @@ def run_e2e(lib, points, dev, shared, steps, world):
     hdx = torch.empty(maxE, dtype=dtype, pin_memory=True)
     # the host inputs are one point's inputs (values do not affect timing)
     p0 = max(points, key=lambda p: p.wl.M * p.wl.N)
-    hx[: p0.x.numel()].copy_(p0.x.view(-1))
-    hdy[: p0.dy.numel()].copy_(p0.dy.view(-1))
+    hx[: p0.x.numel()].copy_(p0.xs.view(-1))
+    hdy[: p0.dy.numel()].copy_(p0.dys.view(-1))
     stream = torch.cuda.current_stream(dev)
     h2d = d2h = 0
     for p in points:
@@ -477,8 +518,8 @@ def run_e2e(lib, points, dev, shared, steps, world):
     for _ in range(steps):
         for p in points:
             E = p.wl.M * p.wl.N
-            p.x.view(-1).copy_(hx[:E], non_blocking=True)
-            p.dy.view(-1).copy_(hdy[:E], non_blocking=True)
+            p.xs.view(-1).copy_(hx[:E], non_blocking=True)
+            p.dys.view(-1).copy_(hdy[:E], non_blocking=True)
             p.run()
             if p.fwd_enabled:
                 hy[:E].copy_(p.y.reshape(-1), non_blocking=True)
@@ -511,9 +552,10 @@ def oracle_sample(wls, target_elems):
         inp = sw.inputs(device="cpu")
 
         def arr(t):
+            t = t.contiguous().reshape(-1, t.shape[-1])
             if t.dtype == torch.bfloat16:
-                return t.contiguous().view(torch.int16).numpy().view(np.uint16)
-            return t.contiguous().numpy()  # float32 and float16 directly
+                return t.view(torch.int16).numpy().view(np.uint16)
+            return t.numpy()  # float32 and float16 directly
         x, dy = arr(inp["x"]), arr(inp["dy"])
         t0 = time.perf_counter()
         if w.op == "dyt":

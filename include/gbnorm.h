@@ -180,6 +180,56 @@ int rmsnorm_bwd_ex(const void* x, const void* dy, const void* w, const float* rs
                    void* dw, int64_t M, int64_t N, float eps, int xt, int wt, int variant,
                    void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Row layouts of the inputs.
+ *   DeepSpeed PR 8645 ("fused RMSNorm", section "Where the kernels run",
+ *   row "Layout") takes any leading shape and copies a non-contiguous input
+ *   before its kernels run; its tests (section "Correctness evidence", 1)
+ *   feed a head-major input and the head-major upstream gradient that
+ *   attention produces.  The *_rows entry points below read such inputs in
+ *   place instead of copying them.
+ * gbn_rows describes where the M rows of an input lie, in ELEMENTS of the
+ *   activation dtype from the input's pointer: row r starts at
+ *     (r % n1) * s1 + ((r / n1) % n2) * s2 + (r / (n1 * n2)) * s3
+ *   and its N elements are contiguous.  That covers every tensor of up to
+ *   four dimensions whose last stride is 1 ([B, S, H, D] viewed as M = B*S*H
+ *   rows of D with n1 = H, n2 = S: s1, s2, s3 its H, S and B strides; the
+ *   head-major [B, H, S, D] transposed to [B, S, H, D] is one such tensor).
+ *   n1, n2 >= 1 and s1, s2, s3 >= 0, else GBN_EINVAL.  Rows may overlap
+ *   (broadcast strides of 0 are allowed); the outputs (y, dx, the statistics)
+ *   stay contiguous [M, N] and must not overlap any input.
+ * A null layout means contiguous rows (row r at r * N), so the *_rows entry
+ *   points with null layouts are the plain entry points.  A layout that
+ *   happens to describe contiguous rows is treated as null.  Otherwise the
+ *   vector path needs the input pointer and s1, s2, s3 times the element size
+ *   to be multiples of 16 bytes (besides the contiguous conditions above);
+ *   other layouts take the general path.  Results do not depend on the layout:
+ *   the same rows give the same bits as a contiguous copy of them would. */
+typedef struct {
+    int64_t n1, s1, n2, s2, s3;
+} gbn_rows;
+
+int dyt_fwd_rows(const void* x, const gbn_rows* xl, const void* alpha, const void* gamma,
+                 const void* beta, void* y, int64_t M, int64_t N, int xt, int pt,
+                 cudaStream_t stream);
+int dyt_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gbn_rows* dyl,
+                 const void* alpha, const void* gamma, void* dx, void* dalpha, void* dgamma,
+                 void* dbeta, int64_t M, int64_t N, int xt, int pt, void* ws, size_t ws_bytes,
+                 cudaStream_t stream);
+int layernorm_fwd_rows(const void* x, const gbn_rows* xl, const void* gamma, const void* beta,
+                       void* y, float* mean, float* rstd, int64_t M, int64_t N, float eps, int xt,
+                       int pt, cudaStream_t stream);
+int layernorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gbn_rows* dyl,
+                       const float* mean, const float* rstd, const void* gamma, void* dx,
+                       void* dgamma, void* dbeta, int64_t M, int64_t N, int xt, int pt, void* ws,
+                       size_t ws_bytes, cudaStream_t stream);
+int rmsnorm_fwd_rows(const void* x, const gbn_rows* xl, const void* w, void* y, float* rstd,
+                     int64_t M, int64_t N, float eps, int xt, int wt, int variant,
+                     cudaStream_t stream);
+int rmsnorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gbn_rows* dyl,
+                     const void* w, const float* rstd, void* dx, void* dw, int64_t M, int64_t N,
+                     float eps, int xt, int wt, int variant, void* ws, size_t ws_bytes,
+                     cudaStream_t stream);
+
 /* rmsnorm_bwd_static_ws: rmsnorm_bwd without a caller workspace.  The pages
  *   have no counterpart; it exists for callers that cannot allocate device
  *   memory (a host program with no device allocator of its own, code under a

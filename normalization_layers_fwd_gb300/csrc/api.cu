@@ -183,6 +183,56 @@ __global__ void selftest_wait_kernel(unsigned* fault, long long limit, int* resu
     if (threadIdx.x == 0) *result = ok ? 1 : 0;
 }
 
+// Row layouts of the inputs (x, dy), null for contiguous rows.
+struct Inputs {
+    bool ok;         // every layout given is valid
+    bool vec_ok;     // every row start is 16-byte aligned (vector path possible)
+    int scattered;   // some input's rows are not at r * N
+    gbn::RowMaps maps;
+};
+
+// Whether layout l places row r at r * N for every r < M.
+bool contiguous_rows(const gbn_rows& l, int64_t M, int64_t N)
+{
+    if (M <= 1) return true;
+    if (l.s1 != N) return false;
+    if (M <= l.n1) return true;
+    if (l.s2 != l.n1 * N) return false;
+    if (M <= l.n1 * l.n2) return true;
+    return l.s3 == l.n1 * l.n2 * N;
+}
+
+Inputs input_layouts(const gbn_rows* xl, const gbn_rows* dyl, const void* x, const void* dy,
+                     int64_t M, int64_t N, int xt)
+{
+    Inputs in{};
+    in.ok = true;
+    in.vec_ok = true;
+    const int64_t e = elem_bytes(xt);
+    const gbn_rows* ls[2] = {xl, dyl};
+    const void* base[2] = {x, dy};
+    for (int t = 0; t < 2; ++t) {
+        gbn::RowMap& m = in.maps.m[t];
+        m = gbn::RowMap{M > 0 ? M : 1, N * e, 1, 0, 0};
+        const gbn_rows* l = ls[t];
+        if (!l) continue;
+        if (l->n1 < 1 || l->n2 < 1 || l->s1 < 0 || l->s2 < 0 || l->s3 < 0) {
+            in.ok = false;
+            continue;
+        }
+        if (contiguous_rows(*l, M, N)) continue;
+        // Levels beyond the M rows change no row offset; capping them keeps
+        // n1 * n2 <= 2 M in the kernels' index arithmetic.
+        const int64_t n1 = l->n1 < M ? l->n1 : M;
+        const int64_t q = (M + n1 - 1) / n1;
+        const int64_t n2 = l->n2 < q ? l->n2 : q;
+        m = gbn::RowMap{n1, l->s1 * e, n2, l->s2 * e, l->s3 * e};
+        in.scattered = 1;
+        if (!aligned16(base[t]) || (m.s1 | m.s2 | m.s3) % 16 != 0) in.vec_ok = false;
+    }
+    return in;
+}
+
 }  // namespace
 
 extern "C" {
@@ -248,19 +298,24 @@ size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int
 }
 
 // ---------------------------------------------------------------------- DyT
-int dyt_fwd(const void* x, const void* alpha, const void* gamma, const void* beta, void* y,
-            int64_t M, int64_t N, int xt, int pt, cudaStream_t stream)
+int dyt_fwd_rows(const void* x, const gbn_rows* xl, const void* alpha, const void* gamma,
+                 const void* beta, void* y, int64_t M, int64_t N, int xt, int pt,
+                 cudaStream_t stream)
 {
     if (!dtype_ok(xt) || !dtype_ok(pt)) return GBN_EDTYPE;
     if (!shape_ok(M, N) || !alpha || !gamma || !beta) return GBN_EINVAL;
     if (M > 0 && (!x || !y)) return GBN_EINVAL;
     if (!all_aligned(xt, {x, y}) || !all_aligned(pt, {alpha, gamma, beta})) return GBN_EINVAL;
+    const Inputs in = input_layouts(xl, nullptr, x, nullptr, M, N, xt);
+    if (!in.ok) return GBN_EINVAL;
     if (M == 0) return GBN_OK;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream, gbn::kFwdDyT,
-                    kWide12 | kWide13);
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
+                    gbn::kFwdDyT, kWide12 | kWide13);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
+    L.scattered = in.scattered;
+    L.maps = in.maps;
     if (!L.fast) {  // elementwise general path: one thread per element, grid-stride
         const int64_t E = M * N;
         const int64_t blocks = (E + gbn::kGenThreads - 1) / gbn::kGenThreads;
@@ -270,9 +325,16 @@ int dyt_fwd(const void* x, const void* alpha, const void* gamma, const void* bet
     return launch_status(gbn::launch_dyt_fwd(L, xt, pt, x, alpha, gamma, beta, y, M, (int)N));
 }
 
-int dyt_bwd(const void* x, const void* dy, const void* alpha, const void* gamma, void* dx,
-            void* dalpha, void* dgamma, void* dbeta, int64_t M, int64_t N, int xt, int pt,
-            void* ws, size_t ws_bytes, cudaStream_t stream)
+int dyt_fwd(const void* x, const void* alpha, const void* gamma, const void* beta, void* y,
+            int64_t M, int64_t N, int xt, int pt, cudaStream_t stream)
+{
+    return dyt_fwd_rows(x, nullptr, alpha, gamma, beta, y, M, N, xt, pt, stream);
+}
+
+int dyt_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gbn_rows* dyl,
+                 const void* alpha, const void* gamma, void* dx, void* dalpha, void* dgamma,
+                 void* dbeta, int64_t M, int64_t N, int xt, int pt, void* ws, size_t ws_bytes,
+                 cudaStream_t stream)
 {
     if (!dtype_ok(xt) || !dtype_ok(pt)) return GBN_EDTYPE;
     if (!shape_ok(M, N) || !alpha || !gamma) return GBN_EINVAL;
@@ -281,11 +343,15 @@ int dyt_bwd(const void* x, const void* dy, const void* alpha, const void* gamma,
         return GBN_EINVAL;
     const bool grads = dalpha || dgamma || dbeta;
     if (grads && ws && !aligned4(ws)) return GBN_EINVAL;
+    const Inputs in = input_layouts(xl, dyl, x, dy, M, N, xt);
+    if (!in.ok) return GBN_EINVAL;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                    gbn::kBwdDyT, kWide12);
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
+                    stream, gbn::kBwdDyT, kWide12);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
+    L.scattered = in.scattered;
+    L.maps = in.maps;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_DYT, L, N))) return GBN_EWORKSPACE;
     float* wsf = grads ? static_cast<float*>(ws) : nullptr;
     if (M > 0) {
@@ -296,10 +362,18 @@ int dyt_bwd(const void* x, const void* dy, const void* alpha, const void* gamma,
     return finish_bwd(stream, wsf, M > 0 ? L.P : 0, GBN_OP_DYT, N, pt, dgamma, dbeta, dalpha);
 }
 
+int dyt_bwd(const void* x, const void* dy, const void* alpha, const void* gamma, void* dx,
+            void* dalpha, void* dgamma, void* dbeta, int64_t M, int64_t N, int xt, int pt,
+            void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    return dyt_bwd_rows(x, nullptr, dy, nullptr, alpha, gamma, dx, dalpha, dgamma, dbeta, M, N,
+                        xt, pt, ws, ws_bytes, stream);
+}
+
 // ---------------------------------------------------------------- LayerNorm
-int layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean,
-                  float* rstd, int64_t M, int64_t N, float eps, int xt, int pt,
-                  cudaStream_t stream)
+int layernorm_fwd_rows(const void* x, const gbn_rows* xl, const void* gamma, const void* beta,
+                       void* y, float* mean, float* rstd, int64_t M, int64_t N, float eps, int xt,
+                       int pt, cudaStream_t stream)
 {
     if (!dtype_ok(xt) || !dtype_ok(pt)) return GBN_EDTYPE;
     if (!shape_ok(M, N) || !eps_ok(eps)) return GBN_EINVAL;
@@ -307,19 +381,31 @@ int layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, f
     if (!all_aligned(xt, {x, y}) || !all_aligned(pt, {gamma, beta}) ||
         !all_aligned(GBN_F32, {mean, rstd}))
         return GBN_EINVAL;
+    const Inputs in = input_layouts(xl, nullptr, x, nullptr, M, N, xt);
+    if (!in.ok) return GBN_EINVAL;
     if (M == 0) return GBN_OK;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream,
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
                     gbn::kFwdLN, kWide12 | kWide13);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
+    L.scattered = in.scattered;
+    L.maps = in.maps;
     return launch_status(
         gbn::launch_ln_fwd(L, xt, pt, x, gamma, beta, y, mean, rstd, M, (int)N, eps));
 }
 
-int layernorm_bwd(const void* x, const void* dy, const float* mean, const float* rstd,
-                  const void* gamma, void* dx, void* dgamma, void* dbeta, int64_t M, int64_t N,
-                  int xt, int pt, void* ws, size_t ws_bytes, cudaStream_t stream)
+int layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, float* mean,
+                  float* rstd, int64_t M, int64_t N, float eps, int xt, int pt,
+                  cudaStream_t stream)
+{
+    return layernorm_fwd_rows(x, nullptr, gamma, beta, y, mean, rstd, M, N, eps, xt, pt, stream);
+}
+
+int layernorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gbn_rows* dyl,
+                       const float* mean, const float* rstd, const void* gamma, void* dx,
+                       void* dgamma, void* dbeta, int64_t M, int64_t N, int xt, int pt, void* ws,
+                       size_t ws_bytes, cudaStream_t stream)
 {
     if (!dtype_ok(xt) || !dtype_ok(pt)) return GBN_EDTYPE;
     if (!shape_ok(M, N)) return GBN_EINVAL;
@@ -329,11 +415,15 @@ int layernorm_bwd(const void* x, const void* dy, const float* mean, const float*
         return GBN_EINVAL;
     const bool grads = dgamma || dbeta;
     if (grads && ws && !aligned4(ws)) return GBN_EINVAL;
+    const Inputs in = input_layouts(xl, dyl, x, dy, M, N, xt);
+    if (!in.ok) return GBN_EINVAL;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                    gbn::kBwdLN, kWide12 | kWide14);
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
+                    stream, gbn::kBwdLN, kWide12 | kWide14);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
+    L.scattered = in.scattered;
+    L.maps = in.maps;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_LAYERNORM, L, N)))
         return GBN_EWORKSPACE;
     float* wsf = grads ? static_cast<float*>(ws) : nullptr;
@@ -344,6 +434,14 @@ int layernorm_bwd(const void* x, const void* dy, const float* mean, const float*
     }
     return finish_bwd(stream, wsf, M > 0 ? L.P : 0, GBN_OP_LAYERNORM, N, pt, dgamma, dbeta,
                       nullptr);
+}
+
+int layernorm_bwd(const void* x, const void* dy, const float* mean, const float* rstd,
+                  const void* gamma, void* dx, void* dgamma, void* dbeta, int64_t M, int64_t N,
+                  int xt, int pt, void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    return layernorm_bwd_rows(x, nullptr, dy, nullptr, mean, rstd, gamma, dx, dgamma, dbeta, M, N,
+                              xt, pt, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------ RMSNorm
@@ -360,8 +458,9 @@ bool rms_dtypes_ok(int xt, int wt, int variant)
 
 bool rms_variant_ok(int v) { return v >= GBN_RMS_CAST_FIRST && v <= GBN_RMS_GEMMA; }
 
-int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
-                   float eps, int xt, int wt, int variant, cudaStream_t stream)
+int rmsnorm_fwd_rows(const void* x, const gbn_rows* xl, const void* w, void* y, float* rstd,
+                     int64_t M, int64_t N, float eps, int xt, int wt, int variant,
+                     cudaStream_t stream)
 {
     if (!rms_variant_ok(variant)) return GBN_EINVAL;
     if (!rms_dtypes_ok(xt, wt, variant)) return GBN_EDTYPE;
@@ -369,18 +468,29 @@ int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M
     if (M > 0 && (!x || !y)) return GBN_EINVAL;
     if (!all_aligned(xt, {x, y}) || !all_aligned(wt, {w}) || !all_aligned(GBN_F32, {rstd}))
         return GBN_EINVAL;
+    const Inputs in = input_layouts(xl, nullptr, x, nullptr, M, N, xt);
+    if (!in.ok) return GBN_EINVAL;
     if (M == 0) return GBN_OK;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y), sms, stream,
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
                     gbn::kFwdNorm, kWide12);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
+    L.scattered = in.scattered;
+    L.maps = in.maps;
     return launch_status(gbn::launch_rms_fwd(L, xt, wt, x, w, y, rstd, M, (int)N, eps, variant));
 }
 
-int rmsnorm_bwd_ex(const void* x, const void* dy, const void* w, const float* rstd, void* dx,
-                   void* dw, int64_t M, int64_t N, float eps, int xt, int wt, int variant,
-                   void* ws, size_t ws_bytes, cudaStream_t stream)
+int rmsnorm_fwd_ex(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,
+                   float eps, int xt, int wt, int variant, cudaStream_t stream)
+{
+    return rmsnorm_fwd_rows(x, nullptr, w, y, rstd, M, N, eps, xt, wt, variant, stream);
+}
+
+int rmsnorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gbn_rows* dyl,
+                     const void* w, const float* rstd, void* dx, void* dw, int64_t M, int64_t N,
+                     float eps, int xt, int wt, int variant, void* ws, size_t ws_bytes,
+                     cudaStream_t stream)
 {
     if (!rms_variant_ok(variant)) return GBN_EINVAL;
     if (!rms_dtypes_ok(xt, wt, variant)) return GBN_EDTYPE;
@@ -389,11 +499,15 @@ int rmsnorm_bwd_ex(const void* x, const void* dy, const void* w, const float* rs
     if (!all_aligned(xt, {x, dy, dx}) || !all_aligned(wt, {w, dw}) || !all_aligned(GBN_F32, {rstd}))
         return GBN_EINVAL;
     if (dw && ws && !aligned4(ws)) return GBN_EINVAL;
+    const Inputs in = input_layouts(xl, dyl, x, dy, M, N, xt);
+    if (!in.ok) return GBN_EINVAL;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
-    Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx), sms, stream,
-                    gbn::kBwdRms, kWide12);
+    Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
+                    stream, gbn::kBwdRms, kWide12);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
+    L.scattered = in.scattered;
+    L.maps = in.maps;
     if (dw && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_RMSNORM, L, N))) return GBN_EWORKSPACE;
     float* wsf = dw ? static_cast<float*>(ws) : nullptr;
     if (M > 0) {
@@ -402,6 +516,14 @@ int rmsnorm_bwd_ex(const void* x, const void* dy, const void* w, const float* rs
         if (rc != GBN_OK) return rc;
     }
     return finish_bwd(stream, wsf, M > 0 ? L.P : 0, GBN_OP_RMSNORM, N, wt, dw, nullptr, nullptr);
+}
+
+int rmsnorm_bwd_ex(const void* x, const void* dy, const void* w, const float* rstd, void* dx,
+                   void* dw, int64_t M, int64_t N, float eps, int xt, int wt, int variant,
+                   void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    return rmsnorm_bwd_rows(x, nullptr, dy, nullptr, w, rstd, dx, dw, M, N, eps, xt, wt, variant,
+                            ws, ws_bytes, stream);
 }
 
 int rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N,

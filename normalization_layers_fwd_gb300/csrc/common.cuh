@@ -14,6 +14,8 @@
 
 #include <type_traits>
 
+#include "internal.h"
+
 namespace gbn {
 
 enum DType : int { kF32 = 0, kBF16 = 1, kF16 = 2 };
@@ -353,15 +355,41 @@ __device__ __forceinline__ uint4 lds128_if(bool ok, const unsigned char* p)
     return ok ? lds128(p) : make_uint4(0, 0, 0, 0);
 }
 
+// Where each row of a non-contiguous input starts: row r begins at byte
+//   (r % n1) * s1 + ((r / n1) % n2) * s2 + (r / (n1 * n2)) * s3
+// from the tensor's base (the row itself is contiguous).  A row stride is
+// (n1 = M, s1 = stride); a head-major [B, S, H, D] view of [B, H, S, D]
+// storage, rows ordered (b, s, h), is (H, S*D*e, S, D*e, H*S*D*e), e the
+// element size.
+__device__ __forceinline__ int64_t row_byte_offset(const RowMap& m, int64_t r)
+{
+    const int64_t q = r / m.n1;
+    return (r - q * m.n1) * m.s1 + (q % m.n2) * m.s2 + (q / m.n2) * m.s3;
+}
+
+// Row r of input t (0: x, 1: dy) for the general kernels: r * N elements
+// in, or where the row map puts it.
+template <typename TX>
+__device__ __forceinline__ const TX* in_row(const TX* base, const RowMaps& maps, int t,
+                                            int scattered, int64_t r, int N)
+{
+    if (!scattered) return base + r * N;
+    return reinterpret_cast<const TX*>(reinterpret_cast<const unsigned char*>(base) +
+                                       row_byte_offset(maps.m[t], r));
+}
+
 // The ring of one CTA.  NT staged tensors, each row `row_bytes` long; row
 // block b covers rows [b*R, min(b*R + R, M)).  Blocks b = blockIdx.x +
-// k*gridDim.x, k = 0..K-1, belong to this CTA.
-template <int NT, int kStages>
+// k*gridDim.x, k = 0..K-1, belong to this CTA.  With kRows the tensors'
+// rows are scattered (map[t]): warp 0 issues one bulk copy per row, and the
+// slot still holds the block's rows back to back.
+template <int NT, int kStages, bool kRows = false>
 struct Ring {
     uint64_t* bar;             // [kStages]
     unsigned char* buf;        // [kStages][NT][slot]
     uint32_t slot;             // bytes per tensor per slot
     const unsigned char* src[NT];
+    RowMap map[kRows ? NT : 1];
     int64_t row_bytes, R, M, nblocks;
     unsigned* fault;
 
@@ -374,25 +402,40 @@ struct Ring {
     {
         return buf + ((k % kStages) * NT + t) * (size_t)slot;
     }
-    // thread 0 only
+    // contiguous rows: thread 0 only; kRows: every lane of warp 0
     __device__ void issue(int64_t k)
     {
         const int s = (int)(k % kStages);
         const int64_t r0 = block(k) * R;
         const int64_t rows = (M - r0) < R ? (M - r0) : R;
         const uint32_t bytes = (uint32_t)(rows * row_bytes);
-        mbar_expect_tx(&bar[s], NT * bytes);
+        if constexpr (!kRows) {
+            mbar_expect_tx(&bar[s], NT * bytes);
 #pragma unroll
-        for (int t = 0; t < NT; ++t)
-            bulk_g2s(buf + (s * NT + t) * (size_t)slot, src[t] + r0 * row_bytes, bytes, &bar[s]);
+            for (int t = 0; t < NT; ++t)
+                bulk_g2s(buf + (s * NT + t) * (size_t)slot, src[t] + r0 * row_bytes, bytes,
+                         &bar[s]);
+        } else {
+            const int lane = threadIdx.x & 31;
+            if (lane == 0) mbar_expect_tx(&bar[s], NT * bytes);
+            __syncwarp();  // the expected byte count is set before any copy lands
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+                for (int64_t i = lane; i < rows; i += 32)
+                    bulk_g2s(buf + (s * NT + t) * (size_t)slot + i * row_bytes,
+                             src[t] + row_byte_offset(map[t], r0 + i), (uint32_t)row_bytes,
+                             &bar[s]);
+        }
     }
+    __device__ bool issuer() const { return kRows ? threadIdx.x < 32 : threadIdx.x == 0; }
 };
 
 // Run `body(b, k, alive)` over this CTA's row blocks with the ring full
 // kStages deep.  `dsm` is the kernel's dynamic shared memory (128-byte
 // aligned).  Every thread makes the same calls (body may __syncthreads).
-template <int NT, int kStages, class Body>
-__device__ __forceinline__ void ring_loop(Ring<NT, kStages>& rg, unsigned char* dsm, Body&& body)
+template <int NT, int kStages, bool kRows, class Body>
+__device__ __forceinline__ void ring_loop(Ring<NT, kStages, kRows>& rg, unsigned char* dsm,
+                                          Body&& body)
 {
     rg.bar = reinterpret_cast<uint64_t*>(dsm);
     rg.buf = dsm + 128;
@@ -402,7 +445,7 @@ __device__ __forceinline__ void ring_loop(Ring<NT, kStages>& rg, unsigned char* 
         fence_mbar_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0)
+    if (rg.issuer())
         for (int64_t k = 0; k < K && k < kStages; ++k) rg.issue(k);
     bool alive = true;
     int64_t failed_at = K;
@@ -413,7 +456,7 @@ __device__ __forceinline__ void ring_loop(Ring<NT, kStages>& rg, unsigned char* 
         }
         body(rg.block(k), k, alive);
         __syncthreads();  // every thread is done with slot k % kStages
-        if (threadIdx.x == 0 && alive && k + kStages < K) {
+        if (rg.issuer() && alive && k + kStages < K) {
             fence_proxy_async();
             rg.issue(k + kStages);
         }

@@ -114,11 +114,11 @@ __device__ __forceinline__ void dyt_tanh_sech2_2(f2 z, f2& t, f2& s)
 // Addressing: a thread's vector of row u of a block sits at soff + u*srow in
 // the ring slot and at row0*N + l*VEC + u*grow in HBM (row0 = the block's
 // first row + g); only the ragged last block compares rows against M.
-template <typename TX, int S>
+template <typename TX, int S, bool kRows>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
     dyt_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ alpha,
                  const void* __restrict__ gamma, const void* __restrict__ beta, int pt,
-                 int64_t M, int N, int64_t nblocks, unsigned* fault)
+                 int64_t M, int N, int64_t nblocks, unsigned* fault, RowMaps maps)
 {
     constexpr int W = kSched[S].W, U = kind_U(S, kFwdDyT), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
@@ -144,8 +144,9 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
         }
     }
 
-    Ring<1, kind_stages(S, kFwdDyT)> rg;
+    Ring<1, kind_stages(S, kFwdDyT), kRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    if constexpr (kRows) rg.map[0] = maps.m[0];
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
@@ -182,11 +183,11 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
 // x and dy stream through the ring.  Full row blocks run without masking;
 // only the ragged last block masks its padded rows, by a select after the
 // arithmetic (its slots past the last row hold stale data).
-template <typename TX, int S>
+template <typename TX, int S, bool kRows>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     dyt_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy, TX* __restrict__ dx,
                  const void* __restrict__ alpha, const void* __restrict__ gamma, int pt,
-                 float* __restrict__ ws, int64_t M, int N, int64_t nblocks, unsigned* fault)
+                 float* __restrict__ ws, int64_t M, int N, int64_t nblocks, unsigned* fault, RowMaps maps)
 {
     constexpr int W = kSched[S].W, U = kind_U(S, kBwdDyT), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
@@ -259,9 +260,13 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
         }
     };
 
-    Ring<2, kind_stages(S, kBwdDyT)> rg;
+    Ring<2, kind_stages(S, kBwdDyT), kRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
+    if constexpr (kRows) {
+        rg.map[0] = maps.m[0];
+        rg.map[1] = maps.m[1];
+    }
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
@@ -311,14 +316,15 @@ template <typename TX>
 __global__ void __launch_bounds__(kGenThreads)
     dyt_fwd_general(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ alpha,
                     const void* __restrict__ gamma, const void* __restrict__ beta, int pt,
-                    int64_t M, int N)
+                    int64_t M, int N, RowMaps maps, int scattered)
 {
     const float a = ld_param(alpha, pt, 0);
     const int64_t E = M * (int64_t)N;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < E;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int c = (int)(i % N);
-        st1(y, i, fmaf(ld_param(gamma, pt, c), dyt_tanh(a * ld1(x, i)), ld_param(beta, pt, c)));
+        const float xv = scattered ? ld1(in_row(x, maps, 0, 1, i / N, N), c) : ld1(x, i);
+        st1(y, i, fmaf(ld_param(gamma, pt, c), dyt_tanh(a * xv), ld_param(beta, pt, c)));
     }
 }
 
@@ -328,7 +334,7 @@ template <typename TX>
 __global__ void __launch_bounds__(kGenThreads)
     dyt_bwd_general(const TX* __restrict__ x, const TX* __restrict__ dy, TX* __restrict__ dx,
                     const void* __restrict__ alpha, const void* __restrict__ gamma, int pt,
-                    float* __restrict__ ws, int64_t M, int N)
+                    float* __restrict__ ws, int64_t M, int N, RowMaps maps, int scattered)
 {
     const int lane = threadIdx.x & 31;
     const int64_t w = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5);
@@ -340,9 +346,11 @@ __global__ void __launch_bounds__(kGenThreads)
     const float a = ld_param(alpha, pt, 0);
     float da = 0.f;
     for (int64_t r = w; r < M; r += nw) {
+        const TX* xr = in_row(x, maps, 0, scattered, r, N);
+        const TX* dr = in_row(dy, maps, 1, scattered, r, N);
         for (int c = lane; c < N; c += 32) {
             const int64_t i = r * N + c;
-            const float xv = ld1(x, i), dv = ld1(dy, i), gmv = ld_param(gamma, pt, c);
+            const float xv = ld1(xr, c), dv = ld1(dr, c), gmv = ld_param(gamma, pt, c);
             float t, s;
             dyt_tanh_sech2(a * xv, t, s);
             const float ds = dv * s;
@@ -367,17 +375,22 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* alp
     TX* yp = static_cast<TX*>(y);
     if (!L.fast) {
         dyt_fwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, yp, alpha, gamma, beta, pt,
-                                                                  M, N);
+                                                                  M, N, L.maps, L.scattered);
         return cudaGetLastError();
     }
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
         constexpr int smem = ring_smem_bytes(S, kFwdDyT, 1);                                   \
-        auto kern = dyt_fwd_fast<TX, S>;                                                     \
-        ring_attributes<dyt_fwd_fast<TX, S>>(smem);                                                         \
-        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, alpha, gamma, beta, pt, M, N, \
-                                                       L.nblocks, L.fault);                  \
+        if (L.scattered) {                                                                         \
+            ring_attributes<dyt_fwd_fast<TX, S, true>>(smem);                                      \
+            dyt_fwd_fast<TX, S, true><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
+                xp, yp, alpha, gamma, beta, pt, M, N, L.nblocks, L.fault, L.maps);                 \
+        } else {                                                                                   \
+            ring_attributes<dyt_fwd_fast<TX, S, false>>(smem);                                     \
+            dyt_fwd_fast<TX, S, false><<<L.grid, kSched[S].T, smem, L.stream>>>(                   \
+                xp, yp, alpha, gamma, beta, pt, M, N, L.nblocks, L.fault, L.maps);                 \
+        }                                                                                          \
         break;                                                                               \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
@@ -398,17 +411,22 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     TX* dxp = static_cast<TX*>(dx);
     if (!L.fast) {
         dyt_bwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, dyp, dxp, alpha, gamma, pt,
-                                                                  ws, M, N);
+                                                                  ws, M, N, L.maps, L.scattered);
         return cudaGetLastError();
     }
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
         constexpr int smem = ring_smem_bytes(S, kBwdDyT, 2);                                    \
-        auto kern = dyt_bwd_fast<TX, S>;                                                     \
-        ring_attributes<dyt_bwd_fast<TX, S>>(smem);                                                         \
-        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, dyp, dxp, alpha, gamma, pt, ws, M, \
-                                                       N, L.nblocks, L.fault);               \
+        if (L.scattered) {                                                                         \
+            ring_attributes<dyt_bwd_fast<TX, S, true>>(smem);                                      \
+            dyt_bwd_fast<TX, S, true><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
+                xp, dyp, dxp, alpha, gamma, pt, ws, M, N, L.nblocks, L.fault, L.maps);             \
+        } else {                                                                                   \
+            ring_attributes<dyt_bwd_fast<TX, S, false>>(smem);                                     \
+            dyt_bwd_fast<TX, S, false><<<L.grid, kSched[S].T, smem, L.stream>>>(                   \
+                xp, dyp, dxp, alpha, gamma, pt, ws, M, N, L.nblocks, L.fault, L.maps);             \
+        }                                                                                          \
         break;                                                                               \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)

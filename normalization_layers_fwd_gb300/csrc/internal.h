@@ -7,6 +7,16 @@
 
 namespace gbn {
 
+// Where each row of a non-contiguous input starts: row r begins at byte
+//   (r % n1) * s1 + ((r / n1) % n2) * s2 + (r / (n1 * n2)) * s3
+// from the tensor's base (the row itself is contiguous).
+struct RowMap {
+    int64_t n1, s1, n2, s2, s3;
+};
+struct RowMaps {
+    RowMap m[2];  // x, then dy
+};
+
 // How one call is laid out on the GPU.  Decided on the host from (M, N,
 // dtypes, pointer alignment, SM count) by a fixed table, never by runtime
 // tuning, so the same inputs always give the same summation order.
@@ -18,6 +28,8 @@ struct Launch {
     int64_t P;          // partial rows the backward writes into the workspace
     cudaStream_t stream;
     unsigned* fault;    // the device's fault word (bounded waits that ran out)
+    int scattered;      // 1: x (and dy) rows follow maps rather than r * N
+    RowMaps maps;
 };
 
 // Workspace row length (floats) per layer: the per-column partial sums of

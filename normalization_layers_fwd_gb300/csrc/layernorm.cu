@@ -25,12 +25,12 @@ namespace {
 // of squares) per row.  Every thread runs every row (row reductions are
 // collective); loads and stores are predicated, and only the ragged last
 // block compares rows against M.
-template <typename TX, int S>
+template <typename TX, int S, bool kRows>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
     ln_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ gamma,
                 const void* __restrict__ beta, int pt, float* __restrict__ mean,
                 float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
-                int64_t nblocks, unsigned* fault)
+                int64_t nblocks, unsigned* fault, RowMaps maps)
 {
     constexpr int W = kSched[S].W, U = kind_U(S, kFwdLN), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
@@ -57,8 +57,9 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
         }
     }
 
-    Ring<1, kind_stages(S, kFwdLN)> rg;
+    Ring<1, kind_stages(S, kFwdLN), kRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    if constexpr (kRows) rg.map[0] = maps.m[0];
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
@@ -134,13 +135,13 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
 // block are prefetched into registers while the current one is processed.
 // Full row blocks run without masking; the ragged last block masks its
 // padded rows by a select after the arithmetic.
-template <typename TX, int S>
+template <typename TX, int S, bool kRows>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     ln_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy,
                 const float* __restrict__ mean, const float* __restrict__ rstd,
                 const void* __restrict__ gamma, int pt, TX* __restrict__ dx,
                 float* __restrict__ ws, int64_t M, int N, float inv_n, int64_t nblocks,
-                unsigned* fault)
+                unsigned* fault, RowMaps maps)
 {
     constexpr int W = kSched[S].W, U = kind_U(S, kBwdLN), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
@@ -247,9 +248,13 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
         }
     };
 
-    Ring<2, kind_stages(S, kBwdLN)> rg;
+    Ring<2, kind_stages(S, kBwdLN), kRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
+    if constexpr (kRows) {
+        rg.map[0] = maps.m[0];
+        rg.map[1] = maps.m[1];
+    }
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
@@ -284,12 +289,12 @@ template <typename TX>
 __global__ void __launch_bounds__(kGenThreads)
     ln_fwd_general(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ gamma,
                    const void* __restrict__ beta, int pt, float* __restrict__ mean,
-                   float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n)
+                   float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n, RowMaps maps, int scattered)
 {
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * kGenWarps;
     for (int64_t r = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5); r < M; r += nw) {
-        const TX* xr = x + r * N;
+        const TX* xr = in_row(x, maps, 0, scattered, r, N);
         float v[1] = {0.f};
         for (int c = lane; c < N; c += 32) v[0] += ld1(xr, c);
         butterfly<32, 1>(v);
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(kGenThreads)
     ln_bwd_general(const TX* __restrict__ x, const TX* __restrict__ dy,
                    const float* __restrict__ mean, const float* __restrict__ rstd,
                    const void* __restrict__ gamma, int pt, TX* __restrict__ dx,
-                   float* __restrict__ ws, int64_t M, int N, float inv_n)
+                   float* __restrict__ ws, int64_t M, int N, float inv_n, RowMaps maps, int scattered)
 {
     const int lane = threadIdx.x & 31;
     const int64_t w = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5);
@@ -327,8 +332,8 @@ __global__ void __launch_bounds__(kGenThreads)
     if (wrow)
         for (int c = lane; c < 2 * N; c += 32) wrow[c] = 0.f;
     for (int64_t r = w; r < M; r += nw) {
-        const TX* xr = x + r * N;
-        const TX* dr = dy + r * N;
+        const TX* xr = in_row(x, maps, 0, scattered, r, N);
+        const TX* dr = in_row(dy, maps, 1, scattered, r, N);
         const float mu = mean[r], rs = rstd[r];
         float s[2] = {0.f, 0.f};
         for (int c = lane; c < N; c += 32) {
@@ -362,16 +367,22 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
     const float inv_n = (float)(1.0 / (double)N);
     if (!L.fast) {
         ln_fwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, yp, gamma, beta, pt, mean,
-                                                                 rstd, M, N, eps, inv_n);
+                                                                 rstd, M, N, eps, inv_n, L.maps, L.scattered);
         return cudaGetLastError();
     }
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
         constexpr int smem = ring_smem_bytes(S, kFwdLN, 1);                                    \
-        auto kern = ln_fwd_fast<TX, S>;                                                      \
-        ring_attributes<ln_fwd_fast<TX, S>>(smem);                                                         \
-        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault);                              \
+        if (L.scattered) {                                                                         \
+            ring_attributes<ln_fwd_fast<TX, S, true>>(smem);                                       \
+            ln_fwd_fast<TX, S, true><<<L.grid, kSched[S].T, smem, L.stream>>>(                     \
+                xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault, L.maps);\
+        } else {                                                                                   \
+            ring_attributes<ln_fwd_fast<TX, S, false>>(smem);                                      \
+            ln_fwd_fast<TX, S, false><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
+                xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault, L.maps);\
+        }                                                                                          \
         break;                                                                               \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
@@ -394,16 +405,22 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     const float inv_n = (float)(1.0 / (double)N);
     if (!L.fast) {
         ln_bwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, dyp, mean, rstd, gamma, pt,
-                                                                 dxp, ws, M, N, inv_n);
+                                                                 dxp, ws, M, N, inv_n, L.maps, L.scattered);
         return cudaGetLastError();
     }
     switch (L.sid) {
 #define GBN_CASE(S)                                                                          \
     case S: {                                                                                \
         constexpr int smem = ring_smem_bytes(S, kBwdLN, 2);                                  \
-        auto kern = ln_bwd_fast<TX, S>;                                                      \
-        ring_attributes<ln_bwd_fast<TX, S>>(smem);                                                         \
-        kern<<<L.grid, kSched[S].T, smem, L.stream>>>(xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.nblocks, L.fault);                              \
+        if (L.scattered) {                                                                         \
+            ring_attributes<ln_bwd_fast<TX, S, true>>(smem);                                       \
+            ln_bwd_fast<TX, S, true><<<L.grid, kSched[S].T, smem, L.stream>>>(                     \
+                xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.nblocks, L.fault, L.maps); \
+        } else {                                                                                   \
+            ring_attributes<ln_bwd_fast<TX, S, false>>(smem);                                      \
+            ln_bwd_fast<TX, S, false><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
+                xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.nblocks, L.fault, L.maps); \
+        }                                                                                          \
         break;                                                                               \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)

@@ -69,11 +69,14 @@ class Workload:
     alpha: float | None = None         # fixed DyT alpha; None: drawn from param_dist
     param_dist: dict = field(default_factory=dict)   # name -> (mean, std)
     bwd_only: bool = False
+    lead: tuple | None = None          # (B, H, S): x and dy head-major, seen as [B, S, H, N]
 
     def inputs(self, device="cpu") -> dict:
-        """x, dy and the parameters, all seeded."""
+        """x, dy and the parameters, all seeded.  With `lead`, x and dy are
+        [B, H, S, N] tensors transposed to [B, S, H, N] views (their storage
+        under "x_storage" and "dy_storage")."""
         s = lambda n: seed_for(self.index, f"{self.name}/{n}")  # noqa: E731
-        shape = (self.M, self.N)
+        shape = (self.M, self.N) if self.lead is None else (*self.lead, self.N)
         if self.outliers:
             frac, factor = self.outliers
             x = with_outliers(shape, frac, factor, self.xdtype, seed=s("x"), mask_seed=s("x_mask"),
@@ -81,6 +84,10 @@ class Workload:
         else:
             x = normal(shape, 0.0, self.x_std, self.xdtype, seed=s("x"), device=device)
         out = {"x": x, "dy": normal(shape, 0.0, 1.0, self.xdtype, seed=s("dy"), device=device)}
+        if self.lead is not None:
+            for k in ("x", "dy"):
+                out[k + "_storage"] = out[k]
+                out[k] = out[k].transpose(1, 2)
         for pname, (mu, sd) in self.param_dist.items():
             n = 1 if pname == "alpha" else self.N
             out[pname] = normal((n,), mu, sd, self.pdtype, seed=s(pname), device=device)
@@ -126,6 +133,17 @@ def sweep(op: str, N: int, xdtype: torch.dtype = torch.bfloat16) -> Workload:
                     param_dist=params)
 
 
+def head_major(op: str, B: int, H: int, S: int, D: int) -> Workload:
+    """Workload 6: per-head normalization of a head-major [B, H, S, D] bf16
+    activation read as [B, S, H, D] rows of D (the query/key norm of
+    DeepSpeed PR 8645, whose head-major inputs and upstream gradients come
+    straight from attention), fp32 parameters as in the sweep."""
+    w = sweep(op, D)
+    from dataclasses import replace
+    return replace(w, name=f"headmajor_{op}_{B}x{H}x{S}x{D}", index=6, M=B * H * S,
+                   lead=(B, H, S))
+
+
 def sweep_all(xdtype: torch.dtype = torch.bfloat16):
     return [sweep(op, n, xdtype) for n in SWEEP_WIDTHS for op in ("dyt", "layernorm", "rmsnorm")]
 
@@ -133,4 +151,4 @@ def sweep_all(xdtype: torch.dtype = torch.bfloat16):
 def scaled(w: Workload, M: int) -> Workload:
     """The same recipe with fewer rows (small parity cases)."""
     from dataclasses import replace
-    return replace(w, M=M, name=f"{w.name}@M{M}")
+    return replace(w, M=M, lead=None, name=f"{w.name}@M{M}")

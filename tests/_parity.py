@@ -40,8 +40,10 @@ MAX_EXCEPTION_FRAC = 1e-3
 # ------------------------------------------------------------ conversions
 
 def to_oracle(t: torch.Tensor) -> np.ndarray:
-    """Activation tensor -> the oracle's input array (exact)."""
+    """Activation tensor -> the oracle's input array (exact), [rows, N]."""
     t = t.detach().cpu().contiguous()
+    if t.dim() > 2:
+        t = t.reshape(-1, t.shape[-1])
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16).reshape(t.shape)
     if t.dtype in (torch.float32, torch.float16):

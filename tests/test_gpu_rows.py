@@ -1,0 +1,245 @@
+"""GPU: inputs read in place through row layouts (gbn_rows).
+
+DeepSpeed PR 8645 ("Where the kernels run", row "Layout") copies a
+non-contiguous input before its kernels run; its tests feed a head-major
+input and the head-major upstream gradient that attention produces
+("Correctness evidence", 1).  Here such inputs are read where they lie:
+
+* layouts whose rows start on 16-byte boundaries take the same vector
+  kernels and launch layout as a contiguous copy of the same rows, so every
+  output, parameter gradients included, must be bit-identical to the call on
+  the contiguous copy;
+* other layouts (odd strides, odd base offsets) take the general kernels and
+  are compared with the float64 oracle element by element.
+All calls go through the C ABI (the ctypes binding)."""
+import pytest
+import torch
+
+from _cases import dyt_case, layernorm_case, rmsnorm_case
+from normalization_layers_fwd_gb300 import _lib, synth
+from normalization_layers_fwd_gb300.functional import rms_norm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from normalization_layers_fwd_gb300 import build
+    build.build()
+    _lib.load()
+    return torch.device("cuda:0")
+
+
+def _normal(shape, dt, seed, mean=0.0, std=1.0):
+    return synth.normal(shape, mean, std, dt, seed=synth.seed_for(91, seed), device="cuda")
+
+
+def _params(N, pdt, seed):
+    return dict(alpha=_normal((1,), pdt, seed + "/a", 0.8, 0.1),
+                gamma=_normal((N,), pdt, seed + "/g", 1.0, 0.1),
+                beta=_normal((N,), pdt, seed + "/b", 0.0, 0.1))
+
+
+# ------------------------------------------------------------------ layouts
+# Each maker returns a view of logical shape [..., N] over fresh storage.
+
+def head_major(lead, N, dt, seed):
+    """[B, H, S, D] storage seen as [B, S, H, D] (lead = (B, S, H))."""
+    B, S, H = lead
+    return _normal((B, H, S, N), dt, seed).transpose(1, 2)
+
+
+def seq_major(lead, N, dt, seed):
+    """[S, B, H, D] storage seen as [B, S, H, D]."""
+    B, S, H = lead
+    return _normal((S, B, H, N), dt, seed).transpose(0, 1)
+
+
+def row_padded(lead, N, dt, seed, pad_bytes=16, offset=0):
+    """Rows of N inside rows of N + pad elements, starting at column offset."""
+    (M,) = lead
+    e = torch.empty((), dtype=dt).element_size()
+    pad = pad_bytes // e
+    return _normal((M, N + pad), dt, seed)[:, offset:offset + N]
+
+
+def broadcast(lead, N, dt, seed):
+    """One row repeated M times (row stride 0)."""
+    (M,) = lead
+    return _normal((1, N), dt, seed).expand(M, N)
+
+
+def _layout_is_vector(v):
+    """Whether the library will take the vector path for view v (16-byte
+    aligned base and row strides), given N * elem a multiple of 16."""
+    e = v.element_size()
+    lay = _lib.fold_rows(tuple(v.shape), tuple(v.stride()))
+    return (v.data_ptr() % 16 == 0 and lay is not None and
+            all((s * e) % 16 == 0 for s in (lay.s1, lay.s2, lay.s3)))
+
+
+# ---------------------------------------------------------------- the ops
+
+def _bits(t):
+    t = t.contiguous()
+    return t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)
+
+
+def run(op, x, dy, P, eps=1e-5):
+    if op == "dyt":
+        y = _lib.dyt_fwd(x, P["alpha"], P["gamma"], P["beta"])
+        dx, da, dg, db = _lib.dyt_bwd(x, dy, P["alpha"], P["gamma"])
+        return dict(y=y, dx=dx, da=da, dg=dg, db=db)
+    if op == "layernorm":
+        y, mean, rstd = _lib.layernorm_fwd(x, P["gamma"], P["beta"], eps)
+        dx, dg, db = _lib.layernorm_bwd(x, dy, mean, rstd, P["gamma"])
+        return dict(y=y, mean=mean, rstd=rstd, dx=dx, dg=dg, db=db)
+    y, rstd = _lib.rmsnorm_fwd(x, P["gamma"], eps)
+    dx, dw = _lib.rmsnorm_bwd(x, dy, P["gamma"], rstd, eps)
+    dx2, dw2 = _lib.rmsnorm_bwd(x, dy, P["gamma"], None, eps)
+    return dict(y=y, rstd=rstd, dx=dx, dw=dw, dx2=dx2, dw2=dw2)
+
+
+def assert_same_bits(a, b):
+    assert a.keys() == b.keys()
+    for k in a:
+        assert a[k].shape == b[k].shape, k
+        assert a[k].is_contiguous(), k
+        assert torch.equal(_bits(a[k]), _bits(b[k])), k
+
+
+OPS = ["dyt", "layernorm", "rmsnorm"]
+DT = [(torch.bfloat16, torch.bfloat16), (torch.float32, torch.float32),
+      (torch.float16, torch.float32)]
+DT_ID = ["bf16", "f32", "f16"]
+
+
+# ------------------------------------------------ vector layouts: bit-exact
+
+VECTOR_CASES = [
+    ("head_major", head_major, (2, 67, 8), 64),
+    ("head_major", head_major, (2, 33, 32), 128),
+    ("head_major", head_major, (1, 19, 4), 256),
+    ("seq_major", seq_major, (3, 21, 8), 128),
+    ("row_padded", row_padded, (1001,), 1024),
+    ("row_padded", row_padded, (601,), 4096),
+    ("row_padded", row_padded, (257,), 8192),
+    ("broadcast", broadcast, (517,), 128),
+]
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dts", DT, ids=DT_ID)
+@pytest.mark.parametrize("case", VECTOR_CASES, ids=lambda c: f"{c[0]}-N{c[3]}")
+def test_vector_layouts_match_contiguous_bits(op, dts, case):
+    name, make, lead, N = case
+    xdt, pdt = dts
+    seed = f"{op}/{name}/{N}/{xdt}"
+    x = make(lead, N, xdt, seed + "/x")
+    dy = make(lead, N, xdt, seed + "/dy")
+    assert not x.is_contiguous() and _layout_is_vector(x)
+    P = _params(N, pdt, seed)
+    got = run(op, x, dy, P)
+    want = run(op, x.contiguous(), dy.contiguous(), P)
+    torch.cuda.synchronize()
+    assert_same_bits(got, want)
+    assert _lib.read_faults() == 0
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_mixed_layouts_x_and_dy(op):
+    """x head-major and dy contiguous, and the other way round."""
+    lead, N = (2, 45, 16), 128
+    for xs, dys in ((True, False), (False, True)):
+        x = head_major(lead, N, torch.bfloat16, f"mix/{op}/x")
+        dy = head_major(lead, N, torch.bfloat16, f"mix/{op}/dy")
+        x = x if xs else x.contiguous()
+        dy = dy if dys else dy.contiguous()
+        P = _params(N, torch.float32, f"mix/{op}")
+        assert_same_bits(run(op, x, dy, P), run(op, x.contiguous(), dy.contiguous(), P))
+
+
+def test_persistent_loop_head_major():
+    """Enough rows that every CTA walks many row blocks through the ring."""
+    lead, N = (4, 520, 32), 128
+    for op in OPS:
+        x = head_major(lead, N, torch.bfloat16, f"pl/{op}/x")
+        dy = head_major(lead, N, torch.bfloat16, f"pl/{op}/dy")
+        P = _params(N, torch.bfloat16, f"pl/{op}")
+        assert_same_bits(run(op, x, dy, P), run(op, x.contiguous(), dy.contiguous(), P))
+
+
+def test_autograd_head_major_rms_norm():
+    lead, N = (2, 40, 16), 128
+    xv = head_major(lead, N, torch.bfloat16, "ag/x").requires_grad_(True)
+    w = _normal((N,), torch.bfloat16, "ag/w", 1.0, 0.1).requires_grad_(True)
+    dy = head_major(lead, N, torch.bfloat16, "ag/dy")
+    y = rms_norm(xv, w, 1e-6)
+    y.backward(dy)
+    xc = xv.detach().contiguous().requires_grad_(True)
+    wc = w.detach().clone().requires_grad_(True)
+    yc = rms_norm(xc, wc, 1e-6)
+    yc.backward(dy.contiguous())
+    assert torch.equal(_bits(y), _bits(yc))
+    assert torch.equal(_bits(xv.grad), _bits(xc.grad))
+    assert torch.equal(_bits(w.grad), _bits(wc.grad))
+
+
+# ------------------------------------------- general layouts: oracle parity
+
+GENERAL_CASES = [
+    ("odd_row_stride", lambda lead, N, dt, s: row_padded(lead, N, dt, s, pad_bytes=4), (999,),
+     128),
+    ("odd_base", lambda lead, N, dt, s: row_padded(lead, N, dt, s, offset=1), (777,), 256),
+    ("odd_stride_wide", lambda lead, N, dt, s: row_padded(lead, N, dt, s, pad_bytes=4), (301,),
+     4096),
+    ("head_major_odd_width", head_major, (2, 29, 8), 100),
+]
+
+
+def _case(op, x, dy, P, eps=1e-5):
+    if op == "dyt":
+        return dyt_case(x, dy, P["alpha"], P["gamma"], P["beta"])
+    if op == "layernorm":
+        return layernorm_case(x, dy, P["gamma"], P["beta"], eps)
+    return rmsnorm_case(x, dy, P["gamma"], eps)
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("dts", DT, ids=DT_ID)
+@pytest.mark.parametrize("case", GENERAL_CASES, ids=lambda c: c[0])
+def test_general_layouts_against_oracle(op, dts, case):
+    name, make, lead, N = case
+    xdt, pdt = dts
+    seed = f"gen/{op}/{name}/{xdt}"
+    x = make(lead, N, xdt, seed + "/x")
+    dy = make(lead, N, xdt, seed + "/dy")
+    assert not x.is_contiguous()
+    if name != "head_major_odd_width":  # (in f32 its rows are 400 bytes: vector path)
+        assert not _layout_is_vector(x)
+    reps, _ = _case(op, x, dy, _params(N, pdt, seed))
+    for r in reps:
+        print(r.line())
+    assert _lib.read_faults() == 0
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_head_major_against_oracle(op):
+    """The vector-path head-major case, checked against the oracle too."""
+    x = head_major((2, 37, 8), 128, torch.bfloat16, f"hmo/{op}/x")
+    dy = head_major((2, 37, 8), 128, torch.bfloat16, f"hmo/{op}/dy")
+    reps, _ = _case(op, x, dy, _params(128, torch.float32, f"hmo/{op}"))
+    for r in reps:
+        print(r.line())
+
+
+def test_more_than_three_levels_is_copied():
+    """A layout the C ABI cannot express is copied by the binding: same bits."""
+    base = _normal((2, 3, 2, 5, 64), torch.bfloat16, "l4/x")
+    x = base.permute(0, 2, 1, 3, 4)
+    assert _lib.fold_rows(tuple(x.shape), tuple(x.stride())) is None
+    P = _params(64, torch.float32, "l4")
+    dy = _normal(tuple(x.shape), torch.bfloat16, "l4/dy")
+    assert_same_bits(run("rmsnorm", x, dy, P), run("rmsnorm", x.contiguous(), dy, P))

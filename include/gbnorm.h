@@ -202,8 +202,15 @@ int rmsnorm_bwd_ex(const void* x, const void* dy, const void* w, const float* rs
  *   happens to describe contiguous rows is treated as null.  Otherwise the
  *   vector path needs the input pointer and s1, s2, s3 times the element size
  *   to be multiples of 16 bytes (besides the contiguous conditions above);
- *   other layouts take the general path.  Results do not depend on the layout:
- *   the same rows give the same bits as a contiguous copy of them would. */
+ *   other layouts take the general path.
+ * Results.  y, dx and the saved statistics are the bits that a contiguous
+ *   copy of the same rows gives.  So are the parameter gradients, except
+ *   when x's layout (and dy's, the same layout) puts the M rows on the M
+ *   contiguous rows of the storage in another order, as a head-major tensor
+ *   does, and M < 2^31 - 2^20: the vector path then reads the storage in
+ *   order and writes each row's outputs to its own row, and the parameter
+ *   gradients are the bits of the call on the storage itself read as
+ *   contiguous rows (the same sums, added in another order). */
 typedef struct {
     int64_t n1, s1, n2, s2, s3;
 } gbn_rows;

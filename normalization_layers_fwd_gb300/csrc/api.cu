@@ -188,8 +188,58 @@ struct Inputs {
     bool ok;         // every layout given is valid
     bool vec_ok;     // every row start is 16-byte aligned (vector path possible)
     int scattered;   // some input's rows are not at r * N
+    int mode;        // gbn::InMode of the fast path
     gbn::RowMaps maps;
 };
+
+// x / d as (q * m) >> s for every x < 2^31, for a divisor 1 <= d < 2^31:
+// with l = ceil(log2 d), m = ceil(2^(31+l) / d) < 2^32 and s = 31 + l
+// (the rounded-up reciprocal of Granlund and Montgomery, 1994: the
+// multiplier's excess over 2^(31+l)/d is below 1, so for x < 2^31 the error
+// of x*m / 2^(31+l) against x/d is below 2^-l <= 1/d).
+void invariant_divisor(int64_t d, uint32_t& m, int& s)
+{
+    int l = 0;
+    while ((int64_t(1) << l) < d) ++l;
+    const uint64_t p = uint64_t(1) << (31 + l);
+    m = (uint32_t)((p + (uint64_t)d - 1) / (uint64_t)d);
+    s = 31 + l;
+}
+
+// Whether a row map (in bytes, rows of rb bytes) puts the M rows on the M
+// contiguous rows of the storage in some order; if so, the map from storage
+// row to output row.
+bool storage_order(const gbn::RowMap& m, int64_t M, int64_t rb, gbn::OutMap& o)
+{
+    if (M < 2 || M > (int64_t(1) << 31) - (int64_t(1) << 20)) return false;
+    if (M % (m.n1 * m.n2) != 0) return false;
+    struct Level { int64_t n, s, w; };
+    Level lv[3] = {{m.n1, m.s1, 1}, {m.n2, m.s2, m.n1}, {M / (m.n1 * m.n2), m.s3, m.n1 * m.n2}};
+    Level use[3];
+    int k = 0;
+    for (const Level& v : lv)
+        if (v.n > 1) use[k++] = v;
+    for (int i = 1; i < k; ++i)  // by storage stride
+        for (int j = i; j > 0 && use[j].s < use[j - 1].s; --j) {
+            const Level t = use[j];
+            use[j] = use[j - 1];
+            use[j - 1] = t;
+        }
+    int64_t expect = rb;
+    for (int i = 0; i < k; ++i) {
+        if (use[i].s != expect) return false;
+        expect *= use[i].n;
+    }
+    for (int i = k; i < 3; ++i) use[i] = Level{1, 0, 0};
+    o.a = (uint32_t)use[0].n;
+    o.b = (uint32_t)use[1].n;
+    o.wa = (uint32_t)use[0].w;
+    o.wb = (uint32_t)use[1].w;
+    o.wc = (uint32_t)use[2].w;
+    invariant_divisor(o.a, o.ma, o.sa);
+    invariant_divisor(o.b, o.mb, o.sb);
+    return true;
+}
 
 // Whether layout l places row r at r * N for every r < M.
 bool contiguous_rows(const gbn_rows& l, int64_t M, int64_t N)
@@ -227,9 +277,21 @@ Inputs input_layouts(const gbn_rows* xl, const gbn_rows* dyl, const void* x, con
         const int64_t q = (M + n1 - 1) / n1;
         const int64_t n2 = l->n2 < q ? l->n2 : q;
         m = gbn::RowMap{n1, l->s1 * e, n2, l->s2 * e, l->s3 * e};
-        in.scattered = 1;
+        in.scattered |= 1 << t;
         if (!aligned16(base[t]) || (m.s1 | m.s2 | m.s3) % 16 != 0) in.vec_ok = false;
     }
+    // Storage order when every input follows one map that permutes whole
+    // storage rows (x alone in a forward; x and dy alike in a backward).
+    const gbn::RowMap& a = in.maps.m[0];
+    const gbn::RowMap& b = in.maps.m[1];
+    const bool both = dy != nullptr;
+    const bool same = !both || (in.scattered == 3 && a.n1 == b.n1 && a.s1 == b.s1 &&
+                                a.n2 == b.n2 && a.s2 == b.s2 && a.s3 == b.s3);
+    if (in.scattered)
+        in.mode = (in.scattered & 1) && same && storage_order(a, M, N * e, in.maps.o)
+                      ? gbn::kInStorage
+                      : gbn::kInRows;
+    in.scattered = in.scattered ? 1 : 0;
     return in;
 }
 
@@ -315,6 +377,7 @@ int dyt_fwd_rows(const void* x, const gbn_rows* xl, const void* alpha, const voi
                     gbn::kFwdDyT, kWide12 | kWide13);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
+    L.in_mode = in.mode;
     L.maps = in.maps;
     if (!L.fast) {  // elementwise general path: one thread per element, grid-stride
         const int64_t E = M * N;
@@ -351,6 +414,7 @@ int dyt_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gbn_ro
                     stream, gbn::kBwdDyT, kWide12);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
+    L.in_mode = in.mode;
     L.maps = in.maps;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_DYT, L, N))) return GBN_EWORKSPACE;
     float* wsf = grads ? static_cast<float*>(ws) : nullptr;
@@ -390,6 +454,7 @@ int layernorm_fwd_rows(const void* x, const gbn_rows* xl, const void* gamma, con
                     gbn::kFwdLN, kWide12 | kWide13);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
+    L.in_mode = in.mode;
     L.maps = in.maps;
     return launch_status(
         gbn::launch_ln_fwd(L, xt, pt, x, gamma, beta, y, mean, rstd, M, (int)N, eps));
@@ -423,6 +488,7 @@ int layernorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const 
                     stream, gbn::kBwdLN, kWide12 | kWide14);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
+    L.in_mode = in.mode;
     L.maps = in.maps;
     if (grads && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_LAYERNORM, L, N)))
         return GBN_EWORKSPACE;
@@ -477,6 +543,7 @@ int rmsnorm_fwd_rows(const void* x, const gbn_rows* xl, const void* w, void* y, 
                     gbn::kFwdNorm, kWide12);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
+    L.in_mode = in.mode;
     L.maps = in.maps;
     return launch_status(gbn::launch_rms_fwd(L, xt, wt, x, w, y, rstd, M, (int)N, eps, variant));
 }
@@ -507,6 +574,7 @@ int rmsnorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gb
                     stream, gbn::kBwdRms, kWide12);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
+    L.in_mode = in.mode;
     L.maps = in.maps;
     if (dw && M > 0 && (!ws || ws_bytes < ws_needed(GBN_OP_RMSNORM, L, N))) return GBN_EWORKSPACE;
     float* wsf = dw ? static_cast<float*>(ws) : nullptr;

@@ -367,6 +367,38 @@ __device__ __forceinline__ int64_t row_byte_offset(const RowMap& m, int64_t r)
     return (r - q * m.n1) * m.s1 + (q % m.n2) * m.s2 + (q / m.n2) * m.s3;
 }
 
+// The output row of storage row q (kInStorage), in 32-bit arithmetic:
+// q < 2^31 and every output row (padded rows' included) below 2^32.
+__device__ __forceinline__ int64_t out_row(const OutMap& o, int64_t q)
+{
+    const uint32_t uq = (uint32_t)q;
+    const uint32_t q1 = (uint32_t)(((uint64_t)uq * o.ma) >> o.sa);
+    const uint32_t q2 = (uint32_t)(((uint64_t)q1 * o.mb) >> o.sb);
+    return (int64_t)((uq - q1 * o.a) * o.wa + (q1 - q2 * o.b) * o.wb + q2 * o.wc);
+}
+
+// The row whose outputs (and saved statistics) belong to this thread's row q.
+template <int kIn>
+__device__ __forceinline__ int64_t stat_row(const RowMaps& maps, int64_t q)
+{
+    if constexpr (kIn == kInStorage)
+        return out_row(maps.o, q);
+    else
+        return q;
+}
+
+// Where this thread's vectors of row q go: at yb + off while rows are in
+// order, else at the storage-order map's row (lvec: the thread's column).
+template <int kIn, typename TX>
+__device__ __forceinline__ TX* out_at(TX* yb, int64_t off, TX* y, const RowMaps& maps, int64_t q,
+                                      int N, int lvec)
+{
+    if constexpr (kIn == kInStorage)
+        return y + out_row(maps.o, q) * N + lvec;
+    else
+        return yb + off;
+}
+
 // Row r of input t (0: x, 1: dy) for the general kernels: r * N elements
 // in, or where the row map puts it.
 template <typename TX>
@@ -858,6 +890,18 @@ __device__ __forceinline__ void cta_store_columns_kv(const f2 (&acc)[KV][P], flo
 // Raise a kernel's dynamic shared-memory limit and prefer the maximum
 // shared-memory carve-out, once per kernel per device (host side).  The
 // template parameter is the kernel itself, so every kernel has its own flag.
+// Call f(std::integral_constant<int, m>) for the launch's input mode m.
+template <class F>
+inline void with_mode(int in_mode, F&& f)
+{
+    if (in_mode == kInRows)
+        f(std::integral_constant<int, kInRows>{});
+    else if (in_mode == kInStorage)
+        f(std::integral_constant<int, kInStorage>{});
+    else
+        f(std::integral_constant<int, kInContig>{});
+}
+
 template <auto Kernel>
 inline void ring_attributes(int smem)
 {

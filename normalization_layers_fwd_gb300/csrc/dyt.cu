@@ -114,7 +114,7 @@ __device__ __forceinline__ void dyt_tanh_sech2_2(f2 z, f2& t, f2& s)
 // Addressing: a thread's vector of row u of a block sits at soff + u*srow in
 // the ring slot and at row0*N + l*VEC + u*grow in HBM (row0 = the block's
 // first row + g); only the ragged last block compares rows against M.
-template <typename TX, int S, bool kRows>
+template <typename TX, int S, int kIn>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
     dyt_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ alpha,
                  const void* __restrict__ gamma, const void* __restrict__ beta, int pt,
@@ -144,9 +144,9 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
         }
     }
 
-    Ring<1, kind_stages(S, kFwdDyT), kRows> rg;
+    Ring<1, kind_stages(S, kFwdDyT), kIn == kInRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
-    if constexpr (kRows) rg.map[0] = maps.m[0];
+    if constexpr (kIn == kInRows) rg.map[0] = maps.m[0];
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const bool okr = alive && (full || row0 + u * G < M);
+            TX* const yr = out_at<kIn>(yb, u * grow, y, maps, row0 + u * G, N, l * VEC);
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
                 const bool ok = okr && colok[j];
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
 #pragma unroll
                 for (int p = 0; p < P; ++p)
                     v[p] = fma2(gm[j][p], dyt_tanh2(mul2(a2, v[p])), bt[j][p]);
-                st_stream_if(ok, yb + u * grow + j * W * VEC, pack2<TX>(v));
+                st_stream_if(ok, yr + j * W * VEC, pack2<TX>(v));
             }
         }
         row0 += rstride;
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
 // x and dy stream through the ring.  Full row blocks run without masking;
 // only the ragged last block masks its padded rows, by a select after the
 // arithmetic (its slots past the last row hold stale data).
-template <typename TX, int S, bool kRows>
+template <typename TX, int S, int kIn>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     dyt_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy, TX* __restrict__ dx,
                  const void* __restrict__ alpha, const void* __restrict__ gamma, int pt,
@@ -228,6 +229,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const bool okr = !kMask || row0 + u * G < M;
+            TX* const dxr = out_at<kIn>(dxb, u * grow, dx, maps, row0 + u * G, N, l * VEC);
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
                 const bool ok = alive && colok[j] && okr;
@@ -255,15 +257,15 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
                         acc_a[j][p] = fma2(dsd, xv[p], acc_a[j][p]);
                     }
                 }
-                st_stream_if(ok, dxb + u * grow + j * W * VEC, pack2<TX>(o));
+                st_stream_if(ok, dxr + j * W * VEC, pack2<TX>(o));
             }
         }
     };
 
-    Ring<2, kind_stages(S, kBwdDyT), kRows> rg;
+    Ring<2, kind_stages(S, kBwdDyT), kIn == kInRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
-    if constexpr (kRows) {
+    if constexpr (kIn == kInRows) {
         rg.map[0] = maps.m[0];
         rg.map[1] = maps.m[1];
     }
@@ -379,19 +381,16 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* alp
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                          \
-    case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, kFwdDyT, 1);                                   \
-        if (L.scattered) {                                                                         \
-            ring_attributes<dyt_fwd_fast<TX, S, true>>(smem);                                      \
-            dyt_fwd_fast<TX, S, true><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
+#define GBN_CASE(S)                                                                                \
+    case S: {                                                                                      \
+        constexpr int smem = ring_smem_bytes(S, kFwdDyT, 1);                                       \
+        with_mode(L.in_mode, [&](auto m_) {                                                        \
+            constexpr int kIn_ = decltype(m_)::value;                                              \
+            ring_attributes<dyt_fwd_fast<TX, S, kIn_>>(smem);                                      \
+            dyt_fwd_fast<TX, S, kIn_><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
                 xp, yp, alpha, gamma, beta, pt, M, N, L.nblocks, L.fault, L.maps);                 \
-        } else {                                                                                   \
-            ring_attributes<dyt_fwd_fast<TX, S, false>>(smem);                                     \
-            dyt_fwd_fast<TX, S, false><<<L.grid, kSched[S].T, smem, L.stream>>>(                   \
-                xp, yp, alpha, gamma, beta, pt, M, N, L.nblocks, L.fault, L.maps);                 \
-        }                                                                                          \
-        break;                                                                               \
+        });                                                                                        \
+        break;                                                                                     \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9)
@@ -415,19 +414,16 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                          \
-    case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, kBwdDyT, 2);                                    \
-        if (L.scattered) {                                                                         \
-            ring_attributes<dyt_bwd_fast<TX, S, true>>(smem);                                      \
-            dyt_bwd_fast<TX, S, true><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
+#define GBN_CASE(S)                                                                                \
+    case S: {                                                                                      \
+        constexpr int smem = ring_smem_bytes(S, kBwdDyT, 2);                                       \
+        with_mode(L.in_mode, [&](auto m_) {                                                        \
+            constexpr int kIn_ = decltype(m_)::value;                                              \
+            ring_attributes<dyt_bwd_fast<TX, S, kIn_>>(smem);                                      \
+            dyt_bwd_fast<TX, S, kIn_><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
                 xp, dyp, dxp, alpha, gamma, pt, ws, M, N, L.nblocks, L.fault, L.maps);             \
-        } else {                                                                                   \
-            ring_attributes<dyt_bwd_fast<TX, S, false>>(smem);                                     \
-            dyt_bwd_fast<TX, S, false><<<L.grid, kSched[S].T, smem, L.stream>>>(                   \
-                xp, dyp, dxp, alpha, gamma, pt, ws, M, N, L.nblocks, L.fault, L.maps);             \
-        }                                                                                          \
-        break;                                                                               \
+        });                                                                                        \
+        break;                                                                                     \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(11)

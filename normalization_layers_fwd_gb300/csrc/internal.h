@@ -13,8 +13,29 @@ namespace gbn {
 struct RowMap {
     int64_t n1, s1, n2, s2, s3;
 };
+// Storage-order reads.  When x (and dy, with the same map) place their M
+// rows on the M contiguous rows of their storage in some order, the fast
+// kernels stream storage row q and write its outputs at row
+//   out_row(q) = (q % a) * wa + ((q / a) % b) * wb + (q / (a * b)) * wc.
+// q / a is (q * ma) >> sa and (q / a) / b is ((q / a) * mb) >> sb: division
+// by an invariant integer as a multiplication by its rounded-up reciprocal
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994), exact for dividends and divisors below 2^31.
+struct OutMap {
+    uint32_t ma, mb;
+    int sa, sb;
+    uint32_t a, b, wa, wb, wc;  // out_row stays below 2^32 for every q < M + 2^20
+};
 struct RowMaps {
     RowMap m[2];  // x, then dy
+    OutMap o;     // storage order (in_mode 2)
+};
+
+// Input modes of the fast kernels.
+enum InMode {
+    kInContig = 0,   // rows at r * N
+    kInRows = 1,     // rows where maps.m put them: one bulk copy per row
+    kInStorage = 2,  // storage rows in order, outputs through maps.o
 };
 
 // How one call is laid out on the GPU.  Decided on the host from (M, N,
@@ -29,6 +50,7 @@ struct Launch {
     cudaStream_t stream;
     unsigned* fault;    // the device's fault word (bounded waits that ran out)
     int scattered;      // 1: x (and dy) rows follow maps rather than r * N
+    int in_mode;        // InMode of the fast path
     RowMaps maps;
 };
 

@@ -25,7 +25,7 @@ namespace {
 // of squares) per row.  Every thread runs every row (row reductions are
 // collective); loads and stores are predicated, and only the ragged last
 // block compares rows against M.
-template <typename TX, int S, bool kRows>
+template <typename TX, int S, int kIn>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
     ln_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ gamma,
                 const void* __restrict__ beta, int pt, float* __restrict__ mean,
@@ -57,9 +57,9 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
         }
     }
 
-    Ring<1, kind_stages(S, kFwdLN), kRows> rg;
+    Ring<1, kind_stages(S, kFwdLN), kIn == kInRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
-    if constexpr (kRows) rg.map[0] = maps.m[0];
+    if constexpr (kIn == kInRows) rg.map[0] = maps.m[0];
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
@@ -115,15 +115,17 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
         for (int u = 0; u < U; ++u) {
             const float rs = rsqrtf(fmaf(q[u], inv_n, eps));
             const f2 r2 = splat2(rs);
+            const int64_t orow = stat_row<kIn>(maps, row0 + u * G);
+            TX* const yr = kIn == kInStorage ? y + orow * N + l * VEC : yb + u * grow;
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
                 f2 o[P];
 #pragma unroll
                 for (int p = 0; p < P; ++p) o[p] = fma2(mul2(xv[u][j][p], r2), gm[j][p], bt[j][p]);
-                st_stream_if(okr[u] && colok[j], yb + u * grow + j * W * VEC, pack2<TX>(o));
+                st_stream_if(okr[u] && colok[j], yr + j * W * VEC, pack2<TX>(o));
             }
-            if (mean) st_f32_if(lead && okr[u], mean + (row0 + u * G), mu[u]);
-            if (rstd) st_f32_if(lead && okr[u], rstd + (row0 + u * G), rs);
+            if (mean) st_f32_if(lead && okr[u], mean + orow, mu[u]);
+            if (rstd) st_f32_if(lead && okr[u], rstd + orow, rs);
         }
         row0 += rstride;
         yb += rstride * N;
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
 // block are prefetched into registers while the current one is processed.
 // Full row blocks run without masking; the ragged last block masks its
 // padded rows by a select after the arithmetic.
-template <typename TX, int S, bool kRows>
+template <typename TX, int S, int kIn>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     ln_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy,
                 const float* __restrict__ mean, const float* __restrict__ rstd,
@@ -178,8 +180,9 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t row = row0 + u * G;
-            mu_n[u] = row < M ? __ldcs(mean + row) : 0.f;
-            rs_n[u] = row < M ? __ldcs(rstd + row) : 0.f;
+            const int64_t srow = row < M ? stat_row<kIn>(maps, row) : 0;
+            mu_n[u] = row < M ? __ldcs(mean + srow) : 0.f;
+            rs_n[u] = row < M ? __ldcs(rstd + srow) : 0.f;
         }
     };
     load_stats((int64_t)blockIdx.x * (G * U) + g);
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
         for (int u = 0; u < U; ++u) {
             const f2 ma = splat2(s[2 * u] * inv_n), nmb = splat2(-(s[2 * u + 1] * inv_n));
             const f2 r2 = splat2(rs[u]);
+            TX* const dxr = out_at<kIn>(dxb, u * grow, dx, maps, row0 + u * G, N, l * VEC);
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
                 const bool ok = alive && colok[j] && okr[u];
@@ -243,15 +247,15 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
 #pragma unroll
                 for (int p = 0; p < P; ++p)
                     o[p] = mul2(r2, fma2(xh[u][j][p], nmb, sub2(gg[u][j][p], ma)));
-                st_stream_if(ok, dxb + u * grow + j * W * VEC, pack2<TX>(o));
+                st_stream_if(ok, dxr + j * W * VEC, pack2<TX>(o));
             }
         }
     };
 
-    Ring<2, kind_stages(S, kBwdLN), kRows> rg;
+    Ring<2, kind_stages(S, kBwdLN), kIn == kInRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
-    if constexpr (kRows) {
+    if constexpr (kIn == kInRows) {
         rg.map[0] = maps.m[0];
         rg.map[1] = maps.m[1];
     }
@@ -371,19 +375,16 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                          \
-    case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, kFwdLN, 1);                                    \
-        if (L.scattered) {                                                                         \
-            ring_attributes<ln_fwd_fast<TX, S, true>>(smem);                                       \
-            ln_fwd_fast<TX, S, true><<<L.grid, kSched[S].T, smem, L.stream>>>(                     \
-                xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault, L.maps);\
-        } else {                                                                                   \
-            ring_attributes<ln_fwd_fast<TX, S, false>>(smem);                                      \
-            ln_fwd_fast<TX, S, false><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
-                xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault, L.maps);\
-        }                                                                                          \
-        break;                                                                               \
+#define GBN_CASE(S)                                                                                \
+    case S: {                                                                                      \
+        constexpr int smem = ring_smem_bytes(S, kFwdLN, 1);                                        \
+        with_mode(L.in_mode, [&](auto m_) {                                                        \
+            constexpr int kIn_ = decltype(m_)::value;                                              \
+            ring_attributes<ln_fwd_fast<TX, S, kIn_>>(smem);                                       \
+            ln_fwd_fast<TX, S, kIn_><<<L.grid, kSched[S].T, smem, L.stream>>>(                     \
+                xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault, L.maps); \
+        });                                                                                        \
+        break;                                                                                     \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9)
@@ -409,19 +410,16 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                          \
-    case S: {                                                                                \
-        constexpr int smem = ring_smem_bytes(S, kBwdLN, 2);                                  \
-        if (L.scattered) {                                                                         \
-            ring_attributes<ln_bwd_fast<TX, S, true>>(smem);                                       \
-            ln_bwd_fast<TX, S, true><<<L.grid, kSched[S].T, smem, L.stream>>>(                     \
+#define GBN_CASE(S)                                                                                \
+    case S: {                                                                                      \
+        constexpr int smem = ring_smem_bytes(S, kBwdLN, 2);                                        \
+        with_mode(L.in_mode, [&](auto m_) {                                                        \
+            constexpr int kIn_ = decltype(m_)::value;                                              \
+            ring_attributes<ln_bwd_fast<TX, S, kIn_>>(smem);                                       \
+            ln_bwd_fast<TX, S, kIn_><<<L.grid, kSched[S].T, smem, L.stream>>>(                     \
                 xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.nblocks, L.fault, L.maps); \
-        } else {                                                                                   \
-            ring_attributes<ln_bwd_fast<TX, S, false>>(smem);                                      \
-            ln_bwd_fast<TX, S, false><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
-                xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.nblocks, L.fault, L.maps); \
-        }                                                                                          \
-        break;                                                                               \
+        });                                                                                        \
+        break;                                                                                     \
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9)

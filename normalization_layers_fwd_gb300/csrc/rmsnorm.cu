@@ -7,7 +7,7 @@ namespace gbn {
 namespace {
 
 // ------------------------------------------------------------ fast forward
-template <typename TX, int S, bool kWF, bool kRows>
+template <typename TX, int S, bool kWF, int kIn>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
     rms_fwd_fast(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ w,
                  int pt, float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
@@ -42,9 +42,9 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
         }
     }
 
-    Ring<1, kind_stages(S, kFwdNorm), kRows> rg;
+    Ring<1, kind_stages(S, kFwdNorm), kIn == kInRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
-    if constexpr (kRows) rg.map[0] = maps.m[0];
+    if constexpr (kIn == kInRows) rg.map[0] = maps.m[0];
     rg.row_bytes = rb;
     rg.R = G * U;
     rg.M = M;
@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
         for (int u = 0; u < U; ++u) {
             const float rs = rsqrtf(fmaf(s[u], inv_n, eps));
             const f2 r2 = splat2(rs);
+            const int64_t orow = stat_row<kIn>(maps, row0 + u * G);
+            TX* const yr = kIn == kInStorage ? y + orow * N + l * VEC : yb + u * grow;
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
                 uint4 out;
@@ -96,9 +98,9 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
                     for (int p = 0; p < P; ++p) o[p] = mul2(wf[j][p], mul2(xv[u][j][p], r2));
                     out = pack2<TX>(o);
                 }
-                st_stream_if(okr[u] && colok[j], yb + u * grow + j * W * VEC, out);
+                st_stream_if(okr[u] && colok[j], yr + j * W * VEC, out);
             }
-            if (rstd) st_f32_if(lead && okr[u], rstd + (row0 + u * G), rs);
+            if (rstd) st_f32_if(lead && okr[u], rstd + orow, rs);
         }
         row0 += rstride;
         yb += rstride * N;
@@ -155,7 +157,6 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
 }
 
 #undef GBN_RMS_LAUNCH
-#undef GBN_RMS_LAUNCH1
 
 }  // namespace
 

@@ -84,26 +84,20 @@ __device__ __forceinline__ float warp_row_rstd(const TX* xr, int N, int lane, fl
 // the weight-first and Gemma expressions with 16-bit activations (with
 // float32 activations both expressions are the same float32 arithmetic),
 // and the scattered-row instance (kRows) for inputs that follow row maps.
-#define GBN_RMS_LAUNCH1(KERNEL, S, R, SMEM, ...)                                                   \
-    do {                                                                                           \
+#define GBN_RMS_LAUNCH(KERNEL, S, SMEM, ...)                                                       \
+    with_mode(L.in_mode, [&](auto m_) {                                                            \
+        constexpr int kIn_ = decltype(m_)::value;                                                  \
         if constexpr (is16<TX>()) {                                                                \
             if (variant != 0) {                                                                    \
-                ring_attributes<KERNEL<TX, S, true, R>>(SMEM);                                     \
-                KERNEL<TX, S, true, R><<<L.grid, kSched[S].T, SMEM, L.stream>>>(__VA_ARGS__,       \
-                                                                                 L.maps);          \
-                break;                                                                             \
+                ring_attributes<KERNEL<TX, S, true, kIn_>>(SMEM);                                  \
+                KERNEL<TX, S, true, kIn_><<<L.grid, kSched[S].T, SMEM, L.stream>>>(__VA_ARGS__,    \
+                                                                                    L.maps);       \
+                return;                                                                            \
             }                                                                                      \
         }                                                                                          \
-        ring_attributes<KERNEL<TX, S, false, R>>(SMEM);                                            \
-        KERNEL<TX, S, false, R><<<L.grid, kSched[S].T, SMEM, L.stream>>>(__VA_ARGS__, L.maps);     \
-    } while (0)
-#define GBN_RMS_LAUNCH(KERNEL, S, SMEM, ...)                                                       \
-    do {                                                                                           \
-        if (L.scattered)                                                                           \
-            GBN_RMS_LAUNCH1(KERNEL, S, true, SMEM, __VA_ARGS__);                                   \
-        else                                                                                       \
-            GBN_RMS_LAUNCH1(KERNEL, S, false, SMEM, __VA_ARGS__);                                  \
-    } while (0)
+        ring_attributes<KERNEL<TX, S, false, kIn_>>(SMEM);                                         \
+        KERNEL<TX, S, false, kIn_><<<L.grid, kSched[S].T, SMEM, L.stream>>>(__VA_ARGS__, L.maps);  \
+    })
 
 }  // namespace
 }  // namespace gbn

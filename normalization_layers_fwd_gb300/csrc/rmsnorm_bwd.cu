@@ -11,7 +11,7 @@ namespace {
 // prefetched into registers, otherwise r is recomputed with the forward's
 // code.  Full row blocks run without masking; the ragged last block masks its
 // padded rows by a select after the arithmetic.
-template <typename TX, int S, bool kWF, bool kRows>
+template <typename TX, int S, bool kWF, int kIn>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
     rms_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy, const void* __restrict__ w,
                  int pt, const float* __restrict__ rstd, TX* __restrict__ dx,
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t row = row0 + u * G;
-                rs_n[u] = row < M ? __ldcs(rstd + row) : 0.f;
+                rs_n[u] = row < M ? __ldcs(rstd + stat_row<kIn>(maps, row)) : 0.f;
             }
         }
     };
@@ -131,20 +131,21 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const f2 r2 = splat2(rs[u]), nm = splat2(-(s[u] * inv_n));
+            TX* const dxr = out_at<kIn>(dxb, u * grow, dx, maps, row0 + u * G, N, l * VEC);
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
                 f2 o[P];
 #pragma unroll
                 for (int p = 0; p < P; ++p) o[p] = mul2(r2, fma2(xh[u][j][p], nm, dn[u][j][p]));
-                st_stream_if(alive && okr[u] && colok[j], dxb + u * grow + j * W * VEC, pack2<TX>(o));
+                st_stream_if(alive && okr[u] && colok[j], dxr + j * W * VEC, pack2<TX>(o));
             }
         }
     };
 
-    Ring<2, kind_stages(S, kBwdRms), kRows> rg;
+    Ring<2, kind_stages(S, kBwdRms), kIn == kInRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
-    if constexpr (kRows) {
+    if constexpr (kIn == kInRows) {
         rg.map[0] = maps.m[0];
         rg.map[1] = maps.m[1];
     }
@@ -246,7 +247,6 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     return cudaGetLastError();
 }
 #undef GBN_RMS_LAUNCH
-#undef GBN_RMS_LAUNCH1
 
 }  // namespace
 

@@ -7,8 +7,11 @@ input and the head-major upstream gradient that attention produces
 
 * layouts whose rows start on 16-byte boundaries take the same vector
   kernels and launch layout as a contiguous copy of the same rows, so every
-  output, parameter gradients included, must be bit-identical to the call on
-  the contiguous copy;
+  output must be bit-identical to the call on the contiguous copy;
+* parameter gradients too, except for layouts that permute the storage's
+  contiguous rows (head-major, sequence-major): those are read in storage
+  order, so their parameter gradients must be bit-identical to the call on
+  the storage read as contiguous rows;
 * other layouts (odd strides, odd base offsets) take the general kernels and
   are compared with the float64 oracle element by element.
 All calls go through the C ABI (the ctypes binding)."""
@@ -80,6 +83,17 @@ def _layout_is_vector(v):
             all((s * e) % 16 == 0 for s in (lay.s1, lay.s2, lay.s3)))
 
 
+def storage_rows(v):
+    """The contiguous rows v's storage holds, when v is a permutation of
+    them (a transposed view of a fresh contiguous tensor), else None."""
+    base = v._base if v._base is not None else None
+    if base is None or not base.is_contiguous() or base.numel() != v.numel():
+        return None
+    if v.storage_offset() != base.storage_offset():
+        return None
+    return base.reshape(-1, v.shape[-1])
+
+
 # ---------------------------------------------------------------- the ops
 
 def _bits(t):
@@ -102,12 +116,30 @@ def run(op, x, dy, P, eps=1e-5):
     return dict(y=y, rstd=rstd, dx=dx, dw=dw, dx2=dx2, dw2=dw2)
 
 
-def assert_same_bits(a, b):
+PARAM_GRADS = {"da", "dg", "db", "dw", "dw2"}
+
+
+def assert_same_bits(a, b, keys=None):
     assert a.keys() == b.keys()
     for k in a:
+        if keys is not None and k not in keys:
+            continue
         assert a[k].shape == b[k].shape, k
         assert a[k].is_contiguous(), k
         assert torch.equal(_bits(a[k]), _bits(b[k])), k
+
+
+def check_layout(op, x, dy, P):
+    """Per-row outputs against a contiguous copy; parameter gradients against
+    the contiguous copy, or for storage permutations against the storage."""
+    got = run(op, x, dy, P)
+    want = run(op, x.contiguous(), dy.contiguous(), P)
+    xs, dys = storage_rows(x), storage_rows(dy)
+    perm = xs is not None and dys is not None and x.stride() == dy.stride()
+    assert_same_bits(got, want, None if not perm else set(got) - PARAM_GRADS)
+    if perm:
+        assert_same_bits(got, run(op, xs, dys, P), set(got) & PARAM_GRADS)
+    return perm
 
 
 OPS = ["dyt", "layernorm", "rmsnorm"]
@@ -140,11 +172,8 @@ def test_vector_layouts_match_contiguous_bits(op, dts, case):
     x = make(lead, N, xdt, seed + "/x")
     dy = make(lead, N, xdt, seed + "/dy")
     assert not x.is_contiguous() and _layout_is_vector(x)
-    P = _params(N, pdt, seed)
-    got = run(op, x, dy, P)
-    want = run(op, x.contiguous(), dy.contiguous(), P)
-    torch.cuda.synchronize()
-    assert_same_bits(got, want)
+    perm = check_layout(op, x, dy, _params(N, pdt, seed))
+    assert perm == (name in ("head_major", "seq_major"))
     assert _lib.read_faults() == 0
 
 
@@ -158,7 +187,7 @@ def test_mixed_layouts_x_and_dy(op):
         x = x if xs else x.contiguous()
         dy = dy if dys else dy.contiguous()
         P = _params(N, torch.float32, f"mix/{op}")
-        assert_same_bits(run(op, x, dy, P), run(op, x.contiguous(), dy.contiguous(), P))
+        assert not check_layout(op, x, dy, P)  # one map for x and dy: not both permuted
 
 
 def test_persistent_loop_head_major():
@@ -168,7 +197,7 @@ def test_persistent_loop_head_major():
         x = head_major(lead, N, torch.bfloat16, f"pl/{op}/x")
         dy = head_major(lead, N, torch.bfloat16, f"pl/{op}/dy")
         P = _params(N, torch.bfloat16, f"pl/{op}")
-        assert_same_bits(run(op, x, dy, P), run(op, x.contiguous(), dy.contiguous(), P))
+        assert check_layout(op, x, dy, P)
 
 
 def test_autograd_head_major_rms_norm():
@@ -184,7 +213,10 @@ def test_autograd_head_major_rms_norm():
     yc.backward(dy.contiguous())
     assert torch.equal(_bits(y), _bits(yc))
     assert torch.equal(_bits(xv.grad), _bits(xc.grad))
-    assert torch.equal(_bits(w.grad), _bits(wc.grad))
+    # the weight gradient sums the rows in storage order
+    ws = w.detach().clone().requires_grad_(True)
+    rms_norm(storage_rows(xv).detach(), ws, 1e-6).backward(storage_rows(dy))
+    assert torch.equal(_bits(w.grad), _bits(ws.grad))
 
 
 # ------------------------------------------- general layouts: oracle parity
@@ -243,3 +275,15 @@ def test_more_than_three_levels_is_copied():
     P = _params(64, torch.float32, "l4")
     dy = _normal(tuple(x.shape), torch.bfloat16, "l4/dy")
     assert_same_bits(run("rmsnorm", x, dy, P), run("rmsnorm", x.contiguous(), dy, P))
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_storage_order_ragged_blocks(op):
+    """Storage permutations whose row count leaves a ragged last row block,
+    with every level size odd (the output map's divisions by 3, 5, 7)."""
+    x = head_major((3, 7, 5), 128, torch.bfloat16, f"rag/{op}/x")
+    dy = head_major((3, 7, 5), 128, torch.bfloat16, f"rag/{op}/dy")
+    assert check_layout(op, x, dy, _params(128, torch.float32, f"rag/{op}"))
+    x = seq_major((5, 331, 3), 64, torch.float16, f"rag2/{op}/x")
+    dy = seq_major((5, 331, 3), 64, torch.float16, f"rag2/{op}/dy")
+    assert check_layout(op, x, dy, _params(64, torch.float32, f"rag2/{op}"))

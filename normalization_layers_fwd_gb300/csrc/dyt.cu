@@ -25,10 +25,14 @@
 namespace gbn {
 namespace {
 
+// The flush-to-zero form: e = 2^v only reaches the subnormal range for
+// |z| > 43.6, where tanh rounds to +-1 either way and sech^2 (below 2^-124)
+// becomes 0, and the ex2 then needs no subnormal handling around it, which
+// the DyT kernels, bound by instruction issue, cannot afford.
 __device__ __forceinline__ float ex2_approx(float v)
 {
     float r;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
     return r;
 }
 
@@ -46,7 +50,8 @@ __device__ __forceinline__ float rcp_approx(float v)
 //    1 - tanh^2 cancellation), so it needs no second branch;
 //  * |z| < 1/8: 1 - e cancels, so tanh takes the Maclaurin series
 //    z - z^3/3 + 2z^5/15 - 17z^7/315 (the next term is below 2e-10 relative).
-// z = +-inf gives tanh = +-1 and sech^2 = 0; NaN propagates.
+// z = +-inf gives tanh = +-1 and sech^2 = 0; NaN propagates.  For |z| > 43.6
+// sech^2 is 0 (flushed), against a true value below 2^-124.
 constexpr float kM2Log2e = -2.0f * 1.44269504088896340736f;
 constexpr float kSmall = 0.125f;
 constexpr float kT3 = -1.0f / 3.0f, kT5 = 2.0f / 15.0f, kT7 = -17.0f / 315.0f;

@@ -281,6 +281,29 @@ def test_tanh_against_cuda_tanhf():
     assert err < 2.0 ** -19  # within 16 float32 ulps everywhere
 
 
+@pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float32])
+def test_dyt_large_arguments(xdt):
+    """|alpha x| beyond 43.6: tanh is +-1 and sech^2 flushes to 0, so y is
+    exactly +-gamma + beta (one rounding) and dx, and every dalpha term, is
+    exactly zero (the true sech^2 is below 2^-124)."""
+    M, N = 300, 64
+    mag = torch.tensor([43.7, 50.0, 88.0, 100.0, 1e4, 3e38])
+    x = mag[torch.arange(M * N) % mag.numel()].view(M, N)
+    x = torch.where(torch.arange(M * N).view(M, N) % 3 == 0, -x, x).to("cuda", xdt)
+    alpha = torch.ones(1, device="cuda")
+    gamma = synth.normal((N,), 1.0, 0.1, torch.float32, seed=5, device="cuda")
+    beta = synth.normal((N,), 0.0, 0.1, torch.float32, seed=6, device="cuda")
+    dy = synth.normal((M, N), 0.0, 1.0, xdt, seed=7, device="cuda")
+    y = _lib.dyt_fwd(x, alpha, gamma, beta)
+    dx, da, dg, db = _lib.dyt_bwd(x, dy, alpha, gamma)
+    sgn = torch.sign(x.float())
+    assert torch.equal(y, (sgn * gamma + beta).to(xdt))
+    assert torch.equal(dx.float().abs(), torch.zeros_like(dx.float()))
+    assert da.item() == 0.0
+    torch.testing.assert_close(db, dy.float().sum(0), rtol=1e-5, atol=1e-5)
+    torch.testing.assert_close(dg, (dy.float() * sgn).sum(0), rtol=1e-5, atol=1e-5)
+
+
 def test_autograd_wrappers_match_direct_calls():
     inp = _inputs(513, 256, torch.bfloat16, torch.float32, "ag")
     for fn, params, direct in [

@@ -92,9 +92,9 @@ int64_t general_warps(int64_t M, int sms) { return M < 4LL * sms ? M : 4LL * sms
 // vectors, as a set (bit s - kNumSched1 for schedule s), chosen per kernel
 // within its register budget and by measurement: the DyT and LayerNorm
 // forwards 12-13, the LayerNorm backward 12 and 14, the DyT backward 12,
-// the RMSNorm forward and backward 12 (the same set, so the backward's
-// recomputed rstd reduces a row in the forward's order).  Other rows, and
-// kernels with an empty set, take the one-vector schedules.
+// the RMSNorm forward and backward 12 and 14 (the same set, so the
+// backward's recomputed rstd reduces a row in the forward's order).  Other
+// rows, and kernels with an empty set, take the one-vector schedules.
 constexpr unsigned kWide12 = 1u, kWide13 = 2u, kWide14 = 4u;
 
 int fast_sid(int64_t N, int xt, unsigned wide)
@@ -350,10 +350,11 @@ size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int
     if (M == 0) return 0;
     const int sms = sm_count(device);
     if (sms <= 0) return (size_t)-1;
+    const int kind =
+        op == GBN_OP_DYT ? gbn::kBwdDyT : op == GBN_OP_LAYERNORM ? gbn::kBwdLN : gbn::kBwdRms;
+    // the vector path with the kernel's wide set, or the general path
     const Launch a =
-        plan(M, N, xt, true, sms, nullptr,
-             op == GBN_OP_DYT ? gbn::kBwdDyT : op == GBN_OP_LAYERNORM ? gbn::kBwdLN : gbn::kBwdRms,
-             op == GBN_OP_LAYERNORM ? kWide12 | kWide14 : kWide12);
+        plan(M, N, xt, true, sms, nullptr, kind, op == GBN_OP_DYT ? kWide12 : kWide12 | kWide14);
     const Launch b = plan(M, N, xt, false, sms, nullptr, gbn::kBwdLN);
     const size_t need = ws_needed(op, a.P > b.P ? a : b, N);
     return (need + 255) & ~(size_t)255;
@@ -540,7 +541,7 @@ int rmsnorm_fwd_rows(const void* x, const gbn_rows* xl, const void* w, void* y, 
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
-                    gbn::kFwdNorm, kWide12);
+                    gbn::kFwdNorm, kWide12 | kWide14);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -570,8 +571,9 @@ int rmsnorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gb
     if (!in.ok) return GBN_EINVAL;
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
+    // the forward's set: a recomputed rstd reduces each row in its order
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
-                    stream, gbn::kBwdRms, kWide12);
+                    stream, gbn::kBwdRms, kWide12 | kWide14);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;

@@ -465,7 +465,11 @@ struct Ring {
 // Run `body(b, k, alive)` over this CTA's row blocks with the ring full
 // kStages deep.  `dsm` is the kernel's dynamic shared memory (128-byte
 // aligned).  Every thread makes the same calls (body may __syncthreads).
-template <int NT, int kStages, bool kRows, class Body>
+// kBodySyncs: every call of body passes a __syncthreads after its last read
+// of the slot (a row reduction across warps, with the row kept in registers
+// past it), so the slot can be refilled as soon as body returns, without a
+// barrier of its own.
+template <bool kBodySyncs = false, int NT, int kStages, bool kRows, class Body>
 __device__ __forceinline__ void ring_loop(Ring<NT, kStages, kRows>& rg, unsigned char* dsm,
                                           Body&& body)
 {
@@ -487,7 +491,7 @@ __device__ __forceinline__ void ring_loop(Ring<NT, kStages, kRows>& rg, unsigned
             if (!alive) failed_at = k;
         }
         body(rg.block(k), k, alive);
-        __syncthreads();  // every thread is done with slot k % kStages
+        if constexpr (!kBodySyncs) __syncthreads();  // every thread is done with slot k % kStages
         if (rg.issuer() && alive && k + kStages < K) {
             fence_proxy_async();
             rg.issue(k + kStages);

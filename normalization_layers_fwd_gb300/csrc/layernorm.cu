@@ -73,7 +73,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
     int64_t row0 = (int64_t)blockIdx.x * (G * U) + g;  // this thread's first row
     TX* yb = y + row0 * N + l * VEC;
     const bool lead = l == 0 && in_group<W>();  // stores the row statistics
-    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+    // rows wider than a warp: the row reduction's barrier releases the slot
+    ring_loop<(W > 32)>(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* xs = rg.tile(k, 0) + soff;
         const bool full = b < nfull;
         bool okr[U];
@@ -269,7 +270,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     const int64_t rstride = (int64_t)gridDim.x * (G * U);
     int64_t row0 = (int64_t)blockIdx.x * (G * U) + g;  // this thread's first row
     TX* dxb = dx + row0 * N + l * VEC;
-    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+    // rows wider than a warp: the row reduction's barrier releases the slot
+    ring_loop<(W > 32)>(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* xs = rg.tile(k, 0) + soff;
         const unsigned char* ds = rg.tile(k, 1) + soff;
         if (b < nfull)

@@ -56,7 +56,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
     int64_t row0 = (int64_t)blockIdx.x * (G * U) + g;  // this thread's first row
     TX* yb = y + row0 * N + l * VEC;
     const bool lead = l == 0 && in_group<W>();  // stores rstd
-    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+    // rows wider than a warp: the row reduction's barrier releases the slot
+    ring_loop<(W > 32)>(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* xs = rg.tile(k, 0) + soff;
         const bool full = b < nfull;
         bool okr[U];
@@ -149,7 +150,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(11)
-        GBN_CASE(12)
+        GBN_CASE(12) GBN_CASE(14)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }

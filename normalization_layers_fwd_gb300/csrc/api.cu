@@ -88,23 +88,38 @@ int64_t general_warps(int64_t M, int sms) { return M < 4LL * sms ? M : 4LL * sms
 
 // Whether [M, N] of dtype xt can take the 16-byte vector path (alignment
 // aside), and its schedule index.
-// Multi-vector schedules a kernel may take for rows of more than 256
-// vectors, as a set (bit s - kNumSched1 for schedule s), chosen per kernel
-// within its register budget and by measurement: the DyT and LayerNorm
-// forwards 12-13, the LayerNorm backward 12 and 14, the DyT backward 12,
-// the RMSNorm forward and backward 12 and 14 (the same set, so the
-// backward's recomputed rstd reduces a row in the forward's order).  Other
-// rows, and kernels with an empty set, take the one-vector schedules.
-constexpr unsigned kWide12 = 1u, kWide13 = 2u, kWide14 = 4u;
+// Multi-vector schedules a kernel may take, as a set (bit s - kNumSched1 for
+// schedule s), chosen per kernel within its register budget and by
+// measurement.  Schedule s serves rows of more than half its capacity and at
+// most its capacity (max_nvec / 2 < nvec <= max_nvec), the first in table
+// order that the set holds; other rows take the one-vector schedules.
+constexpr unsigned kWide12 = 1u, kWide13 = 2u, kWide14 = 4u, kWide15 = 8u, kWide16 = 16u;
+
+// Each kernel's set: the DyT forward 12-13 and backward 12; the LayerNorm
+// forward 12, 13 and 16 and backward 12, 14 and 15; the RMSNorm forward and
+// backward 12 and 14 (one set, so the backward's recomputed rstd reduces a
+// row in the forward's order).  The backwards hold at most 2 vectors per
+// thread.  Schedule 15 measured slower than one vector per thread in the
+// forwards and in the RMSNorm backward, 16 faster in the LayerNorm forward.
+unsigned wide_set(int kind)
+{
+    switch (kind) {
+        case gbn::kFwdDyT: return kWide12 | kWide13;
+        case gbn::kBwdDyT: return kWide12;
+        case gbn::kFwdLN: return kWide12 | kWide13 | kWide16;
+        case gbn::kBwdLN: return kWide12 | kWide14 | kWide15;
+        default: return kWide12 | kWide14;  // RMSNorm forward and backward
+    }
+}
 
 int fast_sid(int64_t N, int xt, unsigned wide)
 {
     const int vec = 16 / elem_bytes(xt);
     if (N % vec != 0) return -1;
     const int64_t nvec = N / vec;
-    if (nvec > 256) {
-        for (int s = gbn::kNumSched1; s < gbn::kNumSched; ++s)
-            if (((wide >> (s - gbn::kNumSched1)) & 1u) && nvec <= gbn::kSched[s].max_nvec) return s;
+    for (int s = gbn::kNumSched1; s < gbn::kNumSched; ++s) {
+        const int cap = gbn::kSched[s].max_nvec;
+        if (((wide >> (s - gbn::kNumSched1)) & 1u) && cap / 2 < nvec && nvec <= cap) return s;
     }
     for (int s = 0; s < gbn::kNumSched1; ++s)
         if (nvec <= gbn::kSched[s].max_nvec) return s;
@@ -353,8 +368,7 @@ size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int
     const int kind =
         op == GBN_OP_DYT ? gbn::kBwdDyT : op == GBN_OP_LAYERNORM ? gbn::kBwdLN : gbn::kBwdRms;
     // the vector path with the kernel's wide set, or the general path
-    const Launch a =
-        plan(M, N, xt, true, sms, nullptr, kind, op == GBN_OP_DYT ? kWide12 : kWide12 | kWide14);
+    const Launch a = plan(M, N, xt, true, sms, nullptr, kind, wide_set(kind));
     const Launch b = plan(M, N, xt, false, sms, nullptr, gbn::kBwdLN);
     const size_t need = ws_needed(op, a.P > b.P ? a : b, N);
     return (need + 255) & ~(size_t)255;
@@ -375,7 +389,7 @@ int dyt_fwd_rows(const void* x, const gbn_rows* xl, const void* alpha, const voi
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
-                    gbn::kFwdDyT, kWide12 | kWide13);
+                    gbn::kFwdDyT, wide_set(gbn::kFwdDyT));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -412,7 +426,7 @@ int dyt_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gbn_ro
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
-                    stream, gbn::kBwdDyT, kWide12);
+                    stream, gbn::kBwdDyT, wide_set(gbn::kBwdDyT));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -452,7 +466,7 @@ int layernorm_fwd_rows(const void* x, const gbn_rows* xl, const void* gamma, con
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
-                    gbn::kFwdLN, kWide12 | kWide13);
+                    gbn::kFwdLN, wide_set(gbn::kFwdLN));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -486,7 +500,7 @@ int layernorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const 
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
-                    stream, gbn::kBwdLN, kWide12 | kWide14);
+                    stream, gbn::kBwdLN, wide_set(gbn::kBwdLN));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -541,7 +555,7 @@ int rmsnorm_fwd_rows(const void* x, const gbn_rows* xl, const void* w, void* y, 
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
-                    gbn::kFwdNorm, kWide12 | kWide14);
+                    gbn::kFwdNorm, wide_set(gbn::kFwdNorm));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -573,7 +587,7 @@ int rmsnorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gb
     if (sms <= 0) return GBN_EDEVICE;
     // the forward's set: a recomputed rstd reduces each row in its order
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
-                    stream, gbn::kBwdRms, kWide12 | kWide14);
+                    stream, gbn::kBwdRms, wide_set(gbn::kBwdRms));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;

@@ -44,15 +44,22 @@ struct SchedEntry {
 // with KV = 2 or 4 vectors each (vector l + j*W for j < KV), one row per
 // CTA.  Against schedules 10-11 they divide the per-row reduction and
 // barrier cost by KV; at 256 threads two independent CTAs share an SM.
+// Schedules 15-16: rows of 33-64 and 65-128 vectors held by one warp with
+// KV = 2 or 4 vectors per lane, 8 rows per pass: the row reductions stay
+// inside the warp (shuffles, no barrier), where one vector per lane would
+// spread a row over 2-4 warps and a __syncthreads per reduction.  They pay
+// where a kernel reduces more than once per row (the LayerNorm backward
+// takes 15, the LayerNorm forward 16).
 // Which kernel takes which is decided per kernel by the planner (api.cu),
 // within each kernel's register budget.
-constexpr int kNumSched = 15;
+constexpr int kNumSched = 17;
 constexpr int kNumSched1 = 12;  // the one-vector schedules
 constexpr SchedEntry kSched[kNumSched] = {
     {1, 1, 256, 1},     {2, 2, 256, 1},     {3, 3, 256, 1},     {4, 4, 256, 1},
     {8, 8, 256, 1},     {16, 16, 256, 1},   {32, 32, 256, 1},   {64, 64, 256, 1},
     {128, 128, 256, 1}, {256, 256, 256, 1}, {512, 512, 512, 1}, {1024, 1024, 1024, 1},
     {512, 256, 256, 2}, {1024, 256, 256, 4}, {1024, 512, 512, 2},
+    {64, 32, 256, 2},   {128, 32, 256, 4},
 };
 constexpr int kMaxFastVec = 1024;
 
@@ -868,16 +875,20 @@ __device__ __forceinline__ void cta_store_columns2(const f2 (&acc)[P], float* bu
 }
 
 // KV vectors per thread (vector l + j*W holds columns (l + j*W)*VEC ...).
-// With one vector this is cta_store_columns2; the multi-vector schedules
-// have one row group per CTA, so each thread writes its own columns.
+// With several row groups per CTA, vector j's columns go through
+// cta_store_columns2 at column offset j*W*VEC; with one group per CTA each
+// thread writes its own columns.
 template <int W, int KV, int P, int T>
 __device__ __forceinline__ void cta_store_columns_kv(const f2 (&acc)[KV][P], float* buf,
                                                      float* __restrict__ out_row, int N)
 {
     if constexpr (KV == 1) {
         cta_store_columns2<W, P, T>(acc[0], buf, out_row, N);
+    } else if constexpr (groups_per_cta(W, T) > 1) {
+#pragma unroll
+        for (int j = 0; j < KV; ++j)
+            cta_store_columns2<W, P, T>(acc[j], buf, out_row + j * W * 2 * P, N - j * W * 2 * P);
     } else {
-        static_assert(groups_per_cta(W, T) == 1, "multi-vector schedules hold one group per CTA");
         const int l = lan<W>();
 #pragma unroll
         for (int j = 0; j < KV; ++j) {

@@ -390,7 +390,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9)
-        GBN_CASE(12) GBN_CASE(13)
+        GBN_CASE(12) GBN_CASE(13) GBN_CASE(16)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }
@@ -425,7 +425,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9)
-        GBN_CASE(12) GBN_CASE(14)
+        GBN_CASE(12) GBN_CASE(14) GBN_CASE(15)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }

@@ -28,7 +28,8 @@ int sm_count(int device)
     if (device < 0 || device >= kMaxDevices) return -1;
     int v = g_sms[device].load(std::memory_order_relaxed);
     if (v > 0) return v;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        v <= 0) {
         cudaGetLastError();  // do not leave a sticky error for the caller
         return -1;
     }

@@ -193,7 +193,8 @@ template <typename TX, int S, int kIn>
 __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     dyt_bwd_fast(const TX* __restrict__ x, const TX* __restrict__ dy, TX* __restrict__ dx,
                  const void* __restrict__ alpha, const void* __restrict__ gamma, int pt,
-                 float* __restrict__ ws, int64_t M, int N, int64_t nblocks, unsigned* fault, RowMaps maps)
+                 float* __restrict__ ws, int64_t M, int N, int64_t nblocks, unsigned* fault,
+                 RowMaps maps)
 {
     constexpr int W = kSched[S].W, U = kind_U(S, kBwdDyT), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;

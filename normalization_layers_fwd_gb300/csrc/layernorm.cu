@@ -108,7 +108,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
                     xv[u][j][p] = sub2(xv[u][j][p], m2);  // x - mu, kept for the output
                     q2 = fma2(xv[u][j][p], xv[u][j][p], q2);
                 }
-                q[u] += colok[j] ? lo2(q2) + hi2(q2) : 0.f;  // vectors past the row's end add nothing
+                // vectors past the row's end add nothing
+                q[u] += colok[j] ? lo2(q2) + hi2(q2) : 0.f;
             }
         }
         group_allreduce<W, T, U>(q, red, parity);
@@ -295,7 +296,8 @@ template <typename TX>
 __global__ void __launch_bounds__(kGenThreads)
     ln_fwd_general(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ gamma,
                    const void* __restrict__ beta, int pt, float* __restrict__ mean,
-                   float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n, RowMaps maps, int scattered)
+                   float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n, RowMaps maps,
+                   int scattered)
 {
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * kGenWarps;
@@ -329,7 +331,8 @@ __global__ void __launch_bounds__(kGenThreads)
     ln_bwd_general(const TX* __restrict__ x, const TX* __restrict__ dy,
                    const float* __restrict__ mean, const float* __restrict__ rstd,
                    const void* __restrict__ gamma, int pt, TX* __restrict__ dx,
-                   float* __restrict__ ws, int64_t M, int N, float inv_n, RowMaps maps, int scattered)
+                   float* __restrict__ ws, int64_t M, int N, float inv_n, RowMaps maps,
+                   int scattered)
 {
     const int lane = threadIdx.x & 31;
     const int64_t w = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5);
@@ -372,8 +375,8 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
     TX* yp = static_cast<TX*>(y);
     const float inv_n = (float)(1.0 / (double)N);
     if (!L.fast) {
-        ln_fwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, yp, gamma, beta, pt, mean,
-                                                                 rstd, M, N, eps, inv_n, L.maps, L.scattered);
+        ln_fwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(
+            xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.maps, L.scattered);
         return cudaGetLastError();
     }
     switch (L.sid) {
@@ -384,7 +387,8 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
             constexpr int kIn_ = decltype(m_)::value;                                              \
             ring_attributes<ln_fwd_fast<TX, S, kIn_>>(smem);                                       \
             ln_fwd_fast<TX, S, kIn_><<<L.grid, kSched[S].T, smem, L.stream>>>(                     \
-                xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault, L.maps); \
+                xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault,         \
+                L.maps);                                                                           \
         });                                                                                        \
         break;                                                                                     \
     }
@@ -407,8 +411,8 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     TX* dxp = static_cast<TX*>(dx);
     const float inv_n = (float)(1.0 / (double)N);
     if (!L.fast) {
-        ln_bwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, dyp, mean, rstd, gamma, pt,
-                                                                 dxp, ws, M, N, inv_n, L.maps, L.scattered);
+        ln_bwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(
+            xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.maps, L.scattered);
         return cudaGetLastError();
     }
     switch (L.sid) {

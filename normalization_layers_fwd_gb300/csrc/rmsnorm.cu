@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(kGenThreads)
         const float rs = warp_row_rstd(xr, N, lane, eps, inv_n);
         for (int c = lane; c < N; c += 32) {
             const float xh = ld1(xr, c) * rs;
-            st1(y, r * N + c, rms_weight(w, pt, c, variant) * (variant == 0 ? round_x<TX>(xh) : xh));
+            const float n = variant == 0 ? round_x<TX>(xh) : xh;
+            st1(y, r * N + c, rms_weight(w, pt, c, variant) * n);
         }
         if (rstd && lane == 0) rstd[r] = rs;
     }
@@ -136,8 +137,8 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
     const float inv_n = (float)(1.0 / (double)N);
     const int gemma = variant == 2;
     if (!L.fast) {
-        rms_fwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, yp, w, pt, rstd, M, N, eps,
-                                                                  inv_n, variant, L.maps, L.scattered);
+        rms_fwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(
+            xp, yp, w, pt, rstd, M, N, eps, inv_n, variant, L.maps, L.scattered);
         return cudaGetLastError();
     }
     switch (L.sid) {

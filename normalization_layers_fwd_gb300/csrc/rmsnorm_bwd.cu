@@ -175,7 +175,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
 
     if (ws == nullptr) return;  // no weight gradient requested (uniform)
     float* wrow = ws + blockIdx.x * (int64_t)N;
-    cta_store_columns_kv<W, KV, P, T>(acc, reinterpret_cast<float*>(dsm + 128), wrow, N);  // drained ring slots
+    // the column buffer: drained ring slots, past the barriers
+    cta_store_columns_kv<W, KV, P, T>(acc, reinterpret_cast<float*>(dsm + 128), wrow, N);
 }
 
 template <typename TX>
@@ -229,8 +230,8 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     const float inv_n = (float)(1.0 / (double)N);
     const int gemma = variant == 2;
     if (!L.fast) {
-        rms_bwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, dyp, w, pt, rstd, dxp, ws,
-                                                                  M, N, eps, inv_n, variant, L.maps, L.scattered);
+        rms_bwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(
+            xp, dyp, w, pt, rstd, dxp, ws, M, N, eps, inv_n, variant, L.maps, L.scattered);
         return cudaGetLastError();
     }
     switch (L.sid) {

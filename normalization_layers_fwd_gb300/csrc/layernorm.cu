@@ -176,18 +176,23 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
         }
     }
 
-    // saved statistics of this thread's rows of the block starting at row0
-    float mu_n[U], rs_n[U];
-    auto load_stats = [&](int64_t row0) {
+    // saved statistics of this thread's rows, loaded one row block ahead of
+    // use (*_n), or two (*_nn too) with one vector per thread: measured
+    // faster for those rows, slower for the multi-vector ones
+    constexpr bool kDeep = KV == 1;
+    float mu_n[U], rs_n[U], mu_nn[U], rs_nn[U];
+    auto load_stats = [&](int64_t row0, float (&mu_d)[U], float (&rs_d)[U]) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t row = row0 + u * G;
             const int64_t srow = row < M ? stat_row<kIn>(maps, row) : 0;
-            mu_n[u] = row < M ? __ldcs(mean + srow) : 0.f;
-            rs_n[u] = row < M ? __ldcs(rstd + srow) : 0.f;
+            mu_d[u] = row < M ? __ldcs(mean + srow) : 0.f;
+            rs_d[u] = row < M ? __ldcs(rstd + srow) : 0.f;
         }
     };
-    load_stats((int64_t)blockIdx.x * (G * U) + g);
+    const int64_t bstride = (int64_t)gridDim.x * (G * U);
+    load_stats((int64_t)blockIdx.x * (G * U) + g, mu_n, rs_n);
+    if constexpr (kDeep) load_stats((int64_t)blockIdx.x * (G * U) + g + bstride, mu_nn, rs_nn);
 
     // Pass 1 (before the row reduction) also accumulates the parameter
     // gradients, which do not depend on it; pass 2 needs only xhat and g.
@@ -233,7 +238,16 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
             s[2 * u] = lo2(s1) + hi2(s1);
             s[2 * u + 1] = lo2(s2) + hi2(s2);
         }
-        load_stats(row0 + (int64_t)gridDim.x * (G * U));  // next block of this CTA
+        if constexpr (kDeep) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                mu_n[u] = mu_nn[u];
+                rs_n[u] = rs_nn[u];
+            }
+            load_stats(row0 + 2 * bstride, mu_nn, rs_nn);  // two blocks of this CTA ahead
+        } else {
+            load_stats(row0 + bstride, mu_n, rs_n);  // the next block of this CTA
+        }
         group_allreduce<W, T, 2 * U>(s, red, parity);
 #pragma unroll
         for (int u = 0; u < U; ++u) {

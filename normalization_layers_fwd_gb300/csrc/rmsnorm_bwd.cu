@@ -49,17 +49,23 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
             acc[j][p] = splat2(0.f);
         }
     }
-    float rs_n[U];
-    auto load_rstd = [&](int64_t row0) {
+    // the given rstd of this thread's rows, loaded one row block ahead of use
+    // (rs_n), or two (rs_nn too) with several vectors per thread: measured
+    // faster for those wide rows, slower for the narrow ones
+    constexpr bool kDeep = KV > 1;
+    float rs_n[U], rs_nn[U];
+    auto load_rstd = [&](int64_t row0, float (&dst)[U]) {
         if (rstd) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t row = row0 + u * G;
-                rs_n[u] = row < M ? __ldcs(rstd + stat_row<kIn>(maps, row)) : 0.f;
+                dst[u] = row < M ? __ldcs(rstd + stat_row<kIn>(maps, row)) : 0.f;
             }
         }
     };
-    load_rstd((int64_t)blockIdx.x * (G * U) + g);
+    const int64_t bstride = (int64_t)gridDim.x * (G * U);
+    load_rstd((int64_t)blockIdx.x * (G * U) + g, rs_n);
+    if constexpr (kDeep) load_rstd((int64_t)blockIdx.x * (G * U) + g + bstride, rs_nn);
 
     // Pass 1 (after r is known) computes dn and xhat, the reduction term and
     // the weight-gradient term (independent of the row reduction); pass 2
@@ -78,8 +84,12 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
                 unpack2<TX>(lds128_if(alive && okr[u] && colok[j], xs + u * srow + j * W * 16),
                         xh[u][j]);
             rs[u] = rs_n[u];
+            if constexpr (kDeep) rs_n[u] = rs_nn[u];
         }
-        load_rstd(row0 + (int64_t)gridDim.x * (G * U));
+        if constexpr (kDeep)
+            load_rstd(row0 + 2 * bstride, rs_nn);
+        else
+            load_rstd(row0 + bstride, rs_n);
         if (!rstd) {  // uniform branch: recompute r exactly as the forward does
 #pragma unroll
             for (int u = 0; u < U; ++u) {

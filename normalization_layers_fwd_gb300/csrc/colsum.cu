@@ -9,6 +9,9 @@
 //
 // Block = 32 columns x kSlices slices: slice s sums rows s, s+kSlices, ...
 // in increasing order, then slice 0 adds the kSlices slice sums in order.
+// The partial rows were just written and sit in L2, so the kernel is bound
+// by load latency, not bandwidth: 32 slices with up to 16 loads in flight
+// per thread cover the usual P (a few hundred rows) in one round trip.
 #include "common.cuh"
 #include "internal.h"
 
@@ -16,7 +19,8 @@ namespace gbn {
 namespace {
 
 constexpr int kCols = 32;
-constexpr int kSlices = 16;
+constexpr int kSlices = 32;
+constexpr int kBatch = 16;  // independent loads in flight per thread
 
 __global__ void __launch_bounds__(kCols * kSlices)
     colsum_kernel(const float* __restrict__ ws, int64_t P, int64_t rowlen, int64_t N, int pt,
@@ -27,16 +31,19 @@ __global__ void __launch_bounds__(kCols * kSlices)
     const int64_t c = blockIdx.x * (int64_t)kCols + tx;
     float s = 0.f;
     if (c < rowlen) {
-        // batches of 8 independent loads (all in flight), added in row order
-        int64_t p = ty;
-        for (; p + 7 * kSlices < P; p += 8 * kSlices) {
-            float v[8];
+        // batches of kBatch independent loads (all in flight, the rows past P
+        // masked), added in row order
+        for (int64_t p0 = ty; p0 < P; p0 += kBatch * kSlices) {
+            float v[kBatch];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = ws[(p + i * kSlices) * rowlen + c];
+            for (int i = 0; i < kBatch; ++i) {
+                const int64_t p = p0 + i * kSlices;
+                v[i] = p < P ? __ldcg(ws + p * rowlen + c) : 0.f;
+            }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) s += v[i];
+            for (int i = 0; i < kBatch; ++i)
+                if (p0 + i * kSlices < P) s += v[i];
         }
-        for (; p < P; p += kSlices) s += ws[p * rowlen + c];
     }
     part[ty][tx] = s;
     __syncthreads();

@@ -287,3 +287,58 @@ def test_storage_order_ragged_blocks(op):
     x = seq_major((5, 331, 3), 64, torch.float16, f"rag2/{op}/x")
     dy = seq_major((5, 331, 3), 64, torch.float16, f"rag2/{op}/dy")
     assert check_layout(op, x, dy, _params(64, torch.float32, f"rag2/{op}"))
+
+
+@pytest.mark.parametrize("variant", [1, 2], ids=["weight_first", "gemma"])
+@pytest.mark.parametrize("xdt,wdt", [(torch.bfloat16, torch.bfloat16), (torch.float16, torch.float32),
+                                     (torch.float32, torch.float32)], ids=["bf16", "f16", "f32"])
+def test_rms_variants_head_major(variant, xdt, wdt):
+    """The RMSNorm expression variants on head-major input: per-row outputs
+    equal the contiguous call's; the weight gradient equals the call on the
+    storage."""
+    lead, N = (2, 37, 8), 128
+    x = head_major(lead, N, xdt, f"var{variant}/{xdt}/x")
+    dy = head_major(lead, N, xdt, f"var{variant}/{xdt}/dy")
+    w = _normal((N,), wdt, f"var{variant}/{xdt}/w", 1.0, 0.1)
+
+    def call(a, b):
+        y, rstd = _lib.rmsnorm_fwd(a, w, 1e-6, variant=variant)
+        dx, dw = _lib.rmsnorm_bwd(a, b, w, rstd, 1e-6, variant=variant)
+        return dict(y=y, rstd=rstd, dx=dx, dw=dw)
+    got = call(x, dy)
+    assert_same_bits(got, call(x.contiguous(), dy.contiguous()), {"y", "rstd", "dx"})
+    assert_same_bits(got, call(storage_rows(x), storage_rows(dy)), {"dw"})
+
+
+@pytest.mark.parametrize("make", [head_major, row_padded], ids=["head_major", "row_padded"])
+def test_layernorm_without_affine_strided(make):
+    """LayerNorm with neither gamma nor beta on strided input."""
+    lead = (2, 41, 8) if make is head_major else (513,)
+    N = 256
+    x = make(lead, N, torch.bfloat16, f"noaff/{make.__name__}/x")
+    dy = make(lead, N, torch.bfloat16, f"noaff/{make.__name__}/dy")
+
+    def call(a, b):
+        y, mean, rstd = _lib.layernorm_fwd(a, None, None, 1e-5)
+        dx, dg, db = _lib.layernorm_bwd(a, b, mean, rstd, None)
+        return dict(y=y, mean=mean, rstd=rstd, dx=dx, dg=dg, db=db)
+    got = call(x, dy)
+    perm = storage_rows(x) is not None
+    assert_same_bits(got, call(x.contiguous(), dy.contiguous()),
+                     {"y", "mean", "rstd", "dx"} | (set() if perm else {"dg", "db"}))
+    if perm:
+        assert_same_bits(got, call(storage_rows(x), storage_rows(dy)), {"dg", "db"})
+
+
+def test_dyt_bf16_params_head_major():
+    """DyT with bf16 parameters on head-major bf16 input, alpha large enough
+    that tanh saturates in part of the tensor."""
+    lead, N = (2, 53, 4), 64
+    x = head_major(lead, N, torch.bfloat16, "dytp/x")
+    dy = head_major(lead, N, torch.bfloat16, "dytp/dy")
+    P = {k: v.to(torch.bfloat16) for k, v in _params(N, torch.float32, "dytp").items()}
+    P["alpha"] = torch.full((1,), 7.0, dtype=torch.bfloat16, device="cuda")
+    got = run("dyt", x, dy, P)
+    assert_same_bits(got, run("dyt", x.contiguous(), dy.contiguous(), P), {"y", "dx"})
+    assert_same_bits(got, run("dyt", storage_rows(x), storage_rows(dy), P), {"da", "dg", "db"})
+

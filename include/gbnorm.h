@@ -250,7 +250,8 @@ int rmsnorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gb
  *   GBN_STATIC_WS_BYTES returns GBN_ESCRATCH before launching anything.  The
  *   need is (rows of partials) x N x 4 bytes; at most 5 MB for 16-byte aligned
  *   activations with N a multiple of 8 (bf16) or 4 (f32) up to N = 8192 (bf16)
- *   or 4096 (f32) on 152 SMs, and about 2.4 KB x N on the general path.
+ *   or 4096 (f32) on 152 SMs; on the general path at most 8 MB up to
+ *   N = 3448 (the warp count adapts) and 2.4 KB x N beyond, on 152 SMs.
  *   gbn_bwd_workspace_bytes(GBN_OP_RMSNORM, ...) <= GBN_STATIC_WS_BYTES is a
  *   sufficient check ahead of a call.  With dw null the array is not used.
  *   Set-up: the first call on a device (made current) looks up the array's

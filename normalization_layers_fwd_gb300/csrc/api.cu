@@ -84,8 +84,29 @@ bool all_aligned(int t, std::initializer_list<const void*> ps)
     return true;
 }
 
-// Cap on the general path's warps: each warp owns one workspace row.
-int64_t general_warps(int64_t M, int sms) { return M < 4LL * sms ? M : 4LL * sms; }
+// Warps of the general path: up to 32 per SM.  In a backward each warp owns
+// one workspace row of L floats, so there the count also stays where the
+// workspace is at most 8 MB (GBN_STATIC_WS_BYTES), but not below 4 per SM.
+int64_t general_warps(int64_t M, int sms, int64_t L)
+{
+    int64_t w = 32LL * sms;
+    if (L > 0) {
+        // whole CTAs of kGenWarps: the workspace holds a row per launched warp
+        const int64_t fit = (int64_t(8) << 20) / (4 * L) / gbn::kGenWarps * gbn::kGenWarps;
+        const int64_t floor4 = 4LL * sms;
+        w = fit < w ? (fit > floor4 ? fit : floor4) : w;
+    }
+    return M < w ? M : w;
+}
+
+// Workspace row length (floats) of a backward kernel kind; 0 for a forward.
+int64_t general_ws_floats(int kind, int64_t N)
+{
+    return kind == gbn::kBwdDyT ? gbn::ws_row_floats(0, N)
+           : kind == gbn::kBwdLN ? gbn::ws_row_floats(1, N)
+           : kind == gbn::kBwdRms ? gbn::ws_row_floats(2, N)
+                                  : 0;
+}
 
 // Whether [M, N] of dtype xt can take the 16-byte vector path (alignment
 // aside), and its schedule index.
@@ -145,7 +166,7 @@ Launch plan(int64_t M, int64_t N, int xt, bool aligned, int sms, cudaStream_t st
         L.grid = (int)(L.nblocks < cap ? L.nblocks : cap);
         L.P = L.grid;
     } else {
-        const int64_t warps = general_warps(M, sms);
+        const int64_t warps = general_warps(M, sms, general_ws_floats(kind, N));
         L.fast = 0;
         L.grid = (int)((warps + gbn::kGenWarps - 1) / gbn::kGenWarps);
         L.P = (int64_t)L.grid * gbn::kGenWarps;
@@ -370,7 +391,7 @@ size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int
         op == GBN_OP_DYT ? gbn::kBwdDyT : op == GBN_OP_LAYERNORM ? gbn::kBwdLN : gbn::kBwdRms;
     // the vector path with the kernel's wide set, or the general path
     const Launch a = plan(M, N, xt, true, sms, nullptr, kind, wide_set(kind));
-    const Launch b = plan(M, N, xt, false, sms, nullptr, gbn::kBwdLN);
+    const Launch b = plan(M, N, xt, false, sms, nullptr, kind);
     const size_t need = ws_needed(op, a.P > b.P ? a : b, N);
     return (need + 255) & ~(size_t)255;
 }

@@ -170,6 +170,10 @@ constexpr int ring_smem_bytes(int S, int kind, int NT)
 // alignment) kernels, which give every warp one row at a time.
 constexpr int kGenThreads = 256;
 constexpr int kGenWarps = kGenThreads / 32;
+// Columns of parameter-gradient partials a general backward warp accumulates
+// in shared memory (8 warps x 1536 floats = 48 KB per CTA); wider partial
+// rows accumulate in the warp's workspace row in global memory.
+constexpr int kGenCols = 1536;
 
 // ------------------------------------------------------------- vector types
 template <typename TX> struct Vec;
@@ -224,6 +228,17 @@ __device__ __forceinline__ float ld1(const __nv_bfloat16* p, int64_t i)
 __device__ __forceinline__ float ld1(const __half* p, int64_t i)
 {
     return __half2float(__ldcs(p + i));
+}
+// Cached element loads for the general kernels, whose passes re-read a row
+// (the first pass brings it into L1, the others hit there).
+__device__ __forceinline__ float ld1c(const float* p, int64_t i) { return __ldg(p + i); }
+__device__ __forceinline__ float ld1c(const __nv_bfloat16* p, int64_t i)
+{
+    return __bfloat162float(__ldg(p + i));
+}
+__device__ __forceinline__ float ld1c(const __half* p, int64_t i)
+{
+    return __half2float(__ldg(p + i));
 }
 __device__ __forceinline__ void st1(float* p, int64_t i, float v) { __stcs(p + i, v); }
 __device__ __forceinline__ void st1(__nv_bfloat16* p, int64_t i, float v)

@@ -344,13 +344,18 @@ __global__ void __launch_bounds__(kGenThreads)
                     const void* __restrict__ alpha, const void* __restrict__ gamma, int pt,
                     float* __restrict__ ws, int64_t M, int N, RowMaps maps, int scattered)
 {
+    __shared__ float accs[kGenWarps * kGenCols];
     const int lane = threadIdx.x & 31;
     const int64_t w = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5);
     const int64_t nw = (int64_t)gridDim.x * kGenWarps;
     const int64_t L = 2 * (int64_t)N + 1;
     float* wrow = ws ? ws + w * L : nullptr;
+    // the warp's column sums: in shared memory when they fit, else in its
+    // workspace row; lane c % 32 alone touches column c, rows in order
+    const bool local = 2 * N <= kGenCols;
+    float* arow = local ? accs + (threadIdx.x >> 5) * kGenCols : wrow;
     if (wrow)
-        for (int c = lane; c < 2 * N; c += 32) wrow[c] = 0.f;
+        for (int c = lane; c < 2 * N; c += 32) arow[c] = 0.f;
     const float a = ld_param(alpha, pt, 0);
     float da = 0.f;
     for (int64_t r = w; r < M; r += nw) {
@@ -364,12 +369,14 @@ __global__ void __launch_bounds__(kGenThreads)
             const float ds = dv * s;
             st1(dx, i, ds * (gmv * a));
             if (wrow) {
-                wrow[c] += dv * t;
-                wrow[N + c] += dv;
+                arow[c] += dv * t;
+                arow[N + c] += dv;
             }
             da = fmaf(gmv, ds * xv, da);
         }
     }
+    if (wrow && local)
+        for (int c = lane; c < 2 * N; c += 32) wrow[c] = arow[c];
     float v[1] = {da};
     butterfly<32, 1>(v);
     if (wrow && lane == 0) wrow[2 * N] = v[0];

@@ -318,12 +318,12 @@ __global__ void __launch_bounds__(kGenThreads)
     for (int64_t r = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5); r < M; r += nw) {
         const TX* xr = in_row(x, maps, 0, scattered, r, N);
         float v[1] = {0.f};
-        for (int c = lane; c < N; c += 32) v[0] += ld1(xr, c);
+        for (int c = lane; c < N; c += 32) v[0] += ld1c(xr, c);
         butterfly<32, 1>(v);
         const float mu = v[0] * inv_n;
         float q[1] = {0.f};
         for (int c = lane; c < N; c += 32) {
-            const float d = ld1(xr, c) - mu;
+            const float d = ld1c(xr, c) - mu;
             q[0] += d * d;
         }
         butterfly<32, 1>(q);
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kGenThreads)
         for (int c = lane; c < N; c += 32) {
             const float gm = gamma ? ld_param(gamma, pt, c) : 1.f;
             const float bt = beta ? ld_param(beta, pt, c) : 0.f;
-            st1(y, r * N + c, fmaf((ld1(xr, c) - mu) * rs, gm, bt));
+            st1(y, r * N + c, fmaf((ld1c(xr, c) - mu) * rs, gm, bt));
         }
         if (lane == 0) {
             if (mean) mean[r] = mu;
@@ -348,36 +348,43 @@ __global__ void __launch_bounds__(kGenThreads)
                    float* __restrict__ ws, int64_t M, int N, float inv_n, RowMaps maps,
                    int scattered)
 {
+    __shared__ float accs[kGenWarps * kGenCols];
     const int lane = threadIdx.x & 31;
     const int64_t w = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5);
     const int64_t nw = (int64_t)gridDim.x * kGenWarps;
     float* wrow = ws ? ws + w * (2 * (int64_t)N) : nullptr;
+    // the warp's column sums: in shared memory when they fit, else in its
+    // workspace row; lane c % 32 alone touches column c, rows in order
+    const bool local = 2 * N <= kGenCols;
+    float* arow = local ? accs + (threadIdx.x >> 5) * kGenCols : wrow;
     if (wrow)
-        for (int c = lane; c < 2 * N; c += 32) wrow[c] = 0.f;
+        for (int c = lane; c < 2 * N; c += 32) arow[c] = 0.f;
     for (int64_t r = w; r < M; r += nw) {
         const TX* xr = in_row(x, maps, 0, scattered, r, N);
         const TX* dr = in_row(dy, maps, 1, scattered, r, N);
         const float mu = mean[r], rs = rstd[r];
         float s[2] = {0.f, 0.f};
         for (int c = lane; c < N; c += 32) {
-            const float xh = (ld1(xr, c) - mu) * rs;
-            const float gg = __fmul_rn(ld1(dr, c), gamma ? ld_param(gamma, pt, c) : 1.f);
+            const float xh = (ld1c(xr, c) - mu) * rs;
+            const float gg = __fmul_rn(ld1c(dr, c), gamma ? ld_param(gamma, pt, c) : 1.f);
             s[0] += gg;
             s[1] += gg * xh;
         }
         butterfly<32, 2>(s);
         const float ma = s[0] * inv_n, mb = s[1] * inv_n;
         for (int c = lane; c < N; c += 32) {
-            const float xh = (ld1(xr, c) - mu) * rs;
-            const float dv = ld1(dr, c);
+            const float xh = (ld1c(xr, c) - mu) * rs;
+            const float dv = ld1c(dr, c);
             const float gg = __fmul_rn(dv, gamma ? ld_param(gamma, pt, c) : 1.f);
             st1(dx, r * N + c, rs * (gg - ma - xh * mb));
             if (wrow) {
-                wrow[c] += dv * xh;
-                wrow[N + c] += dv;
+                arow[c] += dv * xh;
+                arow[N + c] += dv;
             }
         }
     }
+    if (wrow && local)
+        for (int c = lane; c < 2 * N; c += 32) wrow[c] = arow[c];
 }
 
 template <typename TX>

@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kGenThreads)
         const TX* xr = in_row(x, maps, 0, scattered, r, N);
         const float rs = warp_row_rstd(xr, N, lane, eps, inv_n);
         for (int c = lane; c < N; c += 32) {
-            const float xh = ld1(xr, c) * rs;
+            const float xh = ld1c(xr, c) * rs;
             const float n = variant == 0 ? round_x<TX>(xh) : xh;
             st1(y, r * N + c, rms_weight(w, pt, c, variant) * n);
         }

@@ -73,7 +73,7 @@ __device__ __forceinline__ float warp_row_rstd(const TX* xr, int N, int lane, fl
 {
     float v[1] = {0.f};
     for (int c = lane; c < N; c += 32) {
-        const float f = ld1(xr, c);
+        const float f = ld1c(xr, c);
         v[0] = fmaf(f, f, v[0]);
     }
     butterfly<32, 1>(v);

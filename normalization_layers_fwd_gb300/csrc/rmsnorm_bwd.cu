@@ -196,37 +196,44 @@ __global__ void __launch_bounds__(kGenThreads)
                     TX* __restrict__ dx, float* __restrict__ ws, int64_t M, int N, float eps,
                     float inv_n, int variant, RowMaps maps, int scattered)
 {
+    __shared__ float accs[kGenWarps * kGenCols];
     const int lane = threadIdx.x & 31;
     const int64_t wi = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5);
     const int64_t nw = (int64_t)gridDim.x * kGenWarps;
     const bool cast_first = variant == 0;  // the Llama expression's rounding points
     const bool round_terms = cast_first && pt != kF32;
     float* wrow = ws ? ws + wi * (int64_t)N : nullptr;
+    // the warp's column sums: in shared memory when they fit, else in its
+    // workspace row; lane c % 32 alone touches column c, rows in order
+    const bool local = N <= kGenCols;
+    float* arow = local ? accs + (threadIdx.x >> 5) * kGenCols : wrow;
     if (wrow)
-        for (int c = lane; c < N; c += 32) wrow[c] = 0.f;
+        for (int c = lane; c < N; c += 32) arow[c] = 0.f;
     for (int64_t r = wi; r < M; r += nw) {
         const TX* xr = in_row(x, maps, 0, scattered, r, N);
         const TX* dr = in_row(dy, maps, 1, scattered, r, N);
         const float rs = rstd ? rstd[r] : warp_row_rstd(xr, N, lane, eps, inv_n);
         float s[1] = {0.f};
         for (int c = lane; c < N; c += 32) {
-            float dn = ld1(dr, c) * rms_weight(w, pt, c, variant);
+            float dn = ld1c(dr, c) * rms_weight(w, pt, c, variant);
             if (cast_first) dn = round_x<TX>(dn);
-            s[0] = fmaf(dn, ld1(xr, c) * rs, s[0]);
+            s[0] = fmaf(dn, ld1c(xr, c) * rs, s[0]);
         }
         butterfly<32, 1>(s);
         const float m = s[0] * inv_n;
         for (int c = lane; c < N; c += 32) {
-            const float dv = ld1(dr, c);
-            const float xh = ld1(xr, c) * rs;
+            const float dv = ld1c(dr, c);
+            const float xh = ld1c(xr, c) * rs;
             float dn = dv * rms_weight(w, pt, c, variant);
             if (cast_first) dn = round_x<TX>(dn);
             st1(dx, r * N + c, rs * (dn - xh * m));
             float term = dv * (cast_first ? round_x<TX>(xh) : xh);
             if (round_terms) term = round_x<TX>(term);
-            if (wrow) wrow[c] += term;
+            if (wrow) arow[c] += term;
         }
     }
+    if (wrow && local)
+        for (int c = lane; c < N; c += 32) wrow[c] = arow[c];
 }
 
 template <typename TX>

@@ -194,9 +194,10 @@ int rmsnorm_bwd_ex(const void* x, const void* dy, const void* w, const float* rs
  *   four dimensions whose last stride is 1 ([B, S, H, D] viewed as M = B*S*H
  *   rows of D with n1 = H, n2 = S: s1, s2, s3 its H, S and B strides; the
  *   head-major [B, H, S, D] transposed to [B, S, H, D] is one such tensor).
- *   n1, n2 >= 1 and s1, s2, s3 >= 0, else GBN_EINVAL.  Rows may overlap
- *   (broadcast strides of 0 are allowed); the outputs (y, dx, the statistics)
- *   stay contiguous [M, N] and must not overlap any input.
+ *   n1, n2 >= 1, s1, s2, s3 >= 0 and every row start below 2^62 bytes,
+ *   else GBN_EINVAL.  Rows may overlap (broadcast strides of 0 are allowed);
+ *   the outputs (y, dx, the statistics) stay contiguous [M, N] and must not
+ *   overlap any input.
  * A null layout means contiguous rows (row r at r * N), so the *_rows entry
  *   points with null layouts are the plain entry points.  A layout that
  *   happens to describe contiguous rows is treated as null.  Otherwise the

@@ -289,6 +289,24 @@ bool contiguous_rows(const gbn_rows& l, int64_t M, int64_t N)
     return l.s3 == l.n1 * l.n2 * N;
 }
 
+// Whether every row start of layout l over M rows, in bytes (e per element),
+// stays below 2^62: the kernels compute row offsets in int64.
+bool layout_extent_ok(const gbn_rows& l, int64_t M, int64_t e)
+{
+    if (M <= 0) return true;
+    const int64_t last = M - 1;
+    const int64_t i1 = last < l.n1 - 1 ? last : l.n1 - 1;
+    const int64_t q = last / l.n1;
+    const int64_t i2 = q < l.n2 - 1 ? q : l.n2 - 1;
+    const int64_t i3 = q / l.n2;
+    int64_t a, b, c, t;
+    if (__builtin_mul_overflow(i1, l.s1, &a) || __builtin_mul_overflow(i2, l.s2, &b) ||
+        __builtin_mul_overflow(i3, l.s3, &c) || __builtin_add_overflow(a, b, &t) ||
+        __builtin_add_overflow(t, c, &t) || __builtin_mul_overflow(t, e, &t))
+        return false;
+    return t < (int64_t(1) << 62);
+}
+
 Inputs input_layouts(const gbn_rows* xl, const gbn_rows* dyl, const void* x, const void* dy,
                      int64_t M, int64_t N, int xt)
 {
@@ -303,7 +321,8 @@ Inputs input_layouts(const gbn_rows* xl, const gbn_rows* dyl, const void* x, con
         m = gbn::RowMap{M > 0 ? M : 1, N * e, 1, 0, 0};
         const gbn_rows* l = ls[t];
         if (!l) continue;
-        if (l->n1 < 1 || l->n2 < 1 || l->s1 < 0 || l->s2 < 0 || l->s3 < 0) {
+        if (l->n1 < 1 || l->n2 < 1 || l->s1 < 0 || l->s2 < 0 || l->s3 < 0 ||
+            !layout_extent_ok(*l, M, e)) {
             in.ok = false;
             continue;
         }

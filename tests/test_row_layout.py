@@ -80,7 +80,9 @@ def test_rows_entry_points_validate_layouts(lib):
     p = ctypes.c_void_p(16)
     R = _lib.gbn_rows
     bad = [R(0, 8, 1, 0, 0), R(2, 8, 0, 0, 0), R(2, -8, 1, 0, 0), R(2, 8, 2, -1, 0),
-           R(2, 8, 2, 16, -32)]
+           R(2, 8, 2, 16, -32),
+           # row starts beyond 2^62 bytes (or overflowing int64) are rejected
+           R(2, 1 << 61, 1, 0, 0), R(2, 8, 2, 16, (1 << 63) - 1), R(8, 1 << 60, 1, 0, 0)]
     for lay in bad:
         ref = ctypes.byref(lay)
         assert lib.dyt_fwd_rows(p, ref, p, p, p, p, 8, 8, 1, 0, None) == GBN_EINVAL

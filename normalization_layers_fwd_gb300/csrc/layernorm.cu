@@ -20,6 +20,17 @@
 namespace gbn {
 namespace {
 
+// The row mean s / N from the row sum: s * (1/N) plus one residual step
+// (s - mu N, formed exactly by an fma, times 1/N), which gives the
+// correctly rounded quotient where s * fl(1/N) may miss it by an ulp.  A
+// constant row (whose sum is exact) then has x - mean = 0 exactly: its
+// rstd is 1/sqrt(eps), so any error in the mean would reach y magnified.
+__device__ __forceinline__ float row_mean(float s, float n, float inv_n)
+{
+    const float mu = s * inv_n;
+    return fmaf(fmaf(-mu, n, s), inv_n, mu);
+}
+
 // ------------------------------------------------------------ fast forward
 // x streams through the ring; two row all-reduces (sum, then the centred sum
 // of squares) per row.  Every thread runs every row (row reductions are
@@ -45,6 +56,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
     for (int j = 0; j < KV; ++j) colok[j] = in_group<W>() && l + j * W < N / VEC;
     const int rb = N * (int)sizeof(TX);
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
+    const float fN = (float)N;
 
     f2 gm[KV][P], bt[KV][P];
 #pragma unroll
@@ -97,7 +109,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
         float mu[U], q[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            mu[u] = s[u] * inv_n;
+            mu[u] = row_mean(s[u], fN, inv_n);
             const f2 m2 = splat2(mu[u]);
             q[u] = 0.f;
 #pragma unroll
@@ -320,7 +332,7 @@ __global__ void __launch_bounds__(kGenThreads)
         float v[1] = {0.f};
         for (int c = lane; c < N; c += 32) v[0] += ld1c(xr, c);
         butterfly<32, 1>(v);
-        const float mu = v[0] * inv_n;
+        const float mu = row_mean(v[0], (float)N, inv_n);
         float q[1] = {0.f};
         for (int c = lane; c < N; c += 32) {
             const float d = ld1c(xr, c) - mu;

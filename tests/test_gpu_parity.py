@@ -304,6 +304,35 @@ def test_dyt_large_arguments(xdt):
     torch.testing.assert_close(dg, (dy.float() * sgn).sum(0), rtol=1e-5, atol=1e-5)
 
 
+@pytest.mark.parametrize("op", ["dyt", "layernorm", "rmsnorm"])
+@pytest.mark.parametrize("dts", [(torch.bfloat16, torch.float32), (torch.float32, torch.float32),
+                                 (torch.float16, torch.float16)], ids=["bf16", "f32", "f16"])
+@pytest.mark.parametrize("N", [128, 1000])
+def test_degenerate_rows(op, dts, N):
+    """Rows the method treats specially, mixed into random ones: constant
+    rows (LayerNorm: zero variance, so y = beta), all-zero rows (RMSNorm:
+    rstd = 1/sqrt(eps), y = 0; DyT: y = beta), against the oracle; and exact
+    results where they are exact (a constant 1.5 sums exactly at N = 128)."""
+    xdt, pdt = dts
+    M = 301
+    inp = _inputs(M, N, xdt, pdt, f"degenerate/{op}/{N}/{xdt}/{pdt}")
+    x = inp["x"]
+    const = torch.arange(M, device="cuda") % 3 == 0
+    fill = 1.5 if op == "layernorm" else 0.0
+    x[const] = fill
+    inp["x"] = x
+    reps, out = _run(op, inp)
+    for r in reps:
+        print(r.line())
+    beta, gamma = inp["beta"], inp["gamma"]
+    if op == "layernorm" and N == 128:
+        assert torch.equal(out["y"][const], beta.to(xdt).expand(int(const.sum()), N))
+    if op == "dyt":
+        assert torch.equal(out["y"][const], beta.to(xdt).expand(int(const.sum()), N))
+    if op == "rmsnorm":
+        assert torch.all(out["y"][const] == 0)
+
+
 def test_autograd_wrappers_match_direct_calls():
     inp = _inputs(513, 256, torch.bfloat16, torch.float32, "ag")
     for fn, params, direct in [

@@ -37,8 +37,8 @@
  *   reads.  One workspace must not serve two calls that may overlap on the
  *   GPU.  With every parameter-gradient output null, ws may be null.
  * Determinism.  The launch layout is a fixed function of (M, N, dtypes,
- *   alignment, SM count) and no float atomics are used: identical inputs
- *   give bit-identical outputs on the same device.
+ *   alignment, row layout, SM count) and no float atomics are used:
+ *   identical inputs give bit-identical outputs on the same device.
  * Empty input.  M == 0 is a successful call that writes zero parameter
  *   gradients (it still needs `stream` to be valid).
  * Errors.  Invalid arguments return an error status BEFORE anything is

@@ -628,3 +628,65 @@ def test_rms_near_tie_allowance(O):
     assert np.all(al_b == 0)
     _, _, al_f = O.rms_bwd_rows(bf, dy, 1e-6, w, O.F32, O.PARITY)
     assert np.any(al_f > 0)
+
+
+# ------------------------------------------- linearity and equivariance
+# Facts of every layer's backward as a function of its inputs: the gradients
+# are linear in dy; permuting rows permutes the row outputs and leaves the
+# column sums unchanged; permuting columns (with the per-column parameters)
+# permutes every per-column output.  A wrong row or column index, a parameter
+# applied to the wrong column, or dy entering non-linearly fails one of them.
+
+def _backwards(O, x, dy, g, b, eps):
+    """Every backward output of the three layers (math mode, float64)."""
+    out = {}
+    out["dyt dx"] = O.dyt_bwd_rows(x, dy, 0.9, g)
+    c = O.dyt_bwd_cols(x, dy, 0.9, g)
+    out["dyt dgamma"], out["dyt dbeta"] = c["dgamma"], c["dbeta"]
+    out["dyt dalpha"] = np.array([c["dalpha"]])
+    _, _, mu, rs = O.ln_fwd(x, eps, g, b)
+    out["ln dx"] = O.ln_bwd_rows(x, dy, mu, rs, g)[0]
+    c = O.ln_bwd_cols(x, dy, mu, rs)
+    out["ln dgamma"], out["ln dbeta"] = c["dgamma"], c["dbeta"]
+    out["rms dx"] = O.rms_bwd_rows(x, dy, eps, g, O.F32, O.MATH)[0]
+    out["rms dw"] = O.rms_bwd_cols(x, dy, eps, O.F32, O.MATH)[0]
+    return out
+
+
+def test_backwards_linear_in_dy(O):
+    rng = np.random.default_rng(40)
+    M, N = 6, 11
+    x = rng.standard_normal((M, N))
+    d1, d2 = rng.standard_normal((M, N)), rng.standard_normal((M, N))
+    g, b = 1 + 0.3 * rng.standard_normal(N), rng.standard_normal(N)
+    a1, a2 = 0.75, -2.5
+    o1 = _backwards(O, x, d1, g, b, 0.01)
+    o2 = _backwards(O, x, d2, g, b, 0.01)
+    o12 = _backwards(O, x, a1 * d1 + a2 * d2, g, b, 0.01)
+    for k in o12:
+        np.testing.assert_allclose(o12[k], a1 * o1[k] + a2 * o2[k], rtol=1e-12, atol=1e-12,
+                                   err_msg=k)
+
+
+def test_backwards_equivariant_under_row_and_column_permutations(O):
+    rng = np.random.default_rng(41)
+    M, N = 7, 9
+    x = rng.standard_normal((M, N)) + 0.5
+    dy = rng.standard_normal((M, N))
+    g, b = 1 + 0.3 * rng.standard_normal(N), rng.standard_normal(N)
+    base = _backwards(O, x, dy, g, b, 0.02)
+    pr, pc = rng.permutation(M), rng.permutation(N)
+    rows = _backwards(O, x[pr], dy[pr], g, b, 0.02)
+    cols = _backwards(O, x[:, pc], dy[:, pc], g[pc], b[pc], 0.02)
+    for k in base:
+        if k.endswith(" dx"):
+            np.testing.assert_allclose(rows[k], base[k][pr], rtol=1e-13, atol=1e-14, err_msg=k)
+            np.testing.assert_allclose(cols[k], base[k][:, pc], rtol=1e-12, atol=1e-13,
+                                       err_msg=k)
+        elif k == "dyt dalpha":
+            np.testing.assert_allclose(rows[k], base[k], rtol=1e-12, err_msg=k)
+            np.testing.assert_allclose(cols[k], base[k], rtol=1e-12, err_msg=k)
+        else:
+            np.testing.assert_allclose(rows[k], base[k], rtol=1e-12, atol=1e-13, err_msg=k)
+            np.testing.assert_allclose(cols[k], base[k][pc], rtol=1e-12, atol=1e-13,
+                                       err_msg=k)

@@ -519,6 +519,73 @@ def test_rms_parity_rounding_points_f16(O):
     np.testing.assert_allclose(dx, dxm, rtol=0, atol=2.0 ** -8 * np.abs(dxm).max())
 
 
+def _as16(vals, act):
+    """float64 values that are bfloat16 (or binary16) values -> the stored
+    16-bit array the oracle takes (raw bf16 patterns, or float16)."""
+    v = np.asarray(vals, dtype=np.float64)
+    if act == "bf16":
+        return (v.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    return v.astype(np.float16)
+
+
+def _round16(O, vals, act):
+    return O.round_bf16_array(vals) if act == "bf16" else O.round_f16_array(vals)
+
+
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+@pytest.mark.parametrize("wkind", ["f32", "act"])
+def test_rms_parity_dn_is_the_only_backward_rounding(O, act, wkind):
+    """Where the parity backward rounds (DS 8645 "Semantics"): dn = round_x(dy*w)
+    and nothing else before dx.  Pinned by two structural facts:
+    (a) with w = 1, dy*w = dy is already a 16-bit value, so parity dx must be
+        math dx bit for bit; a rounding misplaced onto xhat or onto dn*xhat
+        would change it;
+    (b) with w = 1.75 (3 significant bits, so dy*w needs up to 11 or 14 and
+        is rounded), parity dx on (dy, w) must be math dx on
+        (dy' = round_x(1.75 dy), w = 1) bit for bit, while math dx on
+        (dy, 1.75) differs: skipping the rounding fails (b), and rounding
+        anything but the product fails (a) or (b).
+    The weight's dtype code (f32 or the activation's) must not move it."""
+    rng = np.random.default_rng(40 if act == "bf16" else 41)
+    M, N = 8, 32
+    xs = _as16(_round16(O, rng.standard_normal((M, N)), act), act)
+    dys = _as16(_round16(O, rng.standard_normal((M, N)), act), act)
+    dyv = (dys.astype(np.uint32) << 16).view(np.float32).astype(np.float64) if act == "bf16" \
+        else dys.astype(np.float64)
+    wcode = O.F32 if wkind == "f32" else (O.BF16 if act == "bf16" else O.F16)
+    eps = 1e-6
+    one = np.ones(N)
+    # (a) an exact product: nothing to round before dx
+    dp, *_ = O.rms_bwd_rows(xs, dys, eps, one, wcode, O.PARITY)
+    dm, *_ = O.rms_bwd_rows(xs, dys, eps, one, wcode, O.MATH)
+    np.testing.assert_array_equal(dp, dm)
+    # (b) the product rounded where the page rounds it
+    w = np.full(N, 1.75)
+    dyr = _as16(_round16(O, 1.75 * dyv, act), act)
+    assert not np.array_equal(_round16(O, 1.75 * dyv, act), 1.75 * dyv)  # roundings happen
+    dp, *_ = O.rms_bwd_rows(xs, dys, eps, w, wcode, O.PARITY)
+    want, *_ = O.rms_bwd_rows(xs, dyr, eps, one, wcode, O.MATH)
+    np.testing.assert_array_equal(dp, want)
+    skipped, *_ = O.rms_bwd_rows(xs, dys, eps, w, wcode, O.MATH)
+    assert not np.array_equal(dp, skipped)
+
+
+@pytest.mark.parametrize("act", ["bf16", "f16"])
+def test_rms_parity_forward_rounds_n_before_the_weight(O, act):
+    """The parity forward rounds n = x r, then multiplies by w (DS 8645
+    "Semantics"): y(w) = w * y(1) exactly for w = 1.75 (a 3-bit value times
+    a 16-bit n is exact in float64), which a rounding of w * xhat, or none,
+    would not give."""
+    rng = np.random.default_rng(42 if act == "bf16" else 43)
+    xs = _as16(_round16(O, rng.standard_normal((6, 24)), act), act)
+    y1, *_ = O.rms_fwd(xs, 1e-6, np.ones(24), O.PARITY)
+    yw, *_ = O.rms_fwd(xs, 1e-6, np.full(24, 1.75), O.PARITY)
+    np.testing.assert_array_equal(yw, 1.75 * y1)
+    ym, *_ = O.rms_fwd(xs, 1e-6, np.full(24, 1.75), O.MATH)
+    assert not np.array_equal(yw, ym)
+    assert not np.array_equal(yw, _round16(O, ym, act))
+
+
 def test_rms_variants_math_and_fd(O):
     """In math mode the weight-first expression is the Llama one (only the
     rounding points differ), and Gemma's is the Llama one with w -> 1 + w;

@@ -20,11 +20,18 @@
 namespace gbn {
 namespace {
 
-// The row mean s / N from the row sum: s * (1/N) plus one residual step
-// (s - mu N, formed exactly by an fma, times 1/N), which gives the
-// correctly rounded quotient where s * fl(1/N) may miss it by an ulp.  A
-// constant row (whose sum is exact) then has x - mean = 0 exactly: its
-// rstd is 1/sqrt(eps), so any error in the mean would reach y magnified.
+// The row mean s / N from the row sum by Markstein's correction step
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q = fl(s y) with
+// y = fl(1/N), the residual r = s - q N in one fma, then fl(q + r y) in
+// another.  Markstein's theorem: when y is 1/N rounded to nearest and q is
+// within an ulp of s/N, r is exact and fl(q + r y) is s/N correctly rounded
+// (barring underflow), where q alone may miss it by an ulp.  A constant row
+// of value c has the exact sum s = N c; q is c or a neighbour of c, so
+// r = N (c - q) is exact and q + r y = c + (c - q)(N y - 1), with
+// |N y - 1| <= 2^-24, rounds to c: x - mean = 0 exactly and y = beta
+// (rstd is 1/sqrt(eps) there, so any error in the mean would reach y
+// magnified).
 __device__ __forceinline__ float row_mean(float s, float n, float inv_n)
 {
     const float mu = s * inv_n;

@@ -245,24 +245,31 @@ int rmsnorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gb
  *   cudaMalloc/cudaFree because they can synchronize the device).  Arguments,
  *   kernels, launch layout and results are those of rmsnorm_bwd; the partial
  *   column sums of dw go to a static device array of GBN_STATIC_WS_BYTES
- *   (8 MiB) inside the library, held by every device that loads the library
- *   until the process exits.  The call allocates nothing.
+ *   (8 MiB) inside the library, held by every device (every context) that
+ *   loads the library until the process exits.  The call allocates nothing.
  *   Limit: a call with dw non-null and M > 0 whose partial sums need more than
  *   GBN_STATIC_WS_BYTES returns GBN_ESCRATCH before launching anything.  The
- *   need is (rows of partials) x N x 4 bytes; at most 5 MB for 16-byte aligned
- *   activations with N a multiple of 8 (bf16) or 4 (f32) up to N = 8192 (bf16)
- *   or 4096 (f32) on 152 SMs; on the general path at most 8 MB up to
- *   N = 3448 (the warp count adapts) and 2.4 KB x N beyond, on 152 SMs.
- *   gbn_bwd_workspace_bytes(GBN_OP_RMSNORM, ...) <= GBN_STATIC_WS_BYTES is a
- *   sufficient check ahead of a call.  With dw null the array is not used.
- *   Set-up: the first call on a device (made current) looks up the array's
- *   device address with cudaGetSymbolAddress; make that first call before
- *   any stream capture.  Returns GBN_EDEVICE when the lookup fails.
- *   Sharing: every call on a device uses the same array, which keeps the last
- *   call's contents (nothing in it needs to start at zero: each call writes
- *   every partial row before reading it).  Calls that may overlap on the GPU
- *   (different streams, or host threads without ordering) race on the array
- *   and give wrong dw. */
+ *   need is (rows of partials) x N x 4 bytes, which grows with the device's
+ *   SM count S: on the vector path (16-byte aligned activations, N a multiple
+ *   of 8 for 16-bit or 4 for f32 activations, N <= 8192 or 4096) at most
+ *   32 KiB x S, within the array for S <= 256; on the general path, with
+ *   S' = S rounded up to an even number, at most 8 MiB while N <= 2^19 / S'
+ *   (the number of warps adapts) and 16 x S' x N bytes beyond (for M of at
+ *   least 4 S' rows).  gbn_bwd_workspace_bytes(GBN_OP_RMSNORM, ...), an upper
+ *   bound over both paths, <= GBN_STATIC_WS_BYTES is a sufficient check
+ *   ahead of a call.  With dw null the array is not used.
+ *   Set-up: the array's device address belongs to the CUDA context that
+ *   loaded the library's module, so it is looked up with
+ *   cudaGetSymbolAddress on the first call in each context (made current)
+ *   and cached under that context's id; a new context (after
+ *   cudaDeviceReset, or a second context on the device) looks it up again.
+ *   Make the first call in a context before any stream capture.  Returns
+ *   GBN_EDEVICE when the lookup fails.
+ *   Sharing: every call in a context uses the same array, which keeps the
+ *   last call's contents (nothing in it needs to start at zero: each call
+ *   writes every partial row before reading it).  Calls that may overlap on
+ *   the GPU (different streams, or host threads without ordering) race on the
+ *   array and give wrong dw. */
 #define GBN_STATIC_WS_BYTES (8u << 20)
 int rmsnorm_bwd_static_ws(const void* x, const void* dy, const void* w, const float* rstd,
                           void* dx, void* dw, int64_t M, int64_t N, float eps, int xt, int wt,

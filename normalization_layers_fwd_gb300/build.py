@@ -25,7 +25,7 @@ LIB = os.path.join(OUT, "libgbnorm.so")
 
 SOURCES = ["api.cu", "colsum.cu", "dyt.cu", "layernorm.cu", "rmsnorm.cu", "rmsnorm_bwd.cu",
            "static_ws.cu"]
-HEADERS = ["common.cuh", "internal.h", "rmsnorm.cuh"]
+HEADERS = ["common.cuh", "ctx_cache.h", "internal.h", "rmsnorm.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE,

@@ -1,16 +1,56 @@
 // api.cu -- the extern "C" entry points of libgbnorm.so: argument checks,
 // the fixed launch-layout table, and the launches (kernel files hold the
 // kernels).  Nothing here allocates memory or synchronizes.
+#include <cuda.h>  // CUcontext and CUresult only: the driver is reached through entry points
+
 #include <atomic>
 #include <climits>
 #include <cmath>
 #include <initializer_list>
 
 #include "common.cuh"
+#include "ctx_cache.h"
 #include "gbnorm.h"
 #include "internal.h"
 
 using gbn::Launch;
+
+namespace gbn {
+
+// The unique id of the calling thread's current context, plus one (0 means
+// no context is current, or the driver cannot be reached).  cuCtxGetCurrent
+// and cuCtxGetId come from the runtime's driver entry-point table, so the
+// library needs no link-time dependency on the driver library and loads on
+// a host without one.
+uint64_t current_ctx_id()
+{
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static std::atomic<void*> s_cur{nullptr}, s_id{nullptr};
+    void* cur = s_cur.load(std::memory_order_acquire);
+    void* gid = s_id.load(std::memory_order_acquire);
+    if (!cur || !gid) {
+        cudaDriverEntryPointQueryResult qa{}, qb{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &cur, 12000, cudaEnableDefault,
+                                             &qa) != cudaSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &gid, 12000, cudaEnableDefault, &qb) !=
+                cudaSuccess ||
+            qa != cudaDriverEntryPointSuccess || qb != cudaDriverEntryPointSuccess || !cur ||
+            !gid) {
+            cudaGetLastError();
+            return 0;
+        }
+        s_cur.store(cur, std::memory_order_release);
+        s_id.store(gid, std::memory_order_release);
+    }
+    CUcontext c = nullptr;
+    if (reinterpret_cast<GetCurrent>(cur)(&c) != CUDA_SUCCESS || !c) return 0;
+    unsigned long long id = 0;
+    if (reinterpret_cast<GetId>(gid)(c, &id) != CUDA_SUCCESS) return 0;
+    return (uint64_t)id + 1;
+}
+
+}  // namespace gbn
 
 namespace {
 
@@ -19,9 +59,10 @@ std::atomic<int> g_sms[kMaxDevices];  // 0 = not yet queried
 
 // Fault word: bit 0 = a kernel's bounded barrier wait ran out (the kernel then
 // finished without loading or storing; its outputs are not valid).  One per
-// device (a __device__ variable), read and cleared by gbn_read_faults().
+// device and context (a __device__ variable), read and cleared by
+// gbn_read_faults().  Its address is cached per context.
 __device__ unsigned int g_fault_word;
-std::atomic<unsigned*> g_fault_ptr[kMaxDevices];
+gbn::CtxCache<unsigned*> g_fault_ptr;
 
 int sm_count(int device)
 {
@@ -49,21 +90,21 @@ int current_device()
 
 int current_sms() { return sm_count(current_device()); }
 
-// Device address of the current device's fault word (cached per device).
+// Device address of the fault word in the current context (cached per
+// context: the address belongs to the context that loaded the module).
 unsigned* fault_ptr()
 {
-    const int dev = current_device();
-    if (dev < 0 || dev >= kMaxDevices) return nullptr;
-    unsigned* p = g_fault_ptr[dev].load(std::memory_order_relaxed);
-    if (p) return p;
-    void* a = nullptr;
-    if (cudaGetSymbolAddress(&a, g_fault_word) != cudaSuccess) {
-        cudaGetLastError();
-        return nullptr;
-    }
-    p = static_cast<unsigned*>(a);
-    g_fault_ptr[dev].store(p, std::memory_order_relaxed);
-    return p;
+    unsigned* p = nullptr;
+    const bool ok = g_fault_ptr.get(gbn::current_ctx_id, [](unsigned*& v) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_fault_word) != cudaSuccess || !a) {
+            cudaGetLastError();
+            return false;
+        }
+        v = static_cast<unsigned*>(a);
+        return true;
+    }, p);
+    return ok ? p : nullptr;
 }
 
 bool dtype_ok(int t) { return t == gbn::kF32 || t == gbn::kBF16 || t == gbn::kF16; }
@@ -278,15 +319,18 @@ bool storage_order(const gbn::RowMap& m, int64_t M, int64_t rb, gbn::OutMap& o)
     return true;
 }
 
-// Whether layout l places row r at r * N for every r < M.
+// Whether layout l places row r at r * N for every r < M (levels that no
+// row reaches are ignored; products are checked, so huge sizes of unused
+// levels cannot overflow).
 bool contiguous_rows(const gbn_rows& l, int64_t M, int64_t N)
 {
     if (M <= 1) return true;
     if (l.s1 != N) return false;
     if (M <= l.n1) return true;
-    if (l.s2 != l.n1 * N) return false;
-    if (M <= l.n1 * l.n2) return true;
-    return l.s3 == l.n1 * l.n2 * N;
+    int64_t n12;
+    if (l.s2 != l.n1 * N) return false;  // n1 < M here, so n1 * N <= M * N fits
+    if (__builtin_mul_overflow(l.n1, l.n2, &n12) || M <= n12) return true;
+    return l.s3 == n12 * N;  // n12 < M here
 }
 
 // Whether every row start of layout l over M rows, in bytes (e per element),
@@ -332,7 +376,19 @@ Inputs input_layouts(const gbn_rows* xl, const gbn_rows* dyl, const void* x, con
         const int64_t n1 = l->n1 < M ? l->n1 : M;
         const int64_t q = (M + n1 - 1) / n1;
         const int64_t n2 = l->n2 < q ? l->n2 : q;
-        m = gbn::RowMap{n1, l->s1 * e, n2, l->s2 * e, l->s3 * e};
+        // The stride of a level that no row reaches multiplies only zero
+        // (n1 == 1: every r % n1 is 0; n2 == 1: every (r / n1) % n2 is 0;
+        // n1 * n2 >= M: every r / (n1 n2) is 0), so it is dropped before it
+        // is scaled to bytes: a huge unused stride must not overflow.  The
+        // strides that are reached were bounded by layout_extent_ok.
+        int64_t b1 = 0, b2 = 0, b3 = 0;
+        if ((n1 > 1 && __builtin_mul_overflow(l->s1, e, &b1)) ||
+            (n2 > 1 && __builtin_mul_overflow(l->s2, e, &b2)) ||
+            (n1 * n2 < M && __builtin_mul_overflow(l->s3, e, &b3))) {
+            in.ok = false;
+            continue;
+        }
+        m = gbn::RowMap{n1, b1, n2, b2, b3};
         in.scattered |= 1 << t;
         if (!aligned16(base[t]) || (m.s1 | m.s2 | m.s3) % 16 != 0) in.vec_ok = false;
     }

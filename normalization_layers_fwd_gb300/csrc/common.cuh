@@ -14,6 +14,7 @@
 
 #include <type_traits>
 
+#include "ctx_cache.h"
 #include "internal.h"
 
 namespace gbn {
@@ -917,9 +918,6 @@ __device__ __forceinline__ void cta_store_columns_kv(const f2 (&acc)[KV][P], flo
     }
 }
 
-// Raise a kernel's dynamic shared-memory limit and prefer the maximum
-// shared-memory carve-out, once per kernel per device (host side).  The
-// template parameter is the kernel itself, so every kernel has its own flag.
 // Call f(std::integral_constant<int, m>) for the launch's input mode m.
 template <class F>
 inline void with_mode(int in_mode, F&& f)
@@ -932,18 +930,27 @@ inline void with_mode(int in_mode, F&& f)
         f(std::integral_constant<int, kInContig>{});
 }
 
+// Raise a kernel's dynamic shared-memory limit and prefer the maximum
+// shared-memory carve-out, once per kernel per context (host side: function
+// attributes belong to the context that loaded the module).  The template
+// parameter is the kernel itself, so every kernel has its own cache.  A
+// failed attempt is not cached (the launch then fails and reports it).
 template <auto Kernel>
 inline void ring_attributes(int smem)
 {
-    static unsigned long long done = 0;  // bit d: device d configured
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
-    const unsigned long long bit = 1ull << dev;
-    if (__atomic_load_n(&done, __ATOMIC_RELAXED) & bit) return;
-    cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(Kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
-    __atomic_fetch_or(&done, bit, __ATOMIC_RELAXED);
+    static CtxCache<char> done;
+    char ok = 0;
+    done.get(current_ctx_id, [smem](char& v) {
+        if (cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(Kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        v = 1;
+        return true;
+    }, ok);
 }
 
 }  // namespace gbn

@@ -54,6 +54,11 @@ struct Launch {
     RowMaps maps;
 };
 
+// The unique id of the calling thread's current CUDA context, plus one; 0
+// when no context is current or the driver cannot be reached (api.cu).
+// Host-side caches of device addresses and function attributes key on it.
+uint64_t current_ctx_id();
+
 // Workspace row length (floats) per layer: the per-column partial sums of
 // every parameter gradient, plus one scalar for DyT's alpha.
 inline int64_t ws_row_floats(int op, int64_t N)

@@ -13,35 +13,36 @@
 // launch layout and the same results, as rmsnorm_bwd, but puts the per-CTA
 // partial column sums of dw into g_static_ws below.  It allocates nothing and
 // calls no allocating routine.
-#include <atomic>
-
+#include "ctx_cache.h"
 #include "gbnorm.h"
+#include "internal.h"
 
-// The scratch.  Every device that loads this library holds these
-// GBN_STATIC_WS_BYTES bytes until the process exits.  In host code the name
-// g_static_ws only stands for the device variable; its device address comes
-// from cudaGetSymbolAddress (static_ws_ptr below).
+// The scratch.  Every device (every context) that loads this library holds
+// these GBN_STATIC_WS_BYTES bytes until the process exits.  In host code the
+// name g_static_ws only stands for the device variable; its device address
+// comes from cudaGetSymbolAddress (static_ws_ptr below).
 static __device__ __align__(256) unsigned char g_static_ws[GBN_STATIC_WS_BYTES];
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_static_ws_ptr[kMaxDevices];
+gbn::CtxCache<void*> g_static_ws_ptr;
 
-// Device address of g_static_ws on device `dev`, which must be current.
-// Looked up once per device, on the first call there; later calls read the
-// cached value.  Returns null when the lookup fails.
-void* static_ws_ptr(int dev)
+// Device address of g_static_ws in the current context.  Looked up with
+// cudaGetSymbolAddress on the first call in each context and cached under
+// the context's id: the address belongs to the context that loaded the
+// module, so a new context (after cudaDeviceReset, or a second context on
+// the device) looks it up again.  Returns null when the lookup fails.
+void* static_ws_ptr()
 {
-    void* p = g_static_ws_ptr[dev].load(std::memory_order_acquire);
-    if (p) return p;
-    void* a = nullptr;
-    if (cudaGetSymbolAddress(&a, g_static_ws) != cudaSuccess || !a) {
-        cudaGetLastError();  // leave no sticky error behind
-        return nullptr;
-    }
-    g_static_ws_ptr[dev].store(a, std::memory_order_release);
-    return a;
+    void* p = nullptr;
+    const bool ok = g_static_ws_ptr.get(gbn::current_ctx_id, [](void*& v) {
+        if (cudaGetSymbolAddress(&v, g_static_ws) != cudaSuccess || !v) {
+            cudaGetLastError();  // leave no sticky error behind
+            return false;
+        }
+        return true;
+    }, p);
+    return ok ? p : nullptr;
 }
 
 }  // namespace
@@ -50,13 +51,7 @@ extern "C" int rmsnorm_bwd_static_ws(const void* x, const void* dy, const void* 
                                      const float* rstd, void* dx, void* dw, int64_t M, int64_t N,
                                      float eps, int xt, int wt, cudaStream_t stream)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return GBN_EDEVICE;
-    }
-    if (dev < 0 || dev >= kMaxDevices) return GBN_EDEVICE;
-    void* ws = static_ws_ptr(dev);
+    void* ws = static_ws_ptr();
     if (!ws) return GBN_EDEVICE;
     // Nothing in the array has to start at zero: the first kernel writes
     // every partial row that the column-sum kernel then reads, so what an

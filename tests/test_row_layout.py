@@ -115,3 +115,29 @@ def test_valid_layouts_get_to_the_device_query(lib):
     # an empty input needs no device in the forward
     ref = ctypes.byref(R(4, 16, 2, 64, 128))
     assert lib.dyt_fwd_rows(None, ref, p, p, p, None, 0, 8, 1, 0, None) == GBN_OK
+
+
+def test_unused_levels_take_any_stride(lib):
+    """A level that no row reaches (n1 == 1; n2 == 1; n1 * n2 >= M) may carry
+    any stride, however large: it multiplies only zero and must not be scaled
+    to bytes (INT64_MAX / 2 times the element size would overflow int64).
+    The same stride on a level that rows do reach is rejected."""
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    p = ctypes.c_void_p(16)
+    R = _lib.gbn_rows
+    huge = (1 << 63) // 2
+    unused = [R(1, huge, 8, 16, 0),        # n1 == 1: s1 unused
+              R(8, 16, 1, huge, 128),      # n2 == 1: s2 unused
+              R(4, 16, 2, 64, huge),       # n1 * n2 == M: s3 unused
+              R(1, huge, 1, huge, 16),     # rows only through s3
+              R(8, 16, 1 << 62, huge, huge)]
+    for lay in unused:
+        ref = ctypes.byref(lay)
+        assert lib.dyt_fwd_rows(p, ref, p, p, p, p, 8, 8, 1, 0, None) == GBN_EDEVICE, \
+            (lay.n1, lay.s1, lay.n2, lay.s2, lay.s3)
+        assert lib.layernorm_bwd_rows(p, ref, p, ref, p, p, None, p, None, None, 8, 8, 1, 0,
+                                      None, 0, None) == GBN_EDEVICE
+    for lay in (R(2, huge, 4, 16, 0), R(2, 16, 2, 0, huge), R(4, 16, 2, huge, 0)):
+        ref = ctypes.byref(lay)
+        assert lib.dyt_fwd_rows(p, ref, p, p, p, p, 8, 8, 1, 0, None) == GBN_EINVAL

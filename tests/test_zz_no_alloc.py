@@ -110,3 +110,52 @@ def test_oversize_call_is_rejected_before_launch():
     dx_ref, _ = _lib.rmsnorm_bwd(x, dy, w, need_dw=False)
     assert none is None
     _same("dx without dw", dx2, dx_ref)
+
+
+def test_documented_limits_hold_on_this_device():
+    """The header's limits, as functions of this device's SM count S: the
+    vector path needs at most 32 KiB x S of partial sums (so a workspace of
+    exactly that size is accepted), and the general path at most 8 MiB up to
+    N = 2^19 / S' (S' = S rounded up to even), 16 x S' x N bytes beyond; the
+    static array serves the first two and rejects the third."""
+    lib = _lib.load()
+    S = torch.cuda.get_device_properties(0).multi_processor_count
+    Sp = S + (S & 1)
+    stream = torch.cuda.current_stream().cuda_stream
+    P = lambda t: t.data_ptr()  # noqa: E731
+    # vector path: the widths of each schedule family, M large enough that
+    # every launch uses its full persistent grid
+    for xdt, code, widths in ((torch.bfloat16, _lib.GBN_BF16, (2048, 4096, 8192)),
+                              (torch.float32, _lib.GBN_F32, (1024, 2048, 4096))):
+        for N in widths:
+            M = 8 * S
+            x, dy, w = _inputs(M, N, xdt, xdt, f"limit/{N}/{xdt}")
+            dx = torch.empty_like(x)
+            dw = torch.empty_like(w)
+            ws = torch.empty(32768 * S, dtype=torch.uint8, device="cuda")
+            rc = lib.rmsnorm_bwd(P(x), P(dy), P(w), None, P(dx), P(dw), M, N, 1e-6, code, code,
+                                 P(ws), 32768 * S, stream)
+            assert rc == _lib.GBN_OK, (N, xdt, rc)
+            dx2, dw2 = _lib.rmsnorm_bwd_static_ws(x, dy, w)
+            torch.cuda.synchronize()
+            _same(f"dx N={N}", dx2, dx)
+            _same(f"dw N={N}", dw2, dw)
+    # general path (N not a multiple of 8: 16-bit rows are not 16-byte multiples)
+    n_fit = (1 << 19) // Sp
+    n_fit -= 1 if n_fit % 8 == 0 else 0
+    n_over = n_fit + 1 if (n_fit + 1) % 8 else n_fit + 2
+    M = 64 * S
+    fit = lib.gbn_bwd_workspace_bytes(_lib.GBN_OP_RMSNORM, M, n_fit, _lib.GBN_BF16, _lib.GBN_BF16, 0)
+    over = lib.gbn_bwd_workspace_bytes(_lib.GBN_OP_RMSNORM, M, n_over, _lib.GBN_BF16,
+                                       _lib.GBN_BF16, 0)
+    assert fit <= _lib.GBN_STATIC_WS_BYTES
+    assert over == (16 * Sp * n_over + 255) // 256 * 256 > _lib.GBN_STATIC_WS_BYTES
+    x, dy, w = _inputs(M, n_fit, torch.bfloat16, torch.bfloat16, "limit/general")
+    dx_ref, dw_ref = _lib.rmsnorm_bwd(x, dy, w)
+    dx, dw = _lib.rmsnorm_bwd_static_ws(x, dy, w)
+    torch.cuda.synchronize()
+    _same("dx general", dx, dx_ref)
+    _same("dw general", dw, dw_ref)
+    x, dy, w = _inputs(M, n_over, torch.bfloat16, torch.bfloat16, "limit/over")
+    with pytest.raises(_lib.GbnError):
+        _lib.rmsnorm_bwd_static_ws(x, dy, w)

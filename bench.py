@@ -18,8 +18,16 @@ rank 0.  Under torchrun (N > 1) every rank runs an independent replica on
 its own GPU (no data-path collective); `value` sums all ranks' bytes over
 the slowest rank's time.
 
+The default run adds a "workloads" block: the four fixed-shape workloads
+(DyT fp32 4096x64, the LayerNorm backward at 401408x24, DyT bf16
+1048576x128, RMSNorm bf16 16384x2048), each step timed alone after an L2
+flush and replayed from a CUDA graph; and a "cpu_baseline": the float64
+oracle on a sample of the sweep, on every usable host core (static row
+blocks) and on one.
+
 `--impl reference` times the float64 CPU oracle (the correctness
-reference) on a bounded sample of the same workload instead.
+reference) on a bounded sample of the same workload instead, on every
+usable host core.
 
 The "headmajor" workload runs the three layers per head over head-major
 [B, H, S, D] activations and upstream gradients read in place as
@@ -352,6 +360,54 @@ def graph_step_ms(points, dev, flush, reps):
     return statistics.median(times)
 
 
+def fixed_workloads(lib, dev, steps, peak):
+    """The four fixed-shape workloads (DyT fp32 4096x64, the LayerNorm
+    backward alone at 401408x24, DyT bf16 1048576x128, RMSNorm bf16
+    16384x2048), each step its C-ABI calls (forward, backward, second
+    stage; the backward and second stage alone for the LayerNorm one),
+    timed alone with CUDA events on the launch stream after a 512 MiB write
+    that flushes L2, and replayed from a CUDA graph behind the same flush."""
+    from normalization_layers_fwd_gb300 import synth
+    flush = torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = []
+    for wl in (synth.DYT_F32_SMALL, synth.LN_BWD_TALL, synth.DYT_BF16_TALL, synth.RMS_BF16):
+        E = wl.M * wl.N
+        shared = {"y": torch.empty(E, dtype=wl.xdtype, device=dev),
+                  "dx": torch.empty(E, dtype=wl.xdtype, device=dev),
+                  "mean": torch.empty(wl.M, dtype=torch.float32, device=dev),
+                  "rstd": torch.empty(wl.M, dtype=torch.float32, device=dev)}
+        p = Point(lib, wl, dev, shared)
+        for _ in range(5):
+            flush_l2(flush)
+            p.run()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(steps):
+            flush_l2(flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            p.run()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b))
+        g = graph_step_ms([p], dev, flush, steps)
+        B = p.step_bytes()
+        med = statistics.median(times)
+        gbs = B / (med * 1e-3) / 1e9
+        out.append({"workload": wl.name, "alg_bytes": B, "launches": p.launches(),
+                    "ms_event_median": round(med, 5), "ms_event_mean": round(sum(times) / steps, 5),
+                    "ms_graph_median": round(g, 5), "gbs": round(gbs, 1),
+                    "gbs_graph": round(B / (g * 1e-3) / 1e9, 1),
+                    "frac_measured": round(gbs / peak, 4),
+                    "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+                    "rows_per_s": round(wl.M / (med * 1e-3), 1), "steps": steps,
+                    "l2": "flushed (512 MiB write) before every step"})
+        del p, shared
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, dev):
     from normalization_layers_fwd_gb300 import _lib, build
     build.build()
@@ -449,6 +505,10 @@ def run_ours(args, rank, world, dev):
         total_ms = sum(times)
         dom_ms = statistics.median(dom_t)
         graph_ms = graph_step_ms(points, dev, flush, max(args.steps, 10))
+    peak, peak_kind = measured_peak()
+    fixed = None
+    if args.workload == "sweep" and not (args.no_workloads or args.ops or args.widths):
+        fixed = fixed_workloads(lib, dev, max(args.steps, 20), peak)
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
@@ -457,7 +517,6 @@ def run_ours(args, rank, world, dev):
     step_bytes = sum(p.step_bytes() for p in points)
     rows = sum(p.wl.M for p in points)
     gbs = job_throughput(step_bytes, world, ms_step)
-    peak, peak_kind = measured_peak()
     dom_bytes = dom_point.bytes[dom_dir]
     dom_gbs = dom_bytes / (dom_ms * 1e-3) / 1e9
     dom_name = dom_point.key(dom_dir)
@@ -494,6 +553,7 @@ def run_ours(args, rank, world, dev):
             "note": "the same step replayed from a CUDA graph behind an L2 flush"},
         "e2e": e2e,
         "clocks": clocks,
+        "workloads": fixed,
         "breakdown": breakdown,
     }
     return line
@@ -571,74 +631,133 @@ def run_e2e(points, dev, steps, world):
 
 # --------------------------------------------------------- CPU (oracle) arm
 
-def oracle_sample(wls, target_elems):
-    """Time the float64 oracle (as it stands, one thread) on the first rows of
-    every point of the workload; returns (bytes, seconds, sample text)."""
+def host_cpu():
+    """(usable cores, nproc, CPU model) of the host."""
+    import platform
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        usable = os.cpu_count() or 1
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return usable, os.cpu_count() or usable, model or platform.processor() or platform.machine()
+
+
+def _oracle_block(oracle, w, inp, r0, r1):
+    """The oracle's forward and backward (row outputs and column sums) of
+    rows [r0, r1) of one point, through its unchanged functions."""
     import numpy as np
+
+    def arr(t):
+        t = t.contiguous().reshape(-1, t.shape[-1])[r0:r1]
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()  # float32 and float16 directly
+    x, dy = arr(inp["x"]), arr(inp["dy"])
+    if w.op == "dyt":
+        a = float(inp["alpha"].double()[0])
+        g, b = inp["gamma"].double().numpy(), inp["beta"].double().numpy()
+        oracle.dyt_fwd(x, a, g, b)
+        oracle.dyt_bwd_rows(x, dy, a, g)
+        oracle.dyt_bwd_cols(x, dy, a, g)
+    elif w.op == "layernorm":
+        g, b = inp["gamma"].double().numpy(), inp["beta"].double().numpy()
+        _, _, mu, rs = oracle.ln_fwd(x, w.eps, g, b)
+        oracle.ln_bwd_rows(x, dy, mu, rs, g)
+        oracle.ln_bwd_cols(x, dy, mu, rs)
+    else:
+        wt = inp["weight"].double().numpy()
+        code = {torch.bfloat16: oracle.BF16, torch.float16: oracle.F16}.get(
+            inp["weight"].dtype, oracle.F32)
+        oracle.rms_fwd(x, w.eps, wt)
+        oracle.rms_bwd_rows(x, dy, w.eps, wt, code)
+        oracle.rms_bwd_cols(x, dy, w.eps, code)
+
+
+def oracle_sample(wls, target_elems, threads=1):
+    """Time the float64 oracle, as it stands, on the first rows of every point
+    of the workload; returns (bytes, seconds, sample text).
+
+    threads == 1 runs each point's rows in one call per function.  With more
+    threads each point's rows are split into `threads` static row blocks, one
+    per thread, each running the same oracle functions on its block (the C
+    calls release the interpreter lock, so the blocks run on separate cores);
+    the column sums are then per block, which only changes their summation
+    order.  Inputs are generated outside the timed region."""
+    import concurrent.futures as cf
 
     import oracle
     oracle.build()
+    from normalization_layers_fwd_gb300 import synth
     per = max(1, target_elems // len(wls))
     tot_bytes, tot_s, n_elems = 0, 0.0, 0
-    for w in wls:
-        from normalization_layers_fwd_gb300 import synth
-        rows = max(1, min(w.M, per // w.N))
-        sw = synth.scaled(w, rows)
-        inp = sw.inputs(device="cpu")
-
-        def arr(t):
-            t = t.contiguous().reshape(-1, t.shape[-1])
-            if t.dtype == torch.bfloat16:
-                return t.view(torch.int16).numpy().view(np.uint16)
-            return t.numpy()  # float32 and float16 directly
-        x, dy = arr(inp["x"]), arr(inp["dy"])
-        t0 = time.perf_counter()
-        if w.op == "dyt":
-            a = float(inp["alpha"].double()[0])
-            g, b = inp["gamma"].double().numpy(), inp["beta"].double().numpy()
-            oracle.dyt_fwd(x, a, g, b)
-            oracle.dyt_bwd_rows(x, dy, a, g)
-            oracle.dyt_bwd_cols(x, dy, a, g)
-        elif w.op == "layernorm":
-            g, b = inp["gamma"].double().numpy(), inp["beta"].double().numpy()
-            _, _, mu, rs = oracle.ln_fwd(x, w.eps, g, b)
-            oracle.ln_bwd_rows(x, dy, mu, rs, g)
-            oracle.ln_bwd_cols(x, dy, mu, rs)
-        else:
-            wt = inp["weight"].double().numpy()
-            code = {torch.bfloat16: oracle.BF16, torch.float16: oracle.F16}.get(
-                inp["weight"].dtype, oracle.F32)
-            oracle.rms_fwd(x, w.eps, wt)
-            oracle.rms_bwd_rows(x, dy, w.eps, wt, code)
-            oracle.rms_bwd_cols(x, dy, w.eps, code)
-        tot_s += time.perf_counter() - t0
-        sx, sp = inp["x"].element_size(), 4
-        tot_bytes += (0 if w.bwd_only else alg_bytes(w.op, "fwd", rows, w.N, sx, sp)) + \
-            alg_bytes(w.op, "bwd", rows, w.N, sx, sp)
-        n_elems += rows * w.N
-    desc = f"first rows of each of the {len(wls)} points, {n_elems} elements in total, fwd+bwd"
+    pool = cf.ThreadPoolExecutor(threads) if threads > 1 else None
+    try:
+        for w in wls:
+            rows = max(1, min(w.M, per // w.N))
+            inp = synth.scaled(w, rows).inputs(device="cpu")
+            t0 = time.perf_counter()
+            if pool is None:
+                _oracle_block(oracle, w, inp, 0, rows)
+            else:
+                k = min(threads, rows)
+                cuts = [rows * i // k for i in range(k + 1)]
+                list(pool.map(lambda i: _oracle_block(oracle, w, inp, cuts[i], cuts[i + 1]),
+                              range(k)))
+            tot_s += time.perf_counter() - t0
+            sx, sp = inp["x"].element_size(), 4
+            tot_bytes += (0 if w.bwd_only else alg_bytes(w.op, "fwd", rows, w.N, sx, sp)) + \
+                alg_bytes(w.op, "bwd", rows, w.N, sx, sp)
+            n_elems += rows * w.N
+    finally:
+        if pool is not None:
+            pool.shutdown()
+    how = "one thread" if threads == 1 else f"{threads} threads, static row blocks"
+    desc = (f"first rows of each of the {len(wls)} points, {n_elems} elements in total, "
+            f"fwd+bwd, {how}")
     return tot_bytes, tot_s, desc
+
+
+def cpu_baseline(wls, elems, threads):
+    """The oracle timed on all `threads` host cores and on one, with the host
+    recorded."""
+    usable, nproc, model = host_cpu()
+    b1, s1, d1 = oracle_sample(wls, elems, 1)
+    bn, sn, dn = oracle_sample(wls, elems, threads) if threads > 1 else (b1, s1, d1)
+    return {"value": round(bn / sn / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": dn, "seconds": round(sn, 2), "nproc": nproc, "usable_cores": usable,
+            "cpu_model": model,
+            "single_thread": {"value": round(b1 / s1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                              "sample": d1, "seconds": round(s1, 2)}}
 
 
 def run_reference(args, rank, world):
     wls, wdesc = workloads(args.workload, args.ops, args.widths)
-    target = args.ref_elems
+    threads = args.ref_threads or host_cpu()[0]
     vals = []
     for i in range(args.warmup + args.steps):
-        b, s, desc = oracle_sample(wls, target)
+        b, s, desc = oracle_sample(wls, args.ref_elems, threads)
         if i >= args.warmup:
             vals.append((b, s))
     bytes_ = sum(v[0] for v in vals)
     secs = sum(v[1] for v in vals)
     gbs = bytes_ / secs / 1e9
+    usable, nproc, model = host_cpu()
     return {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * secs / args.steps, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, CPU)",
         "config": {"workload": wdesc, "note": "float64 CPU oracle on a bounded sample per step"},
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": desc, "nproc": nproc, "cpu_model": model},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -653,11 +772,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="sweep")
-    ap.add_argument("--ref-elems", type=int, default=1 << 22,
+    ap.add_argument("--ref-elems", type=int, default=1 << 24,
                     help="elements per step of the CPU oracle sample")
+    ap.add_argument("--ref-threads", type=int, default=0,
+                    help="host threads of the CPU oracle (0: every usable core)")
     ap.add_argument("--cpu-baseline-elems", type=int, default=1 << 28,
                     help="elements of the CPU oracle sample reported as cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the fixed-shape workloads block of the default sweep run")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ops", type=lambda v: v.split(","), default=None,
                     help="restrict the sweep to these layers (profiling runs)")
@@ -684,11 +807,9 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     line = run_ours(args, rank, world, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        b, s, desc = oracle_sample(workloads(args.workload, args.ops, args.widths)[0],
-                                   args.cpu_baseline_elems)
-        line["cpu_baseline"] = {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": 1,
-                                "kind": "oracle", "sample": desc,
-                                "seconds": round(s, 2)}
+        line["cpu_baseline"] = cpu_baseline(workloads(args.workload, args.ops, args.widths)[0],
+                                            args.cpu_baseline_elems,
+                                            args.ref_threads or host_cpu()[0])
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:

@@ -72,3 +72,19 @@ def test_reference_arm_json_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_times_all_cores_and_one():
+    """The CPU baseline runs the oracle on static row blocks over several
+    threads and on one thread, over the same sample (the same bytes), and
+    records the host's core count and CPU model."""
+    wls, _ = bench.workloads("sweep")
+    wls = [w for w in wls if w.N in (24, 512)]
+    b1, s1, d1 = bench.oracle_sample(wls, 60000, 1)
+    b3, s3, d3 = bench.oracle_sample(wls, 60000, 3)
+    assert b1 == b3 and s1 > 0 and s3 > 0
+    assert "one thread" in d1 and "3 threads" in d3
+    cb = bench.cpu_baseline(wls, 60000, 2)
+    assert cb["kind"] == "oracle" and cb["cores"] == 2 and cb["value"] > 0
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+    assert cb["nproc"] >= 1 and cb["usable_cores"] >= 1 and cb["cpu_model"]

@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(kCols * kSlices)
     colsum_kernel(const float* __restrict__ ws, int64_t P, int64_t rowlen, int64_t N, int pt,
                   void* __restrict__ out0, void* __restrict__ out1, void* __restrict__ out2)
 {
+    grid_dependency_sync();
     __shared__ float part[kSlices][kCols + 1];
     const int tx = threadIdx.x % kCols, ty = threadIdx.x / kCols;
     const int64_t c = blockIdx.x * (int64_t)kCols + tx;
@@ -67,8 +68,8 @@ cudaError_t launch_colsum(cudaStream_t s, const float* ws, int64_t P, int64_t ro
                           int pt, void* out0, void* out1, void* out2)
 {
     const int64_t blocks = (rowlen + kCols - 1) / kCols;
-    colsum_kernel<<<(unsigned)blocks, kCols * kSlices, 0, s>>>(ws, P, rowlen, N, pt, out0, out1,
-                                                               out2);
+    launch_pdl(colsum_kernel, (unsigned)blocks, kCols * kSlices, 0, s, ws, P, rowlen, N, pt, out0,
+               out1, out2);
     return cudaGetLastError();
 }
 

@@ -13,6 +13,7 @@
 #include <stdint.h>
 
 #include <type_traits>
+#include <utility>
 
 #include "ctx_cache.h"
 #include "internal.h"
@@ -916,6 +917,47 @@ __device__ __forceinline__ void cta_store_columns_kv(const f2 (&acc)[KV][P], flo
             }
         }
     }
+}
+
+// ------------------------------------------- programmatic dependent launch
+// Every kernel here is launched with programmatic stream serialization
+// (launch_pdl below): the GPU may schedule it while the kernel before it on
+// the stream is still running, once every CTA of that kernel has executed
+// griddepcontrol.launch_dependents (or exited).  Each kernel executes
+// launch_dependents first, so its successor is scheduled as soon as all of
+// its own CTAs are running, and then griddepcontrol.wait, which returns
+// once every prerequisite grid has completed and its memory is visible,
+// before its first global-memory access.  The data dependences are those of
+// plain stream order (nothing is read or written before the wait, and a
+// predecessor that never signals releases its successor when it exits);
+// what overlaps is the successor's launch and CTA scheduling with the
+// predecessor's tail.  A successor is only launched once all of its
+// predecessor's CTAs have started, so waiting CTAs never keep a
+// predecessor's CTAs off the SMs.
+__device__ __forceinline__ void grid_dependency_sync()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch `kernel` on `stream` with programmatic stream serialization.  A
+// failed launch is left in the runtime's last error, which the callers read
+// with cudaGetLastError.
+template <typename... KArgs, typename... Args>
+inline void launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t stream, Args&&... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Call f(std::integral_constant<int, m>) for the launch's input mode m.

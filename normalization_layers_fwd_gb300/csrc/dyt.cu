@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdDyT))
                  const void* __restrict__ gamma, const void* __restrict__ beta, int pt,
                  int64_t M, int N, int64_t nblocks, unsigned* fault, RowMaps maps)
 {
+    grid_dependency_sync();
     constexpr int W = kSched[S].W, U = kind_U(S, kFwdDyT), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
@@ -196,6 +197,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
                  float* __restrict__ ws, int64_t M, int N, int64_t nblocks, unsigned* fault,
                  RowMaps maps)
 {
+    grid_dependency_sync();
     constexpr int W = kSched[S].W, U = kind_U(S, kBwdDyT), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
@@ -326,6 +328,7 @@ __global__ void __launch_bounds__(kGenThreads)
                     const void* __restrict__ gamma, const void* __restrict__ beta, int pt,
                     int64_t M, int N, RowMaps maps, int scattered)
 {
+    grid_dependency_sync();
     const float a = ld_param(alpha, pt, 0);
     const int64_t E = M * (int64_t)N;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < E;
@@ -344,6 +347,7 @@ __global__ void __launch_bounds__(kGenThreads)
                     const void* __restrict__ alpha, const void* __restrict__ gamma, int pt,
                     float* __restrict__ ws, int64_t M, int N, RowMaps maps, int scattered)
 {
+    grid_dependency_sync();
     __shared__ float accs[kGenWarps * kGenCols];
     const int lane = threadIdx.x & 31;
     const int64_t w = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5);
@@ -389,8 +393,8 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* alp
     const TX* xp = static_cast<const TX*>(x);
     TX* yp = static_cast<TX*>(y);
     if (!L.fast) {
-        dyt_fwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, yp, alpha, gamma, beta, pt,
-                                                                  M, N, L.maps, L.scattered);
+        launch_pdl(dyt_fwd_general<TX>, L.grid, kGenThreads, 0, L.stream, xp, yp, alpha, gamma,
+                   beta, pt, M, N, L.maps, L.scattered);
         return cudaGetLastError();
     }
     switch (L.sid) {
@@ -400,7 +404,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* alp
         with_mode(L.in_mode, [&](auto m_) {                                                        \
             constexpr int kIn_ = decltype(m_)::value;                                              \
             ring_attributes<dyt_fwd_fast<TX, S, kIn_>>(smem);                                      \
-            dyt_fwd_fast<TX, S, kIn_><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
+            launch_pdl(dyt_fwd_fast<TX, S, kIn_>, L.grid, kSched[S].T, smem, L.stream,             \
                 xp, yp, alpha, gamma, beta, pt, M, N, L.nblocks, L.fault, L.maps);                 \
         });                                                                                        \
         break;                                                                                     \
@@ -422,8 +426,8 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     const TX* dyp = static_cast<const TX*>(dy);
     TX* dxp = static_cast<TX*>(dx);
     if (!L.fast) {
-        dyt_bwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(xp, dyp, dxp, alpha, gamma, pt,
-                                                                  ws, M, N, L.maps, L.scattered);
+        launch_pdl(dyt_bwd_general<TX>, L.grid, kGenThreads, 0, L.stream, xp, dyp, dxp, alpha,
+                   gamma, pt, ws, M, N, L.maps, L.scattered);
         return cudaGetLastError();
     }
     switch (L.sid) {
@@ -433,7 +437,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         with_mode(L.in_mode, [&](auto m_) {                                                        \
             constexpr int kIn_ = decltype(m_)::value;                                              \
             ring_attributes<dyt_bwd_fast<TX, S, kIn_>>(smem);                                      \
-            dyt_bwd_fast<TX, S, kIn_><<<L.grid, kSched[S].T, smem, L.stream>>>(                    \
+            launch_pdl(dyt_bwd_fast<TX, S, kIn_>, L.grid, kSched[S].T, smem, L.stream,             \
                 xp, dyp, dxp, alpha, gamma, pt, ws, M, N, L.nblocks, L.fault, L.maps);             \
         });                                                                                        \
         break;                                                                                     \

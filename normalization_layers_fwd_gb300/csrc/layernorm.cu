@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdLN))
                 float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
                 int64_t nblocks, unsigned* fault, RowMaps maps)
 {
+    grid_dependency_sync();
     constexpr int W = kSched[S].W, U = kind_U(S, kFwdLN), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
                 float* __restrict__ ws, int64_t M, int N, float inv_n, int64_t nblocks,
                 unsigned* fault, RowMaps maps)
 {
+    grid_dependency_sync();
     constexpr int W = kSched[S].W, U = kind_U(S, kBwdLN), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
@@ -332,6 +334,7 @@ __global__ void __launch_bounds__(kGenThreads)
                    float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n, RowMaps maps,
                    int scattered)
 {
+    grid_dependency_sync();
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * kGenWarps;
     for (int64_t r = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5); r < M; r += nw) {
@@ -367,6 +370,7 @@ __global__ void __launch_bounds__(kGenThreads)
                    float* __restrict__ ws, int64_t M, int N, float inv_n, RowMaps maps,
                    int scattered)
 {
+    grid_dependency_sync();
     __shared__ float accs[kGenWarps * kGenCols];
     const int lane = threadIdx.x & 31;
     const int64_t w = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5);
@@ -415,7 +419,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
     TX* yp = static_cast<TX*>(y);
     const float inv_n = (float)(1.0 / (double)N);
     if (!L.fast) {
-        ln_fwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(
+        launch_pdl(ln_fwd_general<TX>, L.grid, kGenThreads, 0, L.stream,
             xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.maps, L.scattered);
         return cudaGetLastError();
     }
@@ -426,7 +430,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
         with_mode(L.in_mode, [&](auto m_) {                                                        \
             constexpr int kIn_ = decltype(m_)::value;                                              \
             ring_attributes<ln_fwd_fast<TX, S, kIn_>>(smem);                                       \
-            ln_fwd_fast<TX, S, kIn_><<<L.grid, kSched[S].T, smem, L.stream>>>(                     \
+            launch_pdl(ln_fwd_fast<TX, S, kIn_>, L.grid, kSched[S].T, smem, L.stream,              \
                 xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.fault,         \
                 L.maps);                                                                           \
         });                                                                                        \
@@ -451,7 +455,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     TX* dxp = static_cast<TX*>(dx);
     const float inv_n = (float)(1.0 / (double)N);
     if (!L.fast) {
-        ln_bwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(
+        launch_pdl(ln_bwd_general<TX>, L.grid, kGenThreads, 0, L.stream,
             xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.maps, L.scattered);
         return cudaGetLastError();
     }
@@ -462,7 +466,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         with_mode(L.in_mode, [&](auto m_) {                                                        \
             constexpr int kIn_ = decltype(m_)::value;                                              \
             ring_attributes<ln_bwd_fast<TX, S, kIn_>>(smem);                                       \
-            ln_bwd_fast<TX, S, kIn_><<<L.grid, kSched[S].T, smem, L.stream>>>(                     \
+            launch_pdl(ln_bwd_fast<TX, S, kIn_>, L.grid, kSched[S].T, smem, L.stream,              \
                 xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.nblocks, L.fault, L.maps); \
         });                                                                                        \
         break;                                                                                     \

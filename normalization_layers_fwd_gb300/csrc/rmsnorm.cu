@@ -13,6 +13,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kFwdNorm))
                  int pt, float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
                  int64_t nblocks, unsigned* fault, int gemma, RowMaps maps)
 {
+    grid_dependency_sync();
     constexpr int W = kSched[S].W, U = kind_U(S, kFwdNorm), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(kGenThreads)
                     int pt, float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
                     int variant, RowMaps maps, int scattered)
 {
+    grid_dependency_sync();
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * kGenWarps;
     for (int64_t r = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5); r < M; r += nw) {
@@ -137,7 +139,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
     const float inv_n = (float)(1.0 / (double)N);
     const int gemma = variant == 2;
     if (!L.fast) {
-        rms_fwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(
+        launch_pdl(rms_fwd_general<TX>, L.grid, kGenThreads, 0, L.stream,
             xp, yp, w, pt, rstd, M, N, eps, inv_n, variant, L.maps, L.scattered);
         return cudaGetLastError();
     }

@@ -90,13 +90,14 @@ __device__ __forceinline__ float warp_row_rstd(const TX* xr, int N, int lane, fl
         if constexpr (is16<TX>()) {                                                                \
             if (variant != 0) {                                                                    \
                 ring_attributes<KERNEL<TX, S, true, kIn_>>(SMEM);                                  \
-                KERNEL<TX, S, true, kIn_><<<L.grid, kSched[S].T, SMEM, L.stream>>>(__VA_ARGS__,    \
-                                                                                    L.maps);       \
+                launch_pdl(KERNEL<TX, S, true, kIn_>, L.grid, kSched[S].T, SMEM, L.stream,         \
+                           __VA_ARGS__, L.maps);                                                   \
                 return;                                                                            \
             }                                                                                      \
         }                                                                                          \
         ring_attributes<KERNEL<TX, S, false, kIn_>>(SMEM);                                         \
-        KERNEL<TX, S, false, kIn_><<<L.grid, kSched[S].T, SMEM, L.stream>>>(__VA_ARGS__, L.maps);  \
+        launch_pdl(KERNEL<TX, S, false, kIn_>, L.grid, kSched[S].T, SMEM, L.stream, __VA_ARGS__,   \
+                   L.maps);                                                                        \
     })
 
 }  // namespace

@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
                  float* __restrict__ ws, int64_t M, int N, float eps, float inv_n,
                  int64_t nblocks, unsigned* fault, int gemma, RowMaps maps)
 {
+    grid_dependency_sync();
     constexpr int W = kSched[S].W, U = kind_U(S, kBwdRms), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
@@ -196,6 +197,7 @@ __global__ void __launch_bounds__(kGenThreads)
                     TX* __restrict__ dx, float* __restrict__ ws, int64_t M, int N, float eps,
                     float inv_n, int variant, RowMaps maps, int scattered)
 {
+    grid_dependency_sync();
     __shared__ float accs[kGenWarps * kGenCols];
     const int lane = threadIdx.x & 31;
     const int64_t wi = blockIdx.x * (int64_t)kGenWarps + (threadIdx.x >> 5);
@@ -247,7 +249,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     const float inv_n = (float)(1.0 / (double)N);
     const int gemma = variant == 2;
     if (!L.fast) {
-        rms_bwd_general<TX><<<L.grid, kGenThreads, 0, L.stream>>>(
+        launch_pdl(rms_bwd_general<TX>, L.grid, kGenThreads, 0, L.stream,
             xp, dyp, w, pt, rstd, dxp, ws, M, N, eps, inv_n, variant, L.maps, L.scattered);
         return cudaGetLastError();
     }

@@ -23,7 +23,9 @@
  *   dtype `pt`/`wt`; saved statistics (mean, rstd) are float32 [M].
  *   Every pointer must be aligned to its element size (else GBN_EINVAL).
  *   Beyond that any alignment is accepted: 16-byte aligned activations with
- *   N*sizeof a multiple of 16 take the vector path, the rest the general path.
+ *   N*sizeof a multiple of 16 take the vector path, up to N = 8192 (16-bit
+ *   activations; 16384 in the DyT and LayerNorm forwards) or 8192 (float32),
+ *   the rest the general path.
  * Ownership.  The caller owns all memory.  The library never allocates,
  *   never frees, never synchronizes and launches only on `stream` (which may
  *   be 0, the legacy default stream).  Calls are asynchronous: a GBN_OK
@@ -251,7 +253,7 @@ int rmsnorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gb
  *   GBN_STATIC_WS_BYTES returns GBN_ESCRATCH before launching anything.  The
  *   need is (rows of partials) x N x 4 bytes, which grows with the device's
  *   SM count S: on the vector path (16-byte aligned activations, N a multiple
- *   of 8 for 16-bit or 4 for f32 activations, N <= 8192 or 4096) at most
+ *   of 8 for 16-bit or 4 for f32 activations, N <= 8192) at most
  *   32 KiB x S, within the array for S <= 256; on the general path, with
  *   S' = S rounded up to an even number, at most 8 MiB while N <= 2^19 / S'
  *   (the number of warps adapts) and 16 x S' x N bytes beyond (for M of at

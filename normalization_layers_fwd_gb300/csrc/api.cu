@@ -156,22 +156,29 @@ int64_t general_ws_floats(int kind, int64_t N)
 // measurement.  Schedule s serves rows of more than half its capacity and at
 // most its capacity (max_nvec / 2 < nvec <= max_nvec), the first in table
 // order that the set holds; other rows take the one-vector schedules.
-constexpr unsigned kWide12 = 1u, kWide13 = 2u, kWide14 = 4u, kWide15 = 8u, kWide16 = 16u;
+constexpr unsigned kWide12 = 1u, kWide13 = 2u, kWide14 = 4u, kWide15 = 8u, kWide16 = 16u,
+                   kWide17 = 32u;
 
 // Each kernel's set: the DyT forward 12-13 and backward 12; the LayerNorm
 // forward 12, 13 and 16 and backward 12, 14 and 15; the RMSNorm forward and
 // backward 12 and 14 (one set, so the backward's recomputed rstd reduces a
-// row in the forward's order).  The backwards hold at most 2 vectors per
-// thread.  Schedule 15 measured slower than one vector per thread in the
+// row in the forward's order).  The 16-bit backwards hold at most 2 vectors
+// per thread.  Schedule 15 measured slower than one vector per thread in the
 // forwards and in the RMSNorm backward, 16 faster in the LayerNorm forward.
-unsigned wide_set(int kind)
+// Rows of 1025-2048 vectors take schedule 17: in the DyT and LayerNorm
+// forwards for every dtype, and in every kernel for float32 activations
+// (the RMSNorm pair and the backwards fit its registers only there).
+unsigned wide_set(int kind, int xt)
 {
+    const unsigned w17 = (xt == gbn::kF32 || kind == gbn::kFwdDyT || kind == gbn::kFwdLN)
+                             ? kWide17
+                             : 0u;
     switch (kind) {
-        case gbn::kFwdDyT: return kWide12 | kWide13;
-        case gbn::kBwdDyT: return kWide12;
-        case gbn::kFwdLN: return kWide12 | kWide13 | kWide16;
-        case gbn::kBwdLN: return kWide12 | kWide14 | kWide15;
-        default: return kWide12 | kWide14;  // RMSNorm forward and backward
+        case gbn::kFwdDyT: return kWide12 | kWide13 | w17;
+        case gbn::kBwdDyT: return kWide12 | w17;
+        case gbn::kFwdLN: return kWide12 | kWide13 | kWide16 | w17;
+        case gbn::kBwdLN: return kWide12 | kWide14 | kWide15 | w17;
+        default: return kWide12 | kWide14 | w17;  // RMSNorm forward and backward
     }
 }
 
@@ -465,7 +472,7 @@ size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int
     const int kind =
         op == GBN_OP_DYT ? gbn::kBwdDyT : op == GBN_OP_LAYERNORM ? gbn::kBwdLN : gbn::kBwdRms;
     // the vector path with the kernel's wide set, or the general path
-    const Launch a = plan(M, N, xt, true, sms, nullptr, kind, wide_set(kind));
+    const Launch a = plan(M, N, xt, true, sms, nullptr, kind, wide_set(kind, xt));
     const Launch b = plan(M, N, xt, false, sms, nullptr, kind);
     const size_t need = ws_needed(op, a.P > b.P ? a : b, N);
     return (need + 255) & ~(size_t)255;
@@ -486,7 +493,7 @@ int dyt_fwd_rows(const void* x, const gbn_rows* xl, const void* alpha, const voi
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
-                    gbn::kFwdDyT, wide_set(gbn::kFwdDyT));
+                    gbn::kFwdDyT, wide_set(gbn::kFwdDyT, xt));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -523,7 +530,7 @@ int dyt_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gbn_ro
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
-                    stream, gbn::kBwdDyT, wide_set(gbn::kBwdDyT));
+                    stream, gbn::kBwdDyT, wide_set(gbn::kBwdDyT, xt));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -563,7 +570,7 @@ int layernorm_fwd_rows(const void* x, const gbn_rows* xl, const void* gamma, con
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
-                    gbn::kFwdLN, wide_set(gbn::kFwdLN));
+                    gbn::kFwdLN, wide_set(gbn::kFwdLN, xt));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -597,7 +604,7 @@ int layernorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const 
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
-                    stream, gbn::kBwdLN, wide_set(gbn::kBwdLN));
+                    stream, gbn::kBwdLN, wide_set(gbn::kBwdLN, xt));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -652,7 +659,7 @@ int rmsnorm_fwd_rows(const void* x, const gbn_rows* xl, const void* w, void* y, 
     const int sms = current_sms();
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
-                    gbn::kFwdNorm, wide_set(gbn::kFwdNorm));
+                    gbn::kFwdNorm, wide_set(gbn::kFwdNorm, xt));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -684,7 +691,7 @@ int rmsnorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gb
     if (sms <= 0) return GBN_EDEVICE;
     // the forward's set: a recomputed rstd reduces each row in its order
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
-                    stream, gbn::kBwdRms, wide_set(gbn::kBwdRms));
+                    stream, gbn::kBwdRms, wide_set(gbn::kBwdRms, xt));
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;

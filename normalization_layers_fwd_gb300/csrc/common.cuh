@@ -46,6 +46,13 @@ struct SchedEntry {
 // with KV = 2 or 4 vectors each (vector l + j*W for j < KV), one row per
 // CTA.  Against schedules 10-11 they divide the per-row reduction and
 // barrier cost by KV; at 256 threads two independent CTAs share an SM.
+// Schedule 17: rows of 1025-2048 vectors (bf16 N <= 16384, f32 N <= 8192)
+// held by 512 threads with KV = 4 vectors each, one row per CTA, one CTA
+// per SM.  The backwards keep the row's xhat (and g, dn) in registers as
+// well as their column accumulators, which fits the 128-register budget
+// only with float32 activations (half the elements per vector); the
+// planner gives it to the 16-bit backwards never, and to the 16-bit RMSNorm
+// forward never either (its backward must reduce a row in its order).
 // Schedules 15-16: rows of 33-64 and 65-128 vectors held by one warp with
 // KV = 2 or 4 vectors per lane, 8 rows per pass: the row reductions stay
 // inside the warp (shuffles, no barrier), where one vector per lane would
@@ -54,16 +61,15 @@ struct SchedEntry {
 // takes 15, the LayerNorm forward 16).
 // Which kernel takes which is decided per kernel by the planner (api.cu),
 // within each kernel's register budget.
-constexpr int kNumSched = 17;
+constexpr int kNumSched = 18;
 constexpr int kNumSched1 = 12;  // the one-vector schedules
 constexpr SchedEntry kSched[kNumSched] = {
     {1, 1, 256, 1},     {2, 2, 256, 1},     {3, 3, 256, 1},     {4, 4, 256, 1},
     {8, 8, 256, 1},     {16, 16, 256, 1},   {32, 32, 256, 1},   {64, 64, 256, 1},
     {128, 128, 256, 1}, {256, 256, 256, 1}, {512, 512, 512, 1}, {1024, 1024, 1024, 1},
     {512, 256, 256, 2}, {1024, 256, 256, 4}, {1024, 512, 512, 2},
-    {64, 32, 256, 2},   {128, 32, 256, 4},
+    {64, 32, 256, 2},   {128, 32, 256, 4},  {2048, 512, 512, 4},
 };
-constexpr int kMaxFastVec = 1024;
 
 // Row groups of a power-of-two width tile the CTA; a width that is not a
 // power of two packs floor(32/W) groups per warp and leaves the rest of the
@@ -145,13 +151,17 @@ constexpr int kind_minb(int S, int kind)
 // outstanding bulk copies and the forward sweep loses 5-15%.  The wide-row
 // forwards of schedules 12-13 (two CTAs of one row each) want 4, except the
 // LayerNorm forward at 4 vectors per thread (2).  The backward kernels,
-// which spend longer per block, want 3 (RMSNorm) or 4.
+// which spend longer per block, want 3 (RMSNorm) or 4; the RMSNorm backward
+// at 512 threads (one CTA per SM) 4 (N = 8192: 0.91 -> 0.95 of measured
+// copy, where 4 stages cost the 256-thread schedules 1-4%).  Backward slots
+// of 4 vectors per thread (32 KB per tensor) take 3.
 constexpr int kind_stages(int S, int kind)
 {
     return !is_bwd(kind) ? (kSched[S].KV == 1 ? (kSched[S].T == 256 ? 2 : 4)
                             : kSched[S].KV == 4 && kind == kFwdLN ? 2
                                                                     : 4)
-           : kind == kBwdRms ? 3
+           : kSched[S].KV == 4                      ? 3
+           : kind == kBwdRms                        ? (kSched[S].T == 512 ? 4 : 3)
            : kind == kBwdDyT && kSched[S].T == 1024 ? 3
                                                     : 4;
 }
@@ -399,6 +409,22 @@ __device__ __forceinline__ int64_t out_row(const OutMap& o, int64_t q)
     const uint32_t q1 = (uint32_t)(((uint64_t)uq * o.ma) >> o.sa);
     const uint32_t q2 = (uint32_t)(((uint64_t)q1 * o.mb) >> o.sb);
     return (int64_t)((uq - q1 * o.a) * o.wa + (q1 - q2 * o.b) * o.wb + q2 * o.wc);
+}
+
+// A saved per-row statistic of row r.  Contiguous and scattered rows read
+// the statistics in row order, each 32-byte sector by neighbouring CTAs at
+// about the same time, so they stream past the caches (evict first).  In
+// storage order consecutive rows take statistics a level stride apart, and
+// a sector's eight values serve rows far apart in time: there the load
+// keeps the normal L2 policy so the sector is still resident when the
+// other seven are read.
+template <int kIn>
+__device__ __forceinline__ float ld_stat(const float* p, int64_t r)
+{
+    if constexpr (kIn == kInStorage)
+        return __ldcg(p + r);
+    else
+        return __ldcs(p + r);
 }
 
 // The row whose outputs (and saved statistics) belong to this thread's row q.

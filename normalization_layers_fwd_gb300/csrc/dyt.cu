@@ -201,7 +201,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     constexpr int W = kSched[S].W, U = kind_U(S, kBwdDyT), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
-    static_assert(KV <= 2, "the DyT backward takes at most 2 vectors per thread");
+    static_assert(KV <= 2 || sizeof(TX) == 4,
+                  "the 16-bit DyT backward takes at most 2 vectors per thread");
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[T / 32];
     const int g = grp<W>(), l = lan<W>();
@@ -411,7 +412,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* alp
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9)
-        GBN_CASE(12) GBN_CASE(13)
+        GBN_CASE(12) GBN_CASE(13) GBN_CASE(17)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }
@@ -431,8 +432,8 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                                \
-    case S: {                                                                                      \
+#define GBN_CASE_BODY(S)                                                                           \
+    {                                                                                              \
         constexpr int smem = ring_smem_bytes(S, kBwdDyT, 2);                                       \
         with_mode(L.in_mode, [&](auto m_) {                                                        \
             constexpr int kIn_ = decltype(m_)::value;                                              \
@@ -440,12 +441,24 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
             launch_pdl(dyt_bwd_fast<TX, S, kIn_>, L.grid, kSched[S].T, smem, L.stream,             \
                 xp, dyp, dxp, alpha, gamma, pt, ws, M, N, L.nblocks, L.fault, L.maps);             \
         });                                                                                        \
-        break;                                                                                     \
     }
+#define GBN_CASE(S)                                                                                \
+    case S:                                                                                        \
+        GBN_CASE_BODY(S)                                                                           \
+        break;
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(11)
         GBN_CASE(12)
+        // schedule 17 only for float32 activations (the planner's choice)
+        case 17:
+            if constexpr (sizeof(TX) == 4) {
+                GBN_CASE_BODY(17)
+            } else {
+                return cudaErrorInvalidValue;
+            }
+            break;
 #undef GBN_CASE
+#undef GBN_CASE_BODY
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

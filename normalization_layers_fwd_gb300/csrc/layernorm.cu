@@ -172,9 +172,10 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
     // xhat and g of every vector stay in registers across the row reduction;
-    // with the column accumulators that caps this kernel at 2 vectors per
-    // thread (4 spill).
-    static_assert(KV <= 2, "the LayerNorm backward takes at most 2 vectors per thread");
+    // with the column accumulators that caps the 16-bit kernel at 2 vectors
+    // per thread (4 spill); float32 vectors hold half the elements, and 4 fit.
+    static_assert(KV <= 2 || sizeof(TX) == 4,
+                  "the 16-bit LayerNorm backward takes at most 2 vectors per thread");
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, 2 * U>::kFloats];
     int parity = 0;
@@ -207,8 +208,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
         for (int u = 0; u < U; ++u) {
             const int64_t row = row0 + u * G;
             const int64_t srow = row < M ? stat_row<kIn>(maps, row) : 0;
-            mu_d[u] = row < M ? __ldcs(mean + srow) : 0.f;
-            rs_d[u] = row < M ? __ldcs(rstd + srow) : 0.f;
+            mu_d[u] = row < M ? ld_stat<kIn>(mean, srow) : 0.f;
+            rs_d[u] = row < M ? ld_stat<kIn>(rstd, srow) : 0.f;
         }
     };
     const int64_t bstride = (int64_t)gridDim.x * (G * U);
@@ -438,7 +439,7 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9)
-        GBN_CASE(12) GBN_CASE(13) GBN_CASE(16)
+        GBN_CASE(12) GBN_CASE(13) GBN_CASE(16) GBN_CASE(17)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }
@@ -460,8 +461,8 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                                \
-    case S: {                                                                                      \
+#define GBN_CASE_BODY(S)                                                                           \
+    {                                                                                              \
         constexpr int smem = ring_smem_bytes(S, kBwdLN, 2);                                        \
         with_mode(L.in_mode, [&](auto m_) {                                                        \
             constexpr int kIn_ = decltype(m_)::value;                                              \
@@ -469,12 +470,24 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
             launch_pdl(ln_bwd_fast<TX, S, kIn_>, L.grid, kSched[S].T, smem, L.stream,              \
                 xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.nblocks, L.fault, L.maps); \
         });                                                                                        \
-        break;                                                                                     \
     }
+#define GBN_CASE(S)                                                                                \
+    case S:                                                                                        \
+        GBN_CASE_BODY(S)                                                                           \
+        break;
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9)
         GBN_CASE(12) GBN_CASE(14) GBN_CASE(15)
+        // schedule 17 only for float32 activations (the planner's choice)
+        case 17:
+            if constexpr (sizeof(TX) == 4) {
+                GBN_CASE_BODY(17)
+            } else {
+                return cudaErrorInvalidValue;
+            }
+            break;
 #undef GBN_CASE
+#undef GBN_CASE_BODY
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

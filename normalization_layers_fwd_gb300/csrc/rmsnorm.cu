@@ -144,17 +144,29 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                                \
-    case S: {                                                                                      \
+#define GBN_CASE_BODY(S)                                                                           \
+    {                                                                                              \
         constexpr int smem = ring_smem_bytes(S, kFwdNorm, 1);                                      \
         GBN_RMS_LAUNCH(rms_fwd_fast, S, smem, xp, yp, w, pt, rstd, M, N, eps, inv_n, L.nblocks,    \
                        L.fault, gemma);                                                            \
-        break;                                                                                     \
     }
+#define GBN_CASE(S)                                                                                \
+    case S:                                                                                        \
+        GBN_CASE_BODY(S)                                                                           \
+        break;
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(11)
         GBN_CASE(12) GBN_CASE(14)
+        // schedule 17 only for float32 activations (the planner's choice)
+        case 17:
+            if constexpr (sizeof(TX) == 4) {
+                GBN_CASE_BODY(17)
+            } else {
+                return cudaErrorInvalidValue;
+            }
+            break;
 #undef GBN_CASE
+#undef GBN_CASE_BODY
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

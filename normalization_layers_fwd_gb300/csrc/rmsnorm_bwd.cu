@@ -22,7 +22,8 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
     constexpr int W = kSched[S].W, U = kind_U(S, kBwdRms), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
-    static_assert(KV <= 2, "the RMSNorm backward takes at most 2 vectors per thread");
+    static_assert(KV <= 2 || sizeof(TX) == 4,
+                  "the 16-bit RMSNorm backward takes at most 2 vectors per thread");
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
     int parity = 0;
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t row = row0 + u * G;
-                dst[u] = row < M ? __ldcs(rstd + stat_row<kIn>(maps, row)) : 0.f;
+                dst[u] = row < M ? ld_stat<kIn>(rstd, stat_row<kIn>(maps, row)) : 0.f;
             }
         }
     };
@@ -254,17 +255,29 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         return cudaGetLastError();
     }
     switch (L.sid) {
-#define GBN_CASE(S)                                                                                \
-    case S: {                                                                                      \
+#define GBN_CASE_BODY(S)                                                                           \
+    {                                                                                              \
         constexpr int smem = ring_smem_bytes(S, kBwdRms, 2);                                       \
         GBN_RMS_LAUNCH(rms_bwd_fast, S, smem, xp, dyp, w, pt, rstd, dxp, ws, M, N, eps, inv_n,     \
                        L.nblocks, L.fault, gemma);                                                 \
-        break;                                                                                     \
     }
+#define GBN_CASE(S)                                                                                \
+    case S:                                                                                        \
+        GBN_CASE_BODY(S)                                                                           \
+        break;
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(11)
         GBN_CASE(12) GBN_CASE(14)
+        // schedule 17 only for float32 activations (the planner's choice)
+        case 17:
+            if constexpr (sizeof(TX) == 4) {
+                GBN_CASE_BODY(17)
+            } else {
+                return cudaErrorInvalidValue;
+            }
+            break;
 #undef GBN_CASE
+#undef GBN_CASE_BODY
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

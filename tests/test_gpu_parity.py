@@ -47,10 +47,13 @@ def _run(op, inp, eps=1e-5, rows=None):
     return rmsnorm_case(inp["x"], inp["dy"], inp["gamma"], eps, rows)
 
 
+# 16-bit widths 8200-16384 (1025-2048 vectors) run the DyT and LayerNorm
+# forwards on the 4-vector wide schedule; float32 widths 4104-8192 run every
+# kernel on it; 8196 and 16392 are beyond it.
 BF16_WIDTHS = [1, 5, 8, 16, 24, 40, 64, 128, 129, 136, 256, 264, 512, 520, 1000, 1024, 2048,
-               3072, 4096, 6000, 8192, 8200]
-F32_WIDTHS = [1, 3, 4, 12, 64, 100, 256, 1024, 2048, 3000, 4096, 4100]
-F16_WIDTHS = [1, 8, 16, 24, 40, 64, 128, 264, 1000, 2048, 3072, 4096, 6000, 8192, 8200]
+               3072, 4096, 6000, 8192, 8200, 12288, 16384, 16392]
+F32_WIDTHS = [1, 3, 4, 12, 64, 100, 256, 1024, 2048, 3000, 4096, 4100, 4104, 6000, 8192, 8196]
+F16_WIDTHS = [1, 8, 16, 24, 40, 64, 128, 264, 1000, 2048, 3072, 4096, 6000, 8192, 8200, 12288]
 DTYPES = [(torch.bfloat16, torch.float32), (torch.bfloat16, torch.bfloat16),
           (torch.float32, torch.float32), (torch.float32, torch.bfloat16),
           (torch.float16, torch.float32), (torch.float16, torch.float16)]

@@ -126,7 +126,7 @@ def test_documented_limits_hold_on_this_device():
     # vector path: the widths of each schedule family, M large enough that
     # every launch uses its full persistent grid
     for xdt, code, widths in ((torch.bfloat16, _lib.GBN_BF16, (2048, 4096, 8192)),
-                              (torch.float32, _lib.GBN_F32, (1024, 2048, 4096))):
+                              (torch.float32, _lib.GBN_F32, (1024, 2048, 4096, 8192))):
         for N in widths:
             M = 8 * S
             x, dy, w = _inputs(M, N, xdt, xdt, f"limit/{N}/{xdt}")

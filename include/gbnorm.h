@@ -24,8 +24,10 @@
  *   Every pointer must be aligned to its element size (else GBN_EINVAL).
  *   Beyond that any alignment is accepted: 16-byte aligned activations with
  *   N*sizeof a multiple of 16 take the vector path, up to N = 8192 (16-bit
- *   activations; 16384 in the DyT and LayerNorm forwards) or 8192 (float32),
- *   the rest the general path.
+ *   activations; 16384 in the DyT and LayerNorm forwards) or 8192 (float32);
+ *   other contiguous rows up to N = 256 (even N) or 128 (odd N) whose inputs
+ *   start on a 16-byte boundary take the row-batched path; the rest the
+ *   general path.
  * Ownership.  The caller owns all memory.  The library never allocates,
  *   never frees, never synchronizes and launches only on `stream` (which may
  *   be 0, the legacy default stream).  Calls are asynchronous: a GBN_OK

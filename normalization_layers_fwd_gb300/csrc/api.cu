@@ -222,6 +222,35 @@ Launch plan(int64_t M, int64_t N, int xt, bool aligned, int sms, cudaStream_t st
     return L;
 }
 
+// The row-batched layout (common.cuh): contiguous rows whose staged inputs
+// start on 16-byte boundaries, units of an element pair when N is even and
+// every pointer holds whole pairs (pair_ok), else of one element, at most
+// batch_max_units(E) units a lane, and ring blocks of at least 8 rows.  Returns
+// a Launch with batch == 0 when the path does not apply.
+Launch plan_batch(int64_t M, int64_t N, int xt, bool base16, bool pair_ok, int sms,
+                  cudaStream_t stream, int kind)
+{
+    Launch L{};
+    L.stream = stream;
+    if (!base16 || M <= 0) return L;
+    const int E = (N % 2 == 0 && pair_ok) ? 2 : 1;
+    const int64_t nu = N / E;
+    int kmax = 1;
+    while ((int64_t)kmax * 32 < nu) kmax *= 2;
+    if (kmax > gbn::batch_max_units(E)) return L;
+    const int64_t R = (gbn::kBatchSlot / (N * elem_bytes(xt))) / 8 * 8;
+    if (R < 8) return L;
+    L.batch = 1;
+    L.E = E;
+    L.KMAX = kmax;
+    L.R = (int)R;
+    L.nblocks = (M + R - 1) / R;
+    const int64_t cap = (int64_t)sms * gbn::batch_minb(gbn::is_bwd(kind));
+    L.grid = (int)(L.nblocks < cap ? L.nblocks : cap);
+    L.P = L.grid;
+    return L;
+}
+
 bool shape_ok(int64_t M, int64_t N)
 {
     if (M < 0 || N < 1 || N > INT_MAX) return false;
@@ -414,6 +443,24 @@ Inputs input_layouts(const gbn_rows* xl, const gbn_rows* dyl, const void* x, con
     return in;
 }
 
+// Every pointer aligned to an element pair (null passes).
+bool pair_aligned(int t, std::initializer_list<const void*> ps)
+{
+    for (const void* p : ps)
+        if ((reinterpret_cast<uintptr_t>(p) & (uintptr_t)(2 * elem_bytes(t) - 1)) != 0)
+            return false;
+    return true;
+}
+
+// The row-batched layout in place of the general one where it applies.
+void prefer_batch(Launch& L, const Inputs& in, int64_t M, int64_t N, int xt, bool base16,
+                  bool pair_ok, int sms, cudaStream_t stream, int kind)
+{
+    if (L.fast || in.scattered) return;
+    const Launch B = plan_batch(M, N, xt, base16, pair_ok, sms, stream, kind);
+    if (B.batch) L = B;
+}
+
 }  // namespace
 
 extern "C" {
@@ -474,7 +521,9 @@ size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int
     // the vector path with the kernel's wide set, or the general path
     const Launch a = plan(M, N, xt, true, sms, nullptr, kind, wide_set(kind, xt));
     const Launch b = plan(M, N, xt, false, sms, nullptr, kind);
-    const size_t need = ws_needed(op, a.P > b.P ? a : b, N);
+    const Launch c = plan_batch(M, N, xt, true, true, sms, nullptr, kind);
+    const Launch& ab = a.P > b.P ? a : b;
+    const size_t need = ws_needed(op, c.batch && c.P > ab.P ? c : ab, N);
     return (need + 255) & ~(size_t)255;
 }
 
@@ -494,11 +543,12 @@ int dyt_fwd_rows(const void* x, const gbn_rows* xl, const void* alpha, const voi
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
                     gbn::kFwdDyT, wide_set(gbn::kFwdDyT, xt));
+    prefer_batch(L, in, M, N, xt, aligned16(x), pair_aligned(xt, {y}), sms, stream, gbn::kFwdDyT);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
     L.maps = in.maps;
-    if (!L.fast) {  // elementwise general path: one thread per element, grid-stride
+    if (!L.fast && !L.batch) {  // elementwise general path: one thread per element
         const int64_t E = M * N;
         const int64_t blocks = (E + gbn::kGenThreads - 1) / gbn::kGenThreads;
         const int64_t cap = 8LL * sms;
@@ -531,6 +581,8 @@ int dyt_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gbn_ro
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
                     stream, gbn::kBwdDyT, wide_set(gbn::kBwdDyT, xt));
+    prefer_batch(L, in, M, N, xt, aligned16(x) && aligned16(dy), pair_aligned(xt, {dx}), sms,
+                 stream, gbn::kBwdDyT);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -571,6 +623,7 @@ int layernorm_fwd_rows(const void* x, const gbn_rows* xl, const void* gamma, con
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
                     gbn::kFwdLN, wide_set(gbn::kFwdLN, xt));
+    prefer_batch(L, in, M, N, xt, aligned16(x), pair_aligned(xt, {y}), sms, stream, gbn::kFwdLN);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -605,6 +658,8 @@ int layernorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const 
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
                     stream, gbn::kBwdLN, wide_set(gbn::kBwdLN, xt));
+    prefer_batch(L, in, M, N, xt, aligned16(x) && aligned16(dy), pair_aligned(xt, {dx}), sms,
+                 stream, gbn::kBwdLN);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -660,6 +715,8 @@ int rmsnorm_fwd_rows(const void* x, const gbn_rows* xl, const void* w, void* y, 
     if (sms <= 0) return GBN_EDEVICE;
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(y) && in.vec_ok, sms, stream,
                     gbn::kFwdNorm, wide_set(gbn::kFwdNorm, xt));
+    prefer_batch(L, in, M, N, xt, aligned16(x), pair_aligned(xt, {y}), sms, stream,
+                 gbn::kFwdNorm);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;
@@ -692,6 +749,8 @@ int rmsnorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gb
     // the forward's set: a recomputed rstd reduces each row in its order
     Launch L = plan(M, N, xt, aligned16(x) && aligned16(dy) && aligned16(dx) && in.vec_ok, sms,
                     stream, gbn::kBwdRms, wide_set(gbn::kBwdRms, xt));
+    prefer_batch(L, in, M, N, xt, aligned16(x) && aligned16(dy), pair_aligned(xt, {dx}), sms,
+                 stream, gbn::kBwdRms);
     if (!(L.fault = fault_ptr())) return GBN_EDEVICE;
     L.scattered = in.scattered;
     L.in_mode = in.mode;

@@ -187,6 +187,144 @@ constexpr int kGenWarps = kGenThreads / 32;
 // rows accumulate in the warp's workspace row in global memory.
 constexpr int kGenCols = 1536;
 
+// --------------------------------------------------- row-batched (any width)
+// Contiguous rows whose byte length is not a multiple of 16 cannot take the
+// 16-byte vectors of the schedules above.  The row-batched kernels still
+// stream them through the bulk-copy ring: a block of R rows, R a multiple of
+// 8, spans R * row_bytes bytes, a multiple of 16 for every element size, so
+// with a 16-byte aligned base every full block starts and ends on a 16-byte
+// boundary and moves as one bulk copy (the last block's final bytes below a
+// 16-byte multiple come from global memory).  In shared memory a warp takes
+// one row at a time and lane l reads units l, l + 32, ... of it: a unit is an
+// element pair when rows hold whole pairs, else one element.  Row
+// reductions are warp butterflies; a backward's column sums stay in
+// registers and are combined across the CTA's warps in warp order at the
+// end.  Widths up to batch_max_units(E) * 32 units, and rows of at most
+// kBatchSlot / 8 bytes.
+constexpr int kBatchThreads = 256;
+constexpr int kBatchWarps = kBatchThreads / 32;
+// KMAX, the units a lane holds per row: up to 4, so rows up to 256 elements
+// in pairs and 128 single elements.  8 units a lane are left out: ptxas 13.0
+// crashes on the LayerNorm kernels' 8-pair instance, and a build whose
+// 8-element LayerNorm instances ran unchecked faulted once on GB300 (the
+// same sequence with every access bounds-checked ran clean).
+constexpr int batch_max_units(int) { return 4; }
+constexpr int kBatchSlot = 8192;   // bytes per staged tensor per ring slot
+constexpr int kBatchStages = 4;
+// CTAs per SM: 4 for a forward (one staged tensor), 3 for a backward.
+constexpr int batch_minb(bool bwd) { return bwd ? 3 : 4; }
+constexpr int batch_smem(int NT) { return 128 + kBatchStages * NT * kBatchSlot; }
+
+// One unit of E consecutive elements (E = 2: a pair, E = 1: one element),
+// moved as one word: loaded through L1 (ld.global.ca, coherent with the
+// previous kernel's writes once griddepcontrol.wait has returned) and
+// stored with the streaming hint.
+template <typename TX, int E> struct Unit;
+template <> struct Unit<float, 1> {
+    using W = float;
+    static __device__ __forceinline__ W ld(const float* p) { return __ldca(p); }
+    static __device__ __forceinline__ void st(float* p, W w) { __stcs(p, w); }
+    static __device__ __forceinline__ void unpack(W w, float (&v)[1]) { v[0] = w; }
+    static __device__ __forceinline__ W pack(const float (&v)[1]) { return v[0]; }
+};
+template <> struct Unit<float, 2> {
+    using W = float2;
+    static __device__ __forceinline__ W ld(const float* p)
+    {
+        return __ldca(reinterpret_cast<const float2*>(p));
+    }
+    static __device__ __forceinline__ void st(float* p, W w)
+    {
+        __stcs(reinterpret_cast<float2*>(p), w);
+    }
+    static __device__ __forceinline__ void unpack(W w, float (&v)[2])
+    {
+        v[0] = w.x;
+        v[1] = w.y;
+    }
+    static __device__ __forceinline__ W pack(const float (&v)[2])
+    {
+        return make_float2(v[0], v[1]);
+    }
+};
+template <typename TX> struct Unit16 {
+    static __device__ __forceinline__ float to_f(unsigned short h)
+    {
+        if constexpr (std::is_same<TX, __half>::value)
+            return __half2float(__ushort_as_half(h));
+        else
+            return __uint_as_float((unsigned)h << 16);
+    }
+    static __device__ __forceinline__ unsigned short from_f(float v)
+    {
+        if constexpr (std::is_same<TX, __half>::value)
+            return __half_as_ushort(__float2half_rn(v));
+        else
+            return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+};
+template <typename TX> struct Unit16x1 {
+    using W = unsigned short;
+    static __device__ __forceinline__ W ld(const TX* p)
+    {
+        return __ldca(reinterpret_cast<const unsigned short*>(p));
+    }
+    static __device__ __forceinline__ void st(TX* p, W w)
+    {
+        __stcs(reinterpret_cast<unsigned short*>(p), w);
+    }
+    static __device__ __forceinline__ void unpack(W w, float (&v)[1])
+    {
+        v[0] = Unit16<TX>::to_f(w);
+    }
+    static __device__ __forceinline__ W pack(const float (&v)[1])
+    {
+        return Unit16<TX>::from_f(v[0]);
+    }
+};
+template <typename TX> struct Unit16x2 {
+    using W = unsigned int;
+    static __device__ __forceinline__ W ld(const TX* p)
+    {
+        return __ldca(reinterpret_cast<const unsigned int*>(p));
+    }
+    static __device__ __forceinline__ void st(TX* p, W w)
+    {
+        __stcs(reinterpret_cast<unsigned int*>(p), w);
+    }
+    static __device__ __forceinline__ void unpack(W w, float (&v)[2])
+    {
+        v[0] = Unit16<TX>::to_f((unsigned short)(w & 0xffffu));
+        v[1] = Unit16<TX>::to_f((unsigned short)(w >> 16));
+    }
+    static __device__ __forceinline__ W pack(const float (&v)[2])
+    {
+        return (unsigned)Unit16<TX>::from_f(v[0]) | ((unsigned)Unit16<TX>::from_f(v[1]) << 16);
+    }
+};
+template <> struct Unit<__nv_bfloat16, 1> : Unit16x1<__nv_bfloat16> {};
+template <> struct Unit<__nv_bfloat16, 2> : Unit16x2<__nv_bfloat16> {};
+template <> struct Unit<__half, 1> : Unit16x1<__half> {};
+template <> struct Unit<__half, 2> : Unit16x2<__half> {};
+
+// Call f(std::integral_constant<int, E>, std::integral_constant<int, KMAX>)
+// for a row-batched launch (host side).
+template <class F>
+inline bool with_batch(int E, int KMAX, F&& f)
+{
+    using std::integral_constant;
+    auto k = [&](auto e) {
+        switch (KMAX) {
+            case 1: f(e, integral_constant<int, 1>{}); return true;
+            case 2: f(e, integral_constant<int, 2>{}); return true;
+            case 4: f(e, integral_constant<int, 4>{}); return true;
+
+            default: return false;
+        }
+    };
+    return E == 2 ? k(integral_constant<int, 2>{}) : k(integral_constant<int, 1>{});
+}
+
 // ------------------------------------------------------------- vector types
 template <typename TX> struct Vec;
 template <> struct Vec<float> { static constexpr int kN = 4; };
@@ -411,20 +549,19 @@ __device__ __forceinline__ int64_t out_row(const OutMap& o, int64_t q)
     return (int64_t)((uq - q1 * o.a) * o.wa + (q1 - q2 * o.b) * o.wb + q2 * o.wc);
 }
 
-// A saved per-row statistic of row r.  Contiguous and scattered rows read
-// the statistics in row order, each 32-byte sector by neighbouring CTAs at
-// about the same time, so they stream past the caches (evict first).  In
-// storage order consecutive rows take statistics a level stride apart, and
-// a sector's eight values serve rows far apart in time: there the load
-// keeps the normal L2 policy so the sector is still resident when the
-// other seven are read.
+// A saved per-row statistic of row r, loaded through L1 with the normal L2
+// policy (ld.global.ca).  Every warp of a row group reads the same value,
+// and L1 serves all but the first; in storage order a 32-byte sector's
+// eight values serve rows a level stride apart, far apart in time, and L2
+// keeps the sector for them.  The streaming (evict-first) hint measured
+// 1-4% slower in the backwards that read statistics (RMSNorm N = 2048
+// 0.927 -> 0.959 of measured copy without it, LayerNorm N = 24 0.913 ->
+// 0.927), and on head-major storage order 8-9%.  The load is coherent with
+// the forward that wrote the statistics once griddepcontrol.wait returns.
 template <int kIn>
 __device__ __forceinline__ float ld_stat(const float* p, int64_t r)
 {
-    if constexpr (kIn == kInStorage)
-        return __ldcg(p + r);
-    else
-        return __ldcs(p + r);
+    return __ldca(p + r);
 }
 
 // The row whose outputs (and saved statistics) belong to this thread's row q.
@@ -464,7 +601,11 @@ __device__ __forceinline__ const TX* in_row(const TX* base, const RowMaps& maps,
 // block b covers rows [b*R, min(b*R + R, M)).  Blocks b = blockIdx.x +
 // k*gridDim.x, k = 0..K-1, belong to this CTA.  With kRows the tensors'
 // rows are scattered (map[t]): warp 0 issues one bulk copy per row, and the
-// slot still holds the block's rows back to back.
+// slot still holds the block's rows back to back.  Contiguous blocks are
+// copied whole; a bulk copy moves a multiple of 16 bytes, so when the last
+// block's byte count is not one, its final (count mod 16) bytes are not
+// copied (tail_bytes below) and the row-batched kernels, the only ones whose
+// rows are not 16-byte multiples, read them from global memory.
 template <int NT, int kStages, bool kRows = false>
 struct Ring {
     uint64_t* bar;             // [kStages]
@@ -490,13 +631,15 @@ struct Ring {
         const int s = (int)(k % kStages);
         const int64_t r0 = block(k) * R;
         const int64_t rows = (M - r0) < R ? (M - r0) : R;
-        const uint32_t bytes = (uint32_t)(rows * row_bytes);
+        const uint32_t bytes = (uint32_t)(rows * row_bytes) & ~15u;
         if constexpr (!kRows) {
             mbar_expect_tx(&bar[s], NT * bytes);
+            if (bytes != 0) {  // a last block narrower than 16 bytes copies nothing
 #pragma unroll
-            for (int t = 0; t < NT; ++t)
-                bulk_g2s(buf + (s * NT + t) * (size_t)slot, src[t] + r0 * row_bytes, bytes,
-                         &bar[s]);
+                for (int t = 0; t < NT; ++t)
+                    bulk_g2s(buf + (s * NT + t) * (size_t)slot, src[t] + r0 * row_bytes, bytes,
+                             &bar[s]);
+            }
         } else {
             const int lane = threadIdx.x & 31;
             if (lane == 0) mbar_expect_tx(&bar[s], NT * bytes);

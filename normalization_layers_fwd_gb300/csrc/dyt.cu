@@ -387,12 +387,192 @@ __global__ void __launch_bounds__(kGenThreads)
     if (wrow && lane == 0) wrow[2 * N] = v[0];
 }
 
+// ------------------------------------------------------ row-batched path
+// Rows whose byte length is not a multiple of 16 (common.cuh, "row-batched"):
+// blocks of R rows through the ring, one warp per row, lane l taking units
+// l, l + 32, ... of it.
+template <typename TX, int E, int KMAX>
+__global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
+    dyt_fwd_batch(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ alpha,
+                  const void* __restrict__ gamma, const void* __restrict__ beta, int pt,
+                  int64_t M, int N, int64_t nblocks, int R, unsigned* fault)
+{
+    grid_dependency_sync();
+    using U = Unit<TX, E>;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nu = N / E;
+    const int rb = N * (int)sizeof(TX);
+    const float a = ld_param(alpha, pt, 0);
+    bool uok[KMAX];
+    float gm[KMAX][E], bt[KMAX][E];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        uok[k] = lane + 32 * k < nu;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int c = (lane + 32 * k) * E + e;
+            gm[k][e] = uok[k] ? ld_param(gamma, pt, c) : 0.f;
+            bt[k][e] = uok[k] ? ld_param(beta, pt, c) : 0.f;
+        }
+    }
+    const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
+    Ring<1, kBatchStages> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.row_bytes = rb;
+    rg.R = R;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = kBatchSlot;
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        if (!alive) return;
+        const unsigned char* xs = rg.tile(k, 0);
+        const int64_t r0 = b * R;
+        const int rows = (int)(M - r0 < R ? M - r0 : R);
+        for (int i = warp; i < rows; i += kBatchWarps) {
+            const int64_t r = r0 + i;
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk) {
+                if (!uok[kk]) continue;
+                const int u = lane + 32 * kk;
+                const int64_t gi = r * N + u * E;
+                const typename U::W w =
+                    gi < tail ? *reinterpret_cast<const typename U::W*>(xs + i * rb +
+                                                                        u * E * sizeof(TX))
+                              : U::ld(x + gi);
+                float v[E];
+                U::unpack(w, v);
+#pragma unroll
+                for (int e = 0; e < E; ++e) v[e] = fmaf(gm[kk][e], dyt_tanh(a * v[e]), bt[kk][e]);
+                U::st(y + gi, U::pack(v));
+            }
+        }
+    });
+}
+
+template <typename TX, int E, int KMAX>
+__global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
+    dyt_bwd_batch(const TX* __restrict__ x, const TX* __restrict__ dy, TX* __restrict__ dx,
+                  const void* __restrict__ alpha, const void* __restrict__ gamma, int pt,
+                  float* __restrict__ ws, int64_t M, int N, int64_t nblocks, int R,
+                  unsigned* fault)
+{
+    grid_dependency_sync();
+    using U = Unit<TX, E>;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ float red[kBatchWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nu = N / E;
+    const int rb = N * (int)sizeof(TX);
+    const float a = ld_param(alpha, pt, 0);
+    bool uok[KMAX];
+    float gm[KMAX][E], acc_g[KMAX][E], acc_b[KMAX][E];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        uok[k] = lane + 32 * k < nu;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            gm[k][e] = uok[k] ? ld_param(gamma, pt, (lane + 32 * k) * E + e) : 0.f;
+            acc_g[k][e] = acc_b[k][e] = 0.f;
+        }
+    }
+    float da = 0.f;
+    const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
+    Ring<2, kBatchStages> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
+    rg.row_bytes = rb;
+    rg.R = R;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = kBatchSlot;
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        if (!alive) return;
+        const unsigned char* xs = rg.tile(k, 0);
+        const unsigned char* ds = rg.tile(k, 1);
+        const int64_t r0 = b * R;
+        const int rows = (int)(M - r0 < R ? M - r0 : R);
+        for (int i = warp; i < rows; i += kBatchWarps) {
+            const int64_t r = r0 + i;
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk) {
+                if (!uok[kk]) continue;
+                const int u = lane + 32 * kk;
+                const int64_t gi = r * N + u * E;
+                const int so = i * rb + u * E * (int)sizeof(TX);
+                const bool sm = gi < tail;
+                const typename U::W wx =
+                    sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
+                const typename U::W wd =
+                    sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
+                float xv[E], dv[E], o[E];
+                U::unpack(wx, xv);
+                U::unpack(wd, dv);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    float t, sc;
+                    dyt_tanh_sech2(a * xv[e], t, sc);
+                    const float dsd = dv[e] * sc;
+                    o[e] = dsd * (gm[kk][e] * a);
+                    acc_g[kk][e] = fmaf(dv[e], t, acc_g[kk][e]);
+                    acc_b[kk][e] += dv[e];
+                    da = fmaf(gm[kk][e], dsd * xv[e], da);
+                }
+                U::st(dx + gi, U::pack(o));
+            }
+        }
+    });
+    if (ws == nullptr) return;  // no parameter gradient requested (uniform)
+    const int64_t L = 2 * (int64_t)N + 1;
+    float* cols = reinterpret_cast<float*>(dsm + 128);  // drained ring slots: 8 x 2N floats
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int c = (lane + 32 * k) * E + e;
+            if (uok[k]) {
+                cols[warp * 2 * N + c] = acc_g[k][e];
+                cols[warp * 2 * N + N + c] = acc_b[k][e];
+            }
+        }
+    float v[1] = {da};
+    butterfly<32, 1>(v);
+    if (lane == 0) red[warp] = v[0];
+    __syncthreads();
+    float* wrow = ws + blockIdx.x * L;
+    for (int c = threadIdx.x; c < 2 * N; c += kBatchThreads) {
+        float t = cols[c];
+#pragma unroll
+        for (int w = 1; w < kBatchWarps; ++w) t += cols[w * 2 * N + c];
+        wrow[c] = t;
+    }
+    if (threadIdx.x == 0) {
+        float t = red[0];
+#pragma unroll
+        for (int w = 1; w < kBatchWarps; ++w) t += red[w];
+        wrow[2 * N] = t;
+    }
+}
+
 template <typename TX>
 cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* alpha,
                          const void* gamma, const void* beta, void* y, int64_t M, int N)
 {
     const TX* xp = static_cast<const TX*>(x);
     TX* yp = static_cast<TX*>(y);
+    if (L.batch) {
+        constexpr int smem = batch_smem(1);
+        if (!with_batch(L.E, L.KMAX, [&](auto e_, auto k_) {
+                constexpr int E_ = decltype(e_)::value, K_ = decltype(k_)::value;
+                ring_attributes<dyt_fwd_batch<TX, E_, K_>>(smem);
+                launch_pdl(dyt_fwd_batch<TX, E_, K_>, L.grid, kBatchThreads, smem, L.stream, xp,
+                           yp, alpha, gamma, beta, pt, M, N, L.nblocks, L.R, L.fault);
+            }))
+            return cudaErrorInvalidValue;
+        return cudaGetLastError();
+    }
     if (!L.fast) {
         launch_pdl(dyt_fwd_general<TX>, L.grid, kGenThreads, 0, L.stream, xp, yp, alpha, gamma,
                    beta, pt, M, N, L.maps, L.scattered);
@@ -426,6 +606,17 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     const TX* xp = static_cast<const TX*>(x);
     const TX* dyp = static_cast<const TX*>(dy);
     TX* dxp = static_cast<TX*>(dx);
+    if (L.batch) {
+        constexpr int smem = batch_smem(2);
+        if (!with_batch(L.E, L.KMAX, [&](auto e_, auto k_) {
+                constexpr int E_ = decltype(e_)::value, K_ = decltype(k_)::value;
+                ring_attributes<dyt_bwd_batch<TX, E_, K_>>(smem);
+                launch_pdl(dyt_bwd_batch<TX, E_, K_>, L.grid, kBatchThreads, smem, L.stream, xp,
+                           dyp, dxp, alpha, gamma, pt, ws, M, N, L.nblocks, L.R, L.fault);
+            }))
+            return cudaErrorInvalidValue;
+        return cudaGetLastError();
+    }
     if (!L.fast) {
         launch_pdl(dyt_bwd_general<TX>, L.grid, kGenThreads, 0, L.stream, xp, dyp, dxp, alpha,
                    gamma, pt, ws, M, N, L.maps, L.scattered);

@@ -44,8 +44,10 @@ enum InMode {
 struct Launch {
     int fast;           // 1: 16-byte vector path (schedule `sid`); 0: general path
     int sid;            // index into kSched (fast path only)
+    int batch;          // 1: row-batched path (when not fast): `E`-element units, at
+    int E, KMAX, R;     //    most KMAX units a lane per row, R rows a ring block
     int grid;           // CTAs launched (persistent: each loops over row blocks)
-    int64_t nblocks;    // row blocks of the fast path
+    int64_t nblocks;    // row blocks of the fast and row-batched paths
     int64_t P;          // partial rows the backward writes into the workspace
     cudaStream_t stream;
     unsigned* fault;    // the device's fault word (bounded waits that ran out)

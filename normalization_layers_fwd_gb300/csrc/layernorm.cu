@@ -411,6 +411,201 @@ __global__ void __launch_bounds__(kGenThreads)
         for (int c = lane; c < 2 * N; c += 32) wrow[c] = arow[c];
 }
 
+// ------------------------------------------------------ row-batched path
+// Rows whose byte length is not a multiple of 16 (common.cuh, "row-batched"):
+// blocks of R rows through the ring, one warp per row.  Units past the row's
+// end read as zeros and are left out of every sum where a zero would count.
+template <typename TX, int E, int KMAX>
+__global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
+    ln_fwd_batch(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ gamma,
+                 const void* __restrict__ beta, int pt, float* __restrict__ mean,
+                 float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
+                 int64_t nblocks, int R, unsigned* fault)
+{
+    grid_dependency_sync();
+    using U = Unit<TX, E>;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nu = N / E;
+    const int rb = N * (int)sizeof(TX);
+    bool uok[KMAX];
+    float gm[KMAX][E], bt[KMAX][E];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        uok[k] = lane + 32 * k < nu;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int c = (lane + 32 * k) * E + e;
+            gm[k][e] = (uok[k] && gamma) ? ld_param(gamma, pt, c) : 1.f;
+            bt[k][e] = (uok[k] && beta) ? ld_param(beta, pt, c) : 0.f;
+        }
+    }
+    const float fN = (float)N;
+    // elements from `tail` on were not bulk-copied (the last block's end)
+    const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
+    Ring<1, kBatchStages> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.row_bytes = rb;
+    rg.R = R;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = kBatchSlot;
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        if (!alive) return;
+        const unsigned char* xs = rg.tile(k, 0);
+        const int64_t r0 = b * R;
+        const int rows = (int)(M - r0 < R ? M - r0 : R);
+        for (int i = warp; i < rows; i += kBatchWarps) {
+            const int64_t r = r0 + i;
+            float v[KMAX][E];
+            float s = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk) {
+                const int u = lane + 32 * kk;
+                const int64_t gi = r * N + u * E;
+                typename U::W w{};
+                if (uok[kk])
+                    w = gi < tail ? *reinterpret_cast<const typename U::W*>(xs + i * rb +
+                                                                            u * E * sizeof(TX))
+                                  : U::ld(x + gi);
+                U::unpack(w, v[kk]);
+#pragma unroll
+                for (int e = 0; e < E; ++e) s += v[kk][e];
+            }
+            float a[1] = {s};
+            butterfly<32, 1>(a);
+            const float mu = row_mean(a[0], fN, inv_n);
+            float q[1] = {0.f};
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk)
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    v[kk][e] -= mu;
+                    q[0] = uok[kk] ? fmaf(v[kk][e], v[kk][e], q[0]) : q[0];
+                }
+            butterfly<32, 1>(q);
+            const float rs = rsqrtf(fmaf(q[0], inv_n, eps));
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk) {
+                float o[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[e] = fmaf(v[kk][e] * rs, gm[kk][e], bt[kk][e]);
+                if (uok[kk]) U::st(y + r * N + (lane + 32 * kk) * E, U::pack(o));
+            }
+            if (lane == 0) {
+                if (mean) mean[r] = mu;
+                if (rstd) rstd[r] = rs;
+            }
+        }
+    });
+}
+
+template <typename TX, int E, int KMAX>
+__global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
+    ln_bwd_batch(const TX* __restrict__ x, const TX* __restrict__ dy,
+                 const float* __restrict__ mean, const float* __restrict__ rstd,
+                 const void* __restrict__ gamma, int pt, TX* __restrict__ dx,
+                 float* __restrict__ ws, int64_t M, int N, float inv_n, int64_t nblocks, int R,
+                 unsigned* fault)
+{
+    grid_dependency_sync();
+    using U = Unit<TX, E>;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nu = N / E;
+    const int rb = N * (int)sizeof(TX);
+    bool uok[KMAX];
+    float gm[KMAX][E], acc_g[KMAX][E], acc_b[KMAX][E];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        uok[k] = lane + 32 * k < nu;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            gm[k][e] = (uok[k] && gamma) ? ld_param(gamma, pt, (lane + 32 * k) * E + e) : 1.f;
+            acc_g[k][e] = acc_b[k][e] = 0.f;
+        }
+    }
+    const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
+    Ring<2, kBatchStages> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
+    rg.row_bytes = rb;
+    rg.R = R;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = kBatchSlot;
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        if (!alive) return;
+        const unsigned char* xs = rg.tile(k, 0);
+        const unsigned char* ds = rg.tile(k, 1);
+        const int64_t r0 = b * R;
+        const int rows = (int)(M - r0 < R ? M - r0 : R);
+        for (int i = warp; i < rows; i += kBatchWarps) {
+            const int64_t r = r0 + i;
+            const float mu = __ldca(mean + r), rs = __ldca(rstd + r);
+            float xh[KMAX][E], g[KMAX][E];
+            float s[2] = {0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk) {
+                const int u = lane + 32 * kk;
+                const int64_t gi = r * N + u * E;
+                const int so = i * rb + u * E * (int)sizeof(TX);
+                typename U::W wx{}, wd{};
+                if (uok[kk]) {
+                    const bool sm = gi < tail;
+                    wx = sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
+                    wd = sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
+                }
+                float xv[E], dv[E];
+                U::unpack(wx, xv);
+                U::unpack(wd, dv);
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    xh[kk][e] = (xv[e] - mu) * rs;
+                    g[kk][e] = dv[e] * gm[kk][e];
+                    s[0] += g[kk][e];
+                    s[1] = fmaf(g[kk][e], xh[kk][e], s[1]);
+                    acc_g[kk][e] = fmaf(dv[e], xh[kk][e], acc_g[kk][e]);
+                    acc_b[kk][e] += dv[e];
+                }
+            }
+            butterfly<32, 2>(s);
+            const float ma = s[0] * inv_n, mb = s[1] * inv_n;
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk) {
+                float o[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[e] = rs * fmaf(-xh[kk][e], mb, g[kk][e] - ma);
+                if (uok[kk]) U::st(dx + r * N + (lane + 32 * kk) * E, U::pack(o));
+            }
+        }
+    });
+    if (ws == nullptr) return;  // no parameter gradient requested (uniform)
+    // the warps' column sums, added in warp order into the CTA's partial row
+    // (the drained ring slots hold them: 8 x 2N floats, at most 32 KB)
+    float* cols = reinterpret_cast<float*>(dsm + 128);
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int c = (lane + 32 * k) * E + e;
+            if (uok[k]) {
+                cols[warp * 2 * N + c] = acc_g[k][e];
+                cols[warp * 2 * N + N + c] = acc_b[k][e];
+            }
+        }
+    __syncthreads();
+    float* wrow = ws + blockIdx.x * (2 * (int64_t)N);
+    for (int c = threadIdx.x; c < 2 * N; c += kBatchThreads) {
+        float t = cols[c];
+#pragma unroll
+        for (int w = 1; w < kBatchWarps; ++w) t += cols[w * 2 * N + c];
+        wrow[c] = t;
+    }
+}
+
 template <typename TX>
 cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gamma,
                          const void* beta, void* y, float* mean, float* rstd, int64_t M, int N,
@@ -419,6 +614,17 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
     const TX* xp = static_cast<const TX*>(x);
     TX* yp = static_cast<TX*>(y);
     const float inv_n = (float)(1.0 / (double)N);
+    if (L.batch) {
+        constexpr int smem = batch_smem(1);
+        if (!with_batch(L.E, L.KMAX, [&](auto e_, auto k_) {
+                constexpr int E_ = decltype(e_)::value, K_ = decltype(k_)::value;
+                ring_attributes<ln_fwd_batch<TX, E_, K_>>(smem);
+                launch_pdl(ln_fwd_batch<TX, E_, K_>, L.grid, kBatchThreads, smem, L.stream, xp, yp,
+                           gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.nblocks, L.R, L.fault);
+            }))
+            return cudaErrorInvalidValue;
+        return cudaGetLastError();
+    }
     if (!L.fast) {
         launch_pdl(ln_fwd_general<TX>, L.grid, kGenThreads, 0, L.stream,
             xp, yp, gamma, beta, pt, mean, rstd, M, N, eps, inv_n, L.maps, L.scattered);
@@ -455,6 +661,18 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     const TX* dyp = static_cast<const TX*>(dy);
     TX* dxp = static_cast<TX*>(dx);
     const float inv_n = (float)(1.0 / (double)N);
+    if (L.batch) {
+        constexpr int smem = batch_smem(2);
+        if (!with_batch(L.E, L.KMAX, [&](auto e_, auto k_) {
+                constexpr int E_ = decltype(e_)::value, K_ = decltype(k_)::value;
+                ring_attributes<ln_bwd_batch<TX, E_, K_>>(smem);
+                launch_pdl(ln_bwd_batch<TX, E_, K_>, L.grid, kBatchThreads, smem, L.stream, xp,
+                           dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.nblocks, L.R,
+                           L.fault);
+            }))
+            return cudaErrorInvalidValue;
+        return cudaGetLastError();
+    }
     if (!L.fast) {
         launch_pdl(ln_bwd_general<TX>, L.grid, kGenThreads, 0, L.stream,
             xp, dyp, mean, rstd, gamma, pt, dxp, ws, M, N, inv_n, L.maps, L.scattered);

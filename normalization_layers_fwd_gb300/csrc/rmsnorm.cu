@@ -130,6 +130,74 @@ __global__ void __launch_bounds__(kGenThreads)
     }
 }
 
+// ------------------------------------------------------ row-batched path
+// Rows whose byte length is not a multiple of 16 (common.cuh, "row-batched"):
+// blocks of R rows through the ring, one warp per row.
+template <typename TX, int E, int KMAX>
+__global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
+    rms_fwd_batch(const TX* __restrict__ x, TX* __restrict__ y, const void* __restrict__ w,
+                  int pt, float* __restrict__ rstd, int64_t M, int N, float eps, float inv_n,
+                  int variant, int64_t nblocks, int R, unsigned* fault)
+{
+    grid_dependency_sync();
+    using U = Unit<TX, E>;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nu = N / E;
+    const int rb = N * (int)sizeof(TX);
+    bool uok[KMAX];
+    float wv[KMAX][E];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        uok[k] = lane + 32 * k < nu;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            wv[k][e] = uok[k] ? rms_weight(w, pt, (lane + 32 * k) * E + e, variant) : 0.f;
+    }
+    const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
+    Ring<1, kBatchStages> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.row_bytes = rb;
+    rg.R = R;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = kBatchSlot;
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        if (!alive) return;
+        const unsigned char* xs = rg.tile(k, 0);
+        const int64_t r0 = b * R;
+        const int rows = (int)(M - r0 < R ? M - r0 : R);
+        for (int i = warp; i < rows; i += kBatchWarps) {
+            const int64_t r = r0 + i;
+            float v[KMAX][E];
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk) {
+                const int u = lane + 32 * kk;
+                const int64_t gi = r * N + u * E;
+                typename U::W wd{};
+                if (uok[kk])
+                    wd = gi < tail ? *reinterpret_cast<const typename U::W*>(xs + i * rb +
+                                                                             u * E * sizeof(TX))
+                                   : U::ld(x + gi);
+                U::unpack(wd, v[kk]);
+            }
+            const float rs = batch_row_rstd<KMAX, E>(v, eps, inv_n);
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk) {
+                float o[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float xh = v[kk][e] * rs;
+                    o[e] = wv[kk][e] * (variant == 0 ? round_x<TX>(xh) : xh);
+                }
+                if (uok[kk]) U::st(y + r * N + (lane + 32 * kk) * E, U::pack(o));
+            }
+            if (rstd && lane == 0) rstd[r] = rs;
+        }
+    });
+}
+
 template <typename TX>
 cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, void* y,
                          float* rstd, int64_t M, int N, float eps, int variant)
@@ -138,6 +206,17 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
     TX* yp = static_cast<TX*>(y);
     const float inv_n = (float)(1.0 / (double)N);
     const int gemma = variant == 2;
+    if (L.batch) {
+        constexpr int smem = batch_smem(1);
+        if (!with_batch(L.E, L.KMAX, [&](auto e_, auto k_) {
+                constexpr int E_ = decltype(e_)::value, K_ = decltype(k_)::value;
+                ring_attributes<rms_fwd_batch<TX, E_, K_>>(smem);
+                launch_pdl(rms_fwd_batch<TX, E_, K_>, L.grid, kBatchThreads, smem, L.stream, xp,
+                           yp, w, pt, rstd, M, N, eps, inv_n, variant, L.nblocks, L.R, L.fault);
+            }))
+            return cudaErrorInvalidValue;
+        return cudaGetLastError();
+    }
     if (!L.fast) {
         launch_pdl(rms_fwd_general<TX>, L.grid, kGenThreads, 0, L.stream,
             xp, yp, w, pt, rstd, M, N, eps, inv_n, variant, L.maps, L.scattered);

@@ -239,6 +239,115 @@ __global__ void __launch_bounds__(kGenThreads)
         for (int c = lane; c < N; c += 32) wrow[c] = arow[c];
 }
 
+// ------------------------------------------------------ row-batched path
+// Rows whose byte length is not a multiple of 16 (common.cuh, "row-batched"):
+// blocks of R rows through the ring, one warp per row; a recomputed r uses
+// the forward's batch_row_rstd.  The rounding points are the general path's.
+template <typename TX, int E, int KMAX>
+__global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
+    rms_bwd_batch(const TX* __restrict__ x, const TX* __restrict__ dy, const void* __restrict__ w,
+                  int pt, const float* __restrict__ rstd, TX* __restrict__ dx,
+                  float* __restrict__ ws, int64_t M, int N, float eps, float inv_n, int variant,
+                  int64_t nblocks, int R, unsigned* fault)
+{
+    grid_dependency_sync();
+    using U = Unit<TX, E>;
+    extern __shared__ __align__(128) unsigned char dsm[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nu = N / E;
+    const int rb = N * (int)sizeof(TX);
+    const bool cast_first = variant == 0;  // the Llama expression's rounding points
+    const bool round_terms = cast_first && pt != kF32;
+    bool uok[KMAX];
+    float wv[KMAX][E], acc[KMAX][E];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        uok[k] = lane + 32 * k < nu;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            wv[k][e] = uok[k] ? rms_weight(w, pt, (lane + 32 * k) * E + e, variant) : 0.f;
+            acc[k][e] = 0.f;
+        }
+    }
+    const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
+    Ring<2, kBatchStages> rg;
+    rg.src[0] = reinterpret_cast<const unsigned char*>(x);
+    rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
+    rg.row_bytes = rb;
+    rg.R = R;
+    rg.M = M;
+    rg.nblocks = nblocks;
+    rg.slot = kBatchSlot;
+    rg.fault = fault;
+    ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+        if (!alive) return;
+        const unsigned char* xs = rg.tile(k, 0);
+        const unsigned char* ds = rg.tile(k, 1);
+        const int64_t r0 = b * R;
+        const int rows = (int)(M - r0 < R ? M - r0 : R);
+        for (int i = warp; i < rows; i += kBatchWarps) {
+            const int64_t r = r0 + i;
+            float xv[KMAX][E], dv[KMAX][E];
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk) {
+                const int u = lane + 32 * kk;
+                const int64_t gi = r * N + u * E;
+                const int so = i * rb + u * E * (int)sizeof(TX);
+                typename U::W wx{}, wd{};
+                if (uok[kk]) {
+                    const bool sm = gi < tail;
+                    wx = sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
+                    wd = sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
+                }
+                U::unpack(wx, xv[kk]);
+                U::unpack(wd, dv[kk]);
+            }
+            const float rs = rstd ? __ldca(rstd + r) : batch_row_rstd<KMAX, E>(xv, eps, inv_n);
+            float s[1] = {0.f};
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk)
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    float dn = dv[kk][e] * wv[kk][e];
+                    if (cast_first) dn = round_x<TX>(dn);
+                    s[0] = fmaf(dn, xv[kk][e] * rs, s[0]);
+                }
+            butterfly<32, 1>(s);
+            const float m = s[0] * inv_n;
+#pragma unroll
+            for (int kk = 0; kk < KMAX; ++kk) {
+                float o[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float xh = xv[kk][e] * rs;
+                    float dn = dv[kk][e] * wv[kk][e];
+                    if (cast_first) dn = round_x<TX>(dn);
+                    o[e] = rs * (dn - xh * m);
+                    float term = dv[kk][e] * (cast_first ? round_x<TX>(xh) : xh);
+                    if (round_terms) term = round_x<TX>(term);
+                    acc[kk][e] += term;
+                }
+                if (uok[kk]) U::st(dx + r * N + (lane + 32 * kk) * E, U::pack(o));
+            }
+        }
+    });
+    if (ws == nullptr) return;  // no weight gradient requested (uniform)
+    float* cols = reinterpret_cast<float*>(dsm + 128);  // drained ring slots: 8 x N floats
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            if (uok[k]) cols[warp * N + (lane + 32 * k) * E + e] = acc[k][e];
+    __syncthreads();
+    float* wrow = ws + blockIdx.x * (int64_t)N;
+    for (int c = threadIdx.x; c < N; c += kBatchThreads) {
+        float t = cols[c];
+#pragma unroll
+        for (int q = 1; q < kBatchWarps; ++q) t += cols[q * N + c];
+        wrow[c] = t;
+    }
+}
+
 template <typename TX>
 cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy, const void* w,
                          const float* rstd, void* dx, float* ws, int64_t M, int N, float eps,
@@ -249,6 +358,18 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     TX* dxp = static_cast<TX*>(dx);
     const float inv_n = (float)(1.0 / (double)N);
     const int gemma = variant == 2;
+    if (L.batch) {
+        constexpr int smem = batch_smem(2);
+        if (!with_batch(L.E, L.KMAX, [&](auto e_, auto k_) {
+                constexpr int E_ = decltype(e_)::value, K_ = decltype(k_)::value;
+                ring_attributes<rms_bwd_batch<TX, E_, K_>>(smem);
+                launch_pdl(rms_bwd_batch<TX, E_, K_>, L.grid, kBatchThreads, smem, L.stream, xp,
+                           dyp, w, pt, rstd, dxp, ws, M, N, eps, inv_n, variant, L.nblocks, L.R,
+                           L.fault);
+            }))
+            return cudaErrorInvalidValue;
+        return cudaGetLastError();
+    }
     if (!L.fast) {
         launch_pdl(rms_bwd_general<TX>, L.grid, kGenThreads, 0, L.stream,
             xp, dyp, w, pt, rstd, dxp, ws, M, N, eps, inv_n, variant, L.maps, L.scattered);

@@ -67,7 +67,9 @@ def layernorm_case(x, dy, gamma, beta, eps, rows=None, cols=True, stats=None):
     torch.cuda.synchronize()
     mu64, rs64 = f64(mean), f64(rstd)
     dxo, dxs = oracle.ln_bwd_rows(xo, dyo, mu64, rs64, g64, rows)
-    reps.append(check_out("ln dx", _sel(dx, rows), dxo, dxs))
+    # at width two x-hat is +-sqrt(var / (var + eps)), so dx is eps / (var + eps)
+    # times the size of its terms: all cancellation, as at width one
+    reps.append(check_out("ln dx", _sel(dx, rows), dxo, dxs, cap=x.shape[-1] > 2))
     if cols:
         c = oracle.ln_bwd_cols(xo, dyo, mu64, rs64)
         reps.append(check_reduced("ln dgamma", dg, c["dgamma"], c["dgamma_ss"]))

@@ -117,13 +117,16 @@ def check_nan(name, g, o):
     return ng
 
 
-def check_bf16(name, g_t: torch.Tensor, o, scale, allow=None) -> Report:
+def check_bf16(name, g_t: torch.Tensor, o, scale, allow=None, cap=True) -> Report:
     """16-bit (bfloat16 or binary16) output vs oracle value o (float64,
     before rounding).
 
     The cap on counted exceptions does not apply at width one, where the
     input gradient is (nearly) all cancellation: DeepSpeed PR 8664 notes
-    that a width-one norm's computed input gradient is rounding noise."""
+    that a width-one norm's computed input gradient is rounding noise.
+    cap=False lifts it for other such outputs (LayerNorm's input gradient
+    at width two, eps / (var + eps) times the size of its terms); every
+    element must still be within 1 ULP or the cancellation bound."""
     fmt = fmt_of(g_t)
     gb = bf16_bits(g_t).reshape(o.shape)
     g = f64(g_t).reshape(o.shape)
@@ -138,13 +141,14 @@ def check_bf16(name, g_t: torch.Tensor, o, scale, allow=None) -> Report:
         err = np.abs(g - o)
     ok1 = d <= 1
     okc = err <= np.maximum(CANCEL_REL * scale, TINY)
-    oka = np.zeros_like(ok1) if allow is None else ((allow > 0) & (err <= allow + bf16_ulp(ref, fmt)))
+    oka = (np.zeros_like(ok1) if allow is None
+           else ((allow > 0) & (err <= allow + bf16_ulp(ref, fmt))))
     bad = ~(ok1 | okc | oka | nan)
     if bad.any():
         _fail(name, bad, g, o, f"(max ulp {int(d[bad].max())})")
     exc = (~ok1) & ~nan
     n = int(o.size)
-    if o.ndim == 2 and o.shape[1] > 1 and exc.sum() > max(8, MAX_EXCEPTION_FRAC * n):
+    if cap and o.ndim == 2 and o.shape[1] > 1 and exc.sum() > max(8, MAX_EXCEPTION_FRAC * n):
         raise AssertionError(f"{name}: {int(exc.sum())} counted exceptions in {n} elements")
     within1 = float(np.mean(ok1 | nan)) if n else 1.0
     with np.errstate(invalid="ignore"):
@@ -193,7 +197,7 @@ def check_reduced(name, g_t: torch.Tensor, o, ss, allow=None) -> Report:
     return Report(name=name, n=int(o.size), max_rel=float(np.nanmax(rel)) if o.size else 0.0)
 
 
-def check_out(name, g_t, o, scale, allow=None):
+def check_out(name, g_t, o, scale, allow=None, cap=True):
     if fmt_of(g_t):
-        return check_bf16(name, g_t, o, scale, allow)
+        return check_bf16(name, g_t, o, scale, allow, cap)
     return check_f32(name, g_t, o, scale, allow)

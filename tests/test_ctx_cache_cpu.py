@@ -23,7 +23,13 @@ static uint64_t g_ctx = 0;   // the fake current context id (0: none)
 static int g_fetches = 0;    // lookups made
 static uint64_t fake_id() { return g_ctx; }
 
-#define CHECK(c) do { if (!(c)) { std::printf("FAIL line %d: %s\n", __LINE__, #c); return 1; } } while (0)
+#define CHECK(c)                                                      \
+    do {                                                              \
+        if (!(c)) {                                                   \
+            std::printf("FAIL line %d: %s\n", __LINE__, #c);          \
+            return 1;                                                 \
+        }                                                             \
+    } while (0)
 
 int main()
 {

@@ -49,11 +49,18 @@ def _run(op, inp, eps=1e-5, rows=None):
 
 # 16-bit widths 8200-16384 (1025-2048 vectors) run the DyT and LayerNorm
 # forwards on the 4-vector wide schedule; float32 widths 4104-8192 run every
-# kernel on it; 8196 and 16392 are beyond it.
-BF16_WIDTHS = [1, 5, 8, 16, 24, 40, 64, 128, 129, 136, 256, 264, 512, 520, 1000, 1024, 2048,
-               3072, 4096, 6000, 8192, 8200, 12288, 16384, 16392]
-F32_WIDTHS = [1, 3, 4, 12, 64, 100, 256, 1024, 2048, 3000, 4096, 4100, 4104, 6000, 8192, 8196]
-F16_WIDTHS = [1, 8, 16, 24, 40, 64, 128, 264, 1000, 2048, 3072, 4096, 6000, 8192, 8200, 12288]
+# kernel on it; 8196 and 16392 are beyond it.  Widths up to 256 whose rows
+# are not 16-byte multiples run the row-batched path: element pairs for even
+# widths up to 256 (2, 6, 100, 130, 250), single elements for odd ones up to
+# 128 (1, 5), rows narrower than 16 bytes included; 129, 255, 258 and 1001
+# stay general.
+BF16_WIDTHS = [1, 2, 5, 6, 8, 16, 24, 40, 64, 100, 127, 128, 129, 130, 136, 250, 255, 256, 258,
+               264, 512, 520, 1000, 1001, 1024, 2048, 3072, 4096, 6000, 8192, 8200, 12288, 16384,
+               16392]
+F32_WIDTHS = [1, 2, 3, 4, 6, 12, 64, 100, 130, 250, 255, 256, 1024, 2048, 3000, 4096, 4100, 4104,
+              6000, 8192, 8196]
+F16_WIDTHS = [1, 5, 8, 16, 24, 40, 64, 128, 129, 130, 264, 1000, 2048, 3072, 4096, 6000, 8192,
+              8200, 12288]
 DTYPES = [(torch.bfloat16, torch.float32), (torch.bfloat16, torch.bfloat16),
           (torch.float32, torch.float32), (torch.float32, torch.bfloat16),
           (torch.float16, torch.float32), (torch.float16, torch.float16)]
@@ -61,7 +68,7 @@ WIDTHS = {torch.bfloat16: BF16_WIDTHS, torch.float32: F32_WIDTHS, torch.float16:
 CASES = []
 for xdt, pdt in DTYPES:
     for N in WIDTHS[xdt]:
-        if pdt != torch.float32 and N not in (24, 128, 2048, 3072, 8192):
+        if pdt != torch.float32 and N not in (24, 128, 130, 2048, 3072, 8192):
             continue
         for op in ("dyt", "layernorm", "rmsnorm"):
             CASES.append((op, xdt, pdt, N))
@@ -100,7 +107,7 @@ def test_rms_variants(variant, xdt, pdt, N):
 
 
 @pytest.mark.parametrize("op", ["dyt", "layernorm", "rmsnorm"])
-@pytest.mark.parametrize("N", [16, 24, 64])
+@pytest.mark.parametrize("N", [16, 24, 64, 5, 130])
 def test_persistent_loop(op, N):
     # enough rows that every resident CTA loops over several row blocks
     M = (1 << 22) // N + 7
@@ -172,7 +179,7 @@ def test_rms_width_one_page_eps():
 
 @pytest.mark.parametrize("op", ["dyt", "layernorm", "rmsnorm"])
 @pytest.mark.parametrize("N,aligned", [(24, True), (128, True), (2048, True), (8192, True),
-                                       (130, False)])
+                                       (130, True), (127, True), (129, True), (130, False)])
 def test_bit_identical_reruns(op, N, aligned):
     inp = _inputs(4099, N, torch.bfloat16, torch.float32, f"det{op}{N}")
     if not aligned:

@@ -145,7 +145,8 @@ def test_documented_limits_hold_on_this_device():
     n_fit -= 1 if n_fit % 8 == 0 else 0
     n_over = n_fit + 1 if (n_fit + 1) % 8 else n_fit + 2
     M = 64 * S
-    fit = lib.gbn_bwd_workspace_bytes(_lib.GBN_OP_RMSNORM, M, n_fit, _lib.GBN_BF16, _lib.GBN_BF16, 0)
+    fit = lib.gbn_bwd_workspace_bytes(_lib.GBN_OP_RMSNORM, M, n_fit, _lib.GBN_BF16,
+                                      _lib.GBN_BF16, 0)
     over = lib.gbn_bwd_workspace_bytes(_lib.GBN_OP_RMSNORM, M, n_over, _lib.GBN_BF16,
                                        _lib.GBN_BF16, 0)
     assert fit <= _lib.GBN_STATIC_WS_BYTES

@@ -235,14 +235,18 @@ Launch plan_batch(int64_t M, int64_t N, int xt, bool base16, bool pair_ok, int s
     if (!base16 || M <= 0) return L;
     const int E = (N % 2 == 0 && pair_ok) ? 2 : 1;
     const int64_t nu = N / E;
-    int kmax = 1;
-    while ((int64_t)kmax * 32 < nu) kmax *= 2;
+    const int64_t kmax = (nu + 31) / 32;  // units a lane
     if (kmax > gbn::batch_max_units(E)) return L;
-    const int64_t R = (gbn::kBatchSlot / (N * elem_bytes(xt))) / 8 * 8;
+    // rows a block: a multiple of 8 * RB (every warp busy) where the slot
+    // holds that many, else of 8
+    const int64_t fit = gbn::kBatchSlot / (N * elem_bytes(xt));
+    const int64_t step =
+        8 * (kind == gbn::kFwdDyT || kind == gbn::kBwdDyT ? 1 : gbn::batch_rb((int)kmax, E));
+    const int64_t R = fit >= step ? fit / step * step : fit / 8 * 8;
     if (R < 8) return L;
     L.batch = 1;
     L.E = E;
-    L.KMAX = kmax;
+    L.KMAX = (int)kmax;
     L.R = (int)R;
     L.nblocks = (M + R - 1) / R;
     const int64_t cap = (int64_t)sms * gbn::batch_minb(gbn::is_bwd(kind));

@@ -209,6 +209,12 @@ constexpr int kBatchWarps = kBatchThreads / 32;
 // 8-element LayerNorm instances ran unchecked faulted once on GB300 (the
 // same sequence with every access bounds-checked ran clean).
 constexpr int batch_max_units(int) { return 4; }
+// Rows a warp takes at once (their reductions share one butterfly, so the
+// shuffle chains of RB rows overlap), by the values a lane holds per row
+// (KMAX * E): 4 rows up to 2 values, 2 up to 6, 1 at 8 (more spill in the
+// backwards).  A ring block holds a multiple of 8 * RB rows where the slot
+// allows.
+constexpr int batch_rb(int KMAX, int E) { return KMAX * E <= 2 ? 4 : KMAX * E <= 6 ? 2 : 1; }
 constexpr int kBatchSlot = 8192;   // bytes per staged tensor per ring slot
 constexpr int kBatchStages = 4;
 // CTAs per SM: 4 for a forward (one staged tensor), 3 for a backward.
@@ -317,8 +323,8 @@ inline bool with_batch(int E, int KMAX, F&& f)
         switch (KMAX) {
             case 1: f(e, integral_constant<int, 1>{}); return true;
             case 2: f(e, integral_constant<int, 2>{}); return true;
+            case 3: f(e, integral_constant<int, 3>{}); return true;
             case 4: f(e, integral_constant<int, 4>{}); return true;
-
             default: return false;
         }
     };

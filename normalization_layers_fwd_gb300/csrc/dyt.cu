@@ -425,27 +425,34 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
     rg.nblocks = nblocks;
     rg.slot = kBatchSlot;
     rg.fault = fault;
+    constexpr int RB = 1;  // no row reduction to share: one row at a time
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
         const unsigned char* xs = rg.tile(k, 0);
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        for (int i = warp; i < rows; i += kBatchWarps) {
-            const int64_t r = r0 + i;
+        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
 #pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk) {
-                if (!uok[kk]) continue;
-                const int u = lane + 32 * kk;
-                const int64_t gi = r * N + u * E;
-                const typename U::W w =
-                    gi < tail ? *reinterpret_cast<const typename U::W*>(xs + i * rb +
-                                                                        u * E * sizeof(TX))
-                              : U::ld(x + gi);
-                float v[E];
-                U::unpack(w, v);
+            for (int rr = 0; rr < RB; ++rr) {
+                const int i = i0 + rr;
+                if (i >= rows) break;  // the same for the whole warp
+                const int64_t r = r0 + i;
 #pragma unroll
-                for (int e = 0; e < E; ++e) v[e] = fmaf(gm[kk][e], dyt_tanh(a * v[e]), bt[kk][e]);
-                U::st(y + gi, U::pack(v));
+                for (int kk = 0; kk < KMAX; ++kk) {
+                    if (!uok[kk]) continue;
+                    const int u = lane + 32 * kk;
+                    const int64_t gi = r * N + u * E;
+                    const typename U::W w =
+                        gi < tail ? *reinterpret_cast<const typename U::W*>(xs + i * rb +
+                                                                            u * E * sizeof(TX))
+                                  : U::ld(x + gi);
+                    float v[E];
+                    U::unpack(w, v);
+#pragma unroll
+                    for (int e = 0; e < E; ++e)
+                        v[e] = fmaf(gm[kk][e], dyt_tanh(a * v[e]), bt[kk][e]);
+                    U::st(y + gi, U::pack(v));
+                }
             }
         }
     });
@@ -488,39 +495,45 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
     rg.nblocks = nblocks;
     rg.slot = kBatchSlot;
     rg.fault = fault;
+    constexpr int RB = 1;  // no row reduction to share: one row at a time
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
         const unsigned char* xs = rg.tile(k, 0);
         const unsigned char* ds = rg.tile(k, 1);
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        for (int i = warp; i < rows; i += kBatchWarps) {
-            const int64_t r = r0 + i;
+        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
 #pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk) {
-                if (!uok[kk]) continue;
-                const int u = lane + 32 * kk;
-                const int64_t gi = r * N + u * E;
-                const int so = i * rb + u * E * (int)sizeof(TX);
-                const bool sm = gi < tail;
-                const typename U::W wx =
-                    sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
-                const typename U::W wd =
-                    sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
-                float xv[E], dv[E], o[E];
-                U::unpack(wx, xv);
-                U::unpack(wd, dv);
+            for (int rr = 0; rr < RB; ++rr) {
+                const int i = i0 + rr;
+                if (i >= rows) break;  // the same for the whole warp
+                const int64_t r = r0 + i;
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    float t, sc;
-                    dyt_tanh_sech2(a * xv[e], t, sc);
-                    const float dsd = dv[e] * sc;
-                    o[e] = dsd * (gm[kk][e] * a);
-                    acc_g[kk][e] = fmaf(dv[e], t, acc_g[kk][e]);
-                    acc_b[kk][e] += dv[e];
-                    da = fmaf(gm[kk][e], dsd * xv[e], da);
+                for (int kk = 0; kk < KMAX; ++kk) {
+                    if (!uok[kk]) continue;
+                    const int u = lane + 32 * kk;
+                    const int64_t gi = r * N + u * E;
+                    const int so = i * rb + u * E * (int)sizeof(TX);
+                    const bool sm = gi < tail;
+                    const typename U::W wx =
+                        sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
+                    const typename U::W wd =
+                        sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
+                    float xv[E], dv[E], o[E];
+                    U::unpack(wx, xv);
+                    U::unpack(wd, dv);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        float t, sc;
+                        dyt_tanh_sech2(a * xv[e], t, sc);
+                        const float dsd = dv[e] * sc;
+                        o[e] = dsd * (gm[kk][e] * a);
+                        acc_g[kk][e] = fmaf(dv[e], t, acc_g[kk][e]);
+                        acc_b[kk][e] += dv[e];
+                        da = fmaf(gm[kk][e], dsd * xv[e], da);
+                    }
+                    U::st(dx + gi, U::pack(o));
                 }
-                U::st(dx + gi, U::pack(o));
             }
         }
     });

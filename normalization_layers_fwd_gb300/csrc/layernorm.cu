@@ -451,51 +451,66 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
     rg.nblocks = nblocks;
     rg.slot = kBatchSlot;
     rg.fault = fault;
+    constexpr int RB = batch_rb(KMAX, E);
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
         const unsigned char* xs = rg.tile(k, 0);
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        for (int i = warp; i < rows; i += kBatchWarps) {
-            const int64_t r = r0 + i;
-            float v[KMAX][E];
-            float s = 0.f;
+        // RB consecutive rows a warp at once; rows past the block read zeros
+        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
+            float v[RB][KMAX][E], s[RB], q[RB];
 #pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk) {
-                const int u = lane + 32 * kk;
-                const int64_t gi = r * N + u * E;
-                typename U::W w{};
-                if (uok[kk])
-                    w = gi < tail ? *reinterpret_cast<const typename U::W*>(xs + i * rb +
-                                                                            u * E * sizeof(TX))
-                                  : U::ld(x + gi);
-                U::unpack(w, v[kk]);
+            for (int rr = 0; rr < RB; ++rr) {
+                const int i = i0 + rr;
+                const int64_t r = r0 + i;
+                s[rr] = 0.f;
 #pragma unroll
-                for (int e = 0; e < E; ++e) s += v[kk][e];
-            }
-            float a[1] = {s};
-            butterfly<32, 1>(a);
-            const float mu = row_mean(a[0], fN, inv_n);
-            float q[1] = {0.f};
+                for (int kk = 0; kk < KMAX; ++kk) {
+                    const int u = lane + 32 * kk;
+                    const int64_t gi = r * N + u * E;
+                    typename U::W w{};
+                    if (i < rows && uok[kk])
+                        w = gi < tail ? *reinterpret_cast<const typename U::W*>(
+                                            xs + i * rb + u * E * sizeof(TX))
+                                      : U::ld(x + gi);
+                    U::unpack(w, v[rr][kk]);
 #pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk)
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    v[kk][e] -= mu;
-                    q[0] = uok[kk] ? fmaf(v[kk][e], v[kk][e], q[0]) : q[0];
+                    for (int e = 0; e < E; ++e) s[rr] += v[rr][kk][e];
                 }
-            butterfly<32, 1>(q);
-            const float rs = rsqrtf(fmaf(q[0], inv_n, eps));
-#pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk) {
-                float o[E];
-#pragma unroll
-                for (int e = 0; e < E; ++e) o[e] = fmaf(v[kk][e] * rs, gm[kk][e], bt[kk][e]);
-                if (uok[kk]) U::st(y + r * N + (lane + 32 * kk) * E, U::pack(o));
             }
-            if (lane == 0) {
-                if (mean) mean[r] = mu;
-                if (rstd) rstd[r] = rs;
+            butterfly<32, RB>(s);
+#pragma unroll
+            for (int rr = 0; rr < RB; ++rr) {
+                s[rr] = row_mean(s[rr], fN, inv_n);  // the mean
+                q[rr] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < KMAX; ++kk)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        v[rr][kk][e] -= s[rr];
+                        q[rr] = uok[kk] ? fmaf(v[rr][kk][e], v[rr][kk][e], q[rr]) : q[rr];
+                    }
+            }
+            butterfly<32, RB>(q);
+#pragma unroll
+            for (int rr = 0; rr < RB; ++rr) {
+                const int i = i0 + rr;
+                if (i >= rows) break;  // the same for the whole warp
+                const int64_t r = r0 + i;
+                const float rs = rsqrtf(fmaf(q[rr], inv_n, eps));
+#pragma unroll
+                for (int kk = 0; kk < KMAX; ++kk) {
+                    float o[E];
+#pragma unroll
+                    for (int e = 0; e < E; ++e)
+                        o[e] = fmaf(v[rr][kk][e] * rs, gm[kk][e], bt[kk][e]);
+                    if (uok[kk]) U::st(y + r * N + (lane + 32 * kk) * E, U::pack(o));
+                }
+                if (lane == 0) {
+                    if (mean) mean[r] = s[rr];
+                    if (rstd) rstd[r] = rs;
+                }
             }
         }
     });
@@ -536,49 +551,65 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
     rg.nblocks = nblocks;
     rg.slot = kBatchSlot;
     rg.fault = fault;
+    constexpr int RB = batch_rb(KMAX, E);
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
         const unsigned char* xs = rg.tile(k, 0);
         const unsigned char* ds = rg.tile(k, 1);
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        for (int i = warp; i < rows; i += kBatchWarps) {
-            const int64_t r = r0 + i;
-            const float mu = __ldca(mean + r), rs = __ldca(rstd + r);
-            float xh[KMAX][E], g[KMAX][E];
-            float s[2] = {0.f, 0.f};
+        // RB consecutive rows a warp at once; rows past the block read zeros
+        // (and then add exact zeros to the column sums)
+        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
+            float xh[RB][KMAX][E], g[RB][KMAX][E], s[2 * RB], rs[RB];
 #pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk) {
-                const int u = lane + 32 * kk;
-                const int64_t gi = r * N + u * E;
-                const int so = i * rb + u * E * (int)sizeof(TX);
-                typename U::W wx{}, wd{};
-                if (uok[kk]) {
-                    const bool sm = gi < tail;
-                    wx = sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
-                    wd = sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
-                }
-                float xv[E], dv[E];
-                U::unpack(wx, xv);
-                U::unpack(wd, dv);
+            for (int rr = 0; rr < RB; ++rr) {
+                const int i = i0 + rr;
+                const int64_t r = r0 + i;
+                const bool ok = i < rows;
+                const float mu = ok ? __ldca(mean + r) : 0.f;
+                rs[rr] = ok ? __ldca(rstd + r) : 0.f;
+                s[2 * rr] = s[2 * rr + 1] = 0.f;
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    xh[kk][e] = (xv[e] - mu) * rs;
-                    g[kk][e] = dv[e] * gm[kk][e];
-                    s[0] += g[kk][e];
-                    s[1] = fmaf(g[kk][e], xh[kk][e], s[1]);
-                    acc_g[kk][e] = fmaf(dv[e], xh[kk][e], acc_g[kk][e]);
-                    acc_b[kk][e] += dv[e];
+                for (int kk = 0; kk < KMAX; ++kk) {
+                    const int u = lane + 32 * kk;
+                    const int64_t gi = r * N + u * E;
+                    const int so = i * rb + u * E * (int)sizeof(TX);
+                    typename U::W wx{}, wd{};
+                    if (ok && uok[kk]) {
+                        const bool sm = gi < tail;
+                        wx = sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
+                        wd = sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
+                    }
+                    float xv[E], dv[E];
+                    U::unpack(wx, xv);
+                    U::unpack(wd, dv);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        xh[rr][kk][e] = (xv[e] - mu) * rs[rr];
+                        g[rr][kk][e] = dv[e] * gm[kk][e];
+                        s[2 * rr] += g[rr][kk][e];
+                        s[2 * rr + 1] = fmaf(g[rr][kk][e], xh[rr][kk][e], s[2 * rr + 1]);
+                        acc_g[kk][e] = fmaf(dv[e], xh[rr][kk][e], acc_g[kk][e]);
+                        acc_b[kk][e] += dv[e];
+                    }
                 }
             }
-            butterfly<32, 2>(s);
-            const float ma = s[0] * inv_n, mb = s[1] * inv_n;
+            butterfly<32, 2 * RB>(s);
 #pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk) {
-                float o[E];
+            for (int rr = 0; rr < RB; ++rr) {
+                const int i = i0 + rr;
+                if (i >= rows) break;  // the same for the whole warp
+                const int64_t r = r0 + i;
+                const float ma = s[2 * rr] * inv_n, mb = s[2 * rr + 1] * inv_n;
 #pragma unroll
-                for (int e = 0; e < E; ++e) o[e] = rs * fmaf(-xh[kk][e], mb, g[kk][e] - ma);
-                if (uok[kk]) U::st(dx + r * N + (lane + 32 * kk) * E, U::pack(o));
+                for (int kk = 0; kk < KMAX; ++kk) {
+                    float o[E];
+#pragma unroll
+                    for (int e = 0; e < E; ++e)
+                        o[e] = rs[rr] * fmaf(-xh[rr][kk][e], mb, g[rr][kk][e] - ma);
+                    if (uok[kk]) U::st(dx + r * N + (lane + 32 * kk) * E, U::pack(o));
+                }
             }
         }
     });

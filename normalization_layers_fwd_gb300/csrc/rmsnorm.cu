@@ -163,37 +163,50 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
     rg.nblocks = nblocks;
     rg.slot = kBatchSlot;
     rg.fault = fault;
+    constexpr int RB = batch_rb(KMAX, E);
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
         const unsigned char* xs = rg.tile(k, 0);
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        for (int i = warp; i < rows; i += kBatchWarps) {
-            const int64_t r = r0 + i;
-            float v[KMAX][E];
+        // RB consecutive rows a warp at once; rows past the block read zeros
+        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
+            float v[RB][KMAX][E], rs[RB];
 #pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk) {
-                const int u = lane + 32 * kk;
-                const int64_t gi = r * N + u * E;
-                typename U::W wd{};
-                if (uok[kk])
-                    wd = gi < tail ? *reinterpret_cast<const typename U::W*>(xs + i * rb +
-                                                                             u * E * sizeof(TX))
-                                   : U::ld(x + gi);
-                U::unpack(wd, v[kk]);
-            }
-            const float rs = batch_row_rstd<KMAX, E>(v, eps, inv_n);
+            for (int rr = 0; rr < RB; ++rr) {
+                const int i = i0 + rr;
+                const int64_t r = r0 + i;
 #pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk) {
-                float o[E];
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float xh = v[kk][e] * rs;
-                    o[e] = wv[kk][e] * (variant == 0 ? round_x<TX>(xh) : xh);
+                for (int kk = 0; kk < KMAX; ++kk) {
+                    const int u = lane + 32 * kk;
+                    const int64_t gi = r * N + u * E;
+                    typename U::W wd{};
+                    if (i < rows && uok[kk])
+                        wd = gi < tail ? *reinterpret_cast<const typename U::W*>(
+                                             xs + i * rb + u * E * sizeof(TX))
+                                       : U::ld(x + gi);
+                    U::unpack(wd, v[rr][kk]);
                 }
-                if (uok[kk]) U::st(y + r * N + (lane + 32 * kk) * E, U::pack(o));
+                rs[rr] = batch_sumsq<KMAX, E>(v[rr]);
             }
-            if (rstd && lane == 0) rstd[r] = rs;
+            batch_rstd<RB>(rs, eps, inv_n);
+#pragma unroll
+            for (int rr = 0; rr < RB; ++rr) {
+                const int i = i0 + rr;
+                if (i >= rows) break;  // the same for the whole warp
+                const int64_t r = r0 + i;
+#pragma unroll
+                for (int kk = 0; kk < KMAX; ++kk) {
+                    float o[E];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float xh = v[rr][kk][e] * rs[rr];
+                        o[e] = wv[kk][e] * (variant == 0 ? round_x<TX>(xh) : xh);
+                    }
+                    if (uok[kk]) U::st(y + r * N + (lane + 32 * kk) * E, U::pack(o));
+                }
+                if (rstd && lane == 0) rstd[r] = rs[rr];
+            }
         }
     });
 }

@@ -80,20 +80,27 @@ __device__ __forceinline__ float warp_row_rstd(const TX* xr, int N, int lane, fl
     return rsqrtf(fmaf(v[0], inv_n, eps));
 }
 
-// The row-batched kernels' r of one row from the units this lane holds
-// (units past the row's end are zeros): the lane's sum of squares in unit
-// order, then the warp butterfly.  The forward and the backward's
-// recomputation share it, so both give the same bits.
+// The row-batched kernels' r of a row: this lane's sum of squares of its
+// units in unit order (units past the row's end are zeros), then the warp
+// butterfly (one butterfly for several rows adds each value in the same
+// order), then rsqrt.  The forward and the backward's recomputation share
+// these, so both give the same bits.
 template <int KMAX, int E>
-__device__ __forceinline__ float batch_row_rstd(const float (&v)[KMAX][E], float eps, float inv_n)
+__device__ __forceinline__ float batch_sumsq(const float (&v)[KMAX][E])
 {
-    float s[1] = {0.f};
+    float s = 0.f;
 #pragma unroll
     for (int k = 0; k < KMAX; ++k)
 #pragma unroll
-        for (int e = 0; e < E; ++e) s[0] = fmaf(v[k][e], v[k][e], s[0]);
-    butterfly<32, 1>(s);
-    return rsqrtf(fmaf(s[0], inv_n, eps));
+        for (int e = 0; e < E; ++e) s = fmaf(v[k][e], v[k][e], s);
+    return s;
+}
+template <int RB>
+__device__ __forceinline__ void batch_rstd(float (&s)[RB], float eps, float inv_n)
+{
+    butterfly<32, RB>(s);
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr) s[rr] = rsqrtf(fmaf(s[rr], inv_n, eps));
 }
 
 // Launch schedule S of a fast kernel: the weight-first instance (kWF) for

@@ -279,55 +279,72 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
     rg.nblocks = nblocks;
     rg.slot = kBatchSlot;
     rg.fault = fault;
+    constexpr int RB = batch_rb(KMAX, E);
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
         const unsigned char* xs = rg.tile(k, 0);
         const unsigned char* ds = rg.tile(k, 1);
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        for (int i = warp; i < rows; i += kBatchWarps) {
-            const int64_t r = r0 + i;
-            float xv[KMAX][E], dv[KMAX][E];
+        // RB consecutive rows a warp at once; rows past the block read zeros
+        // (and then add exact zeros to the column sums)
+        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
+            float xv[RB][KMAX][E], dv[RB][KMAX][E], rs[RB], s[RB];
 #pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk) {
-                const int u = lane + 32 * kk;
-                const int64_t gi = r * N + u * E;
-                const int so = i * rb + u * E * (int)sizeof(TX);
-                typename U::W wx{}, wd{};
-                if (uok[kk]) {
-                    const bool sm = gi < tail;
-                    wx = sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
-                    wd = sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
+            for (int rr = 0; rr < RB; ++rr) {
+                const int i = i0 + rr;
+                const int64_t r = r0 + i;
+                const bool ok = i < rows;
+#pragma unroll
+                for (int kk = 0; kk < KMAX; ++kk) {
+                    const int u = lane + 32 * kk;
+                    const int64_t gi = r * N + u * E;
+                    const int so = i * rb + u * E * (int)sizeof(TX);
+                    typename U::W wx{}, wd{};
+                    if (ok && uok[kk]) {
+                        const bool sm = gi < tail;
+                        wx = sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
+                        wd = sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
+                    }
+                    U::unpack(wx, xv[rr][kk]);
+                    U::unpack(wd, dv[rr][kk]);
                 }
-                U::unpack(wx, xv[kk]);
-                U::unpack(wd, dv[kk]);
+                rs[rr] = rstd ? (ok ? __ldca(rstd + r) : 0.f) : batch_sumsq<KMAX, E>(xv[rr]);
             }
-            const float rs = rstd ? __ldca(rstd + r) : batch_row_rstd<KMAX, E>(xv, eps, inv_n);
-            float s[1] = {0.f};
+            if (!rstd) batch_rstd<RB>(rs, eps, inv_n);  // uniform branch
 #pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk)
+            for (int rr = 0; rr < RB; ++rr) {
+                s[rr] = 0.f;
 #pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    float dn = dv[kk][e] * wv[kk][e];
-                    if (cast_first) dn = round_x<TX>(dn);
-                    s[0] = fmaf(dn, xv[kk][e] * rs, s[0]);
+                for (int kk = 0; kk < KMAX; ++kk)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        float dn = dv[rr][kk][e] * wv[kk][e];
+                        if (cast_first) dn = round_x<TX>(dn);
+                        s[rr] = fmaf(dn, xv[rr][kk][e] * rs[rr], s[rr]);
+                    }
+            }
+            butterfly<32, RB>(s);
+#pragma unroll
+            for (int rr = 0; rr < RB; ++rr) {
+                const int i = i0 + rr;
+                const int64_t r = r0 + i;
+                const float m = s[rr] * inv_n;
+#pragma unroll
+                for (int kk = 0; kk < KMAX; ++kk) {
+                    float o[E];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float xh = xv[rr][kk][e] * rs[rr];
+                        float dn = dv[rr][kk][e] * wv[kk][e];
+                        if (cast_first) dn = round_x<TX>(dn);
+                        o[e] = rs[rr] * (dn - xh * m);
+                        float term = dv[rr][kk][e] * (cast_first ? round_x<TX>(xh) : xh);
+                        if (round_terms) term = round_x<TX>(term);
+                        acc[kk][e] += term;
+                    }
+                    if (i < rows && uok[kk]) U::st(dx + r * N + (lane + 32 * kk) * E, U::pack(o));
                 }
-            butterfly<32, 1>(s);
-            const float m = s[0] * inv_n;
-#pragma unroll
-            for (int kk = 0; kk < KMAX; ++kk) {
-                float o[E];
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float xh = xv[kk][e] * rs;
-                    float dn = dv[kk][e] * wv[kk][e];
-                    if (cast_first) dn = round_x<TX>(dn);
-                    o[e] = rs * (dn - xh * m);
-                    float term = dv[kk][e] * (cast_first ? round_x<TX>(xh) : xh);
-                    if (round_terms) term = round_x<TX>(term);
-                    acc[kk][e] += term;
-                }
-                if (uok[kk]) U::st(dx + r * N + (lane + 32 * kk) * E, U::pack(o));
             }
         }
     });

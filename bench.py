@@ -78,8 +78,10 @@ def source_hash():
 
 
 def recorded_traffic(kernel_key):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources."""
+    """DRAM bytes (read + write) of one launch of `kernel_key` (as
+    "layernorm_bwd[32768x8192]") from the committed ncu capture of that
+    single point at full size, if it was taken on the current kernel
+    sources; else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(p) as f:
@@ -88,7 +90,8 @@ def recorded_traffic(kernel_key):
         return None
     if rec.get("source_hash") != source_hash():
         return None
-    return rec.get("launches", {}).get(kernel_key)
+    k = rec.get("launches", {}).get(kernel_key)
+    return None if k is None else int(k["dram_read"] + k["dram_write"])
 
 
 class ClockSampler:
@@ -280,16 +283,24 @@ class Point:
         return f"{self.wl.op}_{d}[{self.wl.M}x{self.wl.N}]"
 
 
-def workloads(name, ops=None, widths=None):
+def workloads(name, ops=None, widths=None, elems=None):
+    """The points of workload `name`; `elems` (sweep and head-major only)
+    shrinks every point to about that many elements, for profiling."""
     from normalization_layers_fwd_gb300 import synth
     if name in ("sweep", "sweep_f16"):
         xd = torch.bfloat16 if name == "sweep" else torch.float16
         pts = [w for w in synth.sweep_all(xd)
                if (not ops or w.op in ops) and (not widths or w.N in widths)]
-        return pts, (f"{name}: DyT, LayerNorm, RMSNorm fwd+bwd, {str(xd)[6:]} x, fp32 params, "
-                     "N in {16..8192}, M = 2^28 // N")
+        desc = (f"{name}: DyT, LayerNorm, RMSNorm fwd+bwd, {str(xd)[6:]} x, fp32 params, "
+                "N in {16..8192}, M = 2^28 // N")
+        if elems:
+            pts = [synth.scaled(w, max(1, elems // w.N)) for w in pts]
+            desc += f" (scaled: M = {elems} // N)"
+        return pts, desc
     if name == "headmajor":
         B, H, S, D = HEAD_MAJOR
+        if elems:
+            B = max(1, elems // (H * S * D))
         pts = [synth.head_major(op, B, H, S, D) for op in ("dyt", "layernorm", "rmsnorm")
                if not ops or op in ops]
         return pts, (f"headmajor: DyT, LayerNorm, RMSNorm fwd+bwd per head over head-major bf16 "
@@ -412,7 +423,7 @@ def run_ours(args, rank, world, dev):
     from normalization_layers_fwd_gb300 import _lib, build
     build.build()
     lib = _lib.load()
-    wls, wdesc = workloads(args.workload, args.ops, args.widths)
+    wls, wdesc = workloads(args.workload, args.ops, args.widths, args.elems)
     if args.ops or args.widths:
         wdesc += f" (subset: ops={args.ops}, widths={args.widths})"
     if args.rms_variant:
@@ -507,7 +518,8 @@ def run_ours(args, rank, world, dev):
         graph_ms = graph_step_ms(points, dev, flush, max(args.steps, 10))
     peak, peak_kind = measured_peak()
     fixed = None
-    if args.workload == "sweep" and not (args.no_workloads or args.ops or args.widths):
+    if args.workload == "sweep" and not (args.no_workloads or args.ops or args.widths or
+                                         args.elems):
         fixed = fixed_workloads(lib, dev, max(args.steps, 20), peak)
     clocks = sampler.stop()
     if world > 1:
@@ -786,6 +798,9 @@ def main():
                     help="restrict the sweep to these layers (profiling runs)")
     ap.add_argument("--widths", type=lambda v: [int(x) for x in v.split(",")], default=None,
                     help="restrict the sweep to these widths (profiling runs)")
+    ap.add_argument("--elems", type=int, default=None,
+                    help="shrink every sweep or head-major point to about this many elements "
+                         "(profiling captures; not a bench line)")
     ap.add_argument("--rms-variant", type=int, choices=[0, 1, 2], default=0,
                     help="RMSNorm expression: 0 Llama (default), 1 weight first, 2 Gemma")
     args = ap.parse_args()

@@ -419,6 +419,41 @@ def fixed_workloads(lib, dev, steps, peak):
     return out
 
 
+# Widths outside the sweep, each a path of its own: rows that are not
+# 16-byte multiples (bf16 N = 130 and 250, the row-batched kernels), and the
+# widest rows (bf16 N = 16384, fp32 N = 8192, the 2048-vector schedule).
+EXTRA_WIDTHS = ((130, torch.bfloat16), (250, torch.bfloat16), (16384, torch.bfloat16),
+                (8192, torch.float32))
+
+
+def extra_widths(lib, dev, peak):
+    """Per-kernel device time and fraction of the measured copy peak at the
+    extra widths, each point 2^28 elements built by the sweep's recipe and
+    timed alone like the sweep's breakdown (not part of the headline)."""
+    from normalization_layers_fwd_gb300 import synth
+    out = []
+    for N, xd in EXTRA_WIDTHS:
+        for op in ("dyt", "layernorm", "rmsnorm"):
+            wl = synth.sweep(op, N, xd)
+            E = wl.M * wl.N
+            shared = {"y": torch.empty(E, dtype=xd, device=dev),
+                      "dx": torch.empty(E, dtype=xd, device=dev),
+                      "mean": torch.empty(wl.M, dtype=torch.float32, device=dev),
+                      "rstd": torch.empty(wl.M, dtype=torch.float32, device=dev)}
+            p = Point(lib, wl, dev, shared)
+            for _ in range(3):
+                p.run()
+            torch.cuda.synchronize(dev)
+            for (_, d), ms in sorted(time_launches([p], dev).items(), key=lambda kv: kv[0][1]):
+                b = p.bytes[d]
+                out.append({"kernel": p.key(d), "x_dtype": str(xd)[6:], "ms": round(ms, 4),
+                            "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                            "frac_measured": round(b / (ms * 1e-3) / 1e9 / peak, 3)})
+            del p, shared
+            torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world, dev):
     from normalization_layers_fwd_gb300 import _lib, build
     build.build()
@@ -541,6 +576,10 @@ def run_ours(args, rank, world, dev):
                           "frac_measured": round(b / (ms * 1e-3) / 1e9 / peak, 3)})
 
     e2e = None if args.no_e2e else run_e2e(points, dev, min(args.steps, 3), world)
+    extra = None
+    if args.workload == "sweep" and not (args.no_workloads or args.ops or args.widths or
+                                         args.elems):
+        extra = extra_widths(lib, dev, peak)
     line = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -567,6 +606,7 @@ def run_ours(args, rank, world, dev):
         "clocks": clocks,
         "workloads": fixed,
         "breakdown": breakdown,
+        "extra_widths": extra,
     }
     return line
 

@@ -88,3 +88,14 @@ def test_cpu_baseline_times_all_cores_and_one():
     assert cb["kind"] == "oracle" and cb["cores"] == 2 and cb["value"] > 0
     assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
     assert cb["nproc"] >= 1 and cb["usable_cores"] >= 1 and cb["cpu_model"]
+
+
+def test_extra_widths_are_off_the_sweep_paths():
+    """The extra breakdown points sit outside the sweep's widths: rows that
+    are not 16-byte multiples, and rows wider than 1024 vectors."""
+    for N, xd in bench.EXTRA_WIDTHS:
+        assert N not in synth.SWEEP_WIDTHS or xd != synth.sweep("dyt", N).xdtype
+        row_bytes = N * xd.itemsize
+        assert row_bytes % 16 != 0 or row_bytes // 16 > 1024
+        w = synth.sweep("layernorm", N, xd)
+        assert w.M == (1 << 28) // N and w.xdtype == xd

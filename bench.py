@@ -287,10 +287,13 @@ def workloads(name, ops=None, widths=None, elems=None):
     """The points of workload `name`; `elems` (sweep and head-major only)
     shrinks every point to about that many elements, for profiling."""
     from normalization_layers_fwd_gb300 import synth
-    if name in ("sweep", "sweep_f16"):
-        xd = torch.bfloat16 if name == "sweep" else torch.float16
-        pts = [w for w in synth.sweep_all(xd)
-               if (not ops or w.op in ops) and (not widths or w.N in widths)]
+    if name in ("sweep", "sweep_f16", "sweep_f32"):
+        xd = {"sweep": torch.bfloat16, "sweep_f16": torch.float16,
+              "sweep_f32": torch.float32}[name]
+        # the sweep's widths, or any widths by the same recipe
+        ns = widths or synth.SWEEP_WIDTHS
+        pts = [synth.sweep(op, n, xd) for n in ns for op in ("dyt", "layernorm", "rmsnorm")
+               if not ops or op in ops]
         desc = (f"{name}: DyT, LayerNorm, RMSNorm fwd+bwd, {str(xd)[6:]} x, fp32 params, "
                 "N in {16..8192}, M = 2^28 // N")
         if elems:
@@ -339,8 +342,17 @@ def time_launches(points, dev, reps=3):
     return {k: sum(v) / len(v) for k, v in out.items()}
 
 
-def flush_l2(buf):
+def flush_l2(buf, clean=True):
+    """Evict the step's data from L2: write a buffer four times its size,
+    then (clean) read it back, so that the lines the write left dirty are
+    written back to DRAM before the step rather than during it."""
     buf.add_(1)
+    if clean:
+        buf.amax()
+
+
+L2_FLUSH_NOTE = ("flushed before every step: 512 MiB written, then read back (the write's "
+                 "dirty lines drained first)")
 
 
 def graph_step_ms(points, dev, flush, reps):
@@ -376,8 +388,10 @@ def fixed_workloads(lib, dev, steps, peak):
     backward alone at 401408x24, DyT bf16 1048576x128, RMSNorm bf16
     16384x2048), each step its C-ABI calls (forward, backward, second
     stage; the backward and second stage alone for the LayerNorm one),
-    timed alone with CUDA events on the launch stream after a 512 MiB write
-    that flushes L2, and replayed from a CUDA graph behind the same flush."""
+    timed alone with CUDA events on the launch stream after an L2 flush
+    (flush_l2), and replayed from a CUDA graph behind the same flush.  Each
+    is also timed after the flush's write alone, which leaves L2 full of
+    dirty lines that the step then writes back (ms_event_median_dirty_l2)."""
     from normalization_layers_fwd_gb300 import synth
     flush = torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -393,15 +407,16 @@ def fixed_workloads(lib, dev, steps, peak):
             flush_l2(flush)
             p.run()
         torch.cuda.synchronize(dev)
-        times = []
+        times, dirty = [], []
         for _ in range(steps):
-            flush_l2(flush)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            p.run()
-            b.record(stream)
-            torch.cuda.synchronize(dev)
-            times.append(a.elapsed_time(b))
+            for clean, t in ((True, times), (False, dirty)):
+                flush_l2(flush, clean)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                p.run()
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+                t.append(a.elapsed_time(b))
         g = graph_step_ms([p], dev, flush, steps)
         B = p.step_bytes()
         med = statistics.median(times)
@@ -413,7 +428,10 @@ def fixed_workloads(lib, dev, steps, peak):
                     "frac_measured": round(gbs / peak, 4),
                     "pct_of_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
                     "rows_per_s": round(wl.M / (med * 1e-3), 1), "steps": steps,
-                    "l2": "flushed (512 MiB write) before every step"})
+                    "l2": L2_FLUSH_NOTE,
+                    "ms_event_median_dirty_l2": round(statistics.median(dirty), 5),
+                    "dirty_l2": "the same step after the write alone: L2 left holding about "
+                                "126 MB of the flush's dirty lines, written back during the step"})
         del p, shared
         torch.cuda.empty_cache()
     return out
@@ -588,7 +606,7 @@ def run_ours(args, rank, world, dev):
         "data": "synthetic (seeded, generated on the GPU)",
         "config": {"workload": wdesc, "points": len(points), "rows_per_step": rows,
                    "x_dtype": str(dtype)[6:], "param_dtype": str(wls[0].pdtype)[6:],
-                   "l2": "inputs larger than L2" if big else "L2 flushed (512 MiB write) before every step",
+                   "l2": "inputs larger than L2" if big else "L2 " + L2_FLUSH_NOTE,
                    "parallelism": f"replicas x{world}"},
         "pct_of_8tbs": round(100 * gbs / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_copy": round(100 * gbs / world / peak, 2),
@@ -837,7 +855,8 @@ def main():
     ap.add_argument("--ops", type=lambda v: v.split(","), default=None,
                     help="restrict the sweep to these layers (profiling runs)")
     ap.add_argument("--widths", type=lambda v: [int(x) for x in v.split(",")], default=None,
-                    help="restrict the sweep to these widths (profiling runs)")
+                    help="the sweep's points at these widths only, or at widths "
+                         "outside it by the same recipe (profiling runs)")
     ap.add_argument("--elems", type=int, default=None,
                     help="shrink every sweep or head-major point to about this many elements "
                          "(profiling captures; not a bench line)")

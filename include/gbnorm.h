@@ -23,8 +23,8 @@
  *   dtype `pt`/`wt`; saved statistics (mean, rstd) are float32 [M].
  *   Every pointer must be aligned to its element size (else GBN_EINVAL).
  *   Beyond that any alignment is accepted: 16-byte aligned activations with
- *   N*sizeof a multiple of 16 take the vector path, up to N = 8192 (16-bit
- *   activations; 16384 in the DyT and LayerNorm forwards) or 8192 (float32);
+ *   N*sizeof a multiple of 16 take the vector path, up to N = 16384 (16-bit
+ *   activations) or 8192 (float32);
  *   other contiguous rows up to N = 256 (even N) or 128 (odd N) whose inputs
  *   start on a 16-byte boundary take the row-batched path; the rest the
  *   general path.
@@ -255,8 +255,10 @@ int rmsnorm_bwd_rows(const void* x, const gbn_rows* xl, const void* dy, const gb
  *   GBN_STATIC_WS_BYTES returns GBN_ESCRATCH before launching anything.  The
  *   need is (rows of partials) x N x 4 bytes, which grows with the device's
  *   SM count S: on the vector path (16-byte aligned activations, N a multiple
- *   of 8 for 16-bit or 4 for f32 activations, N <= 8192) at most
- *   32 KiB x S, within the array for S <= 256; on the general path, with
+ *   of 8 for 16-bit or 4 for f32 activations) at most 32 KiB x S for
+ *   N <= 8192, within the array for S <= 256, and 4 x N x S bytes for 16-bit
+ *   N up to 16384 (one partial row per SM), within the array while
+ *   N x S <= 2^21; on the general path, with
  *   S' = S rounded up to an even number, at most 8 MiB while N <= 2^19 / S'
  *   (the number of warps adapts) and 16 x S' x N bytes beyond (for M of at
  *   least 4 S' rows).  gbn_bwd_workspace_bytes(GBN_OP_RMSNORM, ...), an upper

@@ -157,28 +157,28 @@ int64_t general_ws_floats(int kind, int64_t N)
 // most its capacity (max_nvec / 2 < nvec <= max_nvec), the first in table
 // order that the set holds; other rows take the one-vector schedules.
 constexpr unsigned kWide12 = 1u, kWide13 = 2u, kWide14 = 4u, kWide15 = 8u, kWide16 = 16u,
-                   kWide17 = 32u;
+                   kWide17 = 32u, kWide18 = 64u, kWide19 = 128u, kWide20 = 256u,
+                   kWide21 = 512u, kWide22 = 1024u, kWide23 = 2048u;
 
 // Each kernel's set: the DyT forward 12-13 and backward 12; the LayerNorm
-// forward 12, 13 and 16 and backward 12, 14 and 15; the RMSNorm forward and
-// backward 12 and 14 (one set, so the backward's recomputed rstd reduces a
-// row in the forward's order).  The 16-bit backwards hold at most 2 vectors
-// per thread.  Schedule 15 measured slower than one vector per thread in the
-// forwards and in the RMSNorm backward, 16 faster in the LayerNorm forward.
-// Rows of 1025-2048 vectors take schedule 17: in the DyT and LayerNorm
-// forwards for every dtype, and in every kernel for float32 activations
-// (the RMSNorm pair and the backwards fit its registers only there).
-unsigned wide_set(int kind, int xt)
+// forward 4 vectors per lane at every capacity from 32 vectors (22, 20, 16,
+// 18, 21, 13) and the backward 2 (15, 23, 19, 12, 14); the RMSNorm forward
+// and backward 2 as well (one set, so the backward's recomputed rstd
+// reduces a row in the forward's order).  The 16-bit backwards hold at most
+// 2 vectors per thread.
+// Rows of 1025-2048 vectors take schedule 17 in every kernel; the 16-bit
+// backwards in their lean form (common.cuh, lean_bwd).
+unsigned wide_set(int kind, int)
 {
-    const unsigned w17 = (xt == gbn::kF32 || kind == gbn::kFwdDyT || kind == gbn::kFwdLN)
-                             ? kWide17
-                             : 0u;
+    const unsigned w17 = kWide17;
     switch (kind) {
         case gbn::kFwdDyT: return kWide12 | kWide13 | w17;
         case gbn::kBwdDyT: return kWide12 | w17;
-        case gbn::kFwdLN: return kWide12 | kWide13 | kWide16 | w17;
-        case gbn::kBwdLN: return kWide12 | kWide14 | kWide15 | w17;
-        default: return kWide12 | kWide14 | w17;  // RMSNorm forward and backward
+        case gbn::kFwdLN:
+            return kWide22 | kWide20 | kWide16 | kWide18 | kWide21 | kWide13 | w17;
+        case gbn::kBwdLN: return kWide15 | kWide23 | kWide19 | kWide12 | kWide14 | w17;
+        default:  // RMSNorm forward and backward
+            return kWide15 | kWide23 | kWide19 | kWide12 | kWide14 | w17;
     }
 }
 

@@ -59,9 +59,19 @@ struct SchedEntry {
 // spread a row over 2-4 warps and a __syncthreads per reduction.  They pay
 // where a kernel reduces more than once per row (the LayerNorm backward
 // takes 15, the LayerNorm forward 16).
+// Schedules 18-23 complete two families for the LayerNorm kernels, which
+// reduce twice per row: 4 vectors per lane for the forward (W = capacity / 4:
+// 22, 20, 16, 18, 21, 13 for rows of up to 32 ... 1024 vectors) and 2 for
+// the backward (W = capacity / 2: 15, 23, 19, 12, 14), so each row's
+// reductions span a quarter or half as many lanes and warps as one vector
+// per lane would.  Measured on GB300 (fraction of measured copy, bf16,
+// against the one-vector schedule or schedule 12): forward N = 256 0.947 ->
+// 0.974, 512 0.850 -> 0.970, 2048 0.860 -> 0.932, 4096 0.904 -> 0.937,
+// float32 N = 2048 0.908 -> 1.002; backward N = 1024 0.893 -> 0.913, 2048
+// 0.879 -> 0.906.
 // Which kernel takes which is decided per kernel by the planner (api.cu),
 // within each kernel's register budget.
-constexpr int kNumSched = 18;
+constexpr int kNumSched = 24;
 constexpr int kNumSched1 = 12;  // the one-vector schedules
 constexpr SchedEntry kSched[kNumSched] = {
     {1, 1, 256, 1},     {2, 2, 256, 1},     {3, 3, 256, 1},     {4, 4, 256, 1},
@@ -69,6 +79,8 @@ constexpr SchedEntry kSched[kNumSched] = {
     {128, 128, 256, 1}, {256, 256, 256, 1}, {512, 512, 512, 1}, {1024, 1024, 1024, 1},
     {512, 256, 256, 2}, {1024, 256, 256, 4}, {1024, 512, 512, 2},
     {64, 32, 256, 2},   {128, 32, 256, 4},  {2048, 512, 512, 4},
+    {256, 64, 256, 4},  {256, 128, 256, 2}, {64, 16, 256, 4},   {512, 128, 256, 4},
+    {32, 8, 256, 4},    {128, 64, 256, 2},
 };
 
 // Row groups of a power-of-two width tile the CTA; a width that is not a
@@ -145,12 +157,24 @@ constexpr int kind_minb(int S, int kind)
            : kind == kFwdDyT    ? 3
                                 : 4;
 }
+// The lean backward form: 16-bit rows of 1025-2048 vectors (schedule 17, 4
+// vectors a thread), whose row and parameters do not fit the registers next
+// to the column accumulators.  Those kernels keep only the accumulators in
+// registers, read the row from the ring slot again after the row reduction,
+// and read the parameters from L1 at each use.
+template <typename TX>
+constexpr bool lean_bwd(int S)
+{
+    return sizeof(TX) == 2 && S == 17;
+}
+
 // Ring depth.  Every SM keeps (CTAs x stages) row blocks of loads in
 // flight.  The one-vector forward kernels at 256 threads (4 or 3 CTAs per
 // SM) stream best with 2 stages: at 4 the whole GPU holds about 20 MB of
 // outstanding bulk copies and the forward sweep loses 5-15%.  The wide-row
-// forwards of schedules 12-13 (two CTAs of one row each) want 4, except the
-// LayerNorm forward at 4 vectors per thread (2).  The backward kernels,
+// RMSNorm forward wants 4; at 256 threads, the LayerNorm forward at 4
+// vectors per thread and the DyT forward at 2 or 4 want 2 (DyT N = 4096
+// 0.909 -> 0.920 of measured copy).  The backward kernels,
 // which spend longer per block, want 3 (RMSNorm) or 4; the RMSNorm backward
 // at 512 threads (one CTA per SM) 4 (N = 8192: 0.91 -> 0.95 of measured
 // copy, where 4 stages cost the 256-thread schedules 1-4%).  Backward slots
@@ -158,8 +182,10 @@ constexpr int kind_minb(int S, int kind)
 constexpr int kind_stages(int S, int kind)
 {
     return !is_bwd(kind) ? (kSched[S].KV == 1 ? (kSched[S].T == 256 ? 2 : 4)
-                            : kSched[S].KV == 4 && kind == kFwdLN ? 2
-                                                                    : 4)
+                            : kSched[S].T == 256 && (kind == kFwdDyT ||
+                                                      (kind == kFwdLN && kSched[S].KV == 4))
+                                ? 2
+                                : 4)
            : kSched[S].KV == 4                      ? 3
            : kind == kBwdRms                        ? (kSched[S].T == 512 ? 4 : 3)
            : kind == kBwdDyT && kSched[S].T == 1024 ? 3
@@ -176,6 +202,27 @@ constexpr int slot_bytes(int S, int kind)
 constexpr int ring_smem_bytes(int S, int kind, int NT)
 {
     return 128 + kind_stages(S, kind) * NT * slot_bytes(S, kind);
+}
+
+// A backward kernel's ring depth and dynamic shared memory.  The lean form
+// runs a 2-stage ring and keeps the row's parameters, as float32, in shared
+// memory past the ring (kLeanParams floats, loaded once per CTA): read from
+// L1 at each use they cost a scattered load per element pair.
+constexpr int kLeanParams = 2048 * 8;  // the widest lean row, 2048 16-bit vectors
+template <typename TX>
+constexpr int bwd_stages(int S, int kind)
+{
+    return lean_bwd<TX>(S) ? 2 : kind_stages(S, kind);
+}
+template <typename TX>
+constexpr int bwd_ring_bytes(int S, int kind)
+{
+    return 128 + bwd_stages<TX>(S, kind) * 2 * slot_bytes(S, kind);
+}
+template <typename TX>
+constexpr int bwd_smem_bytes(int S, int kind)
+{
+    return bwd_ring_bytes<TX>(S, kind) + (lean_bwd<TX>(S) ? kLeanParams * 4 : 0);
 }
 
 // Threads per CTA and warps per CTA of the general (any width, any
@@ -215,6 +262,8 @@ constexpr int batch_max_units(int) { return 4; }
 // backwards).  A ring block holds a multiple of 8 * RB rows where the slot
 // allows.
 constexpr int batch_rb(int KMAX, int E) { return KMAX * E <= 2 ? 4 : KMAX * E <= 6 ? 2 : 1; }
+static_assert(8 % batch_rb(1, 1) == 0 && 8 % batch_rb(3, 2) == 0 && 8 % batch_rb(4, 2) == 0,
+              "a block of R rows, R a multiple of 8, holds whole groups of RB rows");
 constexpr int kBatchSlot = 8192;   // bytes per staged tensor per ring slot
 constexpr int kBatchStages = 4;
 // CTAs per SM: 4 for a forward (one staged tensor), 3 for a backward.
@@ -223,12 +272,19 @@ constexpr int batch_smem(int NT) { return 128 + kBatchStages * NT * kBatchSlot; 
 
 // One unit of E consecutive elements (E = 2: a pair, E = 1: one element),
 // moved as one word: loaded through L1 (ld.global.ca, coherent with the
-// previous kernel's writes once griddepcontrol.wait has returned) and
-// stored with the streaming hint.
+// previous kernel's writes once griddepcontrol.wait has returned) or from
+// the ring slot by shared-memory address (lds), and stored with the
+// streaming hint.
 template <typename TX, int E> struct Unit;
 template <> struct Unit<float, 1> {
     using W = float;
     static __device__ __forceinline__ W ld(const float* p) { return __ldca(p); }
+    static __device__ __forceinline__ W lds(uint32_t a)
+    {
+        float v;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+        return v;
+    }
     static __device__ __forceinline__ void st(float* p, W w) { __stcs(p, w); }
     static __device__ __forceinline__ void unpack(W w, float (&v)[1]) { v[0] = w; }
     static __device__ __forceinline__ W pack(const float (&v)[1]) { return v[0]; }
@@ -238,6 +294,12 @@ template <> struct Unit<float, 2> {
     static __device__ __forceinline__ W ld(const float* p)
     {
         return __ldca(reinterpret_cast<const float2*>(p));
+    }
+    static __device__ __forceinline__ W lds(uint32_t a)
+    {
+        float2 v;
+        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+        return v;
     }
     static __device__ __forceinline__ void st(float* p, W w)
     {
@@ -275,6 +337,12 @@ template <typename TX> struct Unit16x1 {
     {
         return __ldca(reinterpret_cast<const unsigned short*>(p));
     }
+    static __device__ __forceinline__ W lds(uint32_t a)
+    {
+        unsigned short v;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+        return v;
+    }
     static __device__ __forceinline__ void st(TX* p, W w)
     {
         __stcs(reinterpret_cast<unsigned short*>(p), w);
@@ -294,6 +362,12 @@ template <typename TX> struct Unit16x2 {
     {
         return __ldca(reinterpret_cast<const unsigned int*>(p));
     }
+    static __device__ __forceinline__ W lds(uint32_t a)
+    {
+        unsigned v;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+        return v;
+    }
     static __device__ __forceinline__ void st(TX* p, W w)
     {
         __stcs(reinterpret_cast<unsigned int*>(p), w);
@@ -305,7 +379,14 @@ template <typename TX> struct Unit16x2 {
     }
     static __device__ __forceinline__ W pack(const float (&v)[2])
     {
-        return (unsigned)Unit16<TX>::from_f(v[0]) | ((unsigned)Unit16<TX>::from_f(v[1]) << 16);
+        // one two-lane conversion, round to nearest even (element 0 low)
+        if constexpr (std::is_same<TX, __half>::value) {
+            const __half2 h = __floats2half2_rn(v[0], v[1]);
+            return *reinterpret_cast<const unsigned*>(&h);
+        } else {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[0], v[1]);
+            return *reinterpret_cast<const unsigned*>(&h);
+        }
     }
 };
 template <> struct Unit<__nv_bfloat16, 1> : Unit16x1<__nv_bfloat16> {};
@@ -425,6 +506,14 @@ __device__ __forceinline__ float ld_param(const void* p, int pt, int64_t j)
     if (pt == kF32) return static_cast<const float*>(p)[j];
     if (pt == kBF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[j]);
     return __half2float(static_cast<const __half*>(p)[j]);
+}
+
+// Parameter vector p (N columns of dtype pt) into prm as float32, by all T
+// threads of the CTA; the caller's next __syncthreads publishes it.
+template <int T>
+__device__ __forceinline__ void stage_params(float* prm, const void* p, int pt, int N)
+{
+    for (int c = threadIdx.x; c < N; c += T) prm[c] = ld_param(p, pt, c);
 }
 
 __device__ __forceinline__ void st_param(void* p, int pt, int64_t j, float v)
@@ -929,6 +1018,14 @@ __device__ __forceinline__ f2 round2(f2 a)
 __device__ __forceinline__ f2 ld_param2(const void* p, int pt, int64_t c)
 {
     return mk2(ld_param(p, pt, c), ld_param(p, pt, c + 1));
+}
+// The staged parameters of columns c, c + 1 (a plain load, which the
+// compiler schedules with the arithmetic: measured 2x faster in the lean DyT
+// backward than a volatile one issued in program order)
+__device__ __forceinline__ f2 prm2(const float* prm, int c)
+{
+    const float2 v = *reinterpret_cast<const float2*>(prm + c);
+    return mk2(v.x, v.y);
 }
 
 // ---------------------------------------------------------------- reductions

@@ -201,7 +201,11 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     constexpr int W = kSched[S].W, U = kind_U(S, kBwdDyT), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
-    static_assert(KV <= 2 || sizeof(TX) == 4,
+    // The lean form (16-bit rows of 1025-2048 vectors) reads gamma from shared
+    // memory at each use and sums gamma * dy * x * sech^2 per thread instead
+    // of per column, so that only two column accumulators stay in registers.
+    constexpr bool kLean = lean_bwd<TX>(S);
+    static_assert(KV <= 2 || sizeof(TX) == 4 || kLean,
                   "the 16-bit DyT backward takes at most 2 vectors per thread");
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[T / 32];
@@ -222,13 +226,25 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     // Per-column accumulators: sum dy*t, sum dy, sum dy*x*sech^2 (gamma is
     // applied to the last one once, at the end).
     f2 acc_g[KV][P], acc_b[KV][P], acc_a[KV][P];
+    f2 da2 = splat2(0.f);  // the lean form's sum of gamma * dy * x * sech^2
+    // the lean form's gamma, as float32 past the ring
+    const float* prm = reinterpret_cast<const float*>(dsm + bwd_ring_bytes<TX>(S, kBwdDyT));
+    if constexpr (kLean) stage_params<T>(const_cast<float*>(prm), gamma, pt, N);
+    auto gm_at = [&](int j, int p) -> f2 {
+        const int c = (l + j * W) * VEC + 2 * p;
+        if constexpr (kLean)
+            return colok[j] ? prm2(prm, c) : splat2(0.f);
+        else
+            return colok[j] ? ld_param2(gamma, pt, c) : splat2(0.f);
+    };
 #pragma unroll
     for (int j = 0; j < KV; ++j) {
 #pragma unroll
         for (int p = 0; p < P; ++p) {
-            gm[j][p] = colok[j] ? ld_param2(gamma, pt, (l + j * W) * VEC + 2 * p) : splat2(0.f);
+            if constexpr (!kLean) gm[j][p] = gm_at(j, p);
             if constexpr (KV == 1) ga[p] = mul2(gm[0][p], a2);
-            acc_g[j][p] = acc_b[j][p] = acc_a[j][p] = splat2(0.f);
+            acc_g[j][p] = acc_b[j][p] = splat2(0.f);
+            if constexpr (!kLean) acc_a[j][p] = splat2(0.f);
         }
     }
 
@@ -250,6 +266,22 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
                     f2 t, s;
                     dyt_tanh_sech2_2(mul2(a2, xv[p]), t, s);
                     const f2 dsd = mul2(dv[p], s);
+                    if constexpr (kLean) {
+                        const f2 gmv = gm_at(j, p);
+                        o[p] = mul2(dsd, mul2(gmv, a2));
+                        // lanes past the row's end and padded rows add nothing
+                        // (their x may be anything)
+                        da2 = sel2(ok, fma2(gmv, mul2(dsd, xv[p]), da2), da2);
+                        if constexpr (kMask) {
+                            const f2 z = splat2(0.f);
+                            acc_g[j][p] = add2(acc_g[j][p], sel2(okr, mul2(dv[p], t), z));
+                            acc_b[j][p] = add2(acc_b[j][p], sel2(okr, dv[p], z));
+                        } else {
+                            acc_g[j][p] = fma2(dv[p], t, acc_g[j][p]);
+                            acc_b[j][p] = add2(acc_b[j][p], dv[p]);
+                        }
+                        continue;
+                    }
                     if constexpr (KV == 1)
                         o[p] = mul2(dsd, ga[p]);
                     else
@@ -271,7 +303,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
         }
     };
 
-    Ring<2, kind_stages(S, kBwdDyT), kIn == kInRows> rg;
+    Ring<2, bwd_stages<TX>(S, kBwdDyT), kIn == kInRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     if constexpr (kIn == kInRows) {
@@ -308,13 +340,17 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     // lanes past the row's end hold garbage (tanh(alpha*0) for alpha = inf);
     // they are never stored above and are excluded here
     float da = 0.f;
+    if constexpr (kLean) {
+        da = lo2(da2) + hi2(da2);
+    } else {
 #pragma unroll
-    for (int j = 0; j < KV; ++j) {
-        if (colok[j]) {
+        for (int j = 0; j < KV; ++j) {
+            if (colok[j]) {
 #pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const f2 q = mul2(gm[j][p], acc_a[j][p]);
-                da += lo2(q) + hi2(q);
+                for (int p = 0; p < P; ++p) {
+                    const f2 q = mul2(gm[j][p], acc_a[j][p]);
+                    da += lo2(q) + hi2(q);
+                }
             }
         }
     }
@@ -638,7 +674,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     switch (L.sid) {
 #define GBN_CASE_BODY(S)                                                                           \
     {                                                                                              \
-        constexpr int smem = ring_smem_bytes(S, kBwdDyT, 2);                                       \
+        constexpr int smem = bwd_smem_bytes<TX>(S, kBwdDyT);                                       \
         with_mode(L.in_mode, [&](auto m_) {                                                        \
             constexpr int kIn_ = decltype(m_)::value;                                              \
             ring_attributes<dyt_bwd_fast<TX, S, kIn_>>(smem);                                      \
@@ -653,14 +689,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(11)
         GBN_CASE(12)
-        // schedule 17 only for float32 activations (the planner's choice)
-        case 17:
-            if constexpr (sizeof(TX) == 4) {
-                GBN_CASE_BODY(17)
-            } else {
-                return cudaErrorInvalidValue;
-            }
-            break;
+        GBN_CASE(17)
 #undef GBN_CASE
 #undef GBN_CASE_BODY
         default: return cudaErrorInvalidValue;

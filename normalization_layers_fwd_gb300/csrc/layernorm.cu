@@ -174,7 +174,11 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     // xhat and g of every vector stay in registers across the row reduction;
     // with the column accumulators that caps the 16-bit kernel at 2 vectors
     // per thread (4 spill); float32 vectors hold half the elements, and 4 fit.
-    static_assert(KV <= 2 || sizeof(TX) == 4,
+    // The lean form (16-bit rows of 1025-2048 vectors) holds only the column
+    // accumulators: it reads the row from the ring slot again after the
+    // reduction, and gamma from shared memory at each use.
+    constexpr bool kLean = lean_bwd<TX>(S);
+    static_assert(KV <= 2 || sizeof(TX) == 4 || kLean,
                   "the 16-bit LayerNorm backward takes at most 2 vectors per thread");
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, 2 * U>::kFloats];
@@ -192,11 +196,23 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     for (int j = 0; j < KV; ++j) {
 #pragma unroll
         for (int p = 0; p < P; ++p) {
-            gm[j][p] = (colok[j] && gamma) ? ld_param2(gamma, pt, (l + j * W) * VEC + 2 * p)
-                                           : splat2(1.f);
+            if constexpr (!kLean)
+                gm[j][p] = (colok[j] && gamma) ? ld_param2(gamma, pt, (l + j * W) * VEC + 2 * p)
+                                               : splat2(1.f);
             acc_g[j][p] = acc_b[j][p] = splat2(0.f);
         }
     }
+    // the lean form's gamma, as float32 past the ring
+    const float* prm = reinterpret_cast<const float*>(dsm + bwd_ring_bytes<TX>(S, kBwdLN));
+    if constexpr (kLean)
+        if (gamma) stage_params<T>(const_cast<float*>(prm), gamma, pt, N);
+    // gamma of pair p of vector j
+    auto gam = [&](int j, int p) -> f2 {
+        if constexpr (kLean)
+            return (colok[j] && gamma) ? prm2(prm, (l + j * W) * VEC + 2 * p) : splat2(1.f);
+        else
+            return gm[j][p];
+    };
 
     // saved statistics of this thread's rows, loaded one row block ahead of
     // use (*_n), or two (*_nn too) with one vector per thread: measured
@@ -221,7 +237,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     auto rows = [&](const unsigned char* xs, const unsigned char* ds, TX* dxb, int64_t row0,
                     bool alive, auto masked) {
         constexpr bool kMask = decltype(masked)::value;
-        float rs[U];
+        float rs[U], mu[U];
         f2 xh[U][KV][P], gg[U][KV][P];
         bool okr[U];
         float s[2 * U];
@@ -241,7 +257,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
 #pragma unroll
                 for (int p = 0; p < P; ++p) {
                     const f2 xhv = mul2(sub2(xv[p], m2), r2);
-                    const f2 ggv = mul2(dv[p], gm[j][p]);
+                    const f2 ggv = mul2(dv[p], gam(j, p));
                     s1 = add2(s1, ggv);
                     s2 = fma2(ggv, xhv, s2);
                     if constexpr (kMask) {
@@ -253,12 +269,15 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
                         acc_g[j][p] = fma2(dv[p], xhv, acc_g[j][p]);
                         acc_b[j][p] = add2(acc_b[j][p], dv[p]);
                     }
-                    xh[u][j][p] = xhv;
-                    gg[u][j][p] = ggv;
+                    if constexpr (!kLean) {
+                        xh[u][j][p] = xhv;
+                        gg[u][j][p] = ggv;
+                    }
                 }
             }
             s[2 * u] = lo2(s1) + hi2(s1);
             s[2 * u + 1] = lo2(s2) + hi2(s2);
+            mu[u] = mu_n[u];
         }
         if constexpr (kDeep) {
 #pragma unroll
@@ -279,6 +298,17 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
                 const bool ok = alive && colok[j] && okr[u];
+                if constexpr (kLean) {  // the row again from the slot
+                    const f2 m2 = splat2(mu[u]);
+                    f2 xv[P], dv[P];
+                    unpack2<TX>(lds128_if(ok, xs + u * srow + j * W * 16), xv);
+                    unpack2<TX>(lds128_if(ok, ds + u * srow + j * W * 16), dv);
+#pragma unroll
+                    for (int p = 0; p < P; ++p) {
+                        xh[u][j][p] = mul2(sub2(xv[p], m2), r2);
+                        gg[u][j][p] = mul2(dv[p], gam(j, p));
+                    }
+                }
                 // rstd * (g - mean(g) - xhat * mean(g xhat)); g - mean(g) first,
                 // so a width-one row gives exactly zero
                 f2 o[P];
@@ -290,7 +320,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
         }
     };
 
-    Ring<2, kind_stages(S, kBwdLN), kIn == kInRows> rg;
+    Ring<2, bwd_stages<TX>(S, kBwdLN), kIn == kInRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     if constexpr (kIn == kInRows) {
@@ -307,8 +337,9 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     const int64_t rstride = (int64_t)gridDim.x * (G * U);
     int64_t row0 = (int64_t)blockIdx.x * (G * U) + g;  // this thread's first row
     TX* dxb = dx + row0 * N + l * VEC;
-    // rows wider than a warp: the row reduction's barrier releases the slot
-    ring_loop<(W > 32)>(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+    // rows wider than a warp: the row reduction's barrier releases the slot,
+    // unless the row is read again after it (the lean form)
+    ring_loop<(W > 32) && !kLean>(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* xs = rg.tile(k, 0) + soff;
         const unsigned char* ds = rg.tile(k, 1) + soff;
         if (b < nfull)
@@ -452,67 +483,80 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
     rg.slot = kBatchSlot;
     rg.fault = fault;
     constexpr int RB = batch_rb(KMAX, E);
+    constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
-        const unsigned char* xs = rg.tile(k, 0);
+        const uint32_t xs = smem_u32(rg.tile(k, 0)) + lane * UB;
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        // RB consecutive rows a warp at once; rows past the block read zeros
-        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
-            float v[RB][KMAX][E], s[RB], q[RB];
+        // RB consecutive rows a warp at once.  A whole block (every row group
+        // full, every unit in the slot) runs unmasked; otherwise rows past the
+        // block read zeros and units past the copied bytes come from global
+        // memory.
+        auto pass = [&](auto masked) {
+            constexpr bool kMask = decltype(masked)::value;
+            for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
+                float v[RB][KMAX][E], s[RB], q[RB];
 #pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                const int i = i0 + rr;
-                const int64_t r = r0 + i;
-                s[rr] = 0.f;
+                for (int rr = 0; rr < RB; ++rr) {
+                    const int i = i0 + rr;
+                    s[rr] = 0.f;
 #pragma unroll
-                for (int kk = 0; kk < KMAX; ++kk) {
-                    const int u = lane + 32 * kk;
-                    const int64_t gi = r * N + u * E;
-                    typename U::W w{};
-                    if (i < rows && uok[kk])
-                        w = gi < tail ? *reinterpret_cast<const typename U::W*>(
-                                            xs + i * rb + u * E * sizeof(TX))
-                                      : U::ld(x + gi);
-                    U::unpack(w, v[rr][kk]);
+                    for (int kk = 0; kk < KMAX; ++kk) {
+                        typename U::W w{};
+                        if constexpr (kMask) {
+                            const int64_t gi = (r0 + i) * N + (lane + 32 * kk) * E;
+                            if (i < rows && uok[kk])
+                                w = gi < tail ? U::lds(xs + i * rb + kk * 32 * UB) : U::ld(x + gi);
+                        } else {
+                            if (uok[kk]) w = U::lds(xs + i * rb + kk * 32 * UB);
+                        }
+                        U::unpack(w, v[rr][kk]);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) s[rr] += v[rr][kk][e];
-                }
-            }
-            butterfly<32, RB>(s);
-#pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                s[rr] = row_mean(s[rr], fN, inv_n);  // the mean
-                q[rr] = 0.f;
-#pragma unroll
-                for (int kk = 0; kk < KMAX; ++kk)
-#pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        v[rr][kk][e] -= s[rr];
-                        q[rr] = uok[kk] ? fmaf(v[rr][kk][e], v[rr][kk][e], q[rr]) : q[rr];
+                        for (int e = 0; e < E; ++e) s[rr] += v[rr][kk][e];
                     }
-            }
-            butterfly<32, RB>(q);
-#pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                const int i = i0 + rr;
-                if (i >= rows) break;  // the same for the whole warp
-                const int64_t r = r0 + i;
-                const float rs = rsqrtf(fmaf(q[rr], inv_n, eps));
-#pragma unroll
-                for (int kk = 0; kk < KMAX; ++kk) {
-                    float o[E];
-#pragma unroll
-                    for (int e = 0; e < E; ++e)
-                        o[e] = fmaf(v[rr][kk][e] * rs, gm[kk][e], bt[kk][e]);
-                    if (uok[kk]) U::st(y + r * N + (lane + 32 * kk) * E, U::pack(o));
                 }
-                if (lane == 0) {
-                    if (mean) mean[r] = s[rr];
-                    if (rstd) rstd[r] = rs;
+                butterfly<32, RB>(s);
+#pragma unroll
+                for (int rr = 0; rr < RB; ++rr) {
+                    s[rr] = row_mean(s[rr], fN, inv_n);  // the mean
+                    q[rr] = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < KMAX; ++kk)
+#pragma unroll
+                        for (int e = 0; e < E; ++e) {
+                            v[rr][kk][e] -= s[rr];
+                            q[rr] = uok[kk] ? fmaf(v[rr][kk][e], v[rr][kk][e], q[rr]) : q[rr];
+                        }
+                }
+                butterfly<32, RB>(q);
+#pragma unroll
+                for (int rr = 0; rr < RB; ++rr) {
+                    const int i = i0 + rr;
+                    if (kMask && i >= rows) break;  // the same for the whole warp
+                    const int64_t r = r0 + i;
+                    const float rs = rsqrtf(fmaf(q[rr], inv_n, eps));
+                    TX* const yr = y + r * N + lane * E;
+#pragma unroll
+                    for (int kk = 0; kk < KMAX; ++kk) {
+                        float o[E];
+#pragma unroll
+                        for (int e = 0; e < E; ++e)
+                            o[e] = fmaf(v[rr][kk][e] * rs, gm[kk][e], bt[kk][e]);
+                        if (uok[kk]) U::st(yr + kk * 32 * E, U::pack(o));
+                    }
+                    if (lane == 0) {
+                        if (mean) mean[r] = s[rr];
+                        if (rstd) rstd[r] = rs;
+                    }
                 }
             }
-        }
+        };
+        // R is a multiple of 8 and RB divides 8: a full block has no partial row group
+        if (rows == R && (r0 + R) * N <= tail)
+            pass(std::false_type{});
+        else
+            pass(std::true_type{});
     });
 }
 
@@ -552,66 +596,81 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
     rg.slot = kBatchSlot;
     rg.fault = fault;
     constexpr int RB = batch_rb(KMAX, E);
+    constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
-        const unsigned char* xs = rg.tile(k, 0);
-        const unsigned char* ds = rg.tile(k, 1);
+        const uint32_t xs = smem_u32(rg.tile(k, 0)) + lane * UB;
+        const uint32_t ds = smem_u32(rg.tile(k, 1)) + lane * UB;
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        // RB consecutive rows a warp at once; rows past the block read zeros
-        // (and then add exact zeros to the column sums)
-        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
-            float xh[RB][KMAX][E], g[RB][KMAX][E], s[2 * RB], rs[RB];
+        // RB consecutive rows a warp at once.  A whole block runs unmasked;
+        // otherwise rows past the block read zeros (and then add exact zeros
+        // to the column sums) and units past the copied bytes come from global
+        // memory.
+        auto pass = [&](auto masked) {
+            constexpr bool kMask = decltype(masked)::value;
+            for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
+                float xh[RB][KMAX][E], g[RB][KMAX][E], s[2 * RB], rs[RB];
 #pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                const int i = i0 + rr;
-                const int64_t r = r0 + i;
-                const bool ok = i < rows;
-                const float mu = ok ? __ldca(mean + r) : 0.f;
-                rs[rr] = ok ? __ldca(rstd + r) : 0.f;
-                s[2 * rr] = s[2 * rr + 1] = 0.f;
+                for (int rr = 0; rr < RB; ++rr) {
+                    const int i = i0 + rr;
+                    const int64_t r = r0 + i;
+                    const bool ok = !kMask || i < rows;
+                    const float mu = ok ? __ldca(mean + r) : 0.f;
+                    rs[rr] = ok ? __ldca(rstd + r) : 0.f;
+                    s[2 * rr] = s[2 * rr + 1] = 0.f;
 #pragma unroll
-                for (int kk = 0; kk < KMAX; ++kk) {
-                    const int u = lane + 32 * kk;
-                    const int64_t gi = r * N + u * E;
-                    const int so = i * rb + u * E * (int)sizeof(TX);
-                    typename U::W wx{}, wd{};
-                    if (ok && uok[kk]) {
-                        const bool sm = gi < tail;
-                        wx = sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
-                        wd = sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
+                    for (int kk = 0; kk < KMAX; ++kk) {
+                        const uint32_t so = i * rb + kk * 32 * UB;
+                        typename U::W wx{}, wd{};
+                        if constexpr (kMask) {
+                            const int64_t gi = r * N + (lane + 32 * kk) * E;
+                            if (ok && uok[kk]) {
+                                const bool sm = gi < tail;
+                                wx = sm ? U::lds(xs + so) : U::ld(x + gi);
+                                wd = sm ? U::lds(ds + so) : U::ld(dy + gi);
+                            }
+                        } else if (uok[kk]) {
+                            wx = U::lds(xs + so);
+                            wd = U::lds(ds + so);
+                        }
+                        float xv[E], dv[E];
+                        U::unpack(wx, xv);
+                        U::unpack(wd, dv);
+#pragma unroll
+                        for (int e = 0; e < E; ++e) {
+                            xh[rr][kk][e] = (xv[e] - mu) * rs[rr];
+                            g[rr][kk][e] = dv[e] * gm[kk][e];
+                            s[2 * rr] += g[rr][kk][e];
+                            s[2 * rr + 1] = fmaf(g[rr][kk][e], xh[rr][kk][e], s[2 * rr + 1]);
+                            acc_g[kk][e] = fmaf(dv[e], xh[rr][kk][e], acc_g[kk][e]);
+                            acc_b[kk][e] += dv[e];
+                        }
                     }
-                    float xv[E], dv[E];
-                    U::unpack(wx, xv);
-                    U::unpack(wd, dv);
+                }
+                butterfly<32, 2 * RB>(s);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        xh[rr][kk][e] = (xv[e] - mu) * rs[rr];
-                        g[rr][kk][e] = dv[e] * gm[kk][e];
-                        s[2 * rr] += g[rr][kk][e];
-                        s[2 * rr + 1] = fmaf(g[rr][kk][e], xh[rr][kk][e], s[2 * rr + 1]);
-                        acc_g[kk][e] = fmaf(dv[e], xh[rr][kk][e], acc_g[kk][e]);
-                        acc_b[kk][e] += dv[e];
+                for (int rr = 0; rr < RB; ++rr) {
+                    const int i = i0 + rr;
+                    if (kMask && i >= rows) break;  // the same for the whole warp
+                    const float ma = s[2 * rr] * inv_n, mb = s[2 * rr + 1] * inv_n;
+                    TX* const dxr = dx + (r0 + i) * N + lane * E;
+#pragma unroll
+                    for (int kk = 0; kk < KMAX; ++kk) {
+                        float o[E];
+#pragma unroll
+                        for (int e = 0; e < E; ++e)
+                            o[e] = rs[rr] * fmaf(-xh[rr][kk][e], mb, g[rr][kk][e] - ma);
+                        if (uok[kk]) U::st(dxr + kk * 32 * E, U::pack(o));
                     }
                 }
             }
-            butterfly<32, 2 * RB>(s);
-#pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                const int i = i0 + rr;
-                if (i >= rows) break;  // the same for the whole warp
-                const int64_t r = r0 + i;
-                const float ma = s[2 * rr] * inv_n, mb = s[2 * rr + 1] * inv_n;
-#pragma unroll
-                for (int kk = 0; kk < KMAX; ++kk) {
-                    float o[E];
-#pragma unroll
-                    for (int e = 0; e < E; ++e)
-                        o[e] = rs[rr] * fmaf(-xh[rr][kk][e], mb, g[rr][kk][e] - ma);
-                    if (uok[kk]) U::st(dx + r * N + (lane + 32 * kk) * E, U::pack(o));
-                }
-            }
-        }
+        };
+        // R is a multiple of 8 and RB divides 8: a full block has no partial row group
+        if (rows == R && (r0 + R) * N <= tail)
+            pass(std::false_type{});
+        else
+            pass(std::true_type{});
     });
     if (ws == nullptr) return;  // no parameter gradient requested (uniform)
     // the warps' column sums, added in warp order into the CTA's partial row
@@ -676,7 +735,8 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* gam
     }
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9)
-        GBN_CASE(12) GBN_CASE(13) GBN_CASE(16) GBN_CASE(17)
+        GBN_CASE(13) GBN_CASE(16) GBN_CASE(17) GBN_CASE(18) GBN_CASE(20) GBN_CASE(21)
+        GBN_CASE(22)
 #undef GBN_CASE
         default: return cudaErrorInvalidValue;
     }
@@ -712,7 +772,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     switch (L.sid) {
 #define GBN_CASE_BODY(S)                                                                           \
     {                                                                                              \
-        constexpr int smem = ring_smem_bytes(S, kBwdLN, 2);                                        \
+        constexpr int smem = bwd_smem_bytes<TX>(S, kBwdLN);                                        \
         with_mode(L.in_mode, [&](auto m_) {                                                        \
             constexpr int kIn_ = decltype(m_)::value;                                              \
             ring_attributes<ln_bwd_fast<TX, S, kIn_>>(smem);                                       \
@@ -726,15 +786,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         break;
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9)
-        GBN_CASE(12) GBN_CASE(14) GBN_CASE(15)
-        // schedule 17 only for float32 activations (the planner's choice)
-        case 17:
-            if constexpr (sizeof(TX) == 4) {
-                GBN_CASE_BODY(17)
-            } else {
-                return cudaErrorInvalidValue;
-            }
-            break;
+        GBN_CASE(12) GBN_CASE(14) GBN_CASE(15) GBN_CASE(17) GBN_CASE(19) GBN_CASE(23)
 #undef GBN_CASE
 #undef GBN_CASE_BODY
         default: return cudaErrorInvalidValue;

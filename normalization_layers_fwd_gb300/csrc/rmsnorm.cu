@@ -164,50 +164,62 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
     rg.slot = kBatchSlot;
     rg.fault = fault;
     constexpr int RB = batch_rb(KMAX, E);
+    constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
-        const unsigned char* xs = rg.tile(k, 0);
+        const uint32_t xs = smem_u32(rg.tile(k, 0)) + lane * UB;
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        // RB consecutive rows a warp at once; rows past the block read zeros
-        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
-            float v[RB][KMAX][E], rs[RB];
+        // RB consecutive rows a warp at once.  A whole block runs unmasked;
+        // otherwise rows past the block read zeros and units past the copied
+        // bytes come from global memory.
+        auto pass = [&](auto masked) {
+            constexpr bool kMask = decltype(masked)::value;
+            for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
+                float v[RB][KMAX][E], rs[RB];
 #pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                const int i = i0 + rr;
-                const int64_t r = r0 + i;
+                for (int rr = 0; rr < RB; ++rr) {
+                    const int i = i0 + rr;
 #pragma unroll
-                for (int kk = 0; kk < KMAX; ++kk) {
-                    const int u = lane + 32 * kk;
-                    const int64_t gi = r * N + u * E;
-                    typename U::W wd{};
-                    if (i < rows && uok[kk])
-                        wd = gi < tail ? *reinterpret_cast<const typename U::W*>(
-                                             xs + i * rb + u * E * sizeof(TX))
-                                       : U::ld(x + gi);
-                    U::unpack(wd, v[rr][kk]);
-                }
-                rs[rr] = batch_sumsq<KMAX, E>(v[rr]);
-            }
-            batch_rstd<RB>(rs, eps, inv_n);
-#pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                const int i = i0 + rr;
-                if (i >= rows) break;  // the same for the whole warp
-                const int64_t r = r0 + i;
-#pragma unroll
-                for (int kk = 0; kk < KMAX; ++kk) {
-                    float o[E];
-#pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float xh = v[rr][kk][e] * rs[rr];
-                        o[e] = wv[kk][e] * (variant == 0 ? round_x<TX>(xh) : xh);
+                    for (int kk = 0; kk < KMAX; ++kk) {
+                        typename U::W wd{};
+                        if constexpr (kMask) {
+                            const int64_t gi = (r0 + i) * N + (lane + 32 * kk) * E;
+                            if (i < rows && uok[kk])
+                                wd = gi < tail ? U::lds(xs + i * rb + kk * 32 * UB) : U::ld(x + gi);
+                        } else {
+                            if (uok[kk]) wd = U::lds(xs + i * rb + kk * 32 * UB);
+                        }
+                        U::unpack(wd, v[rr][kk]);
                     }
-                    if (uok[kk]) U::st(y + r * N + (lane + 32 * kk) * E, U::pack(o));
+                    rs[rr] = batch_sumsq<KMAX, E>(v[rr]);
                 }
-                if (rstd && lane == 0) rstd[r] = rs[rr];
+                batch_rstd<RB>(rs, eps, inv_n);
+#pragma unroll
+                for (int rr = 0; rr < RB; ++rr) {
+                    const int i = i0 + rr;
+                    if (kMask && i >= rows) break;  // the same for the whole warp
+                    const int64_t r = r0 + i;
+                    TX* const yr = y + r * N + lane * E;
+#pragma unroll
+                    for (int kk = 0; kk < KMAX; ++kk) {
+                        float o[E];
+#pragma unroll
+                        for (int e = 0; e < E; ++e) {
+                            const float xh = v[rr][kk][e] * rs[rr];
+                            o[e] = wv[kk][e] * (variant == 0 ? round_x<TX>(xh) : xh);
+                        }
+                        if (uok[kk]) U::st(yr + kk * 32 * E, U::pack(o));
+                    }
+                    if (rstd && lane == 0) rstd[r] = rs[rr];
+                }
             }
-        }
+        };
+        // R is a multiple of 8 and RB divides 8: a full block has no partial row group
+        if (rows == R && (r0 + R) * N <= tail)
+            pass(std::false_type{});
+        else
+            pass(std::true_type{});
     });
 }
 
@@ -248,15 +260,8 @@ cudaError_t fwd_dispatch(const Launch& L, int pt, const void* x, const void* w, 
         break;
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(11)
-        GBN_CASE(12) GBN_CASE(14)
-        // schedule 17 only for float32 activations (the planner's choice)
-        case 17:
-            if constexpr (sizeof(TX) == 4) {
-                GBN_CASE_BODY(17)
-            } else {
-                return cudaErrorInvalidValue;
-            }
-            break;
+        GBN_CASE(12) GBN_CASE(14) GBN_CASE(15) GBN_CASE(19) GBN_CASE(23)
+        GBN_CASE(17)
 #undef GBN_CASE
 #undef GBN_CASE_BODY
         default: return cudaErrorInvalidValue;

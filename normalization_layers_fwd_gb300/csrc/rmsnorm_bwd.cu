@@ -22,7 +22,11 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
     constexpr int W = kSched[S].W, U = kind_U(S, kBwdRms), T = kSched[S].T, KV = kSched[S].KV;
     constexpr int VEC = Vec<TX>::kN, P = Pairs<TX>::kP;
     constexpr int G = groups_per_cta(W, T);
-    static_assert(KV <= 2 || sizeof(TX) == 4,
+    // The lean form (16-bit rows of 1025-2048 vectors) holds only the weight
+    // gradient accumulators: it reads the row from the ring slot again after
+    // the row reduction, and the weight from shared memory at each use.
+    constexpr bool kLean = lean_bwd<TX>(S);
+    static_assert(KV <= 2 || sizeof(TX) == 4 || kLean,
                   "the 16-bit RMSNorm backward takes at most 2 vectors per thread");
     extern __shared__ __align__(128) unsigned char dsm[];
     __shared__ float red[GroupRed<W, T, U>::kFloats];
@@ -40,17 +44,65 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
 
     f2 wf[KV][P], acc[KV][P];
     uint32_t wpk[KV][P];
+    // the weight of pair p of vector j, as float32 (1 + w for Gemma) and as a
+    // packed 16-bit pair (used when w16)
+    // the lean form's weight, as float32 past the ring (a 16-bit weight
+    // converts back to its own bits exactly)
+    const float* prm = reinterpret_cast<const float*>(dsm + bwd_ring_bytes<TX>(S, kBwdRms));
+    if constexpr (kLean) stage_params<T>(const_cast<float*>(prm), w, pt, N);
+    auto wf_at = [&](int j, int p) -> f2 {
+        const int c = (l + j * W) * VEC + 2 * p;
+        const f2 v = !colok[j] ? splat2(0.f) : kLean ? prm2(prm, c) : ld_param2(w, pt, c);
+        return gemma ? add2(splat2(1.f), v) : v;  // 1 + w in float32
+    };
+    auto wpk_at = [&](int j, int p) -> uint32_t {
+        const int c = (l + j * W) * VEC + 2 * p;
+        if (!(w16 && colok[j])) return 0u;
+        if constexpr (kLean)
+            return P16<TX>::from_f2(prm2(prm, c));
+        else
+            return static_cast<const uint32_t*>(w)[c / 2];
+    };
 #pragma unroll
     for (int j = 0; j < KV; ++j) {
 #pragma unroll
         for (int p = 0; p < P; ++p) {
-            const int c = (l + j * W) * VEC + 2 * p;
-            wf[j][p] = colok[j] ? ld_param2(w, pt, c) : splat2(0.f);
-            if (gemma) wf[j][p] = add2(splat2(1.f), wf[j][p]);  // 1 + w in float32
-            wpk[j][p] = (w16 && colok[j]) ? static_cast<const uint32_t*>(w)[c / 2] : 0u;
+            if constexpr (!kLean) {
+                wf[j][p] = wf_at(j, p);
+                wpk[j][p] = wpk_at(j, p);
+            }
             acc[j][p] = splat2(0.f);
         }
     }
+    auto wfv = [&](int j, int p) -> f2 {
+        if constexpr (kLean)
+            return wf_at(j, p);
+        else
+            return wf[j][p];
+    };
+    auto wpkv = [&](int j, int p) -> uint32_t {
+        if constexpr (kLean)
+            return wpk_at(j, p);
+        else
+            return wpk[j][p];
+    };
+    // dn = dy w (rounded as the expression says) of one pair, and the weight
+    // gradient accumulator with this row's term dy n added (n = xhat rounded)
+    auto pair_terms = [&](int j, int p, uint32_t dyw, f2 dv, f2 xh, f2 a, f2& dn) -> f2 {
+        if constexpr (is16<TX>() && !kWF) {
+            const uint32_t npk = P16<TX>::from_f2(xh);  // n = round_x(xhat)
+            if (w16) {
+                dn = P16<TX>::to_f2(P16<TX>::mul(dyw, wpkv(j, p)));
+                return add2(a, P16<TX>::to_f2(P16<TX>::mul(dyw, npk)));
+            }
+            // float32 weight: dy*n unrounded, exact product of two 16-bit values
+            dn = round2<TX>(mul2(dv, wfv(j, p)));
+            return mk2(P16<TX>::fma_lo(dyw, npk, lo2(a)), P16<TX>::fma_hi(dyw, npk, hi2(a)));
+        } else {
+            dn = mul2(dv, wfv(j, p));
+            return fma2(dv, xh, a);
+        }
+    };
     // the given rstd of this thread's rows, loaded one row block ahead of use
     // (rs_n), or two (rs_nn too) with several vectors per thread: measured
     // faster for those wide rows, slower for the narrow ones
@@ -116,22 +168,9 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
 #pragma unroll
                 for (int p = 0; p < P; ++p) {
                     xh[u][j][p] = mul2(xh[u][j][p], r2);
-                    f2 nxt;  // the accumulator with this row's dw term added
-                    if constexpr (is16<TX>() && !kWF) {
-                        const uint32_t npk = P16<TX>::from_f2(xh[u][j][p]);  // n = round_x(xhat)
-                        if (w16) {
-                            dn[u][j][p] = P16<TX>::to_f2(P16<TX>::mul(word(dr, p), wpk[j][p]));
-                            nxt = add2(acc[j][p], P16<TX>::to_f2(P16<TX>::mul(word(dr, p), npk)));
-                        } else {
-                            // float32 weight: dy*n unrounded, exact product of two 16-bit values
-                            dn[u][j][p] = round2<TX>(mul2(dv[p], wf[j][p]));
-                            nxt = mk2(P16<TX>::fma_lo(word(dr, p), npk, lo2(acc[j][p])),
-                                      P16<TX>::fma_hi(word(dr, p), npk, hi2(acc[j][p])));
-                        }
-                    } else {
-                        dn[u][j][p] = mul2(dv[p], wf[j][p]);
-                        nxt = fma2(dv[p], xh[u][j][p], acc[j][p]);
-                    }
+                    // the accumulator with this row's dw term added
+                    const f2 nxt = pair_terms(j, p, word(dr, p), dv[p], xh[u][j][p], acc[j][p],
+                                              dn[u][j][p]);
                     a2 = fma2(dn[u][j][p], xh[u][j][p], a2);
                     // padded rows: keep the old sum, a select after the arithmetic
                     acc[j][p] = (!kMask || okr[u]) ? nxt : acc[j][p];
@@ -154,7 +193,86 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
         }
     };
 
-    Ring<2, kind_stages(S, kBwdRms), kIn == kInRows> rg;
+    // The lean form of `rows`: x for the recomputed r, then x and dy for the
+    // reduction and the weight gradient, then x and dy again for dx.
+    auto rows_lean = [&](const unsigned char* xs, const unsigned char* ds, TX* dxb, int64_t row0,
+                         bool alive, auto masked) {
+        constexpr bool kMask = decltype(masked)::value;
+        float rs[U], s[U];
+        bool okr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            okr[u] = !kMask || row0 + u * G < M;
+            rs[u] = rs_n[u];
+            if constexpr (kDeep) rs_n[u] = rs_nn[u];
+        }
+        if constexpr (kDeep)
+            load_rstd(row0 + 2 * bstride, rs_nn);
+        else
+            load_rstd(row0 + bstride, rs_n);
+        if (!rstd) {  // uniform branch: recompute r exactly as the forward does
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                rs[u] = 0.f;
+#pragma unroll
+                for (int j = 0; j < KV; ++j) {
+                    f2 xv[P];
+                    unpack2<TX>(lds128_if(alive && okr[u] && colok[j], xs + u * srow + j * W * 16),
+                                xv);
+                    rs[u] += vec_sumsq2<P>(xv);
+                }
+            }
+            group_allreduce<W, T, U>(rs, red, parity);
+#pragma unroll
+            for (int u = 0; u < U; ++u) rs[u] = rsqrtf(fmaf(rs[u], inv_n, eps));
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const f2 r2 = splat2(rs[u]);
+            f2 a2 = splat2(0.f);
+#pragma unroll
+            for (int j = 0; j < KV; ++j) {
+                const bool ok = alive && okr[u] && colok[j];
+                const uint4 dr = lds128_if(ok, ds + u * srow + j * W * 16);
+                f2 xv[P], dv[P];
+                unpack2<TX>(lds128_if(ok, xs + u * srow + j * W * 16), xv);
+                unpack2<TX>(dr, dv);
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    const f2 xh = mul2(xv[p], r2);
+                    f2 dn;
+                    const f2 nxt = pair_terms(j, p, word(dr, p), dv[p], xh, acc[j][p], dn);
+                    a2 = fma2(dn, xh, a2);
+                    acc[j][p] = (!kMask || okr[u]) ? nxt : acc[j][p];
+                }
+            }
+            s[u] = lo2(a2) + hi2(a2);
+        }
+        group_allreduce<W, T, U>(s, red, parity);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const f2 r2 = splat2(rs[u]), nm = splat2(-(s[u] * inv_n));
+            TX* const dxr = out_at<kIn>(dxb, u * grow, dx, maps, row0 + u * G, N, l * VEC);
+#pragma unroll
+            for (int j = 0; j < KV; ++j) {
+                const bool ok = alive && okr[u] && colok[j];
+                const uint4 dr = lds128_if(ok, ds + u * srow + j * W * 16);
+                f2 xv[P], dv[P], o[P];
+                unpack2<TX>(lds128_if(ok, xs + u * srow + j * W * 16), xv);
+                unpack2<TX>(dr, dv);
+#pragma unroll
+                for (int p = 0; p < P; ++p) {
+                    const f2 xh = mul2(xv[p], r2);
+                    f2 dn;
+                    pair_terms(j, p, word(dr, p), dv[p], xh, splat2(0.f), dn);
+                    o[p] = mul2(r2, fma2(xh, nm, dn));
+                }
+                st_stream_if(ok, dxr + j * W * VEC, pack2<TX>(o));
+            }
+        }
+    };
+
+    Ring<2, bwd_stages<TX>(S, kBwdRms), kIn == kInRows> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     if constexpr (kIn == kInRows) {
@@ -174,13 +292,20 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
     // rows wider than a warp: the row reduction's barrier releases the slot;
     // except at 1024 threads (one CTA per SM), where the ring's own barrier
     // measured 7% faster
-    ring_loop<(W > 32 && T < 1024)>(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
+    ring_loop<(W > 32 && T < 1024 && !kLean)>(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* xs = rg.tile(k, 0) + soff;
         const unsigned char* ds = rg.tile(k, 1) + soff;
-        if (b < nfull)
-            rows(xs, ds, dxb, row0, alive, std::false_type{});
-        else
-            rows(xs, ds, dxb, row0, alive, std::true_type{});
+        if constexpr (kLean) {
+            if (b < nfull)
+                rows_lean(xs, ds, dxb, row0, alive, std::false_type{});
+            else
+                rows_lean(xs, ds, dxb, row0, alive, std::true_type{});
+        } else {
+            if (b < nfull)
+                rows(xs, ds, dxb, row0, alive, std::false_type{});
+            else
+                rows(xs, ds, dxb, row0, alive, std::true_type{});
+        }
         row0 += rstride;
         dxb += rstride * N;
     });
@@ -280,73 +405,89 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
     rg.slot = kBatchSlot;
     rg.fault = fault;
     constexpr int RB = batch_rb(KMAX, E);
+    constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
-        const unsigned char* xs = rg.tile(k, 0);
-        const unsigned char* ds = rg.tile(k, 1);
+        const uint32_t xs = smem_u32(rg.tile(k, 0)) + lane * UB;
+        const uint32_t ds = smem_u32(rg.tile(k, 1)) + lane * UB;
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        // RB consecutive rows a warp at once; rows past the block read zeros
-        // (and then add exact zeros to the column sums)
-        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
-            float xv[RB][KMAX][E], dv[RB][KMAX][E], rs[RB], s[RB];
+        // RB consecutive rows a warp at once.  A whole block runs unmasked;
+        // otherwise rows past the block read zeros (and then add exact zeros
+        // to the column sums) and units past the copied bytes come from global
+        // memory.
+        auto pass = [&](auto masked) {
+            constexpr bool kMask = decltype(masked)::value;
+            for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
+                float xv[RB][KMAX][E], dv[RB][KMAX][E], rs[RB], s[RB];
 #pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                const int i = i0 + rr;
-                const int64_t r = r0 + i;
-                const bool ok = i < rows;
+                for (int rr = 0; rr < RB; ++rr) {
+                    const int i = i0 + rr;
+                    const int64_t r = r0 + i;
+                    const bool ok = !kMask || i < rows;
 #pragma unroll
-                for (int kk = 0; kk < KMAX; ++kk) {
-                    const int u = lane + 32 * kk;
-                    const int64_t gi = r * N + u * E;
-                    const int so = i * rb + u * E * (int)sizeof(TX);
-                    typename U::W wx{}, wd{};
-                    if (ok && uok[kk]) {
-                        const bool sm = gi < tail;
-                        wx = sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
-                        wd = sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
+                    for (int kk = 0; kk < KMAX; ++kk) {
+                        const uint32_t so = i * rb + kk * 32 * UB;
+                        typename U::W wx{}, wd{};
+                        if constexpr (kMask) {
+                            const int64_t gi = r * N + (lane + 32 * kk) * E;
+                            if (ok && uok[kk]) {
+                                const bool sm = gi < tail;
+                                wx = sm ? U::lds(xs + so) : U::ld(x + gi);
+                                wd = sm ? U::lds(ds + so) : U::ld(dy + gi);
+                            }
+                        } else if (uok[kk]) {
+                            wx = U::lds(xs + so);
+                            wd = U::lds(ds + so);
+                        }
+                        U::unpack(wx, xv[rr][kk]);
+                        U::unpack(wd, dv[rr][kk]);
                     }
-                    U::unpack(wx, xv[rr][kk]);
-                    U::unpack(wd, dv[rr][kk]);
+                    rs[rr] = rstd ? (ok ? __ldca(rstd + r) : 0.f) : batch_sumsq<KMAX, E>(xv[rr]);
                 }
-                rs[rr] = rstd ? (ok ? __ldca(rstd + r) : 0.f) : batch_sumsq<KMAX, E>(xv[rr]);
-            }
-            if (!rstd) batch_rstd<RB>(rs, eps, inv_n);  // uniform branch
+                if (!rstd) batch_rstd<RB>(rs, eps, inv_n);  // uniform branch
 #pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                s[rr] = 0.f;
+                for (int rr = 0; rr < RB; ++rr) {
+                    s[rr] = 0.f;
 #pragma unroll
-                for (int kk = 0; kk < KMAX; ++kk)
+                    for (int kk = 0; kk < KMAX; ++kk)
 #pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        float dn = dv[rr][kk][e] * wv[kk][e];
-                        if (cast_first) dn = round_x<TX>(dn);
-                        s[rr] = fmaf(dn, xv[rr][kk][e] * rs[rr], s[rr]);
+                        for (int e = 0; e < E; ++e) {
+                            float dn = dv[rr][kk][e] * wv[kk][e];
+                            if (cast_first) dn = round_x<TX>(dn);
+                            s[rr] = fmaf(dn, xv[rr][kk][e] * rs[rr], s[rr]);
+                        }
+                }
+                butterfly<32, RB>(s);
+#pragma unroll
+                for (int rr = 0; rr < RB; ++rr) {
+                    const int i = i0 + rr;
+                    const bool ok = !kMask || i < rows;
+                    const float m = s[rr] * inv_n;
+                    TX* const dxr = dx + (r0 + i) * N + lane * E;
+#pragma unroll
+                    for (int kk = 0; kk < KMAX; ++kk) {
+                        float o[E];
+#pragma unroll
+                        for (int e = 0; e < E; ++e) {
+                            const float xh = xv[rr][kk][e] * rs[rr];
+                            float dn = dv[rr][kk][e] * wv[kk][e];
+                            if (cast_first) dn = round_x<TX>(dn);
+                            o[e] = rs[rr] * (dn - xh * m);
+                            float term = dv[rr][kk][e] * (cast_first ? round_x<TX>(xh) : xh);
+                            if (round_terms) term = round_x<TX>(term);
+                            acc[kk][e] += term;
+                        }
+                        if (ok && uok[kk]) U::st(dxr + kk * 32 * E, U::pack(o));
                     }
-            }
-            butterfly<32, RB>(s);
-#pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                const int i = i0 + rr;
-                const int64_t r = r0 + i;
-                const float m = s[rr] * inv_n;
-#pragma unroll
-                for (int kk = 0; kk < KMAX; ++kk) {
-                    float o[E];
-#pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float xh = xv[rr][kk][e] * rs[rr];
-                        float dn = dv[rr][kk][e] * wv[kk][e];
-                        if (cast_first) dn = round_x<TX>(dn);
-                        o[e] = rs[rr] * (dn - xh * m);
-                        float term = dv[rr][kk][e] * (cast_first ? round_x<TX>(xh) : xh);
-                        if (round_terms) term = round_x<TX>(term);
-                        acc[kk][e] += term;
-                    }
-                    if (i < rows && uok[kk]) U::st(dx + r * N + (lane + 32 * kk) * E, U::pack(o));
                 }
             }
-        }
+        };
+        // R is a multiple of 8 and RB divides 8: a full block has no partial row group
+        if (rows == R && (r0 + R) * N <= tail)
+            pass(std::false_type{});
+        else
+            pass(std::true_type{});
     });
     if (ws == nullptr) return;  // no weight gradient requested (uniform)
     float* cols = reinterpret_cast<float*>(dsm + 128);  // drained ring slots: 8 x N floats
@@ -395,7 +536,7 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
     switch (L.sid) {
 #define GBN_CASE_BODY(S)                                                                           \
     {                                                                                              \
-        constexpr int smem = ring_smem_bytes(S, kBwdRms, 2);                                       \
+        constexpr int smem = bwd_smem_bytes<TX>(S, kBwdRms);                                       \
         GBN_RMS_LAUNCH(rms_bwd_fast, S, smem, xp, dyp, w, pt, rstd, dxp, ws, M, N, eps, inv_n,     \
                        L.nblocks, L.fault, gemma);                                                 \
     }
@@ -405,15 +546,8 @@ cudaError_t bwd_dispatch(const Launch& L, int pt, const void* x, const void* dy,
         break;
         GBN_CASE(0) GBN_CASE(1) GBN_CASE(2) GBN_CASE(3) GBN_CASE(4) GBN_CASE(5)
         GBN_CASE(6) GBN_CASE(7) GBN_CASE(8) GBN_CASE(9) GBN_CASE(11)
-        GBN_CASE(12) GBN_CASE(14)
-        // schedule 17 only for float32 activations (the planner's choice)
-        case 17:
-            if constexpr (sizeof(TX) == 4) {
-                GBN_CASE_BODY(17)
-            } else {
-                return cudaErrorInvalidValue;
-            }
-            break;
+        GBN_CASE(12) GBN_CASE(14) GBN_CASE(15) GBN_CASE(19) GBN_CASE(23)
+        GBN_CASE(17)
 #undef GBN_CASE
 #undef GBN_CASE_BODY
         default: return cudaErrorInvalidValue;

@@ -47,9 +47,9 @@ def _run(op, inp, eps=1e-5, rows=None):
     return rmsnorm_case(inp["x"], inp["dy"], inp["gamma"], eps, rows)
 
 
-# 16-bit widths 8200-16384 (1025-2048 vectors) run the DyT and LayerNorm
-# forwards on the 4-vector wide schedule; float32 widths 4104-8192 run every
-# kernel on it; 8196 and 16392 are beyond it.  Widths up to 256 whose rows
+# 16-bit widths 8200-16384 (1025-2048 vectors) and float32 widths 4104-8192
+# run every kernel on the 4-vector wide schedule (the 16-bit backwards in
+# their lean form); 8196 and 16392 are beyond it.  Widths up to 256 whose rows
 # are not 16-byte multiples run the row-batched path: element pairs for even
 # widths up to 256 (2, 6, 100, 130, 250), single elements for odd ones up to
 # 128 (1, 5), rows narrower than 16 bytes included; 129, 255, 258 and 1001

@@ -140,6 +140,25 @@ def test_documented_limits_hold_on_this_device():
             torch.cuda.synchronize()
             _same(f"dx N={N}", dx2, dx)
             _same(f"dw N={N}", dw2, dw)
+    # the widest 16-bit vector rows: one partial row of N floats per SM
+    for N in (12288, 16384):
+        M = 2 * S
+        x, dy, w = _inputs(M, N, torch.bfloat16, torch.bfloat16, f"limit/wide/{N}")
+        dx = torch.empty_like(x)
+        dw = torch.empty_like(w)
+        ws = torch.empty(4 * N * S, dtype=torch.uint8, device="cuda")
+        rc = lib.rmsnorm_bwd(P(x), P(dy), P(w), None, P(dx), P(dw), M, N, 1e-6, _lib.GBN_BF16,
+                             _lib.GBN_BF16, P(ws), 4 * N * S, stream)
+        assert rc == _lib.GBN_OK, (N, rc)
+        if 4 * N * S <= _lib.GBN_STATIC_WS_BYTES:
+            dx_ref, dw_ref = _lib.rmsnorm_bwd(x, dy, w)
+            dx2, dw2 = _lib.rmsnorm_bwd_static_ws(x, dy, w)
+            torch.cuda.synchronize()
+            _same(f"dx N={N}", dx2, dx_ref)
+            _same(f"dw N={N}", dw2, dw_ref)
+        else:
+            with pytest.raises(_lib.GbnError):
+                _lib.rmsnorm_bwd_static_ws(x, dy, w)
     # general path (N not a multiple of 8: 16-bit rows are not 16-byte multiples)
     n_fit = (1 << 19) // Sp
     n_fit -= 1 if n_fit % 8 == 0 else 0

@@ -461,36 +461,47 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
     rg.nblocks = nblocks;
     rg.slot = kBatchSlot;
     rg.fault = fault;
-    constexpr int RB = 1;  // no row reduction to share: one row at a time
+    constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
-        const unsigned char* xs = rg.tile(k, 0);
+        const uint32_t xs = smem_u32(rg.tile(k, 0)) + lane * UB;
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
-#pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                const int i = i0 + rr;
-                if (i >= rows) break;  // the same for the whole warp
-                const int64_t r = r0 + i;
+        // one row a warp at a time (no row reduction to share), its units all
+        // loaded before any is used.  A block whose units are all in the slot
+        // runs unmasked; the last one takes units past the copied bytes from
+        // global memory.
+        auto pass = [&](auto masked) {
+            constexpr bool kMask = decltype(masked)::value;
+            for (int i = warp; i < rows; i += kBatchWarps) {
+                const int64_t gr = (r0 + i) * N + lane * E;
+                typename U::W w[KMAX];
 #pragma unroll
                 for (int kk = 0; kk < KMAX; ++kk) {
-                    if (!uok[kk]) continue;
-                    const int u = lane + 32 * kk;
-                    const int64_t gi = r * N + u * E;
-                    const typename U::W w =
-                        gi < tail ? *reinterpret_cast<const typename U::W*>(xs + i * rb +
-                                                                            u * E * sizeof(TX))
-                                  : U::ld(x + gi);
+                    w[kk] = typename U::W{};
+                    if constexpr (kMask) {
+                        const int64_t gi = gr + kk * 32 * E;
+                        if (uok[kk])
+                            w[kk] = gi < tail ? U::lds(xs + i * rb + kk * 32 * UB) : U::ld(x + gi);
+                    } else {
+                        if (uok[kk]) w[kk] = U::lds(xs + i * rb + kk * 32 * UB);
+                    }
+                }
+#pragma unroll
+                for (int kk = 0; kk < KMAX; ++kk) {
                     float v[E];
-                    U::unpack(w, v);
+                    U::unpack(w[kk], v);
 #pragma unroll
                     for (int e = 0; e < E; ++e)
                         v[e] = fmaf(gm[kk][e], dyt_tanh(a * v[e]), bt[kk][e]);
-                    U::st(y + gi, U::pack(v));
+                    if (uok[kk]) U::st(y + gr + kk * 32 * E, U::pack(v));
                 }
             }
-        }
+        };
+        if ((r0 + rows) * N <= tail)
+            pass(std::false_type{});
+        else
+            pass(std::true_type{});
     });
 }
 
@@ -531,33 +542,44 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
     rg.nblocks = nblocks;
     rg.slot = kBatchSlot;
     rg.fault = fault;
-    constexpr int RB = 1;  // no row reduction to share: one row at a time
+    constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         if (!alive) return;
-        const unsigned char* xs = rg.tile(k, 0);
-        const unsigned char* ds = rg.tile(k, 1);
+        const uint32_t xs = smem_u32(rg.tile(k, 0)) + lane * UB;
+        const uint32_t ds = smem_u32(rg.tile(k, 1)) + lane * UB;
         const int64_t r0 = b * R;
         const int rows = (int)(M - r0 < R ? M - r0 : R);
-        for (int i0 = warp * RB; i0 < rows; i0 += kBatchWarps * RB) {
+        // one row a warp at a time (no row reduction to share), its units all
+        // loaded before any is used.  A block whose units are all in the slot
+        // runs unmasked; the last one takes units past the copied bytes from
+        // global memory.
+        auto pass = [&](auto masked) {
+            constexpr bool kMask = decltype(masked)::value;
+            for (int i = warp; i < rows; i += kBatchWarps) {
+                const int64_t gr = (r0 + i) * N + lane * E;
+                typename U::W wx[KMAX], wd[KMAX];
 #pragma unroll
-            for (int rr = 0; rr < RB; ++rr) {
-                const int i = i0 + rr;
-                if (i >= rows) break;  // the same for the whole warp
-                const int64_t r = r0 + i;
+                for (int kk = 0; kk < KMAX; ++kk) {
+                    wx[kk] = wd[kk] = typename U::W{};
+                    const int so = i * rb + kk * 32 * UB;
+                    if constexpr (kMask) {
+                        const int64_t gi = gr + kk * 32 * E;
+                        if (uok[kk]) {
+                            const bool sm = gi < tail;
+                            wx[kk] = sm ? U::lds(xs + so) : U::ld(x + gi);
+                            wd[kk] = sm ? U::lds(ds + so) : U::ld(dy + gi);
+                        }
+                    } else if (uok[kk]) {
+                        wx[kk] = U::lds(xs + so);
+                        wd[kk] = U::lds(ds + so);
+                    }
+                }
 #pragma unroll
                 for (int kk = 0; kk < KMAX; ++kk) {
                     if (!uok[kk]) continue;
-                    const int u = lane + 32 * kk;
-                    const int64_t gi = r * N + u * E;
-                    const int so = i * rb + u * E * (int)sizeof(TX);
-                    const bool sm = gi < tail;
-                    const typename U::W wx =
-                        sm ? *reinterpret_cast<const typename U::W*>(xs + so) : U::ld(x + gi);
-                    const typename U::W wd =
-                        sm ? *reinterpret_cast<const typename U::W*>(ds + so) : U::ld(dy + gi);
                     float xv[E], dv[E], o[E];
-                    U::unpack(wx, xv);
-                    U::unpack(wd, dv);
+                    U::unpack(wx[kk], xv);
+                    U::unpack(wd[kk], dv);
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
                         float t, sc;
@@ -568,10 +590,14 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
                         acc_b[kk][e] += dv[e];
                         da = fmaf(gm[kk][e], dsd * xv[e], da);
                     }
-                    U::st(dx + gi, U::pack(o));
+                    U::st(dx + gr + kk * 32 * E, U::pack(o));
                 }
             }
-        }
+        };
+        if ((r0 + rows) * N <= tail)
+            pass(std::false_type{});
+        else
+            pass(std::true_type{});
     });
     if (ws == nullptr) return;  // no parameter gradient requested (uniform)
     const int64_t L = 2 * (int64_t)N + 1;

@@ -205,6 +205,11 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     // memory at each use and sums gamma * dy * x * sech^2 per thread instead
     // of per column, so that only two column accumulators stay in registers.
     constexpr bool kLean = lean_bwd<TX>(S);
+    // At 2 vectors a thread (16-bit) the same per-thread sum of
+    // gamma * dy * x * sech^2, with gamma in registers: 16 fewer registers
+    // than a per-column accumulator (DyT backward N = 4096 0.871 -> 0.885 of
+    // measured copy; float32 rows measured slower with it).
+    constexpr bool kDaT = kLean || (KV == 2 && sizeof(TX) == 2);
     static_assert(KV <= 2 || sizeof(TX) == 4 || kLean,
                   "the 16-bit DyT backward takes at most 2 vectors per thread");
     extern __shared__ __align__(128) unsigned char dsm[];
@@ -244,12 +249,13 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
             if constexpr (!kLean) gm[j][p] = gm_at(j, p);
             if constexpr (KV == 1) ga[p] = mul2(gm[0][p], a2);
             acc_g[j][p] = acc_b[j][p] = splat2(0.f);
-            if constexpr (!kLean) acc_a[j][p] = splat2(0.f);
+            if constexpr (!kDaT) acc_a[j][p] = splat2(0.f);
         }
     }
 
     auto rows = [&](const unsigned char* xs, const unsigned char* ds, TX* dxb, int64_t row0,
-                    bool alive, auto masked) {
+                    bool alive, auto masked, auto exact_) {
+        constexpr bool kExact = decltype(exact_)::value;  // every lane's vectors in the row
         constexpr bool kMask = decltype(masked)::value;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
             TX* const dxr = out_at<kIn>(dxb, u * grow, dx, maps, row0 + u * G, N, l * VEC);
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
-                const bool ok = alive && colok[j] && okr;
+                const bool ok = kExact ? okr : alive && colok[j] && okr;
                 f2 xv[P], dv[P], o[P];
                 unpack2<TX>(lds128_if(ok, xs + u * srow + j * W * 16), xv);
                 unpack2<TX>(lds128_if(ok, ds + u * srow + j * W * 16), dv);
@@ -266,8 +272,12 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
                     f2 t, s;
                     dyt_tanh_sech2_2(mul2(a2, xv[p]), t, s);
                     const f2 dsd = mul2(dv[p], s);
-                    if constexpr (kLean) {
-                        const f2 gmv = gm_at(j, p);
+                    if constexpr (kDaT) {
+                        f2 gmv;
+                        if constexpr (kLean)
+                            gmv = gm_at(j, p);
+                        else
+                            gmv = gm[j][p];
                         o[p] = mul2(dsd, mul2(gmv, a2));
                         // lanes past the row's end and padded rows add nothing
                         // (their x may be anything)
@@ -320,13 +330,26 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     const int64_t rstride = (int64_t)gridDim.x * (G * U);
     int64_t row0 = (int64_t)blockIdx.x * (G * U) + g;  // this thread's first row
     TX* dxb = dx + row0 * N + l * VEC;
+    // Rows that fill every lane's vectors run their full blocks without
+    // per-vector column predicates and load the slot without the fault
+    // predicate (a failed copy leaves stale bytes in the slot, never an
+    // address outside it; the fault word reports it).  Measured at several
+    // vectors a thread or 1024 threads: N = 4096 0.885 -> 0.916, 8192 0.927
+    // -> 0.935 of measured copy; at one vector in 256 threads 1% slower, so
+    // those keep the predicates, and so does the lean form.
+    constexpr bool kUseExact = !kLean && (KV > 1 || T > 256);
+    using ExactT = std::integral_constant<bool, kUseExact>;
+    const bool exact = kUseExact && !seg_groups(W) && N / VEC == W * KV;
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
         const unsigned char* xs = rg.tile(k, 0) + soff;
         const unsigned char* ds = rg.tile(k, 1) + soff;
         if (b < nfull)
-            rows(xs, ds, dxb, row0, alive, std::false_type{});
+            if (exact)
+                rows(xs, ds, dxb, row0, alive, std::false_type{}, ExactT{});
+            else
+                rows(xs, ds, dxb, row0, alive, std::false_type{}, std::false_type{});
         else
-            rows(xs, ds, dxb, row0, alive, std::true_type{});
+            rows(xs, ds, dxb, row0, alive, std::true_type{}, std::false_type{});
         row0 += rstride;
         dxb += rstride * N;
     });
@@ -340,7 +363,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdDyT))
     // lanes past the row's end hold garbage (tanh(alpha*0) for alpha = inf);
     // they are never stored above and are excluded here
     float da = 0.f;
-    if constexpr (kLean) {
+    if constexpr (kDaT) {
         da = lo2(da2) + hi2(da2);
     } else {
 #pragma unroll

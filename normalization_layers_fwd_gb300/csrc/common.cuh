@@ -659,6 +659,16 @@ __device__ __forceinline__ float ld_stat(const float* p, int64_t r)
     return __ldca(p + r);
 }
 
+// Bring the saved statistics of the rows `ahead` blocks on (the block's
+// first row r0, R rows, rows a CTA stride apart) into L2, one 128-byte line
+// per thread of the first warps; no register holds them.
+__device__ __forceinline__ void prefetch_stats(const float* p, int64_t r0, int R, int64_t M)
+{
+    const int64_t r = r0 + (int64_t)threadIdx.x * 32;
+    if ((int)threadIdx.x * 32 < R && r < M)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p + r));
+}
+
 // The row whose outputs (and saved statistics) belong to this thread's row q.
 template <int kIn>
 __device__ __forceinline__ int64_t stat_row(const RowMaps& maps, int64_t q)

@@ -239,7 +239,7 @@ Launch plan_batch(int64_t M, int64_t N, int xt, bool base16, bool pair_ok, int s
     if (kmax > gbn::batch_max_units(E)) return L;
     // rows a block: a multiple of 8 * RB (every warp busy) where the slot
     // holds that many, else of 8
-    const int64_t fit = gbn::kBatchSlot / (N * elem_bytes(xt));
+    const int64_t fit = gbn::batch_slot(gbn::is_bwd(kind) ? 2 : 1) / (N * elem_bytes(xt));
     const int64_t step =
         8 * (kind == gbn::kFwdDyT || kind == gbn::kBwdDyT ? 1 : gbn::batch_rb((int)kmax, E));
     const int64_t R = fit >= step ? fit / step * step : fit / 8 * 8;

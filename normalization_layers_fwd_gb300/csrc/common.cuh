@@ -247,7 +247,7 @@ constexpr int kGenCols = 1536;
 // reductions are warp butterflies; a backward's column sums stay in
 // registers and are combined across the CTA's warps in warp order at the
 // end.  Widths up to batch_max_units(E) * 32 units, and rows of at most
-// kBatchSlot / 8 bytes.
+// batch_slot / 8 bytes.
 constexpr int kBatchThreads = 256;
 constexpr int kBatchWarps = kBatchThreads / 32;
 // KMAX, the units a lane holds per row: up to 4, so rows up to 256 elements
@@ -264,11 +264,16 @@ constexpr int batch_max_units(int) { return 4; }
 constexpr int batch_rb(int KMAX, int E) { return KMAX * E <= 2 ? 4 : KMAX * E <= 6 ? 2 : 1; }
 static_assert(8 % batch_rb(1, 1) == 0 && 8 % batch_rb(3, 2) == 0 && 8 % batch_rb(4, 2) == 0,
               "a block of R rows, R a multiple of 8, holds whole groups of RB rows");
-constexpr int kBatchSlot = 8192;   // bytes per staged tensor per ring slot
-constexpr int kBatchStages = 4;
+// Bytes per staged tensor per ring slot and ring depth, by the tensors a
+// kernel stages (NT: 1 for a forward, 2 for a backward): 16 KB x 3 and
+// 12 KB x 3, so that a block holds several row groups per warp (a 260-byte
+// row fills 48 or 40 rows of them, where 8 KB held 16: one row group per
+// warp between ring barriers).
+constexpr int batch_slot(int NT) { return NT == 1 ? 16384 : 12288; }
+constexpr int batch_stages(int) { return 3; }
 // CTAs per SM: 4 for a forward (one staged tensor), 3 for a backward.
 constexpr int batch_minb(bool bwd) { return bwd ? 3 : 4; }
-constexpr int batch_smem(int NT) { return 128 + kBatchStages * NT * kBatchSlot; }
+constexpr int batch_smem(int NT) { return 128 + batch_stages(NT) * NT * batch_slot(NT); }
 
 // One unit of E consecutive elements (E = 2: a pair, E = 1: one element),
 // moved as one word: loaded through L1 (ld.global.ca, coherent with the

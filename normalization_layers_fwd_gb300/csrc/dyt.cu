@@ -488,13 +488,13 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
         }
     }
     const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
-    Ring<1, kBatchStages> rg;
+    Ring<1, batch_stages(1)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.row_bytes = rb;
     rg.R = R;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = kBatchSlot;
+    rg.slot = batch_slot(1);
     rg.fault = fault;
     constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {
@@ -568,14 +568,14 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
     }
     float da = 0.f;
     const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
-    Ring<2, kBatchStages> rg;
+    Ring<2, batch_stages(2)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     rg.row_bytes = rb;
     rg.R = R;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = kBatchSlot;
+    rg.slot = batch_slot(2);
     rg.fault = fault;
     constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit
     ring_loop(rg, dsm, [&](int64_t b, int64_t k, bool alive) {

@@ -512,13 +512,13 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
     const float fN = (float)N;
     // elements from `tail` on were not bulk-copied (the last block's end)
     const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
-    Ring<1, kBatchStages> rg;
+    Ring<1, batch_stages(1)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.row_bytes = rb;
     rg.R = R;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = kBatchSlot;
+    rg.slot = batch_slot(1);
     rg.fault = fault;
     constexpr int RB = batch_rb(KMAX, E);
     constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit
@@ -624,14 +624,14 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
         }
     }
     const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
-    Ring<2, kBatchStages> rg;
+    Ring<2, batch_stages(2)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     rg.row_bytes = rb;
     rg.R = R;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = kBatchSlot;
+    rg.slot = batch_slot(2);
     rg.fault = fault;
     constexpr int RB = batch_rb(KMAX, E);
     constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit

@@ -155,13 +155,13 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(false))
             wv[k][e] = uok[k] ? rms_weight(w, pt, (lane + 32 * k) * E + e, variant) : 0.f;
     }
     const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
-    Ring<1, kBatchStages> rg;
+    Ring<1, batch_stages(1)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.row_bytes = rb;
     rg.R = R;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = kBatchSlot;
+    rg.slot = batch_slot(1);
     rg.fault = fault;
     constexpr int RB = batch_rb(KMAX, E);
     constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit

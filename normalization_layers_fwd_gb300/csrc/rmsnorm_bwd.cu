@@ -33,10 +33,9 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
     int parity = 0;
     const int g = grp<W>(), l = lan<W>();
     // vector j of a row is vector l + j*W: in shared memory at +j*W*16 bytes
-    bool colok0[KV];
+    bool colok[KV];
 #pragma unroll
-    for (int j = 0; j < KV; ++j) colok0[j] = in_group<W>() && l + j * W < N / VEC;
-    const bool* const colok = colok0;
+    for (int j = 0; j < KV; ++j) colok[j] = in_group<W>() && l + j * W < N / VEC;
     const int rb = N * (int)sizeof(TX);
     const int soff = g * rb + l * 16, srow = G * rb, grow = G * N;
     // a weight in x's dtype: each dy*n is rounded to x's dtype (bf16 pairs
@@ -133,11 +132,12 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
                     bool alive_, auto masked, auto exact_) {
         constexpr bool kMask = decltype(masked)::value;
         // every lane's vectors in the row: no column or fault predicates
+        // (the fault word still reports a failed copy)
         constexpr bool kExact = decltype(exact_)::value;
         const bool alive = kExact || alive_;
-        bool colok[KV];
+        bool col[KV];
 #pragma unroll
-        for (int j = 0; j < KV; ++j) colok[j] = kExact || colok0[j];
+        for (int j = 0; j < KV; ++j) col[j] = kExact || colok[j];
         float rs[U];
         bool okr[U];
         f2 xh[U][KV][P], dn[U][KV][P];
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
             okr[u] = !kMask || row0 + u * G < M;
 #pragma unroll
             for (int j = 0; j < KV; ++j)  // x, scaled by r below
-                unpack2<TX>(lds128_if(alive && okr[u] && colok[j], xs + u * srow + j * W * 16),
+                unpack2<TX>(lds128_if(alive && okr[u] && col[j], xs + u * srow + j * W * 16),
                         xh[u][j]);
             rs[u] = rs_n[u];
             if constexpr (kDeep) rs_n[u] = rs_nn[u];
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
             f2 a2 = splat2(0.f);
 #pragma unroll
             for (int j = 0; j < KV; ++j) {
-                const uint4 dr = lds128_if(alive && okr[u] && colok[j], ds + u * srow + j * W * 16);
+                const uint4 dr = lds128_if(alive && okr[u] && col[j], ds + u * srow + j * W * 16);
                 f2 dv[P];
                 unpack2<TX>(dr, dv);
 #pragma unroll
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdRms))
                 f2 o[P];
 #pragma unroll
                 for (int p = 0; p < P; ++p) o[p] = mul2(r2, fma2(xh[u][j][p], nm, dn[u][j][p]));
-                st_stream_if(alive && okr[u] && colok[j], dxr + j * W * VEC, pack2<TX>(o));
+                st_stream_if(alive && okr[u] && col[j], dxr + j * W * VEC, pack2<TX>(o));
             }
         }
     };
@@ -417,14 +417,14 @@ __global__ void __launch_bounds__(kBatchThreads, batch_minb(true))
         }
     }
     const int64_t tail = ((M * (int64_t)rb) & ~(int64_t)15) / (int64_t)sizeof(TX);
-    Ring<2, kBatchStages> rg;
+    Ring<2, batch_stages(2)> rg;
     rg.src[0] = reinterpret_cast<const unsigned char*>(x);
     rg.src[1] = reinterpret_cast<const unsigned char*>(dy);
     rg.row_bytes = rb;
     rg.R = R;
     rg.M = M;
     rg.nblocks = nblocks;
-    rg.slot = kBatchSlot;
+    rg.slot = batch_slot(2);
     rg.fault = fault;
     constexpr int RB = batch_rb(KMAX, E);
     constexpr int UB = E * (int)sizeof(TX);  // bytes of a unit

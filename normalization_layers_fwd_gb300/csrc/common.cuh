@@ -265,12 +265,15 @@ constexpr int batch_rb(int KMAX, int E) { return KMAX * E <= 2 ? 4 : KMAX * E <=
 static_assert(8 % batch_rb(1, 1) == 0 && 8 % batch_rb(3, 2) == 0 && 8 % batch_rb(4, 2) == 0,
               "a block of R rows, R a multiple of 8, holds whole groups of RB rows");
 // Bytes per staged tensor per ring slot and ring depth, by the tensors a
-// kernel stages (NT: 1 for a forward, 2 for a backward): 16 KB x 3 and
-// 12 KB x 3, so that a block holds several row groups per warp (a 260-byte
-// row fills 48 or 40 rows of them, where 8 KB held 16: one row group per
-// warp between ring barriers).
-constexpr int batch_slot(int NT) { return NT == 1 ? 16384 : 12288; }
-constexpr int batch_stages(int) { return 3; }
+// kernel stages (NT: 1 for a forward, 2 for a backward): 24 KB x 2 and
+// 16 KB x 2, so that a block holds several row groups per warp (a 260-byte
+// row fills 80 or 48 rows of them, where 8 KB held 16: one row group per
+// warp between ring barriers).  Measured against 8 KB x 4 (fraction of
+// measured copy, bf16 N = 130, forward / backward): DyT 0.54 / 0.49 ->
+// 0.63 / 0.53, LayerNorm 0.48 / 0.55 -> 0.63 / 0.66, RMSNorm 0.61 / 0.47 ->
+// 0.84 / 0.55; 16 KB and 12 KB slots 3 deep came in between.
+constexpr int batch_slot(int NT) { return NT == 1 ? 24576 : 16384; }
+constexpr int batch_stages(int) { return 2; }
 // CTAs per SM: 4 for a forward (one staged tensor), 3 for a backward.
 constexpr int batch_minb(bool bwd) { return bwd ? 3 : 4; }
 constexpr int batch_smem(int NT) { return 128 + batch_stages(NT) * NT * batch_slot(NT); }

@@ -92,8 +92,9 @@ size_t gbn_bwd_workspace_bytes(int op, int64_t M, int64_t N, int xt, int pt, int
 
 /* Fault word of the current device: bit 0 (GBN_FAULT_WAIT_TIMEOUT) is set
  * when a kernel's bounded shared-memory barrier wait ran out (about one
- * second); that kernel then finished without further loads or stores and its
- * outputs are not valid.  Copies the word to host memory *out (this call
+ * second); that kernel then finished without further waits (writing, on some
+ * paths, values computed from stale shared memory into its own outputs, never
+ * outside them) and its outputs are not valid.  Copies the word to host memory *out (this call
  * synchronizes with the device) and zeroes it when `clear` is nonzero.  No
  * counterpart on the pages: it reports the safety bound of the bulk-copy
  * pipeline. */

@@ -667,13 +667,14 @@ __device__ __forceinline__ float ld_stat(const float* p, int64_t r)
     return __ldca(p + r);
 }
 
-// Bring the saved statistics of the rows `ahead` blocks on (the block's
-// first row r0, R rows, rows a CTA stride apart) into L2, one 128-byte line
-// per thread of the first warps; no register holds them.
+// Bring the saved statistics of R rows from row r0 on into L2, one 128-byte
+// line per lane of the CTA's last warp (not the ring issuer's warp, whose
+// delays hold up the bulk copies); no register holds them.
 __device__ __forceinline__ void prefetch_stats(const float* p, int64_t r0, int R, int64_t M)
 {
-    const int64_t r = r0 + (int64_t)threadIdx.x * 32;
-    if ((int)threadIdx.x * 32 < R && r < M)
+    const int t = (int)threadIdx.x - (int)(blockDim.x - 32);  // the last warp's lanes
+    const int64_t r = r0 + (int64_t)t * 32;
+    if (t >= 0 && t * 32 < R && r < M)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(p + r));
 }
 

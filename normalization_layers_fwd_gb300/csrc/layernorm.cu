@@ -232,13 +232,14 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     // use (*_n), or two (*_nn too) with one vector per thread: measured
     // faster for those rows, slower for the multi-vector ones
     constexpr bool kDeep = KV == 1;
-    // and, where one CTA per SM (or two rows per block) leaves too little
-    // work between the load and its use to hide a DRAM miss, prefetched into
-    // L2 four blocks ahead: N = 8192 0.866 -> 0.958 of measured copy, 2048
-    // 0.913 -> 0.925; at N = 16, 128 and 4096 (two or more CTAs per SM hide
-    // it) the prefetches cost 2-4%, and at N = 24 they slowed the 401,408-row
-    // backward from 18.4 to 20.5 us
-    constexpr bool kPrefetch = kIn == kInContig && (S == 14 || S == 17 || S == 19);
+    // and, where one CTA per SM (or two rows per block, or 160 rows of 8
+    // bytes of statistics each) leaves too little work between the load and
+    // its use to hide a DRAM miss, prefetched into L2 four blocks ahead: N =
+    // 8192 0.866 -> 0.958 of measured copy, 2048 0.913 -> 0.925, 24 0.921 ->
+    // 0.941; at N = 16, 128 and 4096 (two or more CTAs per SM hide it) the
+    // prefetches cost 2-4%
+    constexpr bool kPrefetch =
+        kIn == kInContig && (S == 14 || S == 17 || S == 19 || seg_groups(W));
     float mu_n[U], rs_n[U], mu_nn[U], rs_nn[U];
     auto load_stats = [&](int64_t row0, float (&mu_d)[U], float (&rs_d)[U]) {
 #pragma unroll

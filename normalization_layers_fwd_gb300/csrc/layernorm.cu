@@ -237,9 +237,10 @@ __global__ void __launch_bounds__(kSched[S].T, kind_minb(S, kBwdLN))
     // its use to hide a DRAM miss, prefetched into L2 four blocks ahead: N =
     // 8192 0.866 -> 0.958 of measured copy, 2048 0.913 -> 0.925, 24 0.921 ->
     // 0.941; at N = 16, 128 and 4096 (two or more CTAs per SM hide it) the
-    // prefetches cost 2-4%
-    constexpr bool kPrefetch =
-        kIn == kInContig && (S == 14 || S == 17 || S == 19 || seg_groups(W));
+    // prefetches cost 2-4%, and in the lean form (16-bit N = 16384) 0.50 ->
+    // 0.36
+    constexpr bool kPrefetch = kIn == kInContig && !kLean &&
+                               (S == 14 || S == 17 || S == 19 || seg_groups(W));
     float mu_n[U], rs_n[U], mu_nn[U], rs_nn[U];
     auto load_stats = [&](int64_t row0, float (&mu_d)[U], float (&rs_d)[U]) {
 #pragma unroll

@@ -99,3 +99,23 @@ def test_extra_widths_are_off_the_sweep_paths():
         assert row_bytes % 16 != 0 or row_bytes // 16 > 1024
         w = synth.sweep("layernorm", N, xd)
         assert w.M == (1 << 28) // N and w.xdtype == xd
+
+
+def test_recorded_traffic_only_for_the_captured_sources(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed ncu capture only while the
+    kernel sources hash to the value recorded with it; any other hash, or a
+    launch the capture does not hold, gives None."""
+    key = "layernorm_bwd[16777216x16]"
+    rec = {"source_hash": bench.source_hash(),
+           "launches": {key: {"dram_read": 1000, "dram_write": 234}}}
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # source_hash reads the kernel sources under ROOT: keep it on the real tree
+    real_hash = rec["source_hash"]
+    monkeypatch.setattr(bench, "source_hash", lambda: real_hash)
+    assert bench.recorded_traffic(key) == 1234
+    assert bench.recorded_traffic("dyt_fwd[1x16]") is None
+    rec["source_hash"] = "0" * 16
+    (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(rec))
+    assert bench.recorded_traffic(key) is None
